@@ -1,0 +1,155 @@
+// attn_common.cuh -- pieces shared by the decode-attention kernels: the
+// argument block, tensor-core and exponent helpers, and the kernel that
+// merges the split-K partials.
+#pragma once
+#include "split.cuh"
+
+namespace kvarn {
+
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+struct AttnArgs {
+    const void* q;
+    const uint8_t* pool;
+    const uint16_t* staging;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* partials;
+    float* out;
+    uint32_t* err;
+    int64_t n_pool_blocks;
+    int64_t block_bytes;
+    int q_dtype;
+    int max_blocks;
+    int batch;
+    int n_q, n_kv, G;
+    int nw;
+    float sm_scale;
+    uint32_t sb[4];
+};
+
+// ---------------------------------------------------------------- small helpers
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two 2-bit codes at bits 2j and 16+2j of w -> fp16x2 (code * 2^-24 each).
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, int j) {
+    return (w >> (2 * j)) & 0x00030003u;
+}
+constexpr float kCodeUnitInv = 16777216.0f;   // 2^24
+
+// 2^k as a float for k in [-126, 127]
+__device__ __forceinline__ float exp2i(int k) {
+    k = max(-126, min(127, k));
+    return __int_as_float((127 + k) << 23);
+}
+// ceil(log2(x)) for finite x > 0 (normal)
+__device__ __forceinline__ int ceil_log2(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (int)((u >> 23) & 0xff) - 127 + ((u & 0x7fffff) != 0);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    return h2_as_u32(__floats2half2_rn(lo, hi));
+}
+
+__device__ __forceinline__ void load_q4(const AttnArgs& a, int64_t row, int lane, float (&v)[4]) {
+    if (a.q_dtype == KVARN_FP32) {
+        float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + row * kD)[lane];
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+        uint2 u = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.q) + row * kD)[lane];
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xffff0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+}
+
+// ---------------------------------------------------------------- merge kernel
+// One warp per (sequence, query head): LSE-merge the unit's partials. For the
+// 2-bit cache (ROT = true) the merged accumulator is in the rotated space: it
+// is rotated back once and the raw bf16 tail tokens (unrotated) are added;
+// the bf16 cache (ROT = false) has every token in its pages.
+template <int B, bool ROT>
+__global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (gw >= (int64_t)a.batch * a.n_q) return;
+    const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);
+    const int h = hq / a.G, jq = hq % a.G;
+    const int L = a.seq_lens[b];
+    float* out = a.out + gw * kD;
+    if (L < 0 || L > a.max_blocks * B) {
+        if (lane == 0) raise_error(a.err, KVARN_DEVERR_POSITION);
+        reinterpret_cast<float4*>(out)[lane] = make_float4(NAN, NAN, NAN, NAN);
+        return;
+    }
+    const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1};
+    int64_t before, total;
+    split_prefix(sp, b, lane, before, total);
+    const int64_t W = total * a.n_kv;
+    const int nb = split_nblocks(sp, b);
+    float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (nb > 0) {
+        const int64_t Su = before * a.n_kv + (int64_t)h * nb;
+        const int64_t u = (int64_t)b * a.n_kv + h;
+        const int64_t w0 = split_last_warp_at(Su, W, a.nw), w1 = split_last_warp_at(Su + nb - 1, W, a.nw);
+        for (int64_t ww = w0; ww <= w1; ++ww) {
+            const float* base = a.partials + ((u + ww) * a.G + jq) * kPartialStride;
+            const float pm = base[0], pl = base[1];
+            const float4 pa = reinterpret_cast<const float4*>(base + 4)[lane];
+            const float mn = fmaxf(m, pm);
+            const float fa = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+            const float fb = (pm == -INFINITY) ? 0.f : exp2f(pm - mn);
+            l = l * fa + pl * fb;
+            acc[0] = acc[0] * fa + pa.x * fb;
+            acc[1] = acc[1] * fa + pa.y * fb;
+            acc[2] = acc[2] * fa + pa.z * fb;
+            acc[3] = acc[3] * fa + pa.w * fb;
+            m = mn;
+        }
+        if (ROT) {
+            // rotate back: x = sigma . H(acc) / sqrt(128)
+            fwht128(acc, lane);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] *= kInvSqrtD * sign_of(a.sb, 4 * lane + k);
+        }
+    }
+    const int ntail = ROT ? L - nb * B : 0;
+    if (ntail > 0) {
+        float qv[4];
+        load_q4(a, gw, lane, qv);
+        const float qs = a.sm_scale * kLog2e;
+        const uint16_t* kst = a.staging + (((int64_t)b * a.n_kv + h) * 2 + 0) * B * kD;
+        const uint16_t* vst = kst + B * kD;
+        for (int r = 0; r < ntail; ++r) {
+            const uint2 ku = reinterpret_cast<const uint2*>(kst + r * kD)[lane];
+            float d = qv[0] * __uint_as_float(ku.x << 16);
+            d = fmaf(qv[1], __uint_as_float(ku.x & 0xffff0000u), d);
+            d = fmaf(qv[2], __uint_as_float(ku.y << 16), d);
+            d = fmaf(qv[3], __uint_as_float(ku.y & 0xffff0000u), d);
+            const float sc = warp_sum(d) * qs;
+            const float mn = fmaxf(m, sc);
+            const float fa = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+            const float p = exp2f(sc - mn);
+            const uint2 vu = reinterpret_cast<const uint2*>(vst + r * kD)[lane];
+            acc[0] = acc[0] * fa + p * __uint_as_float(vu.x << 16);
+            acc[1] = acc[1] * fa + p * __uint_as_float(vu.x & 0xffff0000u);
+            acc[2] = acc[2] * fa + p * __uint_as_float(vu.y << 16);
+            acc[3] = acc[3] * fa + p * __uint_as_float(vu.y & 0xffff0000u);
+            l = l * fa + p;
+            m = mn;
+        }
+    }
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    reinterpret_cast<float4*>(out)[lane] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+}
+
+}  // namespace kvarn

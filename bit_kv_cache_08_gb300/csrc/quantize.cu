@@ -1,0 +1,409 @@
+// quantize.cu -- KVarN quantise-on-write (bulk and fused into the decode-step
+// KV append) and dequantisation, hand-written for sm_103a.
+//
+// Method: abstract of "KVarN: cuantizacion de KV-Cache normalizada por
+// varianza mitiga la acumulacion de errores en tareas de razonamiento"
+// (Hadamard rotation, then dual-scaling variance normalisation over both axes
+// of K and V, 2-bit) and "KVarN：方差归一化让 2-bit KV 缓存扛住长链推理"
+// section 三 3.1 (randomised Hadamard) and 3.2 (token axis then channel axis
+// to variance 1, repeated; grouped scales kept for dequantisation; computed
+// at decode time inside the KV write kernel).
+//
+// One CTA of 256 threads (8 warps) owns one head-block of B tokens x 128
+// channels. Warp w holds tokens w*B/8 .. (w+1)*B/8-1, lane l channels
+// 4l..4l+3, all in registers:
+//   rotation   sign flip + FWHT-128 (2 in-register + 5 shuffle stages), *1/sqrt(128)
+//   VarN       token pass: two-pass mean/variance by warp reduction;
+//              channel pass: per-warp partial sums through shared memory
+//   factors    fp16 round-to-nearest of the clamped cumulative factors
+//   quantise   y = x_rot / (R16*C16) (IEEE division; the product is exact in
+//              fp32), per (token, 32-channel group): z = fp16 round-down of the
+//              minimum, s = least fp16 with z + 3s >= maximum (directed-rounding
+//              candidate plus one exact check), code = nearest level, ties even
+//   pack       codes OR-ed into the shared-memory image of the head-block in
+//              the attention kernel's record order, then 16-byte stores.
+#include "common.cuh"
+
+namespace kvarn {
+
+template <int B>
+struct QuantSmem {
+    alignas(16) uint8_t image[head_block_bytes(B)];   // exact global layout
+    alignas(16) float part_a[8][kD];
+    alignas(16) float part_b[8][kD];
+};
+
+struct QuantParams {
+    int kind;          // 0 = K record order, 1 = V record order
+    int iters;
+    uint32_t sb[4];    // rotation signs
+};
+
+// Least fp16 s >= 0 with z + 3 s >= M, for fp16 z <= M (all exact comparisons).
+__device__ __forceinline__ float step_for(float zf, float M) {
+    if (zf >= M) return 0.0f;
+    float t = __fdiv_ru(__fsub_ru(M, zf), 3.0f);          // >= exact (M - z)/3
+    __half s = __float2half_ru(t);                         // >= exact minimum
+    float sf = __half2float(s);
+    if (!(sf <= kF16Max)) { s = __float2half_rn(kF16Max); sf = kF16Max; }
+    // the directed roundings may overshoot by one fp16 step: check the one below
+    uint16_t bits = __half_as_ushort(s);
+    if (bits > 0) {
+        float pf = __half2float(__ushort_as_half((uint16_t)(bits - 1)));
+        if (__fadd_rd(zf, 3.0f * pf) >= M) sf = pf;         // rd-sum >= M <=> exact sum >= M
+    }
+    return sf;
+}
+
+// Quantise the tile held in x (rows of this warp) into q.image.
+template <int B>
+__device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantSmem<B>& q,
+                              int warp, int lane) {
+    constexpr int RPW = B / 8;
+    uint32_t* words = reinterpret_cast<uint32_t*>(q.image);
+    uint16_t* s_sec = reinterpret_cast<uint16_t*>(q.image + off_s(B));
+    uint16_t* z_sec = reinterpret_cast<uint16_t*>(q.image + off_z(B));
+    uint16_t* R_sec = reinterpret_cast<uint16_t*>(q.image + off_R(B));
+    uint16_t* C_sec = reinterpret_cast<uint16_t*>(q.image + off_C(B));
+
+    // ---- rotation: x_rot = H (sigma . x) / sqrt(128)
+    float sg[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sg[k] = sign_of(p.sb, 4 * lane + k);
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[i][k] *= sg[k];
+        fwht128(x[i], lane);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[i][k] *= kInvSqrtD;
+    }
+
+    // ---- VarN: token pass then channel pass, p.iters times
+    float y[RPW][4];
+    float Rf[RPW], Cf[4] = {1.f, 1.f, 1.f, 1.f};
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        Rf[i] = 1.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) y[i][k] = x[i][k];
+    }
+    for (int it = 0; it < p.iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            float mu = warp_sum(y[i][0] + y[i][1] + y[i][2] + y[i][3]) * (1.0f / kD);
+            float d0 = y[i][0] - mu, d1 = y[i][1] - mu, d2 = y[i][2] - mu, d3 = y[i][3] - mu;
+            float var = warp_sum(d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3) * (1.0f / kD);
+            if (var > 0.f && isfinite(var)) {
+                float r = sqrtf(var);
+                float inv = __frcp_rn(r);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) y[i][k] *= inv;
+                Rf[i] *= r;
+            }
+        }
+        float cs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < RPW; ++i)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cs[k] += y[i][k];
+        *reinterpret_cast<float4*>(&q.part_a[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+        __syncthreads();
+        float mu[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            float4 v = *reinterpret_cast<const float4*>(&q.part_a[w][4 * lane]);
+            mu[0] += v.x; mu[1] += v.y; mu[2] += v.z; mu[3] += v.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { mu[k] *= (1.0f / B); cs[k] = 0.f; }
+#pragma unroll
+        for (int i = 0; i < RPW; ++i)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float d = y[i][k] - mu[k];
+                cs[k] += d * d;
+            }
+        *reinterpret_cast<float4*>(&q.part_b[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+        __syncthreads();
+        float var[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            float4 v = *reinterpret_cast<const float4*>(&q.part_b[w][4 * lane]);
+            var[0] += v.x; var[1] += v.y; var[2] += v.z; var[3] += v.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float vk = var[k] * (1.0f / B);
+            if (vk > 0.f && isfinite(vk)) {
+                float r = sqrtf(vk);
+                float inv = __frcp_rn(r);
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) y[i][k] *= inv;
+                Cf[k] *= r;
+            }
+        }
+    }
+
+    // ---- fp16 factors (clamped to the normal range) and normalised values
+    float C16[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) C16[k] = __half2float(__float2half_rn(fminf(fmaxf(Cf[k], kF16MinNormal), kF16Max)));
+    const int g = lane >> 3;   // this lane's 32-channel group
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int t = warp * RPW + i;
+        const float R16 = __half2float(__float2half_rn(fminf(fmaxf(Rf[i], kF16MinNormal), kF16Max)));
+        float yq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) yq[k] = __fdiv_rn(x[i][k], R16 * C16[k]);
+        float mn = fminf(fminf(yq[0], yq[1]), fminf(yq[2], yq[3]));
+        float mx = fmaxf(fmaxf(yq[0], yq[1]), fmaxf(yq[2], yq[3]));
+#pragma unroll
+        for (int m = 1; m <= 4; m <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+        }
+        const __half zh = __float2half_rd(fminf(fmaxf(mn, -kF16Max), kF16Max));
+        const float zf = __half2float(zh);
+        const float sf = step_for(zf, mx);
+        uint32_t code[4];
+        if (sf == 0.0f) {
+            code[0] = code[1] = code[2] = code[3] = 0u;
+        } else {
+            const float b0 = zf + 0.5f * sf, b1 = zf + 1.5f * sf, b2 = zf + 2.5f * sf;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                code[k] = (uint32_t)(yq[k] > b0) + (uint32_t)(yq[k] >= b1) + (uint32_t)(yq[k] > b2);
+        }
+        // ---- pack into the record order of this kind
+        const int sb = t >> 5;
+        if (p.kind == KVARN_KIND_K) {
+            const int a = (t & 31) >> 2, ii = t & 3, bq = (lane & 7) >> 1, eh = lane & 1;
+            const int word = (32 * sb + 4 * a + bq) * 8 + 2 * ii + (g >> 1);
+            uint32_t contrib = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = 4 * eh + k;
+                contrib |= code[k] << (2 * (4 * (g & 1) + (e >> 1)) + 16 * (e & 1));
+            }
+            atomicOr(&words[word], contrib);
+        } else {
+            const int a = lane & 7, bq = (t & 31) >> 3, d = t & 7;
+            const int rec = 32 * sb + 4 * a + bq;
+            const int base = 2 * (4 * (d >> 2) + 2 * ((d & 3) >> 1)) + 16 * (d & 1);
+            atomicOr(&words[rec * 8 + 2 * g + 0], (code[0] << base) | (code[1] << (base + 2)));
+            atomicOr(&words[rec * 8 + 2 * g + 1], (code[2] << base) | (code[3] << (base + 2)));
+        }
+        if ((lane & 7) == 0) {
+            s_sec[g * B + t] = __half_as_ushort(__float2half_rn(sf));   // sf is an fp16 value
+            z_sec[g * B + t] = __half_as_ushort(zh);
+        }
+        if (lane == 0) R_sec[t] = __half_as_ushort(__float2half_rn(R16));
+    }
+    if (warp == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) C_sec[4 * lane + k] = __half_as_ushort(__float2half_rn(C16[k]));
+    }
+    __syncthreads();
+}
+
+template <int B>
+__device__ __forceinline__ void zero_code_words(QuantSmem<B>& q, int tid) {
+    uint32_t* words = reinterpret_cast<uint32_t*>(q.image);
+    for (int i = tid; i < B * 8; i += 256) words[i] = 0u;
+}
+
+template <int B>
+__device__ __forceinline__ void store_image(const QuantSmem<B>& q, uint8_t* dst, int tid) {
+    const uint4* src = reinterpret_cast<const uint4*>(q.image);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    for (int i = tid; i < head_block_bytes(B) / 16; i += 256) d[i] = src[i];
+}
+
+__device__ __forceinline__ void load4(const void* src, int dtype, int64_t elem_off, float (&v)[4]) {
+    if (dtype == KVARN_FP32) {
+        float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(src) + elem_off);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
+        uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(src) + elem_off);
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xffff0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+}
+
+// ---------------------------------------------------------------- bulk quantise
+template <int B>
+__global__ void __launch_bounds__(256) quantize_blocks_kernel(
+    const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
+    uint8_t* __restrict__ dst_base, const int64_t* __restrict__ dst_offsets, QuantParams p,
+    uint32_t* err) {
+    __shared__ QuantSmem<B> q;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n = blockIdx.x;
+    zero_code_words<B>(q, tid);
+    float x[B / 8][4];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < B / 8; ++i) {
+        const int t = warp * (B / 8) + i;
+        load4(src, dtype, n * block_stride + (int64_t)t * token_stride + 4 * lane, x[i]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) bad |= !isfinite(x[i][k]);
+    }
+    if (__syncthreads_or(bad) && tid == 0) raise_error(err, KVARN_DEVERR_NONFINITE);
+    quantize_tile<B>(x, p, q, warp, lane);
+    const int64_t off = dst_offsets ? dst_offsets[n] : n * (int64_t)head_block_bytes(B);
+    store_image<B>(q, dst_base + off, tid);
+}
+
+// ---------------------------------------------------------------- fused append
+// grid (batch, n_kv, 2): one CTA per (sequence, kv head, K|V).
+template <int B>
+__global__ void __launch_bounds__(256) append_kernel(
+    uint8_t* __restrict__ pool, int64_t n_pool_blocks, int64_t block_bytes,
+    uint16_t* __restrict__ staging, const int32_t* __restrict__ block_table, int max_blocks,
+    const int32_t* __restrict__ pos_arr, const uint16_t* __restrict__ k_new,
+    const uint16_t* __restrict__ v_new, int n_kv, QuantParams p, uint32_t* err) {
+    __shared__ QuantSmem<B> q;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
+    const int pos = pos_arr[b];
+    if (pos < 0 || pos >= max_blocks * B) {
+        if (tid == 0 && h == 0 && kv == 0) raise_error(err, KVARN_DEVERR_POSITION);
+        return;
+    }
+    const int row = pos % B;
+    const uint16_t* newrow = (kv ? v_new : k_new) + ((int64_t)b * n_kv + h) * kD;
+    uint16_t* stage = staging + (((int64_t)b * n_kv + h) * 2 + kv) * B * kD;
+    if (tid < 16)   // 256 bytes, 16 per thread
+        reinterpret_cast<uint4*>(stage + row * kD)[tid] = reinterpret_cast<const uint4*>(newrow)[tid];
+    if (row != B - 1) return;
+
+    const int64_t phys = block_table[(int64_t)b * max_blocks + pos / B];
+    if (phys < 0 || phys >= n_pool_blocks) {
+        if (tid == 0) raise_error(err, KVARN_DEVERR_BLOCK_ID);
+        return;
+    }
+    p.kind = kv;
+    zero_code_words<B>(q, tid);
+    float x[B / 8][4];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < B / 8; ++i) {
+        const int t = warp * (B / 8) + i;
+        const uint16_t* r = (t == B - 1) ? newrow : stage + t * kD;
+        load4(r, KVARN_BF16, 4 * lane, x[i]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) bad |= !isfinite(x[i][k]);
+    }
+    if (__syncthreads_or(bad) && tid == 0) raise_error(err, KVARN_DEVERR_NONFINITE);
+    quantize_tile<B>(x, p, q, warp, lane);
+    store_image<B>(q, pool + phys * block_bytes + (int64_t)(2 * h + kv) * head_block_bytes(B), tid);
+}
+
+// ---------------------------------------------------------------- dequantise
+template <int B>
+__global__ void __launch_bounds__(256) dequantize_kernel(
+    const uint8_t* __restrict__ src_base, const int64_t* __restrict__ src_offsets, int kind,
+    int rotated, QuantParams p, float* __restrict__ out) {
+    __shared__ alignas(16) uint8_t img[head_block_bytes(B)];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n = blockIdx.x;
+    const int64_t off = src_offsets ? src_offsets[n] : n * (int64_t)head_block_bytes(B);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src_base + off);
+    for (int i = tid; i < head_block_bytes(B) / 16; i += 256) reinterpret_cast<uint4*>(img)[i] = s4[i];
+    __syncthreads();
+    const uint32_t* words = reinterpret_cast<const uint32_t*>(img);
+    const uint16_t* s_sec = reinterpret_cast<const uint16_t*>(img + off_s(B));
+    const uint16_t* z_sec = reinterpret_cast<const uint16_t*>(img + off_z(B));
+    const uint16_t* R_sec = reinterpret_cast<const uint16_t*>(img + off_R(B));
+    const uint16_t* C_sec = reinterpret_cast<const uint16_t*>(img + off_C(B));
+    const int g = lane >> 3;
+    for (int i = 0; i < B / 8; ++i) {
+        const int t = warp * (B / 8) + i, sb = t >> 5;
+        const float s = h2f(s_sec[g * B + t]), z = h2f(z_sec[g * B + t]), R = h2f(R_sec[t]);
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = 4 * lane + k;
+            int word, bit;
+            if (kind == KVARN_KIND_K) {
+                const int a = (t & 31) >> 2, ii = t & 3, bq = (c & 31) >> 3, e = c & 7;
+                word = (32 * sb + 4 * a + bq) * 8 + 2 * ii + (g >> 1);
+                bit = 2 * (4 * (g & 1) + (e >> 1)) + 16 * (e & 1);
+            } else {
+                const int bq = (t & 31) >> 3, d = t & 7, a = (c & 31) >> 2, f = c & 3;
+                word = (32 * sb + 4 * a + bq) * 8 + 2 * g + (f >> 1);
+                bit = 2 * (4 * (d >> 2) + 2 * ((d & 3) >> 1) + (f & 1)) + 16 * (d & 1);
+            }
+            const float code = (float)((words[word] >> bit) & 3u);
+            v[k] = fmaf(code, s, z) * R * h2f(C_sec[c]);
+        }
+        if (!rotated) {
+            fwht128(v, lane);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD * sign_of(p.sb, 4 * lane + k);
+        }
+        *reinterpret_cast<float4*>(out + (n * B + t) * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// ---------------------------------------------------------------- host launchers
+static QuantParams make_params(const kvarn_config& cfg, int kind) {
+    QuantParams p;
+    p.kind = kind;
+    p.iters = cfg.varn_iters;
+    for (int i = 0; i < 4; ++i) p.sb[i] = cfg.sign_bits[i];
+    return p;
+}
+
+cudaError_t launch_quantize_blocks(const kvarn_config& cfg, int kind, const void* src, int dtype,
+                                   int64_t n, int64_t block_stride, int64_t token_stride,
+                                   void* dst_base, const int64_t* dst_offsets, uint32_t* err,
+                                   cudaStream_t st) {
+    QuantParams p = make_params(cfg, kind);
+    if (cfg.block_size == 32)
+        quantize_blocks_kernel<32><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
+                                                                (uint8_t*)dst_base, dst_offsets, p, err);
+    else
+        quantize_blocks_kernel<64><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
+                                                                (uint8_t*)dst_base, dst_offsets, p, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_blocks,
+                          int64_t block_bytes, void* staging, const int32_t* block_table,
+                          int max_blocks, const int32_t* pos, const void* k_new, const void* v_new,
+                          int batch, uint32_t* err, cudaStream_t st) {
+    QuantParams p = make_params(cfg, 0);
+    dim3 grid(batch, cfg.n_kv_heads, 2);
+    if (cfg.block_size == 32)
+        append_kernel<32><<<grid, 256, 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
+                                                (uint16_t*)staging, block_table, max_blocks, pos,
+                                                (const uint16_t*)k_new, (const uint16_t*)v_new,
+                                                cfg.n_kv_heads, p, err);
+    else
+        append_kernel<64><<<grid, 256, 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
+                                                (uint16_t*)staging, block_table, max_blocks, pos,
+                                                (const uint16_t*)k_new, (const uint16_t*)v_new,
+                                                cfg.n_kv_heads, p, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const kvarn_config& cfg, int kind, const void* src_base,
+                              const int64_t* src_offsets, int64_t n, int rotated, float* out,
+                              cudaStream_t st) {
+    QuantParams p = make_params(cfg, kind);
+    if (cfg.block_size == 32)
+        dequantize_kernel<32><<<(unsigned)n, 256, 0, st>>>((const uint8_t*)src_base, src_offsets, kind,
+                                                           rotated, p, out);
+    else
+        dequantize_kernel<64><<<(unsigned)n, 256, 0, st>>>((const uint8_t*)src_base, src_offsets, kind,
+                                                           rotated, p, out);
+    return cudaGetLastError();
+}
+
+}  // namespace kvarn

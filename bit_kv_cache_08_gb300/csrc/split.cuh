@@ -1,0 +1,99 @@
+// split.cuh -- balanced split-K partition shared by the decode-attention
+// kernels. The (sequence, kv head) units are laid end to end, block by block
+// (sequence-major, then head, then block); warp w of nw takes global blocks
+// [floor(w*W/nw), floor((w+1)*W/nw)). A unit's partial from warp w lives in
+// slot (unit + w), which is unique because consecutive units share at most
+// one warp.
+#pragma once
+#include "common.cuh"
+
+namespace kvarn {
+
+constexpr int kPartialStride = 132;   // floats per (slot, head): m, l, pad, pad, acc[128]
+
+struct SplitArgs {
+    const int32_t* seq_lens;
+    int batch;
+    int n_kv;
+    int max_blocks;
+    int B;
+    int ceil_blocks;   // 1: a partial last block counts (bf16 pages); 0: full blocks only
+};
+
+__device__ __forceinline__ int split_nblocks(const SplitArgs& s, int b) {
+    const int L = s.seq_lens[b];
+    if (L < 0 || L > s.max_blocks * s.B) return 0;   // flagged by the merge kernel
+    return s.ceil_blocks ? (L + s.B - 1) / s.B : L / s.B;
+}
+
+// Warp-cooperative: returns W (total blocks over all units); if x < W, sets
+// (b, h, j) of global position x.
+__device__ inline int64_t split_locate(const SplitArgs& s, int64_t x, int lane, int& b_out,
+                                       int& h_out, int& j_out) {
+    int64_t prefix = 0;
+    int found_b = -1;
+    int64_t found_base = 0;
+    for (int b0 = 0; b0 < s.batch; b0 += 32) {
+        const int b = b0 + lane;
+        const int64_t nb = (b < s.batch) ? (int64_t)split_nblocks(s, b) * s.n_kv : 0;
+        int64_t inc = nb;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int64_t o = __shfl_up_sync(kFull, inc, m);
+            if (lane >= m) inc += o;
+        }
+        const int64_t excl = prefix + inc - nb;
+        const bool hit = found_b < 0 && nb > 0 && x >= excl && x < excl + nb;
+        const uint32_t ball = __ballot_sync(kFull, hit);
+        if (ball) {
+            const int src = __ffs(ball) - 1;
+            found_b = b0 + src;
+            found_base = __shfl_sync(kFull, excl, src);
+        }
+        prefix += __shfl_sync(kFull, inc, 31);
+    }
+    if (found_b >= 0) {
+        const int nb = split_nblocks(s, found_b);
+        const int64_t local = x - found_base;
+        b_out = found_b;
+        h_out = (int)(local / nb);
+        j_out = (int)(local % nb);
+    }
+    return prefix;
+}
+
+struct Cursor {
+    int b, h, j, nb;
+};
+
+__device__ __forceinline__ void split_advance(const SplitArgs& s, Cursor& c) {
+    if (++c.j < c.nb) return;
+    c.j = 0;
+    if (++c.h < s.n_kv) return;
+    c.h = 0;
+    do {
+        ++c.b;
+        c.nb = (c.b < s.batch) ? split_nblocks(s, c.b) : 1;
+    } while (c.nb == 0);
+}
+
+// Blocks of all sequences before b, and of all sequences (warp-cooperative).
+__device__ inline void split_prefix(const SplitArgs& s, int b, int lane, int64_t& before,
+                                    int64_t& total) {
+    before = 0;
+    total = 0;
+    for (int b0 = 0; b0 < s.batch; b0 += 32) {
+        const int bb = b0 + lane;
+        const int64_t nb = (bb < s.batch) ? (int64_t)split_nblocks(s, bb) : 0;
+        total += warp_sum_i64(nb);
+        before += warp_sum_i64(bb < b ? nb : 0);
+    }
+}
+
+// Largest w in [0, nw) with floor(w*W/nw) <= x.
+__host__ __device__ __forceinline__ int64_t split_last_warp_at(int64_t x, int64_t W, int64_t nw) {
+    const int64_t r = ((x + 1) * nw - 1) / W;
+    return r < nw - 1 ? r : nw - 1;
+}
+
+}  // namespace kvarn

@@ -1,0 +1,232 @@
+/*
+ * kvarn.h -- C ABI of the GB300 (sm_103a) KVarN 2-bit KV-cache library.
+ *
+ * KVarN stores the K and V caches at 2 bits per element without calibration
+ * data: each block of tokens is rotated by a randomised Hadamard matrix over
+ * head_dim, normalised along the token axis and the channel axis in turn
+ * until both have unit variance, and quantised in 32-channel groups; the
+ * scales are kept and applied again when the cache is read. Decode attention
+ * reads the packed cache directly, with the query rotated by the same matrix
+ * and the inverse rotation applied once to the output.
+ *
+ * Sources (page title, section):
+ *   "KVarN: cuantizacion de KV-Cache normalizada por varianza mitiga la
+ *    acumulacion de errores en tareas de razonamiento" -- English abstract:
+ *    Hadamard rotation then dual-scaling variance normalisation over both
+ *    axes of K and V, calibration-free, 2-bit.
+ *   "KVarN：方差归一化让 2-bit KV 缓存扛住长链推理" -- section 三, 3.1
+ *    (randomised Hadamard on K and V; q multiplied by the same matrix so
+ *    Q K^T is unchanged) and 3.2 (token-axis then channel-axis variance to 1,
+ *    repeated 2-3 times; grouped scales kept for dequantisation; statistics
+ *    computed at decode time and fusable into the KV write kernel).
+ *
+ * Conventions for every entry point
+ *   - Pointers marked "device" must be device memory of the current CUDA
+ *     device; "host" pointers are host memory. Nothing is allocated, freed or
+ *     synchronised by the library except where stated (kvarn_read_error).
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All device work is enqueued on it, in order.
+ *   - The caller owns every buffer. Buffers written by a call must not be
+ *     read or written by other work until that call's stream work completes.
+ *   - Return value: KVARN_OK, or a negative kvarn_status when the arguments
+ *     are rejected on the host (nothing enqueued) or a launch fails.
+ *     Data-dependent faults found on the device (a block id outside the
+ *     pool, a position beyond the block table, non-finite input, a wait that
+ *     ran out of time) never trap: the kernel skips the affected unit and
+ *     ORs a KVARN_DEVERR_* flag into the workspace error word, which
+ *     kvarn_read_error returns. Outputs of a call that raised a flag are
+ *     unspecified.
+ *
+ * Data layouts (little-endian; fp16/bf16 are IEEE binary16 / bfloat16)
+ *   Head-block: one (physical block, kv head, K or V): B tokens x 128
+ *   channels, packed as
+ *     [0, 32B)        2-bit codes, in 32-byte records (order below)
+ *     [32B, 40B)      s: fp16 [4][B]   per (group, token) step
+ *     [40B, 48B)      z: fp16 [4][B]   per (group, token) zero (lowest level)
+ *     [48B, 50B)      R: fp16 [B]      per-token factor
+ *     [50B, 50B+256)  C: fp16 [128]    per-channel factor
+ *   = 1856 bytes (B = 32) or 3456 bytes (B = 64). The value of element
+ *   (t, c) in the rotated space is (code * s[g][t] + z[g][t]) * R[t] * C[c]
+ *   with g = c / 32. Code records: record r = 32*sb + 4a + b (sb = t / 32)
+ *   holds 8 little-endian 32-bit words; a code sits at bit position p of
+ *   word w of its record:
+ *     kind K: a = (t%32)/4, i = t%4, g = c/32, b = (c%32)/8, e = c%8;
+ *             w = 2i + g/2, p = 2*(4*(g%2) + e/2) + 16*(e%2)
+ *     kind V: b = (t%32)/8, d = t%8, g = c/32, a = (c%32)/4, f = c%4;
+ *             w = 2g + f/2, p = 2*(4*(d/4) + 2*((d%4)/2) + f%2) + 16*(d%2)
+ *   (each lane of the attention kernel's warp reads exactly one 32-byte
+ *   record per 32 tokens and turns it into tensor-core operands with one
+ *   shift and one mask per pair of codes).
+ *   Pool: physical block p holds its head-blocks at
+ *     pool + p*kvarn_block_bytes + (2*h + kind)*kvarn_head_block_bytes,
+ *   kind 0 = K, 1 = V. pool must be 16-byte aligned.
+ *   Staging (the incomplete tail block, raw unrotated values):
+ *     bf16 [max_seqs][n_kv][2][B][128]; token t of sequence b is row t % B.
+ *   Block table: int32 [batch][max_blocks_per_seq], logical -> physical.
+ */
+#ifndef KVARN_H_
+#define KVARN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVARN_OK = 0,
+    KVARN_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size or config field */
+    KVARN_ERR_UNSUPPORTED = -2,   /* a valid config this build does not implement */
+    KVARN_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
+    KVARN_ERR_WORKSPACE = -4      /* workspace_bytes below kvarn_workspace_bytes */
+} kvarn_status;
+
+/* device error word flags (sticky, OR-ed) */
+#define KVARN_DEVERR_BLOCK_ID 0x1u      /* physical block id < 0 or >= n_pool_blocks */
+#define KVARN_DEVERR_POSITION 0x2u      /* pos / seq_len outside [0, max_blocks*B] */
+#define KVARN_DEVERR_NONFINITE 0x4u     /* NaN or Inf in a block being quantised */
+#define KVARN_DEVERR_WAIT_TIMEOUT 0x8u  /* a shared-memory copy wait hit its limit */
+
+typedef enum { KVARN_BF16 = 0, KVARN_FP32 = 1 } kvarn_dtype;
+typedef enum { KVARN_KIND_K = 0, KVARN_KIND_V = 1 } kvarn_kind;
+
+typedef struct kvarn_config {
+    int32_t head_dim;       /* must be 128 */
+    int32_t block_size;     /* tokens per block B: 32 or 64 */
+    int32_t group_size;     /* channels per quantisation group: must be 32 */
+    int32_t bits;           /* must be 2 */
+    int32_t varn_iters;     /* VarN iterations (token pass then channel pass): 1..8 */
+    int32_t n_q_heads;      /* query heads */
+    int32_t n_kv_heads;     /* kv heads; n_q_heads / n_kv_heads in 1..4 */
+    float sm_scale;         /* softmax scale; 0 means 1/sqrt(head_dim) */
+    uint32_t sign_bits[4];  /* rotation signs: bit c set => channel c negated */
+} kvarn_config;
+
+/* Library version string, e.g. "kvarn 0.1 sm_103a". */
+const char* kvarn_version(void);
+
+/* Human-readable text for a kvarn_status value. */
+const char* kvarn_status_string(int status);
+
+/* Bytes of one packed head-block: 50*B + 256. 0 for an invalid config. */
+size_t kvarn_head_block_bytes(const kvarn_config* cfg);
+
+/* Bytes of one physical block: n_kv_heads * 2 * kvarn_head_block_bytes. */
+size_t kvarn_block_bytes(const kvarn_config* cfg);
+
+/* Bytes of the bf16 staging buffer for max_seqs sequences:
+ * max_seqs * n_kv * 2 * B * 128 * 2. */
+size_t kvarn_staging_bytes(const kvarn_config* cfg, int32_t max_seqs);
+
+/* Minimum workspace for kvarn_decode_attn / kvarn_decode_attn_bf16 with this
+ * batch on the CURRENT device (the split-K partial results depend on its SM
+ * count): 256 header bytes (the error word is the first uint32) plus one
+ * partial (max, sum, 128 accumulators per query head) per (sequence, kv
+ * head) and per resident warp. batch = 0 gives the 256 bytes that
+ * kvarn_quantize_block and kvarn_append need. 0 on a bad config. */
+size_t kvarn_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks_per_seq);
+
+/*
+ * kvarn_quantize_block -- bulk quantise-on-write of complete head-blocks
+ * (prefill). Passage: abstract (rotation then dual-axis normalisation, 2-bit);
+ * section 三 3.1-3.2 of the method page.
+ *
+ * For each n in [0, n_head_blocks): reads the B x 128 block
+ *   src[n*src_block_stride + t*src_token_stride + c]  (elements, dtype
+ *   src_dtype: KVARN_BF16 or KVARN_FP32; device)
+ * rotates each token by H diag(sigma)/sqrt(128), runs varn_iters passes of
+ * token-axis then channel-axis variance normalisation, rounds the factors to
+ * fp16, quantises each (token, 32-channel group) to 2 bits with an fp16
+ * step and zero, and writes one packed head-block of `kind` layout to
+ *   dst_base + dst_offsets[n]   (bytes; device int64 array, NULL means
+ *                               n * kvarn_head_block_bytes)
+ * dst_base + offset must be 16-byte aligned. workspace: >= 256 bytes of
+ * device memory whose first uint32 is the error word (KVARN_DEVERR_NONFINITE).
+ */
+int kvarn_quantize_block(const kvarn_config* cfg, int32_t kind, const void* src, int32_t src_dtype,
+                         int64_t n_head_blocks, int64_t src_block_stride,
+                         int64_t src_token_stride, void* dst_base, const int64_t* dst_offsets,
+                         void* workspace, void* stream);
+
+/*
+ * kvarn_append -- one decode step's KV write (quantise-on-append). Passage:
+ * section 三 3.2 of the method page (scales computed at decode time from the
+ * data itself, fused into the KV write kernel).
+ *
+ * For each sequence b < batch and kv head h, the new token's K and V
+ * (k_new, v_new: device bf16 [batch][n_kv][128]) are written to staging row
+ * pos[b] % B (pos: device int32 [batch], the index of the new token, i.e.
+ * the length before this step). When that row completes the block
+ * (pos[b] % B == B - 1), the whole block is quantised exactly as
+ * kvarn_quantize_block does and written to physical block
+ * block_table[b][pos[b] / B] of the pool (n_pool_blocks blocks); the staging
+ * rows are left as they are. Nothing is re-quantised later. Device faults:
+ * KVARN_DEVERR_POSITION (pos < 0 or pos >= max_blocks_per_seq * B),
+ * KVARN_DEVERR_BLOCK_ID, KVARN_DEVERR_NONFINITE.
+ */
+int kvarn_append(const kvarn_config* cfg, void* pool, int64_t n_pool_blocks, void* staging,
+                 const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* pos,
+                 const void* k_new, const void* v_new, int32_t batch, void* workspace,
+                 void* stream);
+
+/*
+ * kvarn_decode_attn -- decode attention over the packed cache. Passage:
+ * section 三 3.1 of the method page (the query is multiplied by the same
+ * Hadamard matrix, so q.k is unchanged).
+ *
+ * q: device [batch][n_q][128], dtype q_dtype (KVARN_BF16 or KVARN_FP32).
+ * seq_lens: device int32 [batch], tokens per sequence including the newest.
+ * For query head j of sequence b (kv head h = j / (n_q / n_kv)):
+ *   out[b][j][:] = sum_t softmax_t(sm_scale * q.k_t) v_t
+ * over the first floor(L/B)*B tokens from the pool (dequantised on the fly)
+ * and the remaining L % B tokens from staging (raw bf16). out: device fp32
+ * [batch][n_q][128]. L = 0 gives zeros. workspace: device, at least
+ * kvarn_workspace_bytes(cfg, batch, max_blocks_per_seq) bytes, 16-byte
+ * aligned, passed as workspace_bytes. The work is split evenly over the
+ * GPU's resident warps (split-K over each sequence's blocks) and merged by a
+ * second kernel on the same stream. Device faults: KVARN_DEVERR_BLOCK_ID,
+ * KVARN_DEVERR_POSITION, KVARN_DEVERR_WAIT_TIMEOUT.
+ */
+int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,
+                      int64_t n_pool_blocks, const void* staging, const int32_t* block_table,
+                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch,
+                      float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kvarn_dequantize -- packed head-blocks back to fp32 values. Passage:
+ * section 三 3.2 of the method page (the kept scales restore the data).
+ * Reads n_head_blocks head-blocks of `kind` layout at src_base +
+ * src_offsets[n] (device int64 bytes; NULL = contiguous) and writes out
+ * (device fp32 [n][B][128]): rotated != 0 gives the rotated-space values
+ * (code*s + z)*R*C; rotated == 0 also applies the inverse rotation.
+ */
+int kvarn_dequantize(const kvarn_config* cfg, int32_t kind, const void* src_base,
+                     const int64_t* src_offsets, int64_t n_head_blocks, int32_t rotated,
+                     float* out, void* stream);
+
+/*
+ * kvarn_decode_attn_bf16 -- the same decode attention over a plain bf16
+ * paged cache (the comparison point for the 2-bit path; no rotation, no
+ * staging). kv_pool: device bf16 [n_pool_blocks][n_kv][2][B][128]; every
+ * token of a sequence, the last block partly filled, is in the pool.
+ * Other arguments as kvarn_decode_attn.
+ */
+int kvarn_decode_attn_bf16(const kvarn_config* cfg, const void* q, int32_t q_dtype,
+                           const void* kv_pool, int64_t n_pool_blocks,
+                           const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t batch, float* out, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Copies the workspace error word to *code (host) after synchronising
+ * stream. Returns KVARN_OK or KVARN_ERR_CUDA. */
+int kvarn_read_error(const void* workspace, uint32_t* code, void* stream);
+
+/* Zeroes the workspace error word (enqueued on stream). */
+int kvarn_clear_error(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H_ */

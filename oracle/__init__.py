@@ -71,6 +71,7 @@ def lib():
                 "orc_round_factor": (_d, [_d]),
                 "orc_group_params": (None, [_f64p, _i, _f64p, _f64p, _f64p, _f64p]),
                 "orc_code": (_i, [_d, _d, _d]),
+                "orc_step_for": (_d, [_d, _d]),
                 "orc_code_position": (None, [_i, _i, _i, _i32p, _i32p]),
                 "orc_head_block_bytes": (ctypes.c_size_t, [_i]),
                 "orc_pack": (None, [_i, _i, _i32p, _f64p, _f64p, _f64p, _f64p, _u8p]),
@@ -218,6 +219,11 @@ def group_params(y):
     lib().orc_group_params(_p(y, _f64p), y.size, ctypes.byref(z), ctypes.byref(s),
                            ctypes.byref(m), ctypes.byref(M))
     return z.value, s.value, m.value, M.value
+
+
+def step_for(z16: float, M: float) -> float:
+    """Least fp16 s >= 0 with z16 + 3 s >= M."""
+    return lib().orc_step_for(float(z16), float(M))
 
 
 def code(y: float, z16: float, s16: float) -> int:

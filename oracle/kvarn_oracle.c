@@ -316,6 +316,22 @@ double orc_round_factor(double f)
 /*   code = clamp(round-half-even((y - z) / s), 0, 3); all 0 when s = 0      */
 /* ------------------------------------------------------------------------ */
 
+/* least fp16 s >= 0 with z16 + 3 s >= M (clamped to 65504); 0 when z16 >= M */
+double orc_step_for(double z16, double M)
+{
+    if (z16 >= M) return 0.0;
+    double s = orc_f16_ru((M - z16) / 3.0);
+    if (s > 65504.0) s = 65504.0;
+    /* the division above rounds in fp64: settle the exact minimum by
+     * comparing z + 3 s against M (exact in fp64 for fp16 operands) */
+    while (s > 0.0 && s < 65504.0 && z16 + 3.0 * s < M) s = f16_next_pos(s);
+    while (s > 0.0) {
+        double p = f16_prev_pos(s);
+        if (z16 + 3.0 * p >= M) s = p; else break;
+    }
+    return s;
+}
+
 void orc_group_params(const double* y, int n, double* z16, double* s16,
                       double* m_out, double* M_out)
 {
@@ -326,22 +342,8 @@ void orc_group_params(const double* y, int n, double* z16, double* s16,
     }
     double mc = m < -65504.0 ? -65504.0 : (m > 65504.0 ? 65504.0 : m);
     double z = orc_f16_rd(mc);
-    double s;
-    if (z >= M) {
-        s = 0.0;
-    } else {
-        s = orc_f16_ru((M - z) / 3.0);
-        if (s > 65504.0) s = 65504.0;
-        /* the division above rounds in fp64: settle the exact minimum by
-         * comparing z + 3 s against M (exact in fp64 for fp16 operands) */
-        while (s > 0.0 && s < 65504.0 && z + 3.0 * s < M) s = f16_next_pos(s);
-        while (s > 0.0) {
-            double p = f16_prev_pos(s);
-            if (z + 3.0 * p >= M) s = p; else break;
-        }
-    }
     *z16 = z;
-    *s16 = s;
+    *s16 = orc_step_for(z, M);
     if (m_out) *m_out = m;
     if (M_out) *M_out = M;
 }

@@ -1,0 +1,172 @@
+"""Shared helpers for the KVarN tests: the staged quantiser parity check and
+paged-cache construction on the GPU through the C ABI.
+
+Parity rules (staged hand-off; each stage is recomputed from the GPU's
+already-validated rounded values so one boundary case cannot cascade):
+  factors  R16, C16 equal the oracle's fp16 rounding of its fp64 factors, or
+           the oracle value lies within 1e-5 relative of the rounding midpoint
+           between the two (counted);
+  z16/s16  recomputed by the oracle from its fp64 rotated values and the GPU's
+           R16, C16: equal, or the pre-rounding value (group minimum for z,
+           (M - z)/3 for s) lies within 1e-5 relative of an fp16 value (counted);
+  codes    recomputed from that y with the GPU's z16, s16: equal, or y lies
+           within 1e-6 * max(1, |b|) of a decision boundary b (counted, and the
+           count must stay <= 1e-6 of all codes).
+"""
+from __future__ import annotations
+
+import math
+from collections import Counter
+
+import numpy as np
+import torch
+
+import oracle
+
+D = 128
+
+
+def f16_near_grid(v: np.ndarray, rel: float) -> np.ndarray:
+    """|v - nearest fp16 value| <= rel * |v| (numpy's float16 rounding)."""
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        n = v.astype(np.float16).astype(np.float64)
+        return np.abs(v - n) <= rel * np.maximum(np.abs(v), 2.0 ** -24)
+
+
+def f16_neighbours(v: float):
+    lo, hi = oracle.f16_rd(v), oracle.f16_ru(v)
+    return lo, hi
+
+
+def staged_quantize_parity(X: np.ndarray, gpu_bytes: np.ndarray, B: int, iters: int, kind: int,
+                           sign_bits) -> Counter:
+    """X: [n][B][128] float64 inputs exactly as the GPU read them; gpu_bytes:
+    [n][head_block_bytes] uint8. Raises AssertionError on a violation."""
+    st = Counter()
+    X = np.asarray(X, dtype=np.float64)
+    n = X.shape[0]
+    for i in range(n):
+        ref = oracle.quantize_block(X[i], iters, kind, sign_bits)
+        f = oracle.unpack(B, kind, gpu_bytes[i])
+        # ---- factors
+        raw = np.concatenate([ref["R"], ref["C"]])
+        got = np.concatenate([f["R16"], f["C16"]])
+        want = np.concatenate([ref["R16"], ref["C16"]])
+        bad = np.nonzero(got != want)[0]
+        for k in bad:
+            v = min(max(raw[k], 2.0 ** -14), 65504.0)
+            lo, hi = f16_neighbours(v)
+            mid = 0.5 * (lo + hi)
+            ok = got[k] in (lo, hi) and want[k] in (lo, hi) and abs(v - mid) <= 1e-5 * v
+            assert ok, f"block {i} factor {k}: gpu {got[k]!r} oracle {want[k]!r} (value {raw[k]!r})"
+            st["factor_excused"] += 1
+        st["factors"] += raw.size
+        # ---- group zero and step from the GPU's factors
+        y = oracle.normalise(ref["Xr"], f["R16"], f["C16"])
+        z_o, _, m, M = oracle.group_params_all(y)
+        zb = np.nonzero(f["z16"] != z_o)
+        if zb[0].size:
+            mc = np.clip(m[zb], -65504, 65504)
+            assert np.all(f16_near_grid(mc, 1e-5)), f"block {i}: z16 mismatch off the fp16 grid"
+            st["zero_excused"] += zb[0].size
+        s_o = np.array([[oracle.step_for(f["z16"][t, g], M[t, g]) for g in range(4)] for t in range(B)])
+        sb_ = np.nonzero(f["s16"] != s_o)
+        if sb_[0].size:
+            pre = (M[sb_] - f["z16"][sb_]) / 3.0
+            assert np.all(f16_near_grid(pre, 1e-5)), (
+                f"block {i}: s16 mismatch gpu {f['s16'][sb_]} oracle {s_o[sb_]} pre {pre}")
+            st["step_excused"] += sb_[0].size
+        st["groups"] += B * 4
+        # ---- codes from y with the GPU's z16, s16
+        codes, dist = oracle.codes_given(y, f["z16"], f["s16"])
+        cb = np.nonzero(codes != f["codes"])
+        if cb[0].size:
+            window = 1e-6 * np.maximum(1.0, np.abs(y[cb]))
+            assert np.all(dist[cb] <= window), (
+                f"block {i}: {cb[0].size} code mismatches, distances {dist[cb][:8]}")
+            st["code_excused"] += cb[0].size
+        st["codes_in_window"] += int(np.sum(dist <= 1e-6 * np.maximum(1.0, np.abs(y))))
+        st["codes"] += B * D
+    assert st["code_excused"] <= 1e-6 * st["codes"] or st["code_excused"] == 0, dict(st)
+    return st
+
+
+def attn_close(got: np.ndarray, ref: np.ndarray, tol: float = 2e-3):
+    """|got - ref| <= tol * max(1, |ref|) elementwise; returns the worst ratio."""
+    err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+    worst = float(np.nanmax(err)) if err.size else 0.0
+    assert np.all(np.isfinite(got)), "non-finite attention output"
+    assert worst <= tol, f"attention error {worst:.3e} > {tol}"
+    return worst
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class PagedCache:
+    """A 2-bit paged cache built through the C ABI.
+
+    block_table[b][j] is a physical block id (a seeded permutation when
+    perm_seed is given); staging holds the raw tail rows.
+    """
+
+    def __init__(self, kv, cfg, batch: int, max_blocks: int, perm_seed=None, device="cuda",
+                 extra_blocks: int = 0):
+        self.kv, self.cfg = kv, cfg
+        self.B = cfg.block_size
+        self.batch, self.max_blocks = batch, max_blocks
+        n_pool = batch * max_blocks + extra_blocks
+        ids = np.arange(batch * max_blocks, dtype=np.int32)
+        if perm_seed is not None:
+            ids = np.random.default_rng(perm_seed).permutation(batch * max_blocks).astype(np.int32)
+        self.block_table_np = ids.reshape(batch, max_blocks)
+        self.block_table = torch.from_numpy(self.block_table_np).to(device)
+        self.pool = kv.alloc_pool(cfg, n_pool, device)
+        self.staging = kv.alloc_staging(cfg, batch, device)
+        self.ws = kv.alloc_workspace(cfg, 0, 0, device)
+        self.hb = kv.head_block_bytes(cfg)
+        self.bb = kv.block_bytes(cfg)
+
+    def head_block_offset(self, b, h, j, kind):
+        return int(self.block_table_np[b, j]) * self.bb + (2 * h + kind) * self.hb
+
+    def prefill(self, K: torch.Tensor, V: torch.Tensor, lens):
+        """K, V: bf16 or fp32 [batch][n_kv][Lmax][128] on the GPU."""
+        B = self.B
+        n_kv = self.cfg.n_kv_heads
+        for b, L in enumerate(lens):
+            nb = L // B
+            for h in range(n_kv):
+                for kind, T in ((0, K), (1, V)):
+                    if nb > 0:
+                        offs = torch.tensor([self.head_block_offset(b, h, j, kind) for j in range(nb)],
+                                            dtype=torch.int64, device=T.device)
+                        src = T[b, h, :nb * B].contiguous()
+                        self.kv.quantize_block(self.cfg, kind, src, self.pool, self.ws, dst_offsets=offs,
+                                               n_head_blocks=nb)
+                    tail = L - nb * B
+                    if tail > 0:
+                        self.staging[b, h, kind, :tail] = T[b, h, nb * B:L].to(torch.bfloat16)
+        torch.cuda.synchronize()
+
+    def head_block(self, b, h, j, kind) -> np.ndarray:
+        o = self.head_block_offset(b, h, j, kind)
+        return self.pool.view(-1)[o:o + self.hb].cpu().numpy()
+
+
+def oracle_attention(cache: PagedCache, q: torch.Tensor, seq_lens, sign_bits, sm_scale=None, seqs=None,
+                     pool_np=None):
+    """Oracle attention over the GPU's own cache bytes; seqs selects a sample
+    of sequences (the result then has one row per selected sequence)."""
+    cfg = cache.cfg
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    seqs = list(range(q.shape[0])) if seqs is None else list(seqs)
+    qn = q[seqs].double().cpu().numpy()
+    stg = bf16_bits(cache.staging[seqs])
+    pool_np = cache.pool.cpu().numpy() if pool_np is None else pool_np
+    return oracle.decode_attention(cfg.block_size, cfg.n_q_heads, cfg.n_kv_heads, sign_bits, sm_scale, qn,
+                                   pool_np, stg, np.ascontiguousarray(cache.block_table_np[seqs]),
+                                   np.asarray(seq_lens, dtype=np.int32)[seqs])

@@ -1,0 +1,66 @@
+"""The C ABI library builds, loads and exports every symbol include/kvarn.h
+declares; size queries and host-side argument validation work without a GPU
+(no compute is launched here)."""
+import ctypes
+
+import pytest
+
+import bit_kv_cache_08_gb300 as kv
+import synth
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    kv.build()
+
+
+def _cfg(**kw):
+    base = dict(n_q_heads=32, n_kv_heads=8, block_size=32, varn_iters=3, sign_bits=synth.sign_bits(1))
+    base.update(kw)
+    return kv.make_config(**base)
+
+
+def test_library_exports_every_declared_symbol():
+    names = kv.header_symbols()
+    assert len(names) >= 13
+    L = kv.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert kv.version().startswith("kvarn")
+
+
+def test_sizes_match_the_format():
+    c32, c64 = _cfg(), _cfg(block_size=64)
+    assert kv.head_block_bytes(c32) == 1856 and kv.head_block_bytes(c64) == 3456
+    assert kv.block_bytes(c32) == 8 * 2 * 1856
+    assert kv.staging_bytes(c32, 16) == 16 * 8 * 2 * 32 * 128 * 2
+    assert kv.workspace_bytes(c32, 0, 0) == 256
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 16), ("bits", 4),
+                                         ("group_size", 64), ("n_q_heads", 48)])
+def test_unsupported_configs_are_rejected(field, value):
+    c = _cfg()
+    setattr(c, field, value)
+    assert kv.head_block_bytes(c) == 0
+    r = kv.lib().kvarn_quantize_block(ctypes.byref(c), 0, None, 0, 1, 4096, 128, None, None, None, None)
+    assert r == kv._abi.ERR_UNSUPPORTED
+
+
+def test_invalid_arguments_are_rejected_before_any_launch():
+    L = kv.lib()
+    c = _cfg()
+    INV = -1
+    assert L.kvarn_quantize_block(None, 0, None, 0, 1, 4096, 128, None, None, None, None) == INV
+    assert L.kvarn_quantize_block(ctypes.byref(c), 2, None, 0, 1, 4096, 128, None, None, None, None) == INV
+    assert L.kvarn_quantize_block(ctypes.byref(c), 0, None, 0, 1, 4096, 128, None, None, None, None) == INV
+    # zero blocks is a no-op
+    assert L.kvarn_quantize_block(ctypes.byref(c), 0, None, 0, 0, 4096, 128, None, None, None, None) == 0
+    # misaligned pointers
+    p = ctypes.c_void_p(0x1000 + 2)
+    assert L.kvarn_append(ctypes.byref(c), p, 10, p, p, 4, p, p, p, 1, p, None) == INV
+    assert L.kvarn_decode_attn(ctypes.byref(c), None, 0, None, 1, None, None, 4, None, 1, None, None, 0,
+                               None) == INV
+    bad = _cfg(varn_iters=0)
+    assert L.kvarn_dequantize(ctypes.byref(bad), 0, None, None, 1, 0, None, None) == INV
+    assert kv.status_string(-4) == "workspace too small"

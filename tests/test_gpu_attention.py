@@ -1,0 +1,159 @@
+"""GPU decode attention over the 2-bit paged cache (and the bf16 comparison
+kernel) against the fp64 oracle over the same cache bytes."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from kvtest_util import PagedCache, attn_close, bf16_bits, oracle_attention
+
+pytestmark = pytest.mark.gpu
+D = 128
+
+
+def _run_attn(kv, cache, q, seq_lens):
+    cfg = cache.cfg
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    out = torch.full((q.shape[0], cfg.n_q_heads, D), float("nan"), device="cuda")
+    ws = kv.alloc_workspace(cfg, q.shape[0], cache.max_blocks)
+    kv.decode_attn(cfg, q, cache.pool, cache.staging, cache.block_table, sl, out, ws)
+    torch.cuda.synchronize()
+    return out.cpu().double().numpy(), kv.read_error(ws)
+
+
+def test_tiny_single_head(kvlib):
+    """One kv head, 256 fp32 tokens (8 blocks of 32), 3 iterations, fp32 query."""
+    kv = kvlib
+    w = synth.TINY
+    sb = synth.sign_bits(w.seed)
+    cfg = kv.make_config(w.n_q, w.n_kv, w.block, w.iters, sb)
+    g = synth.make_gen(w.seed)
+    K = synth.kv_values(g, 1, 1, w.ctx, w.sigma_m, w.n_out, w.out_factor).cuda()
+    V = synth.kv_values(g, 1, 1, w.ctx, w.sigma_m, w.n_out, w.out_factor).cuda()
+    q = synth.queries(g, 1, 1).cuda()
+    cache = PagedCache(kv, cfg, 1, w.ctx // w.block)
+    cache.prefill(K, V, [w.ctx])
+    got, err = _run_attn(kv, cache, q, [w.ctx])
+    assert err == 0
+    ref = oracle_attention(cache, q, [w.ctx], sb)
+    attn_close(got, ref)
+
+
+@pytest.mark.parametrize("B,iters", [(32, 3), (64, 2)])
+@pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float32])
+def test_ragged_paged_with_tails(kvlib, B, iters, qdtype):
+    kv = kvlib
+    n_q, n_kv = 8, 2
+    lens = [0, 1, B - 1, B, B + 1, 3 * B + 7, 700]
+    batch = len(lens)
+    max_blocks = (max(lens) + B - 1) // B + 1
+    sb = synth.sign_bits(100 + B)
+    cfg = kv.make_config(n_q, n_kv, B, iters, sb)
+    g = synth.make_gen(B)
+    K = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    V = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    q = synth.queries(g, batch, n_q).to(qdtype).cuda()
+    cache = PagedCache(kv, cfg, batch, max_blocks, perm_seed=B)
+    cache.prefill(K, V, lens)
+    got, err = _run_attn(kv, cache, q, lens)
+    assert err == 0
+    ref = oracle_attention(cache, q, lens, sb)
+    assert np.all(got[0] == 0.0)            # empty sequence -> zeros
+    attn_close(got, ref)
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4])
+def test_group_sizes(kvlib, G):
+    kv = kvlib
+    B, n_kv = 32, 2
+    n_q = G * n_kv
+    lens = [5 * B + 3, 2 * B]
+    sb = synth.sign_bits(G)
+    cfg = kv.make_config(n_q, n_kv, B, 3, sb)
+    g = synth.make_gen(40 + G)
+    K = synth.kv_values(g, 2, n_kv, max(lens), 1.0, 2, 10.0).to(torch.bfloat16).cuda()
+    V = synth.kv_values(g, 2, n_kv, max(lens), 1.0, 2, 10.0).to(torch.bfloat16).cuda()
+    q = synth.queries(g, 2, n_q).cuda()
+    cache = PagedCache(kv, cfg, 2, 8, perm_seed=G)
+    cache.prefill(K, V, lens)
+    got, err = _run_attn(kv, cache, q, lens)
+    assert err == 0
+    attn_close(got, oracle_attention(cache, q, lens, sb))
+
+
+def test_closed_form_uniform_keys(kvlib):
+    """All keys equal (constant block) -> uniform weights -> mean of the values."""
+    kv = kvlib
+    B, n_kv, n_q = 32, 1, 4
+    sb = synth.sign_bits(8)
+    cfg = kv.make_config(n_q, n_kv, B, 3, sb)
+    L = 4 * B
+    K = torch.ones(1, 1, L, D).cuda() * 0.5
+    g = synth.make_gen(8)
+    V = synth.kv_values(g, 1, 1, L, 1.0, 2, 10.0).to(torch.bfloat16).cuda()
+    q = synth.queries(g, 1, n_q).cuda()
+    cache = PagedCache(kv, cfg, 1, 4)
+    cache.prefill(K, V, [L])
+    got, _ = _run_attn(kv, cache, q, [L])
+    vhat = np.concatenate([oracle.decode_blocks(cache.head_block(0, 0, j, 1), B, 1, sb, False)[0]
+                           for j in range(4)])
+    for j in range(n_q):
+        attn_close(got[0, j], vhat.mean(axis=0))
+
+
+def test_bad_block_id_and_length_are_flagged(kvlib):
+    kv = kvlib
+    B = 32
+    sb = synth.sign_bits(2)
+    cfg = kv.make_config(4, 1, B, 3, sb)
+    g = synth.make_gen(2)
+    K = synth.kv_values(g, 2, 1, 3 * B, 1.0, 2, 10.0).to(torch.bfloat16).cuda()
+    cache = PagedCache(kv, cfg, 2, 3)
+    cache.prefill(K, K, [3 * B, 3 * B])
+    q = synth.queries(g, 2, 4).cuda()
+    cache.block_table[0, 1] = 10_000          # outside the pool
+    _, err = _run_attn(kv, cache, q, [3 * B, 3 * B])
+    assert err & kv.DEVERR_BLOCK_ID
+    cache.block_table[0, 1] = 1
+    got, err = _run_attn(kv, cache, q, [3 * B, 10 * B])   # beyond the table
+    assert err & kv.DEVERR_POSITION
+    assert np.all(np.isnan(got[1]))
+
+
+def test_bf16_cache_kernel(kvlib):
+    """The comparison kernel: same attention over a plain bf16 paged cache."""
+    kv = kvlib
+    for B in (32, 64):
+        n_q, n_kv = 8, 2
+        lens = [1, 17, B, 5 * B + 9, 300]
+        batch = len(lens)
+        max_blocks = (max(lens) + B - 1) // B
+        cfg = kv.make_config(n_q, n_kv, B, 3, synth.sign_bits(0))
+        g = synth.make_gen(60 + B)
+        K = synth.kv_values(g, batch, n_kv, max_blocks * B, 1.5, 4, 20.0).to(torch.bfloat16)
+        V = synth.kv_values(g, batch, n_kv, max_blocks * B, 1.5, 4, 20.0).to(torch.bfloat16)
+        q = synth.queries(g, batch, n_q).cuda()
+        perm = np.random.default_rng(B).permutation(batch * max_blocks).astype(np.int32)
+        bt = perm.reshape(batch, max_blocks)
+        pool = torch.zeros(batch * max_blocks, n_kv, 2, B, D, dtype=torch.bfloat16)
+        for b in range(batch):
+            for j in range(max_blocks):
+                pool[bt[b, j], :, 0] = K[b, :, j * B:(j + 1) * B]
+                pool[bt[b, j], :, 1] = V[b, :, j * B:(j + 1) * B]
+        out = torch.empty(batch, n_q, D, device="cuda")
+        ws = kv.alloc_workspace(cfg, batch, max_blocks)
+        kv.decode_attn_bf16(cfg, q, pool.cuda(), torch.from_numpy(bt).cuda(),
+                            torch.tensor(lens, dtype=torch.int32, device="cuda"), out, ws)
+        torch.cuda.synchronize()
+        assert kv.read_error(ws) == 0
+        got = out.cpu().double().numpy()
+        Kd, Vd, qd = K.double().numpy(), V.double().numpy(), q.double().cpu().numpy()
+        G = n_q // n_kv
+        for b in range(batch):
+            for j in range(n_q):
+                ref = oracle.attention(qd[b, j], Kd[b, j // G, :lens[b]], Vd[b, j // G, :lens[b]],
+                                       1 / math.sqrt(D))
+                attn_close(got[b, j], ref)

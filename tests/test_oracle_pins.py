@@ -214,6 +214,18 @@ def test_group_params_are_the_brute_force_extremes():
         assert s == ok.min()                              # smallest fp16 covering the max
 
 
+def test_step_rule_is_the_brute_force_minimum():
+    grid = _all_f16_nonneg()
+    rng = np.random.default_rng(15)
+    for _ in range(200):
+        z = float(np.float16(rng.uniform(-50, 50)))
+        M = z + abs(rng.standard_normal()) * np.exp(rng.uniform(-12, 8))
+        s = oracle.step_for(z, M)
+        ok = grid[z + 3.0 * grid >= M]
+        assert s == (ok.min() if ok.size else 65504.0)
+    assert oracle.step_for(1.0, 1.0) == 0.0 and oracle.step_for(2.0, 1.0) == 0.0
+
+
 def test_codes_are_nearest_levels_with_ties_to_even_and_error_at_most_half_step():
     sb = synth.sign_bits(2)
     for seed in range(3):
