@@ -1,0 +1,475 @@
+"""Benchmark of the KVarN 2-bit KV-cache hot path on GB300.
+
+One step = one decode step of the Qwen3-4B-shaped full cache: for each of the
+36 layers, the append of every sequence's new token (which completes the
+open 64-token block and quantises it into the paged pool) followed by decode
+attention over the 2-bit cache (8192 tokens x 64 sequences x 8 kv heads,
+physical blocks randomly permuted per layer). The per-step cache (16.3 GB)
+is far larger than L2, so no flush is needed between steps.
+
+Prints one JSON line (see the keys below). --impl reference times the fp64
+CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "2-bit KV decode-attn GB/s (% of HBM peak) + quantize-append tokens/s"
+CPU_SAMPLE_SEQS = 4
+FALLBACK_HBM_GBS = 6800.0
+D = 128
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
+    p.add_argument("--layers", type=int, default=None, help="(testing only) fewer layers")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-bf16", action="store_true")
+    return p.parse_args()
+
+
+def workload():
+    import synth
+    return synth.QWEN3_4B_CACHE
+
+
+def algorithmic_bytes(w, layers):
+    """Bytes the step must move at minimum (what the design doc calls algorithmic)."""
+    B, n_kv, n_q, batch, L = w.block, w.n_kv, w.n_q, w.batch, w.ctx
+    per_token_head = 2 * (32 + 16 + 2) + 2 * 256 / B          # K+V: codes, s/z, R + C share
+    attn_cache = batch * L * n_kv * per_token_head
+    attn_other = batch * n_q * (D * 2 + D * 4) + batch * (L // B) * 4   # q bf16, out fp32, table
+    attn = attn_cache + attn_other
+    # append: new rows in (bf16), the open block's staged rows read, packed block written
+    hb = 50 * B + 256
+    app = batch * n_kv * 2 * (D * 2 + (B - 1) * D * 2 + hb)
+    return attn * layers, app * layers, attn, app
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record():
+    """ncu DRAM bytes per attention launch, valid only for the kernel source it
+    was captured from (profiles/attention_traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for f in ("attention.cu", "attn_common.cuh", "split.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "bit_kv_cache_08_gb300", "csrc", f), "rb").read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    def __init__(self, device_index):
+        self.proc = None
+        self.idx = device_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def build_layers(kv, w, layers, device):
+    """Prefill every layer's 2-bit cache to ctx-1 tokens (ctx-1 = 8191: 127
+    full blocks in the pool, 63 rows in staging); per-layer permuted tables."""
+    import numpy as np
+    import torch
+    import synth
+    B, n_kv, batch, L = w.block, w.n_kv, w.batch, w.ctx
+    nb = L // B
+    state = []
+    for layer in range(layers):
+        sb = synth.sign_bits(1000 + layer)
+        cfg = kv.make_config(w.n_q, n_kv, B, w.iters, sb)
+        g = synth.make_gen(w.seed * 1000 + layer, device)
+        pool = kv.alloc_pool(cfg, batch * nb, device)
+        staging = kv.alloc_staging(cfg, batch, device)
+        ws0 = kv.alloc_workspace(cfg, 0, 0, device)
+        perm = np.random.default_rng([w.seed, layer]).permutation(batch * nb).astype(np.int32)
+        bt = torch.from_numpy(perm.reshape(batch, nb)).to(device)
+        hb, bb = kv.head_block_bytes(cfg), kv.block_bytes(cfg)
+        jj = torch.arange(nb - 1, device=device)
+        for kind in (0, 1):
+            T = synth.kv_values(g, batch, n_kv, L, w.sigma_m, w.n_out, w.out_factor, device).to(torch.bfloat16)
+            # every full block of every (sequence, head) in one call: offsets from the table
+            src = T[:, :, :(nb - 1) * B].contiguous()                   # [batch][n_kv][(nb-1)B][128]
+            offs = (bt[:, None, :nb - 1].long() * bb + (2 * torch.arange(n_kv, device=device)[None, :, None] + kind)
+                    * hb).reshape(-1).contiguous()
+            kv.quantize_block(cfg, kind, src, pool, ws0, dst_offsets=offs, n_head_blocks=offs.numel())
+            staging[:, :, kind, :B - 1] = T[:, :, (nb - 1) * B:L - 1]
+            if kind == 0:
+                k_last = T[:, :, L - 1].contiguous()
+            else:
+                v_last = T[:, :, L - 1].contiguous()
+            del T, src
+        torch.cuda.synchronize()
+        assert kv.read_error(ws0) == 0
+        q = synth.queries(g, batch, w.n_q, device).to(torch.bfloat16)
+        state.append(dict(cfg=cfg, pool=pool, staging=staging, bt=bt, q=q, k_new=k_last, v_new=v_last))
+        del jj
+    return state
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import bit_kv_cache_08_gb300 as kv
+    kv.build()
+    device = f"cuda:{rank % max(1, torch.cuda.device_count())}"
+    torch.cuda.set_device(device)
+    w = workload()
+    layers = args.layers or w.layers
+    state = build_layers(kv, w, layers, device)
+    B, batch = w.block, w.batch
+    nb = w.ctx // B
+    cfg0 = state[0]["cfg"]
+    ws = kv.alloc_workspace(cfg0, batch, nb, device)
+    pos = torch.full((batch,), w.ctx - 1, dtype=torch.int32, device=device)
+    lens = torch.full((batch,), w.ctx, dtype=torch.int32, device=device)
+    out = torch.empty(layers, batch, w.n_q, D, device=device)
+
+    def step(events=None):
+        for l, st in enumerate(state):
+            if events is not None:
+                events[l][0].record()
+            kv.append(st["cfg"], st["pool"], st["staging"], st["bt"], pos, st["k_new"], st["v_new"], ws)
+            if events is not None:
+                events[l][1].record()
+            kv.decode_attn(st["cfg"], st["q"], st["pool"], st["staging"], st["bt"], lens, out[l], ws)
+            if events is not None:
+                events[l][2].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert kv.read_error(ws) == 0, "device error during warm-up"
+
+    attn_ms, app_ms = [], []
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(layers)]
+               for _ in range(args.steps)]
+        t0.record()
+        for s in range(args.steps):
+            step(evs[s])
+        t1.record()
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    for s in range(args.steps):
+        for l in range(layers):
+            e = evs[s][l]
+            app_ms.append(e[0].elapsed_time(e[1]))
+            attn_ms.append(e[1].elapsed_time(e[2]))
+    if dist:
+        import torch.distributed as tdist
+        t = torch.tensor([total_ms], device=device)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        tdist.barrier()
+    assert kv.read_error(ws) == 0, "device error during the timed steps"
+    clocks = clk.summary()
+
+    attn_bytes, app_bytes, attn_launch_bytes, app_launch_bytes = algorithmic_bytes(w, layers)
+    ms_per_step = total_ms / args.steps
+    value = world * (attn_bytes + app_bytes) / (ms_per_step * 1e-3) / 1e9
+    attn_launch_ms = sum(attn_ms) / len(attn_ms)
+    achieved = attn_launch_bytes / (attn_launch_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    app_launch_ms = sum(app_ms) / len(app_ms)
+    appended_tokens = batch * layers            # per step: one token per sequence per layer
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded lognormal token scales, outlier channels; no weights or datasets)",
+        "config": {"workload": w.name, "layers": layers, "batch": batch, "seq_len": w.ctx,
+                   "n_q_heads": w.n_q, "n_kv_heads": w.n_kv, "head_dim": D, "block": B, "varn_iters": w.iters,
+                   "step": "per layer: kvarn_append (completes every open block) + kvarn_decode_attn",
+                   "l2": "no flush: per-step cache 16.3 GB >> 129 MB L2",
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "decode_attn": {"GB_per_s": round(achieved, 1), "us_per_layer": round(attn_launch_ms * 1e3, 2),
+                        "algorithmic_bytes_per_layer": int(attn_launch_bytes),
+                        "frac_of_hbm_peak": round(achieved / peak, 4),
+                        "tokens_per_s": round(world * batch * layers / (ms_per_step * 1e-3), 1)},
+        "append": {"tokens_per_s": round(world * appended_tokens * w.n_kv * 2 / (sum(app_ms) * 1e-3 / args.steps), 1),
+                   "seq_tokens_per_s": round(world * appended_tokens / (sum(app_ms) * 1e-3 / args.steps), 1),
+                   "us_per_layer": round(app_launch_ms * 1e3, 2),
+                   "note": "tokens_per_s counts (sequence, layer, kv head, K|V) rows quantised"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic_record(),
+                     "kernel": "kvarn_decode_attn (split-K kernel + merge), one layer",
+                     "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "gpu_launches": args.steps * layers * 3,
+        "clocks": clocks,
+    }
+    return res, state, (kv, ws, pos, lens, out)
+
+
+def e2e_gpu(args, ctx_objs, state, w, rank):
+    """The same step through the C ABI with host buffers: every step copies the
+    step's queries and new K/V rows from pinned host memory and reads the
+    outputs back."""
+    import torch
+    kv, ws, pos, lens, out = ctx_objs
+    layers = len(state)
+    hq = torch.stack([st["q"] for st in state]).cpu().pin_memory()
+    hk = torch.stack([st["k_new"] for st in state]).cpu().pin_memory()
+    hv = torch.stack([st["v_new"] for st in state]).cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = hq.to(out.device), hk.to(out.device), hv.to(out.device)
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        for l, st in enumerate(state):
+            kv.append(st["cfg"], st["pool"], st["staging"], st["bt"], pos, dk[l], dv[l], ws)
+            kv.decode_attn(st["cfg"], dq[l], st["pool"], st["staging"], st["bt"], lens, out[l], ws)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    attn_bytes, app_bytes, _, _ = algorithmic_bytes(w, layers)
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = hout.numel() * 4
+    return {"value": round((attn_bytes + app_bytes) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def bf16_comparison(kv, w, device):
+    """The repo's bf16-cache decode attention on one layer of the same shape."""
+    import numpy as np
+    import torch
+    import synth
+    B, n_kv, batch, L = w.block, w.n_kv, w.batch, w.ctx
+    nb = L // B
+    cfg = kv.make_config(w.n_q, n_kv, B, w.iters, synth.sign_bits(0))
+    g = synth.make_gen(7, device)
+    pool = torch.empty(batch * nb, n_kv, 2, B, D, dtype=torch.bfloat16, device=device)
+    pool.normal_(generator=g)
+    perm = np.random.default_rng(7).permutation(batch * nb).astype(np.int32)
+    bt = torch.from_numpy(perm.reshape(batch, nb)).to(device)
+    q = synth.queries(g, batch, w.n_q, device).to(torch.bfloat16)
+    lens = torch.full((batch,), L, dtype=torch.int32, device=device)
+    out = torch.empty(batch, w.n_q, D, device=device)
+    ws = kv.alloc_workspace(cfg, batch, nb, device)
+    for _ in range(3):
+        kv.decode_attn_bf16(cfg, q, pool, bt, lens, out, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    e0.record()
+    for _ in range(reps):
+        kv.decode_attn_bf16(cfg, q, pool, bt, lens, out, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = batch * L * n_kv * 2 * D * 2 + batch * w.n_q * D * 6
+    del pool
+    return {"GB_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1), "us_per_layer": round(ms * 1e3, 2),
+            "tokens_per_s_per_layer": round(batch / (ms * 1e-3), 1),
+            "bytes_per_layer": int(nbytes), "note": "same shape, bf16 pages, fp32 arithmetic"}
+
+
+# ---------------------------------------------------------------------------- oracle (CPU)
+
+def cpu_sample(w, seqs, seed=0):
+    """A bounded sample of the workload for the fp64 oracle: `seqs` sequences
+    of one layer (all kv heads): quantise the completed block, then decode
+    attention over all 8192 tokens. Returns (seconds, algorithmic bytes,
+    threads)."""
+    import numpy as np
+    import torch
+    import oracle
+    import synth
+    B, n_kv, L = w.block, w.n_kv, w.ctx
+    nb = L // B
+    sb = synth.sign_bits(1000)
+    g = synth.make_gen(seed)
+    K = synth.kv_values(g, seqs, n_kv, L, w.sigma_m, w.n_out, w.out_factor).to(torch.bfloat16)
+    V = synth.kv_values(g, seqs, n_kv, L, w.sigma_m, w.n_out, w.out_factor).to(torch.bfloat16)
+    q = synth.queries(g, seqs, w.n_q).to(torch.bfloat16).double().numpy()
+    hb = oracle.head_block_bytes(B)
+    pool = np.zeros((seqs * nb, n_kv, 2, hb), dtype=np.uint8)
+    # the cache as prefill left it (not timed)
+    for kind, T in ((0, K), (1, V)):
+        X = T[:, :, :(nb - 1) * B].double().numpy().reshape(seqs, n_kv, nb - 1, B, D)
+        qb = oracle.quantize_blocks(X.transpose(0, 2, 1, 3, 4).reshape(-1, B, D), w.iters, kind, sb)
+        pool[np.arange(seqs)[:, None] * nb + np.arange(nb - 1)[None, :], :, kind] = \
+            qb.reshape(seqs, nb - 1, n_kv, hb)
+    bt = (np.arange(seqs)[:, None] * nb + np.arange(nb)[None, :]).astype(np.int32)
+    staging = np.zeros((seqs, n_kv, 2, B, D), dtype=np.uint16)
+    lens = np.full(seqs, L, dtype=np.int32)
+    t0 = time.perf_counter()
+    # timed: the append's quantisation of the completed block, then attention
+    for kind, T in ((0, K), (1, V)):
+        X = T[:, :, (nb - 1) * B:].double().numpy().reshape(seqs * n_kv, B, D)
+        qb = oracle.quantize_blocks(X, w.iters, kind, sb)
+        pool[np.arange(seqs) * nb + nb - 1, :, kind] = qb.reshape(seqs, n_kv, hb)
+    oracle.decode_attention(B, w.n_q, n_kv, sb, 1 / math.sqrt(D), q, pool, staging, bt, lens)
+    secs = time.perf_counter() - t0
+    attn_bytes = seqs * L * n_kv * (2 * (32 + 16 + 2) + 2 * 256 / B) + seqs * w.n_q * D * 6
+    app_bytes = seqs * n_kv * 2 * (D * 2 + (B - 1) * D * 2 + hb)
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return secs, attn_bytes + app_bytes, threads
+
+
+def run_reference(args):
+    w = workload()
+    seqs = CPU_SAMPLE_SEQS
+    cpu_sample(w, 1)                       # warm the oracle build / caches
+    secs_list = []
+    nbytes = 0
+    threads = 1
+    for _ in range(args.warmup):
+        cpu_sample(w, seqs)
+    for _ in range(args.steps):
+        s, nbytes, threads = cpu_sample(w, seqs)
+        secs_list.append(s)
+    secs = sum(secs_list) / len(secs_list)
+    value = nbytes / secs / 1e9
+    sample = (f"{seqs} of {w.batch} sequences x 1 of {w.layers} layers (all {w.n_kv} kv heads): "
+              f"block quantise + attention")
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        tdist.init_process_group("nccl")
+        if rank == 0:                      # one in-tree build, the other ranks then load it
+            from bit_kv_cache_08_gb300.build import build as build_lib
+            build_lib()
+        tdist.barrier()
+    res, state, objs = run_gpu(args, rank, world)
+    w = workload()
+    res["e2e"] = e2e_gpu(args, objs, state, w, rank)
+    res["e2e"]["value"] = round(res["e2e"]["value"] * world, 2)
+    import torch
+    if rank == 0 and not args.no_bf16:
+        del state
+        torch.cuda.empty_cache()
+        res["bf16_cache_comparison"] = bf16_comparison(objs[0], w, torch.cuda.current_device())
+    if rank == 0 and not args.no_cpu_baseline:
+        seqs = CPU_SAMPLE_SEQS
+        secs, nbytes, threads = cpu_sample(w, seqs)
+        res["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
+                               "kind": "oracle",
+                               "sample": f"{seqs} of {w.batch} sequences x 1 of {w.layers} layers, all kv heads: "
+                                         f"block quantise + attention ({secs:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

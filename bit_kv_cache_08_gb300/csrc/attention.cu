@@ -19,16 +19,17 @@
 // shared-memory stages with 1-D bulk copies (cp.async.bulk) counted on
 // mbarriers; all lanes wait with a bounded try_wait. Each lane reads one
 // 32-byte code record per 32 tokens and turns every pair of 2-bit codes into
-// an fp16x2 tensor-core operand with one shift and one mask (codes become
-// fp16 subnormals code*2^-24, exact). The contractions run on mma.sync
-// m16n8k16 (f16 in, f32 accumulate):
-//   QK: D[token][col] = sum_c code[t][c] * q'[c][col], per 32-channel group,
+// an fp16x2 tensor-core operand a = 1 + code/4 (exact) with one shift and
+// one LOP3. The contractions run on mma.sync m16n8k16 (f16 in, f32
+// accumulate); since code*s + z = 4s*a + (z - 4s):
+//   QK: D[token][col] = sum_c a[t][c] * q'[c][col], per 32-channel group,
 //       col = (query head, hi|lo) with q' = q_rot*C split into two fp16s, so
 //       the scores keep fp32 accuracy; then
-//       score[t][h] = R_t*(sum_g s_tg*acc_g + z_tg*Q'_g[h]),  Q'_g = sum_{c in g} q'_c
-//   PV: O^T[c][col] = sum_t code[t][c] * P'[t][col],  P' = p_t*R_t*s_tg (hi|lo),
-//       plus the zero-point term sum_t p_t R_t z_tg in fp32, scaled by C_c
-//       per block into the running accumulator.
+//       score[t][h] = R_t*(sum_g 4 s_tg*acc_g + (z_tg - 4 s_tg)*Q'_g[h]),
+//       Q'_g = sum_{c in g} q'_c
+//   PV: O^T[c][col] = sum_t a[t][c] * P'[t][col],  P' = p_t*R_t*s_tg*lam (hi|lo),
+//       plus the zero term sum_t p_t R_t lam (z_tg - 4 s_tg) in fp32; the
+//       running accumulator gets C_c/lam*(4 O_blk + zero term) per block.
 // Operand order inside each MMA (which token is row r, which channel is
 // k-slot j) is chosen so that the packed record order gives every lane its
 // operands directly; the writer packs codes in that order.
@@ -298,8 +299,9 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
                             const float ag = acc[g][mt][2 * rh] + acc[g][mt][2 * rh + 1];
-                            s = fmaf(sv[g][i] * kCodeUnitInv, ag, s);
-                            s = fmaf(zv[g][i], Qp[g], s);
+                            const float s4 = 4.0f * sv[g][i];
+                            s = fmaf(s4, ag, s);
+                            s = fmaf(zv[g][i] - s4, Qp[g], s);
                         }
                         sc[i] = s * Rv[i] * kmul;
                     }
@@ -344,37 +346,42 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 4));
                 pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 8));
                 pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 16));
-                // scale so that p*R <= 2^14 and p*R*s <= 2^12 (fp16 range for P' and its split)
+                // power-of-two scale so that p*R <= 2^14 and p*R*s <= 2^12 (fp16
+                // range for P' and its hi|lo split); undone in the update of O
                 float lam = 1.f;
                 if (pmax > 0.f) {
                     int k = 14 - ceil_log2(pmax);
                     if (smax > 0.f) k = min(k, 12 - ceil_log2(pmax * smax));
                     lam = exp2i(k);
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) pR[i] *= lam;
                 {
                     uint16_t* ph = pex + tq * 32 + 4 * gq;            // [hi][head][token]
                     uint16_t* pl = pex + 128 + tq * 32 + 4 * gq;      // [lo][head][token]
                     float hi[4], lo[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float v = pR[i] * lam;
-                        hi[i] = __half2float(__float2half_rn(v));
-                        lo[i] = v - hi[i];
+                        hi[i] = __half2float(__float2half_rn(pR[i]));
+                        lo[i] = pR[i] - hi[i];
                     }
                     *reinterpret_cast<uint2*>(ph) = make_uint2(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]));
                     *reinterpret_cast<uint2*>(pl) = make_uint2(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]));
                 }
-                // zero-point term per group for head tq over this sub-block (fp32)
+                // zero term per group for head tq over this sub-block (fp32):
+                // sum_t p R lam (z - 4 s)
                 float zs[4];
                 {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         const uint2 z2 = *reinterpret_cast<const uint2*>(Vz + g * B + t0);
+                        const uint2 s2 = *reinterpret_cast<const uint2*>(Vs + g * B + t0);
                         const float2 z01 = __half22float2(u32_as_h2(z2.x)), z23 = __half22float2(u32_as_h2(z2.y));
-                        float zz = pR[0] * z01.x;
-                        zz = fmaf(pR[1], z01.y, zz);
-                        zz = fmaf(pR[2], z23.x, zz);
-                        zz = fmaf(pR[3], z23.y, zz);
+                        const float2 s01 = __half22float2(u32_as_h2(s2.x)), s23 = __half22float2(u32_as_h2(s2.y));
+                        float zz = pR[0] * fmaf(-4.0f, s01.x, z01.x);
+                        zz = fmaf(pR[1], fmaf(-4.0f, s01.y, z01.y), zz);
+                        zz = fmaf(pR[2], fmaf(-4.0f, s23.x, z23.x), zz);
+                        zz = fmaf(pR[3], fmaf(-4.0f, s23.y, z23.y), zz);
                         zz += __shfl_xor_sync(kFull, zz, 4);
                         zz += __shfl_xor_sync(kFull, zz, 8);
                         zz += __shfl_xor_sync(kFull, zz, 16);
@@ -434,7 +441,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                                  bv[g][2 * kt], bv[g][2 * kt + 1]);
                     }
                 }
-                // ---------------- O += C_c / lam * (2^24 * O_blk + zs_g)
+                // ---------------- O += C_c / lam * (4 O_blk + zs_g)
                 {
                     const float il = 1.f / lam;
 #pragma unroll
@@ -448,8 +455,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
                             for (int rh = 0; rh < 2; ++rh) {
                                 const float cs = cf[2 * m + rh] * il;
-                                O[mt][2 * rh] = fmaf(cs, fmaf(Ob[mt][2 * rh], kCodeUnitInv, zs[g]), O[mt][2 * rh]);
-                                O[mt][2 * rh + 1] = fmaf(cs * kCodeUnitInv, Ob[mt][2 * rh + 1], O[mt][2 * rh + 1]);
+                                O[mt][2 * rh] = fmaf(cs, fmaf(Ob[mt][2 * rh], 4.0f, zs[g]), O[mt][2 * rh]);
+                                O[mt][2 * rh + 1] = fmaf(cs * 4.0f, Ob[mt][2 * rh + 1], O[mt][2 * rh + 1]);
                             }
                         }
                     }

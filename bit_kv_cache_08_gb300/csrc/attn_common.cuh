@@ -38,11 +38,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two 2-bit codes at bits 2j and 16+2j of w -> fp16x2 (code * 2^-24 each).
+// Two 2-bit codes at bits 2j and 16+2j of w -> an fp16x2 operand whose
+// halves are 1 + code/4 (code placed in the top two fraction bits of 1.0):
+// exact, one shift and one LOP3. The constant 1 is removed in the fp32
+// epilogue through the zero-point term (z - 4s).
 __device__ __forceinline__ uint32_t code_pair(uint32_t w, int j) {
-    return (w >> (2 * j)) & 0x00030003u;
+    const uint32_t x = (j <= 4) ? (w << (8 - 2 * j)) : (w >> (2 * j - 8));
+    return (x & 0x03000300u) | 0x3C003C00u;
 }
-constexpr float kCodeUnitInv = 16777216.0f;   // 2^24
 
 // 2^k as a float for k in [-126, 127]
 __device__ __forceinline__ float exp2i(int k) {

@@ -39,6 +39,12 @@ struct QuantParams {
     uint32_t sb[4];    // rotation signs
 };
 
+// A variance that is zero up to rounding (v <= 2^-30 mu^2), not positive or
+// not finite leaves its row/column factor unchanged (a constant column keeps C).
+__device__ __forceinline__ bool usable_variance(float v, float mu) {
+    return v > 0.f && isfinite(v) && v > 0x1p-30f * (mu * mu);
+}
+
 // Least fp16 s >= 0 with z + 3 s >= M, for fp16 z <= M (all exact comparisons).
 __device__ __forceinline__ float step_for(float zf, float M) {
     if (zf >= M) return 0.0f;
@@ -94,7 +100,7 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
             float mu = warp_sum(y[i][0] + y[i][1] + y[i][2] + y[i][3]) * (1.0f / kD);
             float d0 = y[i][0] - mu, d1 = y[i][1] - mu, d2 = y[i][2] - mu, d3 = y[i][3] - mu;
             float var = warp_sum(d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3) * (1.0f / kD);
-            if (var > 0.f && isfinite(var)) {
+            if (usable_variance(var, mu)) {
                 float r = sqrtf(var);
                 float inv = __frcp_rn(r);
 #pragma unroll
@@ -135,7 +141,7 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             float vk = var[k] * (1.0f / B);
-            if (vk > 0.f && isfinite(vk)) {
+            if (usable_variance(vk, mu[k])) {
                 float r = sqrtf(vk);
                 float inv = __frcp_rn(r);
 #pragma unroll

@@ -244,7 +244,10 @@ static void col_stats(const double* Y, int B, int c, double* mu, double* var)
     *var = v / B;
 }
 
-static int usable_variance(double v) { return v > 0.0 && isfinite(v); }
+static int usable_variance(double v, double mu)
+{
+    return v > 0.0 && isfinite(v) && v > ldexp(mu * mu, -30);
+}
 
 void orc_varn(int B, int iters, const double* Xr, double* Y, double* R, double* C,
               double* trace)
@@ -257,7 +260,7 @@ void orc_varn(int B, int iters, const double* Xr, double* Y, double* R, double* 
         for (int t = 0; t < B; t++) {
             double mu, v;
             row_stats(Y, t, &mu, &v);
-            if (!usable_variance(v)) continue;
+            if (!usable_variance(v, mu)) continue;
             double r = sqrt(v);
             for (int c = 0; c < ORC_D; c++) Y[t * ORC_D + c] /= r;
             R[t] *= r;
@@ -267,7 +270,7 @@ void orc_varn(int B, int iters, const double* Xr, double* Y, double* R, double* 
             for (int t = 0; t < B; t++) {
                 double mu, v;
                 row_stats(Y, t, &mu, &v);
-                if (usable_variance(v) && fabs(v - 1.0) > worst) worst = fabs(v - 1.0);
+                if (usable_variance(v, mu) && fabs(v - 1.0) > worst) worst = fabs(v - 1.0);
             }
             trace[3 * it + 0] = worst;
         }
@@ -275,7 +278,7 @@ void orc_varn(int B, int iters, const double* Xr, double* Y, double* R, double* 
         for (int c = 0; c < ORC_D; c++) {
             double mu, v;
             col_stats(Y, B, c, &mu, &v);
-            if (!usable_variance(v)) continue;
+            if (!usable_variance(v, mu)) continue;
             double r = sqrt(v);
             for (int t = 0; t < B; t++) Y[t * ORC_D + c] /= r;
             C[c] *= r;
@@ -285,12 +288,12 @@ void orc_varn(int B, int iters, const double* Xr, double* Y, double* R, double* 
             for (int c = 0; c < ORC_D; c++) {
                 double mu, v;
                 col_stats(Y, B, c, &mu, &v);
-                if (usable_variance(v) && fabs(v - 1.0) > wc) wc = fabs(v - 1.0);
+                if (usable_variance(v, mu) && fabs(v - 1.0) > wc) wc = fabs(v - 1.0);
             }
             for (int t = 0; t < B; t++) {
                 double mu, v;
                 row_stats(Y, t, &mu, &v);
-                if (usable_variance(v) && fabs(v - 1.0) > wr) wr = fabs(v - 1.0);
+                if (usable_variance(v, mu) && fabs(v - 1.0) > wr) wr = fabs(v - 1.0);
             }
             trace[3 * it + 1] = wc;
             trace[3 * it + 2] = wr;

@@ -185,6 +185,13 @@ def test_varn_degenerate_rows_and_columns_keep_factor_one():
     assert np.all(r["codes"] == 0) and np.all(r["s16"] == 0) and np.all(r["z16"] == 0)
     dec = oracle.decode_blocks(r["bytes"], 32, oracle.KIND_V, synth.sign_bits(1), rotated=False)
     assert np.all(dec == 0.0)
+    # identical tokens: after the token pass every channel is constant, so the
+    # channel factors stay 1 and every token reconstructs to the same row
+    row = np.random.default_rng(3).standard_normal(D)
+    r = oracle.quantize_block(np.tile(row, (32, 1)), 3, oracle.KIND_K, synth.sign_bits(2))
+    assert np.all(r["C"] == 1.0) and np.all(r["R"] == r["R"][0])
+    dec = oracle.decode_blocks(r["bytes"], 32, oracle.KIND_K, synth.sign_bits(2), rotated=False)[0]
+    assert np.all(dec == dec[0])
 
 
 def test_round_factor_clamps_to_fp16_normal_range():
