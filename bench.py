@@ -26,7 +26,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "2-bit KV decode-attn GB/s (% of HBM peak) + quantize-append tokens/s"
-CPU_SAMPLE_SEQS = 4
+CPU_SAMPLE_SEQS = 16
 FALLBACK_HBM_GBS = 6800.0
 D = 128
 
@@ -34,8 +34,8 @@ D = 128
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=5)
-    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     p.add_argument("--layers", type=int, default=None, help="(testing only) fewer layers")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -365,11 +365,11 @@ def bf16_comparison(kv, w, device):
 
 # ---------------------------------------------------------------------------- oracle (CPU)
 
-def cpu_sample(w, seqs, seed=0):
+def cpu_sample_setup(w, seqs, seed=0):
     """A bounded sample of the workload for the fp64 oracle: `seqs` sequences
-    of one layer (all kv heads): quantise the completed block, then decode
-    attention over all 8192 tokens. Returns (seconds, algorithmic bytes,
-    threads)."""
+    of one layer (all kv heads), with the cache as prefill left it (not
+    timed). The timed step (cpu_sample_step) quantises the completed block of
+    every (sequence, head, K|V), then runs decode attention over all tokens."""
     import numpy as np
     import torch
     import oracle
@@ -383,25 +383,34 @@ def cpu_sample(w, seqs, seed=0):
     q = synth.queries(g, seqs, w.n_q).to(torch.bfloat16).double().numpy()
     hb = oracle.head_block_bytes(B)
     pool = np.zeros((seqs * nb, n_kv, 2, hb), dtype=np.uint8)
-    # the cache as prefill left it (not timed)
+    last = []
     for kind, T in ((0, K), (1, V)):
         X = T[:, :, :(nb - 1) * B].double().numpy().reshape(seqs, n_kv, nb - 1, B, D)
         qb = oracle.quantize_blocks(X.transpose(0, 2, 1, 3, 4).reshape(-1, B, D), w.iters, kind, sb)
         pool[np.arange(seqs)[:, None] * nb + np.arange(nb - 1)[None, :], :, kind] = \
             qb.reshape(seqs, nb - 1, n_kv, hb)
+        last.append(np.ascontiguousarray(T[:, :, (nb - 1) * B:].double().numpy().reshape(seqs * n_kv, B, D)))
     bt = (np.arange(seqs)[:, None] * nb + np.arange(nb)[None, :]).astype(np.int32)
-    staging = np.zeros((seqs, n_kv, 2, B, D), dtype=np.uint16)
-    lens = np.full(seqs, L, dtype=np.int32)
+    return dict(w=w, seqs=seqs, sb=sb, q=q, pool=pool, last=last, bt=bt, hb=hb,
+                staging=np.zeros((seqs, n_kv, 2, B, D), dtype=np.uint16),
+                lens=np.full(seqs, L, dtype=np.int32))
+
+
+def cpu_sample_step(st):
+    """Returns (seconds, algorithmic bytes, threads) of one timed oracle step."""
+    import numpy as np
+    import oracle
+    w, seqs, B, n_kv, L = st["w"], st["seqs"], st["w"].block, st["w"].n_kv, st["w"].ctx
+    nb = L // B
     t0 = time.perf_counter()
-    # timed: the append's quantisation of the completed block, then attention
-    for kind, T in ((0, K), (1, V)):
-        X = T[:, :, (nb - 1) * B:].double().numpy().reshape(seqs * n_kv, B, D)
-        qb = oracle.quantize_blocks(X, w.iters, kind, sb)
-        pool[np.arange(seqs) * nb + nb - 1, :, kind] = qb.reshape(seqs, n_kv, hb)
-    oracle.decode_attention(B, w.n_q, n_kv, sb, 1 / math.sqrt(D), q, pool, staging, bt, lens)
+    for kind in (0, 1):
+        qb = oracle.quantize_blocks(st["last"][kind], w.iters, kind, st["sb"])
+        st["pool"][np.arange(seqs) * nb + nb - 1, :, kind] = qb.reshape(seqs, n_kv, st["hb"])
+    oracle.decode_attention(B, w.n_q, n_kv, st["sb"], 1 / math.sqrt(D), st["q"], st["pool"], st["staging"],
+                            st["bt"], st["lens"])
     secs = time.perf_counter() - t0
     attn_bytes = seqs * L * n_kv * (2 * (32 + 16 + 2) + 2 * 256 / B) + seqs * w.n_q * D * 6
-    app_bytes = seqs * n_kv * 2 * (D * 2 + (B - 1) * D * 2 + hb)
+    app_bytes = seqs * n_kv * 2 * (D * 2 + (B - 1) * D * 2 + st["hb"])
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return secs, attn_bytes + app_bytes, threads
 
@@ -409,14 +418,14 @@ def cpu_sample(w, seqs, seed=0):
 def run_reference(args):
     w = workload()
     seqs = CPU_SAMPLE_SEQS
-    cpu_sample(w, 1)                       # warm the oracle build / caches
+    st = cpu_sample_setup(w, seqs)
     secs_list = []
     nbytes = 0
     threads = 1
     for _ in range(args.warmup):
-        cpu_sample(w, seqs)
+        cpu_sample_step(st)
     for _ in range(args.steps):
-        s, nbytes, threads = cpu_sample(w, seqs)
+        s, nbytes, threads = cpu_sample_step(st)
         secs_list.append(s)
     secs = sum(secs_list) / len(secs_list)
     value = nbytes / secs / 1e9
@@ -459,7 +468,7 @@ def main():
         res["bf16_cache_comparison"] = bf16_comparison(objs[0], w, torch.cuda.current_device())
     if rank == 0 and not args.no_cpu_baseline:
         seqs = CPU_SAMPLE_SEQS
-        secs, nbytes, threads = cpu_sample(w, seqs)
+        secs, nbytes, threads = cpu_sample_step(cpu_sample_setup(w, seqs))
         res["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads,
                                "kind": "oracle",
                                "sample": f"{seqs} of {w.batch} sequences x 1 of {w.layers} layers, all kv heads: "
