@@ -8,7 +8,7 @@ the C entry points of the same names.
 from ._abi import (BF16, FP32, KIND_K, KIND_V, DEVERR_BLOCK_ID, DEVERR_NONFINITE,  # noqa: F401
                    DEVERR_POSITION, DEVERR_WAIT_TIMEOUT, Config, KVarNError, alloc_pool,
                    alloc_staging, alloc_workspace, append, block_bytes, clear_error, decode_attn,
-                   decode_attn_bf16, dequantize, head_block_bytes, header_symbols, lib, make_config,
+                   decode_attn_bf16, decode_attn_noalloc, dequantize, head_block_bytes, header_symbols, lib, make_config,
                    quantize_block, read_error, staging_bytes, status_string, version,
                    workspace_bytes)
 from .build import build  # noqa: F401

@@ -70,6 +70,8 @@ _SIGS = {
     "kvarn_dequantize": (ctypes.c_int, [_cfgp, _i32, _vp, _vp, _i64, _i32, _vp, _vp]),
     "kvarn_decode_attn_bf16": (ctypes.c_int, [_cfgp, _vp, _i32, _vp, _i64, _vp, _i32, _vp, _i32, _vp, _vp,
                                               _sz, _vp]),
+    "kvarn_decode_attn_noalloc": (ctypes.c_int, [_cfgp, _vp, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp,
+                                                 _vp, _vp]),
     "kvarn_read_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "kvarn_clear_error": (ctypes.c_int, [_vp, _vp]),
 }
@@ -232,6 +234,25 @@ def decode_attn_bf16(cfg: Config, q: torch.Tensor, kv_pool: torch.Tensor, block_
                                         kv_pool.shape[0], _ptr(block_table), block_table.shape[1],
                                         _ptr(seq_lens), q.shape[0], _ptr(out), _ptr(workspace),
                                         workspace.numel(), _stream()), "kvarn_decode_attn_bf16")
+
+
+def decode_attn_noalloc(cfg: Config, q: torch.Tensor, pool: torch.Tensor, staging: torch.Tensor,
+                        block_table: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor,
+                        error_word: Optional[torch.Tensor] = None):
+    """kvarn_decode_attn with the library's built-in scratch (no workspace):
+    for callers that cannot allocate device memory."""
+    _need_cuda(q, "q")
+    _need_cuda(pool, "pool", torch.uint8)
+    _need_cuda(staging, "staging", torch.bfloat16)
+    _need_cuda(block_table, "block_table", torch.int32)
+    _need_cuda(seq_lens, "seq_lens", torch.int32)
+    _need_cuda(out, "out", torch.float32)
+    if error_word is not None:
+        _need_cuda(error_word, "error_word", torch.int32)
+    _check(lib().kvarn_decode_attn_noalloc(ctypes.byref(cfg), _ptr(q), _dtype_code(q), _ptr(pool),
+                                           pool.shape[0], _ptr(staging), _ptr(block_table),
+                                           block_table.shape[1], _ptr(seq_lens), q.shape[0], _ptr(out),
+                                           _ptr(error_word), _stream()), "kvarn_decode_attn_noalloc")
 
 
 def dequantize(cfg: Config, kind: int, src_base: torch.Tensor, out: torch.Tensor, rotated: bool,

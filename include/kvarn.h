@@ -218,6 +218,34 @@ int kvarn_decode_attn_bf16(const kvarn_config* cfg, const void* q, int32_t q_dty
                            const int32_t* seq_lens, int32_t batch, float* out, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/*
+ * kvarn_decode_attn_noalloc -- kvarn_decode_attn for callers that cannot
+ * allocate device memory. (The paper has no counterpart; this is a library
+ * convenience.) Some callers can only hand over their inputs and outputs: a
+ * plug-in interface with no workspace argument, a runtime whose memory
+ * planner owns all device memory, or a loop that must not call cudaMalloc
+ * because allocation can synchronise the device. This entry point allocates
+ * nothing: its split-K scratch is a 16 MiB array compiled into the library
+ * (held on every GPU that loads the library until the process exits).
+ *
+ * Arguments and results are those of kvarn_decode_attn, without the
+ * workspace. error_word (device uint32, may be NULL) receives this call's
+ * KVARN_DEVERR_* flags (0 when none). The scratch must hold 256 + (batch *
+ * n_kv + resident warps) * G * 528 bytes; larger problems are refused with
+ * KVARN_ERR_WORKSPACE before anything is enqueued.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. Every call shares the one array: calls whose GPU work overlaps
+ * (other streams, other host threads) race on it and must be serialised by
+ * the caller. Each call clears the error word it uses before its kernels run.
+ */
+int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q, int32_t q_dtype,
+                              const void* pool, int64_t n_pool_blocks, const void* staging,
+                              const int32_t* block_table, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t batch, float* out,
+                              uint32_t* error_word, void* stream);
+
 /* Copies the workspace error word to *code (host) after synchronising
  * stream. Returns KVARN_OK or KVARN_ERR_CUDA. */
 int kvarn_read_error(const void* workspace, uint32_t* code, void* stream);
