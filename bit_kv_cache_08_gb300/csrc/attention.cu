@@ -1,5 +1,5 @@
 // attention.cu -- split-K decode attention over the KVarN 2-bit paged cache
-// (sm_103a), and the merge kernel that finishes it.
+// (sm_103a); the merge kernel that finishes it is in attn_common.cuh.
 //
 // Method: "KVarN：方差归一化让 2-bit KV 缓存扛住长链推理", section 三 3.1: the
 // query is multiplied by the same randomised Hadamard matrix as K and V, so
@@ -19,17 +19,23 @@
 // shared-memory stages with 1-D bulk copies (cp.async.bulk) counted on
 // mbarriers; all lanes wait with a bounded try_wait. Each lane reads one
 // 32-byte code record per 32 tokens and turns every pair of 2-bit codes into
-// an fp16x2 tensor-core operand a = 1 + code/4 (exact) with one shift and
-// one LOP3. The contractions run on mma.sync m16n8k16 (f16 in, f32
-// accumulate); since code*s + z = 4s*a + (z - 4s):
-//   QK: D[token][col] = sum_c a[t][c] * q'[c][col], per 32-channel group,
-//       col = (query head, hi|lo) with q' = q_rot*C split into two fp16s, so
-//       the scores keep fp32 accuracy; then
-//       score[t][h] = R_t*(sum_g 4 s_tg*acc_g + (z_tg - 4 s_tg)*Q'_g[h]),
-//       Q'_g = sum_{c in g} q'_c
-//   PV: O^T[c][col] = sum_t a[t][c] * P'[t][col],  P' = p_t*R_t*s_tg*lam (hi|lo),
-//       plus the zero term sum_t p_t R_t lam (z_tg - 4 s_tg) in fp32; the
-//       running accumulator gets C_c/lam*(4 O_blk + zero term) per block.
+// an fp16x2 tensor-core operand a = 1 + code/4 (exact) with one LOP3 after a
+// left shift. Everything below runs on mma.sync m16n8k16 (f16 in, f32
+// accumulate) with fp32 epilogues; code*s + z = 4 s (a - 1) + z.
+//   q'  = q_rot * C per block, as two fp16 halves (hi | lo) so the tensor
+//         cores keep fp32 accuracy; q_rot is scaled to 2^12 per unit and C by
+//         a power of two per block so both halves stay normal fp16 (fp16
+//         subnormal operands lose precision on the tensor cores).
+//   Q'_g = sum_{c in g} q'_c            (MMA with an all-ones A operand)
+//   QK:  acc_g[t][h] = -Q'_g + sum_{c in g} a[t][c] q'[c][h]  (one accumulator
+//        per 32-channel group, started at -Q'_g), then
+//        score[t][h] = 4 R_t (sum_g s_tg acc_g + z_tg Q'_g / 4)
+//   softmax over the block (running max and sum per head, log2 domain)
+//   PV:  P'[t][h,g] = p_t R_t s_tg lam (hi | lo), lam a power of two per
+//        (head, block) keeping P' inside fp16;
+//        Ob[c][h] = sum_t a[t][c] P'[t][h, g(c)]
+//        zs[h][g] = sum_t p_t R_t lam (z_tg - 4 s_tg)  (MMA with p as A, z|s as B)
+//        O[c][h] += 4 C_c / lam * (Ob[c][h] + zs[h][g(c)] / 4)  once per block.
 // Operand order inside each MMA (which token is row r, which channel is
 // k-slot j) is chosen so that the packed record order gives every lane its
 // operands directly; the writer packs codes in that order.
@@ -46,13 +52,26 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     uint8_t* stages = smem;                                              // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);     // S mbarriers
     float* qsm = reinterpret_cast<float*>(smem + S * 2 * HB + 64);       // [4][128]
-    uint16_t* pex = reinterpret_cast<uint16_t*>(qsm + 4 * kD);           // [2][4][32]: hi, lo
+    uint16_t* pex = reinterpret_cast<uint16_t*>(qsm + 4 * kD);           // [hi|lo][4 heads][B]
 
     const int lane = threadIdx.x;
     const int gq = lane >> 2, tq = lane & 3;   // mma groupID, thread-in-group
     const int w = blockIdx.x;
+    constexpr uint32_t kOnes = 0x3C003C00u;    // fp16x2 (1, 1)
 
-    const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, 0};
+    // scalar copies of the arguments (the lambdas below must not take the
+    // address of the kernel parameter block)
+    const uint8_t* __restrict__ pool = a.pool;
+    const int32_t* __restrict__ btab = a.block_table;
+    const int max_blocks = a.max_blocks, G = a.G, n_q = a.n_q, n_kv = a.n_kv, q_dtype = a.q_dtype;
+    const int64_t n_pool_blocks = a.n_pool_blocks, block_bytes = a.block_bytes;
+    const void* qptr = a.q;
+    float* partials = a.partials;
+    uint32_t* err = a.err;
+    const float sm_scale = a.sm_scale;
+    const uint32_t sb0 = a.sb[0], sb1 = a.sb[1], sb2 = a.sb[2], sb3 = a.sb[3];
+
+    const SplitArgs sp{a.seq_lens, a.batch, n_kv, max_blocks, B, 0};
     Cursor cc;
     cc.b = cc.h = cc.j = 0;
     const int64_t W = split_locate(sp, 0, lane, cc.b, cc.h, cc.j);
@@ -70,18 +89,18 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 
     // block-table chunk cache for the issue cursor
     int bt_b = -1, bt_j0 = 0, bt_val = 0;
-    auto issue = [&](int64_t x, int stage) {
+    auto issue = [&](int stage) {
         if (ic.b != bt_b || ic.j < bt_j0 || ic.j >= bt_j0 + 32) {
             bt_b = ic.b;
             bt_j0 = ic.j;
             const int jj = bt_j0 + lane;
-            bt_val = (jj < a.max_blocks) ? a.block_table[(int64_t)bt_b * a.max_blocks + jj] : -1;
+            bt_val = (jj < max_blocks) ? btab[(int64_t)bt_b * max_blocks + jj] : -1;
         }
         int64_t phys = __shfl_sync(kFull, bt_val, ic.j - bt_j0);
-        const bool ok = phys >= 0 && phys < a.n_pool_blocks;
+        const bool ok = phys >= 0 && phys < n_pool_blocks;
         if (!ok) phys = 0;   // read a valid block, result discarded below
         if (lane == 0) {
-            const uint8_t* src = a.pool + phys * a.block_bytes + (int64_t)(2 * ic.h) * HB;
+            const uint8_t* src = pool + phys * block_bytes + (int64_t)(2 * ic.h) * HB;
             mbar_arrive_expect_tx(&bars[stage], 2 * HB);
             bulk_g2s(stages + stage * 2 * HB, src, 2 * HB, &bars[stage]);
         }
@@ -92,26 +111,28 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     {
         int64_t x = s_beg;
         for (int s = 0; s < S && x < s_end; ++s, ++x)
-            if (issue(x, s)) okmask |= 1u << s;
+            if (issue(s)) okmask |= 1u << s;
     }
 
     // per-unit state
-    uint32_t Qh[16], Qlm[16], Qhm[16];
-    float qsQ[16];
-    float kmul = 0.f;
+    uint32_t Qh[16], Ql[16];   // q_rot*2^(12-e) as fp16 hi | lo (lo kept only by the lo-column lanes)
+    float kmul = 0.f;          // 4 * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
     float m_run = -INFINITY, l_part = 0.f;
-    float O[8][4];
-    const float sgn4[4] = {sign_of(a.sb, 4 * lane), sign_of(a.sb, 4 * lane + 1),
-                           sign_of(a.sb, 4 * lane + 2), sign_of(a.sb, 4 * lane + 3)};
-    const bool head_ok = tq < a.G;          // this lane's score/accumulator head
+    float O[8][2];             // rotated output, channels 32g + 4gq + 2m + rh, head tq
+    const float sgn4[4] = {sign_of4(sb0, sb1, sb2, sb3, 4 * lane), sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 1),
+                           sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 2), sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 3)};
+    const bool head_ok = tq < G;            // this lane's score / accumulator head
     const int hbq = gq >> 1, part = gq & 1;  // this lane's B-fragment column: (head, hi|lo)
-    const bool bcol_ok = hbq < a.G;
+    const bool bcol_ok = hbq < G;
+    // (-1,-1) on the lanes holding a lo column, (0,0) on the hi ones: the
+    // two-product's correction term is multiplied by it instead of selected
+    const __half2 nmask = part ? __float2half2_rn(-1.f) : __float2half2_rn(0.f);
 
     auto unit_setup = [&]() {
         __syncwarp();
-        for (int j = 0; j < a.G; ++j) {
+        for (int j = 0; j < G; ++j) {
             float v[4];
-            load_q4(a, (int64_t)cc.b * a.n_q + (int64_t)cc.h * a.G + j, lane, v);
+            load_q4(qptr, q_dtype, (int64_t)cc.b * n_q + (int64_t)cc.h * G + j, lane, v);
 #pragma unroll
             for (int k = 0; k < 4; ++k) v[k] *= sgn4[k];
             fwht128(v, lane);
@@ -123,10 +144,10 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             }
             amax = warp_max(amax);
             const int e = (amax > 0.f && isfinite(amax)) ? ceil_log2(amax) : 0;
-            const float sc = exp2i(-e);
+            const float sc = exp2i(12 - e);
             *reinterpret_cast<float4*>(&qsm[j * kD + 4 * lane]) =
                 make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
-            if (j == tq) kmul = exp2i(e) * a.sm_scale * kLog2e;
+            if (j == tq) kmul = 4.0f * exp2i(e - 12) * sm_scale * kLog2e;
         }
         __syncwarp();
 #pragma unroll
@@ -140,19 +161,13 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 lv = pack_h2(v0 - __half2float(h0), v1 - __half2float(h1));
             }
             Qh[i] = hv;
-            Qlm[i] = part ? lv : 0u;
-            Qhm[i] = part ? hv : 0u;
+            Ql[i] = part ? lv : 0u;
         }
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            qsQ[k] = head_ok ? qsm[tq * kD + 32 * (gq >> 1) + 16 * (gq & 1) + k] : 0.f;
         if (!head_ok) kmul = 0.f;
         m_run = -INFINITY;
         l_part = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) O[mt][r] = 0.f;
+        for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = 0.f;
     };
 
     auto unit_flush = [&]() {
@@ -161,22 +176,16 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         l += __shfl_xor_sync(kFull, l, 8);
         l += __shfl_xor_sync(kFull, l, 16);
         if (head_ok) {
-            const int64_t slot = (int64_t)cc.b * a.n_kv + cc.h + w;
-            float* base = a.partials + (slot * a.G + tq) * kPartialStride;
+            const int64_t slot = (int64_t)cc.b * n_kv + cc.h + w;
+            float* base = partials + (slot * G + tq) * kPartialStride;
             if (gq == 0) {
                 base[0] = m_run;
                 base[1] = l;
             }
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                // rows gq / gq+8 of m-tiles 2g, 2g+1 -> channels 32g + 4gq + {0,1,2,3}
-                float4 o;
-                o.x = O[2 * g][0] + O[2 * g][1];
-                o.y = O[2 * g][2] + O[2 * g][3];
-                o.z = O[2 * g + 1][0] + O[2 * g + 1][1];
-                o.w = O[2 * g + 1][2] + O[2 * g + 1][3];
-                *reinterpret_cast<float4*>(base + 4 + 32 * g + 4 * gq) = o;
-            }
+            for (int g = 0; g < 4; ++g)   // channels 32g + 4gq + {0,1,2,3}
+                *reinterpret_cast<float4*>(base + 4 + 32 * g + 4 * gq) =
+                    make_float4(O[2 * g][0], O[2 * g][1], O[2 * g + 1][0], O[2 * g + 1][1]);
         }
     };
 
@@ -185,7 +194,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     uint32_t phase = 0;
     for (int64_t x = s_beg; x < s_end; ++x) {
         if (!mbar_wait_bounded(&bars[stage], phase, kWaitLimit)) {
-            if (lane == 0) raise_error(a.err, KVARN_DEVERR_WAIT_TIMEOUT);
+            if (lane == 0) raise_error(err, KVARN_DEVERR_WAIT_TIMEOUT);
             // let every copy still in flight into this CTA's shared memory land
             // (again with a limit) before the CTA exits
             uint32_t ph = phase;
@@ -198,44 +207,47 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         const uint8_t* Kb = stages + stage * 2 * HB;
         const uint8_t* Vb = Kb + HB;
         const bool valid = (okmask >> stage) & 1u;
-        if (!valid && lane == 0) raise_error(a.err, KVARN_DEVERR_BLOCK_ID);
+        if (!valid && lane == 0) raise_error(err, KVARN_DEVERR_BLOCK_ID);
 
         if (valid) {
-            // ---- QK B operand for this block: q' = q_rot * C, split hi|lo
+            const uint16_t* KC = reinterpret_cast<const uint16_t*>(Kb + off_C(B));
+            // ---- per-block power of two bringing max C to (1/2, 1]
+            float cmax;
+            {
+                const uint2 c2 = *reinterpret_cast<const uint2*>(KC + 4 * lane);
+                const __half2 m2 = __hmax2(u32_as_h2(c2.x), u32_as_h2(c2.y));
+                cmax = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
+            }
+            const int ec = ceil_log2(fmaxf(cmax, kF16MinNormal));
+            const __half2 cinv = __float2half2_rn(exp2i(-ec));
+            const float kmb = kmul * exp2i(ec);
+            // ---- QK B operand: q' = q_s * C * 2^-ec as fp16 hi | lo (two-product)
             uint32_t bq[16];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                const uint4 c4 = *reinterpret_cast<const uint4*>(Kb + off_C(B) + 2 * (32 * g + 8 * tq));
+                const uint4 c4 = *reinterpret_cast<const uint4*>(KC + 32 * g + 8 * tq);
                 const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
                     const int i = 4 * g + e2;
-                    const __half2 C2 = u32_as_h2(cw[e2]);
-                    const __half2 mhi = __hmul2(u32_as_h2(Qhm[i]), C2);
-                    __half2 r = __hfma2(u32_as_h2(Qh[i]), C2, __hneg2(mhi));
-                    r = __hfma2(u32_as_h2(Qlm[i]), C2, r);
+                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
+                    const __half2 qh = u32_as_h2(Qh[i]);
+                    const __half2 mneg = __hmul2(__hmul2(qh, C2), nmask);   // -RN(qh*C) | 0
+                    __half2 r = __hfma2(qh, C2, mneg);
+                    r = __hfma2(u32_as_h2(Ql[i]), C2, r);
                     bq[i] = h2_as_u32(r);
                 }
             }
-            // ---- Q'_g for this lane's head: sum over the group of q_rot * C (fp32)
-            float Qp[4];
-            {
-                const uint4* cp = reinterpret_cast<const uint4*>(Kb + off_C(B) + 2 * (32 * (gq >> 1) + 16 * (gq & 1)));
-                float qp = 0.f;
+            // ---- Q'_g for this lane's head: an MMA with all-ones A sums each group
+            float Qneg[4], Qq[4];
 #pragma unroll
-                for (int v4 = 0; v4 < 2; ++v4) {
-                    const uint4 c4 = cp[v4];
-                    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const float2 cf = __half22float2(u32_as_h2(cw[e2]));
-                        qp = fmaf(qsQ[8 * v4 + 2 * e2], cf.x, qp);
-                        qp = fmaf(qsQ[8 * v4 + 2 * e2 + 1], cf.y, qp);
-                    }
-                }
-                qp += __shfl_xor_sync(kFull, qp, 4);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) Qp[g] = __shfl_sync(kFull, qp, 8 * g + tq);
+            for (int g = 0; g < 4; ++g) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(d, kOnes, kOnes, kOnes, kOnes, bq[4 * g], bq[4 * g + 1]);
+                mma16816(d, kOnes, kOnes, kOnes, kOnes, bq[4 * g + 2], bq[4 * g + 3]);
+                const float qg = d[0] + d[1];
+                Qneg[g] = -qg;
+                Qq[g] = 0.25f * qg;
             }
             const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B));
             const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B));
@@ -244,23 +256,27 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             const uint16_t* Vz = reinterpret_cast<const uint16_t*>(Vb + off_z(B));
             const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B));
 
+            // ---------------- QK for every 32-token sub-block
+            float sc[NSB][4];
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
-                // ---------------- QK
-                uint32_t kw[8];
+                uint32_t kw[8], kw8[8];
                 {
                     const uint4* rec = reinterpret_cast<const uint4*>(Kb) + 2 * (32 * sb + lane);
                     const uint4 r0 = rec[0], r1 = rec[1];
                     kw[0] = r0.x; kw[1] = r0.y; kw[2] = r0.z; kw[3] = r0.w;
                     kw[4] = r1.x; kw[5] = r1.y; kw[6] = r1.z; kw[7] = r1.w;
                 }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) kw8[k] = kw[k] >> 8;
                 float acc[4][2][4];
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) acc[g][mt][r] = 0.f;
+                    for (int mt = 0; mt < 2; ++mt) {
+                        acc[g][mt][0] = Qneg[g]; acc[g][mt][1] = 0.f;
+                        acc[g][mt][2] = Qneg[g]; acc[g][mt][3] = 0.f;
+                    }
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
@@ -269,195 +285,201 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         const int j = 4 * (g & 1) + 2 * kk;
 #pragma unroll
                         for (int mt = 0; mt < 2; ++mt) {
-                            const uint32_t w0 = kw[2 * (2 * mt) + (g >> 1)];
-                            const uint32_t w1 = kw[2 * (2 * mt + 1) + (g >> 1)];
-                            mma16816(acc[g][mt], code_pair(w0, j), code_pair(w1, j),
-                                     code_pair(w0, j + 1), code_pair(w1, j + 1), b0, b1);
+                            const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
+                            mma16816(acc[g][mt], code_pair(kw[i0], kw8[i0], j), code_pair(kw[i1], kw8[i1], j),
+                                     code_pair(kw[i0], kw8[i0], j + 1), code_pair(kw[i1], kw8[i1], j + 1), b0, b1);
                         }
                     }
                 // scores of tokens 32sb + 4gq + i, head tq
                 const int t0 = 32 * sb + 4 * gq;
-                float sc[4];
-                {
-                    const uint2 Rr = *reinterpret_cast<const uint2*>(KR + t0);
-                    const float2 R01 = __half22float2(u32_as_h2(Rr.x)), R23 = __half22float2(u32_as_h2(Rr.y));
-                    const float Rv[4] = {R01.x, R01.y, R23.x, R23.y};
-                    float sv[4][4], zv[4][4];   // [group][token]
+                const uint2 Rr = *reinterpret_cast<const uint2*>(KR + t0);
+                const float2 R01 = __half22float2(u32_as_h2(Rr.x)), R23 = __half22float2(u32_as_h2(Rr.y));
+                const float Rv[4] = {R01.x, R01.y, R23.x, R23.y};
+                float s_[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint2 s2 = *reinterpret_cast<const uint2*>(Ks + g * B + t0);
-                        const uint2 z2 = *reinterpret_cast<const uint2*>(Kz + g * B + t0);
-                        const float2 s01 = __half22float2(u32_as_h2(s2.x)), s23 = __half22float2(u32_as_h2(s2.y));
-                        const float2 z01 = __half22float2(u32_as_h2(z2.x)), z23 = __half22float2(u32_as_h2(z2.y));
-                        sv[g][0] = s01.x; sv[g][1] = s01.y; sv[g][2] = s23.x; sv[g][3] = s23.y;
-                        zv[g][0] = z01.x; zv[g][1] = z01.y; zv[g][2] = z23.x; zv[g][3] = z23.y;
-                    }
+                for (int g = 0; g < 4; ++g) {
+                    const uint2 s2 = *reinterpret_cast<const uint2*>(Ks + g * B + t0);
+                    const uint2 z2 = *reinterpret_cast<const uint2*>(Kz + g * B + t0);
+                    const float2 s01 = __half22float2(u32_as_h2(s2.x)), s23 = __half22float2(u32_as_h2(s2.y));
+                    const float2 z01 = __half22float2(u32_as_h2(z2.x)), z23 = __half22float2(u32_as_h2(z2.y));
+                    const float sv[4] = {s01.x, s01.y, s23.x, s23.y};
+                    const float zv[4] = {z01.x, z01.y, z23.x, z23.y};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int mt = i >> 1, rh = i & 1;
-                        float s = 0.f;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const float ag = acc[g][mt][2 * rh] + acc[g][mt][2 * rh + 1];
-                            const float s4 = 4.0f * sv[g][i];
-                            s = fmaf(s4, ag, s);
-                            s = fmaf(zv[g][i] - s4, Qp[g], s);
-                        }
-                        sc[i] = s * Rv[i] * kmul;
+                        const float d = acc[g][mt][2 * rh] + acc[g][mt][2 * rh + 1];
+                        s_[i] = fmaf(sv[i], d, s_[i]);
+                        s_[i] = fmaf(zv[i], Qq[g], s_[i]);
                     }
                 }
-                // ---------------- online softmax (head tq, 32 tokens over 8 lanes)
-                float bm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-                bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
-                bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
-                bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
-                const float m_new = fmaxf(m_run, bm);
-                const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-                float pv[4], psum = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sc[sb][i] = s_[i] * Rv[i] * kmb;
+            }
+
+            // ---------------- online softmax over the block (head tq: 8 lanes x 4 tokens per sub-block)
+            float bm = -INFINITY;
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb)
+                bm = fmaxf(bm, fmaxf(fmaxf(sc[sb][0], sc[sb][1]), fmaxf(sc[sb][2], sc[sb][3])));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+            const float m_new = fmaxf(m_run, bm);
+            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+            float pR[NSB][4], psum = 0.f, pmax = 0.f;
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb) {
+                const uint2 Rr = *reinterpret_cast<const uint2*>(VR + 32 * sb + 4 * gq);
+                const float2 R01 = __half22float2(u32_as_h2(Rr.x)), R23 = __half22float2(u32_as_h2(Rr.y));
+                const float Rv[4] = {R01.x, R01.y, R23.x, R23.y};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    pv[i] = (m_new == -INFINITY) ? 0.f : exp2f(sc[i] - m_new);
-                    psum += pv[i];
+                    const float p = (m_new == -INFINITY) ? 0.f : exp2f(sc[sb][i] - m_new);
+                    psum += p;
+                    pR[sb][i] = p * Rv[i];
+                    pmax = fmaxf(pmax, pR[sb][i]);
                 }
-                l_part = l_part * alpha + psum;
-                m_run = m_new;
-                if (__any_sync(kFull, alpha != 1.f)) {
+            }
+            l_part = l_part * alpha + psum;
+            m_run = m_new;
+            if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt)
+                for (int mt = 0; mt < 8; ++mt) {
+                    O[mt][0] *= alpha;
+                    O[mt][1] *= alpha;
+                }
+            }
+            pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 4));
+            pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 8));
+            pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 16));
+            // largest V step of the block (all groups and tokens)
+            float smax;
+            if (B == 32) {
+                const uint2 s2 = *reinterpret_cast<const uint2*>(Vs + 4 * lane);
+                const __half2 m2 = __hmax2(u32_as_h2(s2.x), u32_as_h2(s2.y));
+                smax = fmaxf(__low2float(m2), __high2float(m2));
+            } else {
+                const uint4 s4 = *reinterpret_cast<const uint4*>(Vs + 8 * lane);
+                const __half2 m2 = __hmax2(__hmax2(u32_as_h2(s4.x), u32_as_h2(s4.y)),
+                                           __hmax2(u32_as_h2(s4.z), u32_as_h2(s4.w)));
+                smax = fmaxf(__low2float(m2), __high2float(m2));
+            }
+            smax = warp_max(smax);
+            // power of two lam so that p*R*lam <= 2^14 and p*R*s*lam <= 2^12 (fp16 range
+            // of P' and of its hi | lo halves); undone in the update of O
+            float lam = 1.f;
+            if (pmax > 0.f) {
+                int k = 14 - ceil_log2(pmax);
+                if (smax > 0.f) k = min(k, 12 - ceil_log2(pmax * smax));
+                lam = exp2i(k);
+            }
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) O[mt][r] *= alpha;
-                }
-                // ---------------- P' = p * R_v * s_v, normalised per (head, 32 tokens)
-                float pR[4];
-                {
-                    const uint2 Rr = *reinterpret_cast<const uint2*>(VR + t0);
-                    const float2 R01 = __half22float2(u32_as_h2(Rr.x)), R23 = __half22float2(u32_as_h2(Rr.y));
-                    pR[0] = pv[0] * R01.x; pR[1] = pv[1] * R01.y; pR[2] = pv[2] * R23.x; pR[3] = pv[3] * R23.y;
-                }
-                // largest step of this V sub-block (all groups)
-                float smax;
-                {
-                    const uint2 s2 = *reinterpret_cast<const uint2*>(Vs + (lane >> 3) * B + 32 * sb + 4 * (lane & 7));
-                    const __half2 m2 = __hmax2(u32_as_h2(s2.x), u32_as_h2(s2.y));
-                    smax = fmaxf(__low2float(m2), __high2float(m2));
-                    smax = warp_max(smax);
-                }
-                float pmax = fmaxf(fmaxf(pR[0], pR[1]), fmaxf(pR[2], pR[3]));
-                pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 4));
-                pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 8));
-                pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 16));
-                // power-of-two scale so that p*R <= 2^14 and p*R*s <= 2^12 (fp16
-                // range for P' and its hi|lo split); undone in the update of O
-                float lam = 1.f;
-                if (pmax > 0.f) {
-                    int k = 14 - ceil_log2(pmax);
-                    if (smax > 0.f) k = min(k, 12 - ceil_log2(pmax * smax));
-                    lam = exp2i(k);
-                }
+            for (int sb = 0; sb < NSB; ++sb) {
+                float hi[4], lo[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) pR[i] *= lam;
-                {
-                    uint16_t* ph = pex + tq * 32 + 4 * gq;            // [hi][head][token]
-                    uint16_t* pl = pex + 128 + tq * 32 + 4 * gq;      // [lo][head][token]
-                    float hi[4], lo[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        hi[i] = __half2float(__float2half_rn(pR[i]));
-                        lo[i] = pR[i] - hi[i];
-                    }
-                    *reinterpret_cast<uint2*>(ph) = make_uint2(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]));
-                    *reinterpret_cast<uint2*>(pl) = make_uint2(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]));
+                for (int i = 0; i < 4; ++i) {
+                    const float v = pR[sb][i] * lam;
+                    hi[i] = __half2float(__float2half_rn(v));
+                    lo[i] = v - hi[i];
                 }
-                // zero term per group for head tq over this sub-block (fp32):
-                // sum_t p R lam (z - 4 s)
-                float zs[4];
-                {
+                uint16_t* ph = pex + (0 * 4 + tq) * B + 32 * sb + 4 * gq;
+                uint16_t* pl = pex + (1 * 4 + tq) * B + 32 * sb + 4 * gq;
+                *reinterpret_cast<uint2*>(ph) = make_uint2(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]));
+                *reinterpret_cast<uint2*>(pl) = make_uint2(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]));
+            }
+            __syncwarp();
+
+            // ---------------- PV over the block's tokens
+            float Ob[8][4], Dz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint2 z2 = *reinterpret_cast<const uint2*>(Vz + g * B + t0);
-                        const uint2 s2 = *reinterpret_cast<const uint2*>(Vs + g * B + t0);
-                        const float2 z01 = __half22float2(u32_as_h2(z2.x)), z23 = __half22float2(u32_as_h2(z2.y));
-                        const float2 s01 = __half22float2(u32_as_h2(s2.x)), s23 = __half22float2(u32_as_h2(s2.y));
-                        float zz = pR[0] * fmaf(-4.0f, s01.x, z01.x);
-                        zz = fmaf(pR[1], fmaf(-4.0f, s01.y, z01.y), zz);
-                        zz = fmaf(pR[2], fmaf(-4.0f, s23.x, z23.x), zz);
-                        zz = fmaf(pR[3], fmaf(-4.0f, s23.y, z23.y), zz);
-                        zz += __shfl_xor_sync(kFull, zz, 4);
-                        zz += __shfl_xor_sync(kFull, zz, 8);
-                        zz += __shfl_xor_sync(kFull, zz, 16);
-                        zs[g] = zz;
-                    }
+            for (int mt = 0; mt < 8; ++mt) Ob[mt][0] = Ob[mt][1] = Ob[mt][2] = Ob[mt][3] = 0.f;
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb) {
+                // this lane's B column (head hbq, part) for tokens 32sb + 8tq .. +7
+                uint4 phv = make_uint4(0, 0, 0, 0), plv = make_uint4(0, 0, 0, 0);
+                if (bcol_ok) {
+                    phv = *reinterpret_cast<const uint4*>(pex + (0 * 4 + hbq) * B + 32 * sb + 8 * tq);
+                    plv = *reinterpret_cast<const uint4*>(pex + (1 * 4 + hbq) * B + 32 * sb + 8 * tq);
                 }
-                __syncwarp();
-                // ---------------- PV B operand: tokens 8tq..8tq+7, column (hbq, part)
+                const uint32_t ph[4] = {phv.x, phv.y, phv.z, phv.w};
+                const uint32_t pl[4] = {plv.x, plv.y, plv.z, plv.w};
+                uint32_t plm[4], pa[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    plm[k] = part ? pl[k] : 0u;
+                    pa[k] = part ? pl[k] : ph[k];
+                }
                 uint32_t bv[4][4];   // [group][token pair]
-                {
-                    uint4 phv = make_uint4(0, 0, 0, 0), plv = make_uint4(0, 0, 0, 0);
-                    if (bcol_ok) {
-                        phv = *reinterpret_cast<const uint4*>(pex + hbq * 32 + 8 * tq);
-                        plv = *reinterpret_cast<const uint4*>(pex + 128 + hbq * 32 + 8 * tq);
-                    }
-                    const uint32_t ph[4] = {phv.x, phv.y, phv.z, phv.w};
-                    const uint32_t pl[4] = {plv.x, plv.y, plv.z, plv.w};
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint4 s4 = *reinterpret_cast<const uint4*>(Vs + g * B + 32 * sb + 8 * tq);
-                        const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 s4 = *reinterpret_cast<const uint4*>(Vs + g * B + 32 * sb + 8 * tq);
+                    const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const __half2 s2 = u32_as_h2(sw[k]);
-                            const __half2 hp = u32_as_h2(ph[k]);
-                            const __half2 mhi = __hmul2(hp, s2);
-                            if (part == 0) {
-                                bv[g][k] = h2_as_u32(mhi);
-                            } else {
-                                __half2 r = __hfma2(hp, s2, __hneg2(mhi));
-                                r = __hfma2(u32_as_h2(pl[k]), s2, r);
-                                bv[g][k] = h2_as_u32(r);
-                            }
-                        }
+                    for (int k = 0; k < 4; ++k) {
+                        const __half2 s2 = u32_as_h2(sw[k]);
+                        const __half2 hp = u32_as_h2(ph[k]);
+                        const __half2 mneg = __hmul2(__hmul2(hp, s2), nmask);   // -RN(p*s) | 0
+                        __half2 r = __hfma2(hp, s2, mneg);
+                        r = __hfma2(u32_as_h2(plm[k]), s2, r);
+                        bv[g][k] = h2_as_u32(r);
                     }
                 }
-                __syncwarp();
-                // ---------------- PV: O_blk^T[c][col] over this sub-block's 32 tokens
-                uint32_t vw[8];
+                // zero-point sums: rows (head, part) x columns z_0..z_3, s_0..s_3
+                {
+                    const uint16_t* src = (gq < 4 ? Vz : Vs) + (gq & 3) * B + 32 * sb + 8 * tq;
+                    const uint4 z4 = *reinterpret_cast<const uint4*>(src);
+                    mma16816(Dz, pa[0], 0u, pa[1], 0u, z4.x, z4.y);
+                    mma16816(Dz, pa[2], 0u, pa[3], 0u, z4.z, z4.w);
+                }
+                uint32_t vw[8], vw8[8];
                 {
                     const uint4* rec = reinterpret_cast<const uint4*>(Vb) + 2 * (32 * sb + lane);
                     const uint4 r0 = rec[0], r1 = rec[1];
                     vw[0] = r0.x; vw[1] = r0.y; vw[2] = r0.z; vw[3] = r0.w;
                     vw[4] = r1.x; vw[5] = r1.y; vw[6] = r1.z; vw[7] = r1.w;
                 }
-                float Ob[8][4];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) vw8[k] = vw[k] >> 8;
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) Ob[mt][r] = 0.f;
                     const int g = mt >> 1, m = mt & 1;
-                    const uint32_t wd = vw[2 * g + m];
+                    const uint32_t wd = vw[2 * g + m], wd8 = vw8[2 * g + m];
 #pragma unroll
-                    for (int kt = 0; kt < 2; ++kt) {
-                        mma16816(Ob[mt], code_pair(wd, 4 * kt + 0), code_pair(wd, 4 * kt + 1),
-                                 code_pair(wd, 4 * kt + 2), code_pair(wd, 4 * kt + 3),
+                    for (int kt = 0; kt < 2; ++kt)
+                        mma16816(Ob[mt], code_pair(wd, wd8, 4 * kt + 0), code_pair(wd, wd8, 4 * kt + 1),
+                                 code_pair(wd, wd8, 4 * kt + 2), code_pair(wd, wd8, 4 * kt + 3),
                                  bv[g][2 * kt], bv[g][2 * kt + 1]);
-                    }
                 }
-                // ---------------- O += C_c / lam * (4 O_blk + zs_g)
-                {
-                    const float il = 1.f / lam;
+            }
+            __syncwarp();   // pex is rewritten by the next block
+            // zs[h][g] = z-sum - 4 s-sum, hi + lo rows; delivered to the lanes of head tq
+            float zq[4];
+            {
+                const float v0 = Dz[0] + __shfl_xor_sync(kFull, Dz[0], 4);
+                const float v1 = Dz[1] + __shfl_xor_sync(kFull, Dz[1], 4);
+                const float zA = v0 - 4.0f * __shfl_xor_sync(kFull, v0, 2);   // valid where tq < 2:
+                const float zB = v1 - 4.0f * __shfl_xor_sync(kFull, v1, 2);   // groups 2tq, 2tq+1 of head gq/2
+                zq[0] = 0.25f * __shfl_sync(kFull, zA, 8 * tq);
+                zq[1] = 0.25f * __shfl_sync(kFull, zB, 8 * tq);
+                zq[2] = 0.25f * __shfl_sync(kFull, zA, 8 * tq + 1);
+                zq[3] = 0.25f * __shfl_sync(kFull, zB, 8 * tq + 1);
+            }
+            // ---------------- O += 4 C_c / lam * (Ob + zs / 4)
+            {
+                const float il4 = 4.0f / lam;
+                const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B));
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const uint2 c2 = *reinterpret_cast<const uint2*>(Vb + off_C(B) + 2 * (32 * g + 4 * gq));
-                        const float2 c01 = __half22float2(u32_as_h2(c2.x)), c23 = __half22float2(u32_as_h2(c2.y));
-                        const float cf[4] = {c01.x, c01.y, c23.x, c23.y};   // channels 32g+4gq+{0..3}
+                for (int g = 0; g < 4; ++g) {
+                    const uint2 c2 = *reinterpret_cast<const uint2*>(VC + 32 * g + 4 * gq);
+                    const float2 c01 = __half22float2(u32_as_h2(c2.x)), c23 = __half22float2(u32_as_h2(c2.y));
+                    const float cf[4] = {c01.x, c01.y, c23.x, c23.y};   // channels 32g+4gq+{0..3}
 #pragma unroll
-                        for (int m = 0; m < 2; ++m) {
-                            const int mt = 2 * g + m;
+                    for (int m = 0; m < 2; ++m) {
+                        const int mt = 2 * g + m;
 #pragma unroll
-                            for (int rh = 0; rh < 2; ++rh) {
-                                const float cs = cf[2 * m + rh] * il;
-                                O[mt][2 * rh] = fmaf(cs, fmaf(Ob[mt][2 * rh], 4.0f, zs[g]), O[mt][2 * rh]);
-                                O[mt][2 * rh + 1] = fmaf(cs * 4.0f, Ob[mt][2 * rh + 1], O[mt][2 * rh + 1]);
-                            }
+                        for (int rh = 0; rh < 2; ++rh) {
+                            const float t = (Ob[mt][2 * rh] + Ob[mt][2 * rh + 1]) + zq[g];
+                            O[mt][rh] = fmaf(cf[2 * m + rh] * il4, t, O[mt][rh]);
                         }
                     }
                 }
@@ -465,9 +487,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         }
         // ---- retire the stage and refill it
         __syncwarp();
-        const int64_t xn = x + S;
         okmask &= ~(1u << stage);
-        if (xn < s_end && issue(xn, stage)) okmask |= 1u << stage;
+        if (x + S < s_end && issue(stage)) okmask |= 1u << stage;
         if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -488,11 +509,11 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 
 // ---------------------------------------------------------------- host side
 template <int B>
-constexpr int stages_for() { return B == 32 ? 4 : 3; }
+constexpr int stages_for() { return B == 32 ? 4 : 2; }
 
 template <int B>
 size_t attn_smem_bytes() {
-    return (size_t)stages_for<B>() * 2 * head_block_bytes(B) + 64 + 4 * kD * sizeof(float) + 256 * sizeof(uint16_t);
+    return (size_t)stages_for<B>() * 2 * head_block_bytes(B) + 64 + 4 * kD * sizeof(float) + 2 * 4 * B * sizeof(uint16_t);
 }
 
 // Resident warps of the split-K kernel on `device` (cached per device).

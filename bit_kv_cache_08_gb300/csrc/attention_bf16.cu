@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (h < a.G) load_q4(a, (int64_t)cc.b * a.n_q + (int64_t)cc.h * a.G + h, lane, v);
+            if (h < a.G) load_q4(a.q, a.q_dtype, (int64_t)cc.b * a.n_q + (int64_t)cc.h * a.G + h, lane, v);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 qv[h][k] = v[k] * qs;

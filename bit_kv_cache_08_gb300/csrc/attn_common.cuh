@@ -40,10 +40,11 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 
 // Two 2-bit codes at bits 2j and 16+2j of w -> an fp16x2 operand whose
 // halves are 1 + code/4 (code placed in the top two fraction bits of 1.0):
-// exact, one shift and one LOP3. The constant 1 is removed in the fp32
-// epilogue through the zero-point term (z - 4s).
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, int j) {
-    const uint32_t x = (j <= 4) ? (w << (8 - 2 * j)) : (w >> (2 * j - 8));
+// exact, one LOP3 after a left shift (a multiply by a power of two). w8 is
+// w >> 8, taken once per word, so pairs j >= 4 need no right shift. The
+// constant 1 is removed in the fp32 epilogues.
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int j) {
+    const uint32_t x = (j < 4) ? w * (1u << (8 - 2 * j)) : (j == 4 ? w : w8 * (1u << (16 - 2 * j)));
     return (x & 0x03000300u) | 0x3C003C00u;
 }
 
@@ -62,12 +63,12 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return h2_as_u32(__floats2half2_rn(lo, hi));
 }
 
-__device__ __forceinline__ void load_q4(const AttnArgs& a, int64_t row, int lane, float (&v)[4]) {
-    if (a.q_dtype == KVARN_FP32) {
-        float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + row * kD)[lane];
+__device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t row, int lane, float (&v)[4]) {
+    if (q_dtype == KVARN_FP32) {
+        float4 f = reinterpret_cast<const float4*>(static_cast<const float*>(q) + row * kD)[lane];
         v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
     } else {
-        uint2 u = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.q) + row * kD)[lane];
+        uint2 u = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(q) + row * kD)[lane];
         v[0] = __uint_as_float(u.x << 16);
         v[1] = __uint_as_float(u.x & 0xffff0000u);
         v[2] = __uint_as_float(u.y << 16);
@@ -122,13 +123,13 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
             // rotate back: x = sigma . H(acc) / sqrt(128)
             fwht128(acc, lane);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] *= kInvSqrtD * sign_of(a.sb, 4 * lane + k);
+            for (int k = 0; k < 4; ++k) acc[k] *= kInvSqrtD * sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + k);
         }
     }
     const int ntail = ROT ? L - nb * B : 0;
     if (ntail > 0) {
         float qv[4];
-        load_q4(a, gw, lane, qv);
+        load_q4(a.q, a.q_dtype, gw, lane, qv);
         const float qs = a.sm_scale * kLog2e;
         const uint16_t* kst = a.staging + (((int64_t)b * a.n_kv + h) * 2 + 0) * B * kD;
         const uint16_t* vst = kst + B * kD;

@@ -35,6 +35,12 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t flag) {
 __device__ __forceinline__ float sign_of(const uint32_t (&sb)[4], int c) {
     return ((sb[c >> 5] >> (c & 31)) & 1u) ? -1.0f : 1.0f;
 }
+// Same, from four scalar words (keeps kernel parameters out of local memory).
+__device__ __forceinline__ float sign_of4(uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3, int c) {
+    const int w = c >> 5;
+    const uint32_t word = w == 0 ? s0 : (w == 1 ? s1 : (w == 2 ? s2 : s3));
+    return ((word >> (c & 31)) & 1u) ? -1.0f : 1.0f;
+}
 
 // ---------------------------------------------------------------- warp reductions
 __device__ __forceinline__ float warp_sum(float v) {

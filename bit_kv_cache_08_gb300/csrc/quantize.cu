@@ -16,8 +16,9 @@
 //   VarN       token pass: two-pass mean/variance by warp reduction;
 //              channel pass: per-warp partial sums through shared memory
 //   factors    fp16 round-to-nearest of the clamped cumulative factors
-//   quantise   y = x_rot / (R16*C16) (IEEE division; the product is exact in
-//              fp32), per (token, 32-channel group): z = fp16 round-down of the
+//   quantise   y = x_rot * (1/R16) * (1/C16) (correctly rounded reciprocals;
+//              a few fp32 ulps from the quotient), per (token, 32-channel group):
+//              z = fp16 round-down of the
 //              minimum, s = least fp16 with z + 3s >= maximum (directed-rounding
 //              candidate plus one exact check), code = nearest level, ties even
 //   pack       codes OR-ed into the shared-memory image of the head-block in
@@ -48,7 +49,8 @@ __device__ __forceinline__ bool usable_variance(float v, float mu) {
 // Least fp16 s >= 0 with z + 3 s >= M, for fp16 z <= M (all exact comparisons).
 __device__ __forceinline__ float step_for(float zf, float M) {
     if (zf >= M) return 0.0f;
-    float t = __fdiv_ru(__fsub_ru(M, zf), 3.0f);          // >= exact (M - z)/3
+    // >= exact (M - z)/3: every step rounds up, 0x1.555556p-2f = RU(1/3)
+    float t = __fmul_ru(__fsub_ru(M, zf), 0x1.555556p-2f);
     __half s = __float2half_ru(t);                         // >= exact minimum
     float sf = __half2float(s);
     if (!(sf <= kF16Max)) { s = __float2half_rn(kF16Max); sf = kF16Max; }
@@ -152,17 +154,21 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
     }
 
     // ---- fp16 factors (clamped to the normal range) and normalised values
-    float C16[4];
+    float C16[4], rC[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) C16[k] = __half2float(__float2half_rn(fminf(fmaxf(Cf[k], kF16MinNormal), kF16Max)));
+    for (int k = 0; k < 4; ++k) {
+        C16[k] = __half2float(__float2half_rn(fminf(fmaxf(Cf[k], kF16MinNormal), kF16Max)));
+        rC[k] = __frcp_rn(C16[k]);
+    }
     const int g = lane >> 3;   // this lane's 32-channel group
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
         const int t = warp * RPW + i;
         const float R16 = __half2float(__float2half_rn(fminf(fmaxf(Rf[i], kF16MinNormal), kF16Max)));
+        const float rR = __frcp_rn(R16);
         float yq[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) yq[k] = __fdiv_rn(x[i][k], R16 * C16[k]);
+        for (int k = 0; k < 4; ++k) yq[k] = (x[i][k] * rR) * rC[k];
         float mn = fminf(fminf(yq[0], yq[1]), fminf(yq[2], yq[3]));
         float mx = fmaxf(fmaxf(yq[0], yq[1]), fmaxf(yq[2], yq[3]));
 #pragma unroll

@@ -28,7 +28,7 @@ __device__ __forceinline__ int split_nblocks(const SplitArgs& s, int b) {
 
 // Warp-cooperative: returns W (total blocks over all units); if x < W, sets
 // (b, h, j) of global position x.
-__device__ inline int64_t split_locate(const SplitArgs& s, int64_t x, int lane, int& b_out,
+__device__ __forceinline__ int64_t split_locate(const SplitArgs& s, int64_t x, int lane, int& b_out,
                                        int& h_out, int& j_out) {
     int64_t prefix = 0;
     int found_b = -1;
@@ -78,7 +78,7 @@ __device__ __forceinline__ void split_advance(const SplitArgs& s, Cursor& c) {
 }
 
 // Blocks of all sequences before b, and of all sequences (warp-cooperative).
-__device__ inline void split_prefix(const SplitArgs& s, int b, int lane, int64_t& before,
+__device__ __forceinline__ void split_prefix(const SplitArgs& s, int b, int lane, int64_t& before,
                                     int64_t& total) {
     before = 0;
     total = 0;

@@ -7,11 +7,13 @@ already-validated rounded values so one boundary case cannot cascade):
            the oracle value lies within 1e-5 relative of the rounding midpoint
            between the two (counted);
   z16/s16  recomputed by the oracle from its fp64 rotated values and the GPU's
-           R16, C16: equal, or the pre-rounding value (group minimum for z,
-           (M - z)/3 for s) lies within 1e-5 relative of an fp16 value (counted);
+           R16, C16: equal, or the pre-rounding value lies within 1e-5 of an
+           fp16 value, relative to the group's own scale: max(|m|, M - m) for
+           the zero (group minimum m, maximum M), (M - z)/3 for the step (counted);
   codes    recomputed from that y with the GPU's z16, s16: equal, or y lies
-           within 1e-6 * max(1, |b|) of a decision boundary b (counted, and the
-           count must stay <= 1e-6 of all codes).
+           within 1e-6 * max(1, |b|) of a decision boundary b (counted; the
+           count over a test's whole population must stay <= 1e-6 of its codes,
+           checked by assert_code_flip_rate).
 """
 from __future__ import annotations
 
@@ -68,7 +70,10 @@ def staged_quantize_parity(X: np.ndarray, gpu_bytes: np.ndarray, B: int, iters: 
         zb = np.nonzero(f["z16"] != z_o)
         if zb[0].size:
             mc = np.clip(m[zb], -65504, 65504)
-            assert np.all(f16_near_grid(mc, 1e-5)), f"block {i}: z16 mismatch off the fp16 grid"
+            near = np.abs(mc - mc.astype(np.float16).astype(np.float64))
+            scale = np.maximum(np.abs(mc), M[zb] - m[zb])
+            assert np.all(near <= 1e-5 * scale), (
+                f"block {i}: z16 mismatch gpu {f['z16'][zb]} oracle {z_o[zb]} min {m[zb]} max {M[zb]}")
             st["zero_excused"] += zb[0].size
         s_o = np.array([[oracle.step_for(f["z16"][t, g], M[t, g]) for g in range(4)] for t in range(B)])
         sb_ = np.nonzero(f["s16"] != s_o)
@@ -88,8 +93,12 @@ def staged_quantize_parity(X: np.ndarray, gpu_bytes: np.ndarray, B: int, iters: 
             st["code_excused"] += cb[0].size
         st["codes_in_window"] += int(np.sum(dist <= 1e-6 * np.maximum(1.0, np.abs(y))))
         st["codes"] += B * D
-    assert st["code_excused"] <= 1e-6 * st["codes"] or st["code_excused"] == 0, dict(st)
     return st
+
+
+def assert_code_flip_rate(st: Counter, rate: float = 1e-6):
+    """Excused code flips over a test's whole population stay <= rate."""
+    assert st["code_excused"] <= rate * st["codes"] or st["code_excused"] == 0, dict(st)
 
 
 def attn_close(got: np.ndarray, ref: np.ndarray, tol: float = 2e-3):

@@ -5,7 +5,9 @@ import pytest
 import torch
 
 import synth
-from kvtest_util import PagedCache, staged_quantize_parity
+from collections import Counter
+
+from kvtest_util import PagedCache, assert_code_flip_rate, staged_quantize_parity
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -32,6 +34,7 @@ def test_append_token_by_token(kvlib, B, iters):
     torch.cuda.synchronize()
     assert kv.read_error(ws) == 0
     hb = kv.head_block_bytes(cfg)
+    total = Counter()
     for b in range(batch):
         L = start[b] + steps - max(start)
         # staging holds the rows of the open block (raw)
@@ -50,8 +53,9 @@ def test_append_token_by_token(kvlib, B, iters):
                     got = cache.head_block(b, h, j, kind)
                     if (j * B) >= start[b]:
                         assert np.array_equal(got, dst.cpu().numpy())
-                        staged_quantize_parity(rows.double().cpu().numpy()[None], got[None], B, iters,
-                                               kind, sb)
+                        total.update(staged_quantize_parity(rows.double().cpu().numpy()[None], got[None], B,
+                                                            iters, kind, sb))
+    assert_code_flip_rate(total)
 
 
 def test_append_position_out_of_range(kvlib):

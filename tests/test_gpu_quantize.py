@@ -1,11 +1,14 @@
 """GPU quantise / dequantise parity with the fp64 oracle (staged hand-off)."""
+import zlib
+from collections import Counter
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from kvtest_util import staged_quantize_parity
+from kvtest_util import assert_code_flip_rate, staged_quantize_parity
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -31,19 +34,23 @@ def _quantize(kv, cfg, kind, x):
     ("llama-bf16", 32, 3, "bf16", 96, 1.5, 4, 20.0),
     ("qwen-bf16", 64, 2, "bf16", 48, 1.5, 4, 20.0),
     ("iters1", 32, 1, "bf16", 16, 1.5, 4, 20.0),
+    ("llama-bf16-2M-codes", 32, 3, "bf16", 256, 1.5, 4, 20.0),
     ("iters4-b64", 64, 4, "bf16", 16, 1.0, 2, 10.0),
 ])
 def test_quantize_matches_oracle_staged(kvlib, name, B, iters, dtype, n, sigma_m, n_out, factor):
     kv = kvlib
     sb = synth.sign_bits(B + iters)
     cfg = kv.make_config(4, 1, B, iters, sb)
-    x = _values(hash(name) & 0xFFFF, n, B, sigma_m, n_out, factor, dtype)
+    x = _values(zlib.crc32(name.encode()) & 0xFFFF, n, B, sigma_m, n_out, factor, dtype)
     X = x.double().numpy()
+    total = Counter()
     for kind in (0, 1):
         got, err = _quantize(kv, cfg, kind, x)
         assert err == 0
         st = staged_quantize_parity(X, got, B, iters, kind, sb)
         print(name, kind, dict(st))
+        total.update(st)
+    assert_code_flip_rate(total)
 
 
 def test_dequantize_matches_oracle_decode(kvlib):

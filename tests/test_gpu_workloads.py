@@ -7,7 +7,9 @@ import pytest
 import torch
 
 import synth
-from kvtest_util import PagedCache, attn_close, oracle_attention, staged_quantize_parity
+from collections import Counter
+
+from kvtest_util import PagedCache, assert_code_flip_rate, attn_close, oracle_attention, staged_quantize_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -36,10 +38,13 @@ def _layer(kv, w, seed_extra=0, perm=True):
 def _check_appended(w, sb, K, V, cache, samples):
     B = w.block
     j = w.ctx // B - 1
+    total = Counter()
     for (b, h) in samples:
         for kind, T in ((0, K), (1, V)):
             rows = T[b, h, j * B:(j + 1) * B].double().cpu().numpy()
-            staged_quantize_parity(rows[None], cache.head_block(b, h, j, kind)[None], B, w.iters, kind, sb)
+            total.update(staged_quantize_parity(rows[None], cache.head_block(b, h, j, kind)[None], B, w.iters,
+                                                kind, sb))
+    assert_code_flip_rate(total)
 
 
 def test_llama8b_layer(kvlib):
