@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -40,7 +41,39 @@ def parse():
     p.add_argument("--layers", type=int, default=None, help="(testing only) fewer layers")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-bf16", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
+                        "lengths), 2-bit vs bf16-cache decode attention, one JSON line per point")
     return p.parse_args()
+
+
+# ---------------------------------------------------------------------------- ranks
+
+def barrier():
+    """torch.distributed barrier when a process group is up (N > 1), else nothing."""
+    import torch.distributed as tdist
+    if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
+        tdist.barrier()
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself at N = 1.
+    `device` is where the one-element tensor lives: the GPU under NCCL, the
+    host under gloo."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    barrier()
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank moves bytes_per_rank per step; the job's step
+    time is the slowest rank's."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 def workload():
@@ -49,7 +82,7 @@ def workload():
 
 
 def algorithmic_bytes(w, layers):
-    """Bytes the step must move at minimum (what the design doc calls algorithmic)."""
+    """Bytes the step must move at minimum: the algorithmic bytes of the roofline."""
     B, n_kv, n_q, batch, L = w.block, w.n_kv, w.n_q, w.batch, w.ctx
     per_token_head = 2 * (32 + 16 + 2) + 2 * 256 / B          # K+V: codes, s/z, R + C share
     attn_cache = batch * L * n_kv * per_token_head
@@ -93,7 +126,9 @@ class ClockSampler:
     def __init__(self, device_index):
         self.proc = None
         self.idx = device_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples go to $KVARN_CLOCKS_DIR (kept for inspection) or the temp directory
+        d = os.environ.get("KVARN_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -188,7 +223,8 @@ def run_gpu(args, rank, world):
     import torch
     import bit_kv_cache_08_gb300 as kv
     kv.build()
-    device = f"cuda:{rank % max(1, torch.cuda.device_count())}"
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    device = f"cuda:{local % max(1, torch.cuda.device_count())}"
     torch.cuda.set_device(device)
     w = workload()
     layers = args.layers or w.layers
@@ -218,10 +254,7 @@ def run_gpu(args, rank, world):
     assert kv.read_error(ws) == 0, "device error during warm-up"
 
     attn_ms, app_ms = [], []
-    dist = world > 1
-    if dist:
-        import torch.distributed as tdist
-        tdist.barrier()
+    barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
@@ -239,18 +272,13 @@ def run_gpu(args, rank, world):
             e = evs[s][l]
             app_ms.append(e[0].elapsed_time(e[1]))
             attn_ms.append(e[1].elapsed_time(e[2]))
-    if dist:
-        import torch.distributed as tdist
-        t = torch.tensor([total_ms], device=device)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        tdist.barrier()
+    total_ms = max_over_ranks(total_ms, device)
     assert kv.read_error(ws) == 0, "device error during the timed steps"
     clocks = clk.summary()
 
     attn_bytes, app_bytes, attn_launch_bytes, app_launch_bytes = algorithmic_bytes(w, layers)
     ms_per_step = total_ms / args.steps
-    value = world * (attn_bytes + app_bytes) / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(attn_bytes + app_bytes, world, ms_per_step)
     attn_launch_ms = sum(attn_ms) / len(attn_ms)
     achieved = attn_launch_bytes / (attn_launch_ms * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
@@ -273,7 +301,8 @@ def run_gpu(args, rank, world):
                    "n_q_heads": w.n_q, "n_kv_heads": w.n_kv, "head_dim": D, "block": B, "varn_iters": w.iters,
                    "step": "per layer: kvarn_append (completes every open block) + kvarn_decode_attn",
                    "l2": "no flush: per-step cache 16.3 GB >> 129 MB L2",
-                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+                   "parallelism": f"replicas x{world} (each rank its own {batch} sequences; no collective "
+                                  "on the data path)"},
         "decode_attn": {"GB_per_s": round(achieved, 1), "us_per_layer": round(attn_launch_ms * 1e3, 2),
                         "algorithmic_bytes_per_layer": int(attn_launch_bytes),
                         "frac_of_hbm_peak": round(achieved / peak, 4),
@@ -292,7 +321,7 @@ def run_gpu(args, rank, world):
     return res, state, (kv, ws, pos, lens, out)
 
 
-def e2e_gpu(args, ctx_objs, state, w, rank):
+def e2e_gpu(args, ctx_objs, state, w, world):
     """The same step through the C ABI with host buffers: every step copies the
     step's queries and new K/V rows from pinned host memory and reads the
     outputs back."""
@@ -317,15 +346,17 @@ def e2e_gpu(args, ctx_objs, state, w, rank):
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()
+    barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     torch.cuda.synchronize()
     ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    ms = max_over_ranks(ms, out.device)
     attn_bytes, app_bytes, _, _ = algorithmic_bytes(w, layers)
     h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
     d2h = hout.numel() * 4
-    return {"value": round((attn_bytes + app_bytes) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    return {"value": round(whole_job_gbs(attn_bytes + app_bytes, world, ms), 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
@@ -440,8 +471,105 @@ def run_reference(args):
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------------------- sweep
+
+SWEEP_BATCH = (1, 8, 32, 128, 256)
+SWEEP_CTX = (1024, 8192, 32768, 131072)
+
+
+def _time_events(fn, reps, flush):
+    """Median of `reps` launches of fn, each timed alone with CUDA events on the
+    current stream. Before every launch a 1 GiB write flushes L2; it also keeps
+    the GPU busy while the host queues the start event and the launch, so the
+    events bracket device time only (not the host's launch latency)."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_sweep(args):
+    import numpy as np
+    import torch
+    import bit_kv_cache_08_gb300 as kv
+    import synth
+    kv.build()
+    dev = "cuda"
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    for batch in SWEEP_BATCH:
+        for ctx in SWEEP_CTX:
+            w = synth.sweep_point(batch, ctx)
+            B, n_kv, n_q = w.block, w.n_kv, w.n_q
+            lens = np.array(w.seq_lens, dtype=np.int64)
+            nbs = (lens + B - 1) // B
+            max_blocks = int(nbs.max())
+            cfg = kv.make_config(n_q, n_kv, B, w.iters, synth.sign_bits(w.seed))
+            g = synth.make_gen(w.seed + batch + ctx, dev)
+            n_phys = int(nbs.sum())
+            perm = np.random.default_rng([batch, ctx]).permutation(n_phys).astype(np.int32)
+            bt_np = np.full((batch, max_blocks), -1, dtype=np.int32)
+            o = 0
+            for b in range(batch):
+                bt_np[b, :nbs[b]] = perm[o:o + nbs[b]]
+                o += nbs[b]
+            bt = torch.from_numpy(bt_np).to(dev)
+            sl = torch.from_numpy(lens.astype(np.int32)).to(dev)
+            q = synth.queries(g, batch, n_q, dev).to(torch.bfloat16)
+            out = torch.empty(batch, n_q, D, device=dev)
+            ws = kv.alloc_workspace(cfg, batch, max_blocks, dev)
+            big = ctx * batch >= 1 << 22
+            reps = 5 if big else 30
+            # 2-bit cache: valid packed head-blocks (512 quantised K and V tiles repeated)
+            hb = kv.head_block_bytes(cfg)
+            tile = torch.empty(2, 256, hb, dtype=torch.uint8, device=dev)
+            for kind in (0, 1):
+                x = synth.kv_values(g, 1, 256, B, w.sigma_m, w.n_out, w.out_factor, dev)[0].to(torch.bfloat16)
+                kv.quantize_block(cfg, kind, x.contiguous(), tile[kind], kv.alloc_workspace(cfg, 0, 0, dev))
+            pool = kv.alloc_pool(cfg, n_phys, dev).view(n_phys, n_kv, 2, hb)
+            for c0 in range(0, n_phys, 1 << 15):
+                c1 = min(n_phys, c0 + (1 << 15))
+                idx = (torch.arange(c0 * n_kv, c1 * n_kv, device=dev) % 256).view(c1 - c0, n_kv)
+                pool[c0:c1, :, 0] = tile[0][idx]
+                pool[c0:c1, :, 1] = tile[1][idx]
+            pool = pool.view(n_phys, -1)
+            staging = kv.alloc_staging(cfg, batch, dev)
+            staging.normal_(generator=g)
+            full = (lens // B) * B
+            b2 = float((full * n_kv * (2 * (32 + 16 + 2) + 2 * 256 / B)).sum()
+                       + ((lens - full) * n_kv * 512).sum() + batch * n_q * 768 + nbs.sum() * 4)
+            ms2 = _time_events(lambda: kv.decode_attn(cfg, q, pool, staging, bt, sl, out, ws), reps, flush)
+            assert kv.read_error(ws) == 0
+            del pool, staging
+            torch.cuda.empty_cache()
+            kvp = torch.empty(n_phys, n_kv, 2, B, D, dtype=torch.bfloat16, device=dev)
+            kvp.normal_(generator=g)
+            b16 = float((lens * n_kv * 512).sum() + batch * n_q * 768 + nbs.sum() * 4)
+            ms16 = _time_events(lambda: kv.decode_attn_bf16(cfg, q, kvp, bt, sl, out, ws), reps, flush)
+            assert kv.read_error(ws) == 0
+            del kvp
+            torch.cuda.empty_cache()
+            print(json.dumps({"sweep_point": w.name, "batch": batch, "ctx": ctx,
+                              "mean_len": float(lens.mean()),
+                              "timing": "CUDA events, median of launches each queued behind a 1 GiB L2-flushing write",
+                              "2bit": {"us": round(ms2 * 1e3, 2), "GB_per_s": round(b2 / ms2 / 1e6, 1),
+                                       "tokens_per_s": round(batch / ms2 * 1e3, 1), "bytes": int(b2)},
+                              "bf16": {"us": round(ms16 * 1e3, 2), "GB_per_s": round(b16 / ms16 / 1e6, 1),
+                                       "tokens_per_s": round(batch / ms16 * 1e3, 1), "bytes": int(b16)},
+                              "speedup_2bit_vs_bf16": round(ms16 / ms2, 2)}), flush=True)
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
@@ -459,8 +587,7 @@ def main():
         tdist.barrier()
     res, state, objs = run_gpu(args, rank, world)
     w = workload()
-    res["e2e"] = e2e_gpu(args, objs, state, w, rank)
-    res["e2e"]["value"] = round(res["e2e"]["value"] * world, 2)
+    res["e2e"] = e2e_gpu(args, objs, state, w, world)
     import torch
     if rank == 0 and not args.no_bf16:
         del state

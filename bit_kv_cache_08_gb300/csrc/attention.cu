@@ -269,14 +269,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) kw8[k] = kw[k] >> 8;
-                float acc[4][2][4];
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        acc[g][mt][0] = Qneg[g]; acc[g][mt][1] = 0.f;
-                        acc[g][mt][2] = Qneg[g]; acc[g][mt][3] = 0.f;
-                    }
+                float acc[4][2][4];   // chains start from (-Q'_g, 0) per row
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
@@ -286,8 +279,13 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
                         for (int mt = 0; mt < 2; ++mt) {
                             const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
-                            mma16816(acc[g][mt], code_pair(kw[i0], kw8[i0], j), code_pair(kw[i1], kw8[i1], j),
-                                     code_pair(kw[i0], kw8[i0], j + 1), code_pair(kw[i1], kw8[i1], j + 1), b0, b1);
+                            const uint32_t a0 = code_pair(kw[i0], kw8[i0], j), a1 = code_pair(kw[i1], kw8[i1], j);
+                            const uint32_t a2 = code_pair(kw[i0], kw8[i0], j + 1);
+                            const uint32_t a3 = code_pair(kw[i1], kw8[i1], j + 1);
+                            if (kk == 0)
+                                mma16816_from(acc[g][mt], a0, a1, a2, a3, b0, b1, Qneg[g], 0.f);
+                            else
+                                mma16816(acc[g][mt], a0, a1, a2, a3, b0, b1);
                         }
                     }
                 // scores of tokens 32sb + 4gq + i, head tq

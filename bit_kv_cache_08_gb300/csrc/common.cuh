@@ -66,11 +66,12 @@ __device__ __forceinline__ void fwht128(float (&v)[4], int lane) {
     v[1] = a1 + a3; v[3] = a1 - a3;
 #pragma unroll
     for (int m = 1; m <= 16; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+        // lower lane: v + o; upper lane: o - v (one fma with a +-1 factor, exact)
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             float o = __shfl_xor_sync(kFull, v[k], m);
-            v[k] = upper ? (o - v[k]) : (v[k] + o);
+            v[k] = fmaf(sgn, v[k], o);
         }
     }
 }

@@ -9,13 +9,18 @@
 // to variance 1, repeated; grouped scales kept for dequantisation; computed
 // at decode time inside the KV write kernel).
 //
-// One CTA of 256 threads (8 warps) owns one head-block of B tokens x 128
-// channels. Warp w holds tokens w*B/8 .. (w+1)*B/8-1, lane l channels
-// 4l..4l+3, all in registers:
+// One CTA of 8B threads (B/4 warps) owns one head-block of B tokens x 128
+// channels. Warp w holds tokens 4w .. 4w+3, lane l channels 4l..4l+3, all in
+// registers:
 //   rotation   sign flip + FWHT-128 (2 in-register + 5 shuffle stages), *1/sqrt(128)
-//   VarN       token pass: two-pass mean/variance by warp reduction;
-//              channel pass: per-warp partial sums through shared memory
-//   factors    fp16 round-to-nearest of the clamped cumulative factors
+//   VarN       each pass sets a factor from the rotated tile directly: scaling a
+//              row by a constant scales its spread by the same constant, so after
+//              a token pass R_t = std_c(x_rot[t][c] / C_c) and after a channel
+//              pass C_c = std_t(x_rot[t][c] / R_t) -- the values the pages'
+//              divide-and-accumulate iteration reaches, without keeping the
+//              normalised tile. Token pass: two-pass mean/variance by warp
+//              reduction; channel pass: per-warp partial sums through shared memory
+//   factors    fp16 round-to-nearest of the clamped factors
 //   quantise   y = x_rot * (1/R16) * (1/C16) (correctly rounded reciprocals;
 //              a few fp32 ulps from the quotient), per (token, 32-channel group):
 //              z = fp16 round-down of the
@@ -27,11 +32,15 @@
 
 namespace kvarn {
 
+constexpr int kRowsPerWarp = 4;
+template <int B> constexpr int quant_warps() { return B / kRowsPerWarp; }
+template <int B> constexpr int quant_threads() { return 32 * quant_warps<B>(); }
+
 template <int B>
 struct QuantSmem {
     alignas(16) uint8_t image[head_block_bytes(B)];   // exact global layout
-    alignas(16) float part_a[8][kD];
-    alignas(16) float part_b[8][kD];
+    alignas(16) float part_a[quant_warps<B>()][kD];
+    alignas(16) float part_b[quant_warps<B>()][kD];
 };
 
 struct QuantParams {
@@ -65,9 +74,9 @@ __device__ __forceinline__ float step_for(float zf, float M) {
 
 // Quantise the tile held in x (rows of this warp) into q.image.
 template <int B>
-__device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantSmem<B>& q,
+__device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p, QuantSmem<B>& q,
                               int warp, int lane) {
-    constexpr int RPW = B / 8;
+    constexpr int RPW = kRowsPerWarp, NW = quant_warps<B>();
     uint32_t* words = reinterpret_cast<uint32_t*>(q.image);
     uint16_t* s_sec = reinterpret_cast<uint16_t*>(q.image + off_s(B));
     uint16_t* z_sec = reinterpret_cast<uint16_t*>(q.image + off_z(B));
@@ -75,51 +84,44 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
     uint16_t* C_sec = reinterpret_cast<uint16_t*>(q.image + off_C(B));
 
     // ---- rotation: x_rot = H (sigma . x) / sqrt(128)
-    float sg[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) sg[k] = sign_of(p.sb, 4 * lane + k);
+    uint32_t sw = p.sb[lane >> 3] >> (4 * (lane & 7));    // this lane's 4 sign bits
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) x[i][k] *= sg[k];
+        for (int k = 0; k < 4; ++k) x[i][k] = ((sw >> k) & 1u) ? -x[i][k] : x[i][k];
         fwht128(x[i], lane);
 #pragma unroll
         for (int k = 0; k < 4; ++k) x[i][k] *= kInvSqrtD;
     }
 
     // ---- VarN: token pass then channel pass, p.iters times
-    float y[RPW][4];
-    float Rf[RPW], Cf[4] = {1.f, 1.f, 1.f, 1.f};
+    float Rf[RPW], rR[RPW], Cf[4] = {1.f, 1.f, 1.f, 1.f}, rCf[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
-    for (int i = 0; i < RPW; ++i) {
-        Rf[i] = 1.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) y[i][k] = x[i][k];
-    }
+    for (int i = 0; i < RPW; ++i) { Rf[i] = 1.f; rR[i] = 1.f; }
     for (int it = 0; it < p.iters; ++it) {
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
-            float mu = warp_sum(y[i][0] + y[i][1] + y[i][2] + y[i][3]) * (1.0f / kD);
-            float d0 = y[i][0] - mu, d1 = y[i][1] - mu, d2 = y[i][2] - mu, d3 = y[i][3] - mu;
+            float u[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u[k] = x[i][k] * rCf[k];
+            float mu = warp_sum(u[0] + u[1] + u[2] + u[3]) * (1.0f / kD);
+            float d0 = u[0] - mu, d1 = u[1] - mu, d2 = u[2] - mu, d3 = u[3] - mu;
             float var = warp_sum(d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3) * (1.0f / kD);
             if (usable_variance(var, mu)) {
-                float r = sqrtf(var);
-                float inv = __frcp_rn(r);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) y[i][k] *= inv;
-                Rf[i] *= r;
+                Rf[i] = sqrtf(var);
+                rR[i] = __frcp_rn(Rf[i]);
             }
         }
         float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < RPW; ++i)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cs[k] += y[i][k];
+            for (int k = 0; k < 4; ++k) cs[k] += x[i][k] * rR[i];
         *reinterpret_cast<float4*>(&q.part_a[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
         __syncthreads();
         float mu[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < NW; ++w) {
             float4 v = *reinterpret_cast<const float4*>(&q.part_a[w][4 * lane]);
             mu[0] += v.x; mu[1] += v.y; mu[2] += v.z; mu[3] += v.w;
         }
@@ -129,14 +131,14 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
         for (int i = 0; i < RPW; ++i)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                float d = y[i][k] - mu[k];
+                float d = x[i][k] * rR[i] - mu[k];
                 cs[k] += d * d;
             }
         *reinterpret_cast<float4*>(&q.part_b[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
         __syncthreads();
         float var[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < NW; ++w) {
             float4 v = *reinterpret_cast<const float4*>(&q.part_b[w][4 * lane]);
             var[0] += v.x; var[1] += v.y; var[2] += v.z; var[3] += v.w;
         }
@@ -144,11 +146,8 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
         for (int k = 0; k < 4; ++k) {
             float vk = var[k] * (1.0f / B);
             if (usable_variance(vk, mu[k])) {
-                float r = sqrtf(vk);
-                float inv = __frcp_rn(r);
-#pragma unroll
-                for (int i = 0; i < RPW; ++i) y[i][k] *= inv;
-                Cf[k] *= r;
+                Cf[k] = sqrtf(vk);
+                rCf[k] = __frcp_rn(Cf[k]);
             }
         }
     }
@@ -165,10 +164,10 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
     for (int i = 0; i < RPW; ++i) {
         const int t = warp * RPW + i;
         const float R16 = __half2float(__float2half_rn(fminf(fmaxf(Rf[i], kF16MinNormal), kF16Max)));
-        const float rR = __frcp_rn(R16);
+        const float rRq = __frcp_rn(R16);
         float yq[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) yq[k] = (x[i][k] * rR) * rC[k];
+        for (int k = 0; k < 4; ++k) yq[k] = (x[i][k] * rRq) * rC[k];
         float mn = fminf(fminf(yq[0], yq[1]), fminf(yq[2], yq[3]));
         float mx = fmaxf(fmaxf(yq[0], yq[1]), fmaxf(yq[2], yq[3]));
 #pragma unroll
@@ -223,14 +222,14 @@ __device__ void quantize_tile(float (&x)[B / 8][4], const QuantParams& p, QuantS
 template <int B>
 __device__ __forceinline__ void zero_code_words(QuantSmem<B>& q, int tid) {
     uint32_t* words = reinterpret_cast<uint32_t*>(q.image);
-    for (int i = tid; i < B * 8; i += 256) words[i] = 0u;
+    for (int i = tid; i < B * 8; i += quant_threads<B>()) words[i] = 0u;
 }
 
 template <int B>
 __device__ __forceinline__ void store_image(const QuantSmem<B>& q, uint8_t* dst, int tid) {
     const uint4* src = reinterpret_cast<const uint4*>(q.image);
     uint4* d = reinterpret_cast<uint4*>(dst);
-    for (int i = tid; i < head_block_bytes(B) / 16; i += 256) d[i] = src[i];
+    for (int i = tid; i < head_block_bytes(B) / 16; i += quant_threads<B>()) d[i] = src[i];
 }
 
 __device__ __forceinline__ void load4(const void* src, int dtype, int64_t elem_off, float (&v)[4]) {
@@ -248,7 +247,7 @@ __device__ __forceinline__ void load4(const void* src, int dtype, int64_t elem_o
 
 // ---------------------------------------------------------------- bulk quantise
 template <int B>
-__global__ void __launch_bounds__(256) quantize_blocks_kernel(
+__global__ void __launch_bounds__(quant_threads<B>()) quantize_blocks_kernel(
     const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
     uint8_t* __restrict__ dst_base, const int64_t* __restrict__ dst_offsets, QuantParams p,
     uint32_t* err) {
@@ -256,11 +255,11 @@ __global__ void __launch_bounds__(256) quantize_blocks_kernel(
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
     zero_code_words<B>(q, tid);
-    float x[B / 8][4];
+    float x[kRowsPerWarp][4];
     bool bad = false;
 #pragma unroll
-    for (int i = 0; i < B / 8; ++i) {
-        const int t = warp * (B / 8) + i;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int t = warp * kRowsPerWarp + i;
         load4(src, dtype, n * block_stride + (int64_t)t * token_stride + 4 * lane, x[i]);
 #pragma unroll
         for (int k = 0; k < 4; ++k) bad |= !isfinite(x[i][k]);
@@ -274,7 +273,7 @@ __global__ void __launch_bounds__(256) quantize_blocks_kernel(
 // ---------------------------------------------------------------- fused append
 // grid (batch, n_kv, 2): one CTA per (sequence, kv head, K|V).
 template <int B>
-__global__ void __launch_bounds__(256) append_kernel(
+__global__ void __launch_bounds__(quant_threads<B>()) append_kernel(
     uint8_t* __restrict__ pool, int64_t n_pool_blocks, int64_t block_bytes,
     uint16_t* __restrict__ staging, const int32_t* __restrict__ block_table, int max_blocks,
     const int32_t* __restrict__ pos_arr, const uint16_t* __restrict__ k_new,
@@ -301,11 +300,11 @@ __global__ void __launch_bounds__(256) append_kernel(
     }
     p.kind = kv;
     zero_code_words<B>(q, tid);
-    float x[B / 8][4];
+    float x[kRowsPerWarp][4];
     bool bad = false;
 #pragma unroll
-    for (int i = 0; i < B / 8; ++i) {
-        const int t = warp * (B / 8) + i;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int t = warp * kRowsPerWarp + i;
         const uint16_t* r = (t == B - 1) ? newrow : stage + t * kD;
         load4(r, KVARN_BF16, 4 * lane, x[i]);
 #pragma unroll
@@ -378,10 +377,10 @@ cudaError_t launch_quantize_blocks(const kvarn_config& cfg, int kind, const void
                                    cudaStream_t st) {
     QuantParams p = make_params(cfg, kind);
     if (cfg.block_size == 32)
-        quantize_blocks_kernel<32><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
+        quantize_blocks_kernel<32><<<(unsigned)n, quant_threads<32>(), 0, st>>>(src, dtype, block_stride, token_stride,
                                                                 (uint8_t*)dst_base, dst_offsets, p, err);
     else
-        quantize_blocks_kernel<64><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
+        quantize_blocks_kernel<64><<<(unsigned)n, quant_threads<64>(), 0, st>>>(src, dtype, block_stride, token_stride,
                                                                 (uint8_t*)dst_base, dst_offsets, p, err);
     return cudaGetLastError();
 }
@@ -393,12 +392,12 @@ cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_bl
     QuantParams p = make_params(cfg, 0);
     dim3 grid(batch, cfg.n_kv_heads, 2);
     if (cfg.block_size == 32)
-        append_kernel<32><<<grid, 256, 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
+        append_kernel<32><<<grid, quant_threads<32>(), 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
                                                 (uint16_t*)staging, block_table, max_blocks, pos,
                                                 (const uint16_t*)k_new, (const uint16_t*)v_new,
                                                 cfg.n_kv_heads, p, err);
     else
-        append_kernel<64><<<grid, 256, 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
+        append_kernel<64><<<grid, quant_threads<64>(), 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
                                                 (uint16_t*)staging, block_table, max_blocks, pos,
                                                 (const uint16_t*)k_new, (const uint16_t*)v_new,
                                                 cfg.n_kv_heads, p, err);
