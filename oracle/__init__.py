@@ -28,6 +28,10 @@ D = 128
 NG = 4
 GS = 32
 KIND_K, KIND_V = 0, 1
+# ablation switches (the pages' 消融 study): no rotation, VarN without the
+# token pass, VarN without the channel pass
+NO_ROTATION, NO_TOKEN_PASS, NO_CHANNEL_PASS = 1, 2, 4
+_u32 = ctypes.c_uint32
 
 
 def build(force: bool = False) -> str:
@@ -67,7 +71,7 @@ def lib():
                 "orc_hadamard": (None, [_i, _i32p]),
                 "orc_rotate": (None, [_f64p, _u32p, _f64p]),
                 "orc_unrotate": (None, [_f64p, _u32p, _f64p]),
-                "orc_varn": (None, [_i, _i, _f64p, _f64p, _f64p, _f64p, _f64p]),
+                "orc_varn": (None, [_i, _i, ctypes.c_uint32, _f64p, _f64p, _f64p, _f64p, _f64p]),
                 "orc_round_factor": (_d, [_d]),
                 "orc_group_params": (None, [_f64p, _i, _f64p, _f64p, _f64p, _f64p]),
                 "orc_code": (_i, [_d, _d, _d]),
@@ -76,15 +80,15 @@ def lib():
                 "orc_head_block_bytes": (ctypes.c_size_t, [_i]),
                 "orc_pack": (None, [_i, _i, _i32p, _f64p, _f64p, _f64p, _f64p, _u8p]),
                 "orc_unpack": (None, [_i, _i, _u8p, _i32p, _f64p, _f64p, _f64p, _f64p]),
-                "orc_quantize_block": (None, [_i, _i, _i, _u32p, _f64p, _u8p, _f64p, _f64p,
+                "orc_quantize_block": (None, [_i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p, _f64p,
                                               _f64p, _f64p, _f64p, _f64p, _f64p, _f64p,
                                               _i32p, _f64p]),
-                "orc_quantize_blocks": (None, [_i64, _i, _i, _i, _u32p, _f64p, _u8p]),
-                "orc_decode_block": (None, [_i, _i, _u32p, _u8p, _i, _f64p]),
-                "orc_decode_blocks": (None, [_i64, _i, _i, _u32p, _u8p, _i, _f64p]),
+                "orc_quantize_blocks": (None, [_i64, _i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p]),
+                "orc_decode_block": (None, [_i, ctypes.c_uint32, _i, _u32p, _u8p, _i, _f64p]),
+                "orc_decode_blocks": (None, [_i64, _i, ctypes.c_uint32, _i, _u32p, _u8p, _i, _f64p]),
                 "orc_attention": (None, [_f64p, _f64p, _f64p, _i64, _d, _f64p]),
                 "orc_attention_rotated": (None, [_f64p, _f64p, _f64p, _i64, _d, _u32p, _f64p]),
-                "orc_decode_attention": (None, [_i, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
+                "orc_decode_attention": (None, [_i, ctypes.c_uint32, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
                                                 _i32p, _i, _i32p, _i, _f64p]),
                 "orc_normalise": (None, [_i, _f64p, _f64p, _f64p, _f64p]),
                 "orc_group_params_all": (None, [_i, _f64p, _f64p, _f64p, _f64p, _f64p]),
@@ -193,7 +197,7 @@ def unrotate(y, sign_bits) -> np.ndarray:
 # VarN and quantisation
 # --------------------------------------------------------------------------
 
-def varn(Xr, iters: int):
+def varn(Xr, iters: int, flags: int = 0):
     """Returns (Y, R, C, trace[iters][3]) for one head-block of rotated values."""
     Xr = _f64(Xr)
     B = Xr.shape[0]
@@ -201,7 +205,7 @@ def varn(Xr, iters: int):
     R = np.empty(B)
     C = np.empty(D)
     tr = np.empty((max(iters, 1), 3))
-    lib().orc_varn(B, iters, _p(Xr, _f64p), _p(Y, _f64p), _p(R, _f64p), _p(C, _f64p),
+    lib().orc_varn(B, iters, flags, _p(Xr, _f64p), _p(Y, _f64p), _p(R, _f64p), _p(C, _f64p),
                    _p(tr, _f64p))
     return Y, R, C, tr[:iters]
 
@@ -259,7 +263,7 @@ def unpack(B, kind, hb_bytes):
     return dict(codes=codes, s16=s16, z16=z16, R16=R16, C16=C16)
 
 
-def quantize_block(X, iters: int, kind: int, sign_bits) -> dict:
+def quantize_block(X, iters: int, kind: int, sign_bits, flags: int = 0) -> dict:
     """All intermediate results of one head-block (X: [B][128] values)."""
     X = _f64(X)
     B = X.shape[0]
@@ -268,7 +272,7 @@ def quantize_block(X, iters: int, kind: int, sign_bits) -> dict:
              R=np.empty(B), C=np.empty(D), R16=np.empty(B), C16=np.empty(D),
              y=np.empty((B, D)), z16=np.empty((B, NG)), s16=np.empty((B, NG)),
              codes=np.empty((B, D), dtype=np.int32), trace=np.empty((max(iters, 1), 3)))
-    lib().orc_quantize_block(B, iters, kind, _p(s, _u32p), _p(X, _f64p), _p(r["bytes"], _u8p),
+    lib().orc_quantize_block(B, iters, flags, kind, _p(s, _u32p), _p(X, _f64p), _p(r["bytes"], _u8p),
                              _p(r["Xr"], _f64p), _p(r["R"], _f64p), _p(r["C"], _f64p),
                              _p(r["R16"], _f64p), _p(r["C16"], _f64p), _p(r["y"], _f64p),
                              _p(r["z16"], _f64p), _p(r["s16"], _f64p), _p(r["codes"], _i32p),
@@ -277,23 +281,23 @@ def quantize_block(X, iters: int, kind: int, sign_bits) -> dict:
     return r
 
 
-def quantize_blocks(X, iters: int, kind: int, sign_bits) -> np.ndarray:
+def quantize_blocks(X, iters: int, kind: int, sign_bits, flags: int = 0) -> np.ndarray:
     """X: [n][B][128] -> packed bytes [n][head_block_bytes(B)]."""
     X = _f64(X)
     n, B = X.shape[0], X.shape[1]
     out = np.zeros((n, head_block_bytes(B)), dtype=np.uint8)
     s = _signs(sign_bits)
-    lib().orc_quantize_blocks(n, B, iters, kind, _p(s, _u32p), _p(X, _f64p), _p(out, _u8p))
+    lib().orc_quantize_blocks(n, B, iters, flags, kind, _p(s, _u32p), _p(X, _f64p), _p(out, _u8p))
     return out
 
 
-def decode_blocks(hb_bytes, B: int, kind: int, sign_bits, rotated: bool) -> np.ndarray:
+def decode_blocks(hb_bytes, B: int, kind: int, sign_bits, rotated: bool, flags: int = 0) -> np.ndarray:
     """Packed head-blocks [n][bytes] -> values [n][B][128]."""
     hb = np.ascontiguousarray(hb_bytes, dtype=np.uint8).reshape(-1, head_block_bytes(B))
     n = hb.shape[0]
     out = np.empty((n, B, D))
     s = _signs(sign_bits)
-    lib().orc_decode_blocks(n, B, kind, _p(s, _u32p), _p(hb, _u8p), 1 if rotated else 0,
+    lib().orc_decode_blocks(n, B, flags, kind, _p(s, _u32p), _p(hb, _u8p), 1 if rotated else 0,
                             _p(out, _f64p))
     return out
 
@@ -320,7 +324,7 @@ def attention_rotated(q, K, V, sm_scale: float, sign_bits) -> np.ndarray:
 
 
 def decode_attention(B, n_q, n_kv, sign_bits, sm_scale, q, pool, staging, block_table,
-                     seq_lens) -> np.ndarray:
+                     seq_lens, flags: int = 0) -> np.ndarray:
     """Attention of every (sequence, query head) over the paged 2-bit cache.
 
     q: [batch][n_q][128] values; pool: raw bytes of the physical blocks;
@@ -335,7 +339,7 @@ def decode_attention(B, n_q, n_kv, sign_bits, sm_scale, q, pool, staging, block_
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32).reshape(batch)
     out = np.zeros((batch, n_q, D))
     s = _signs(sign_bits)
-    lib().orc_decode_attention(B, n_q, n_kv, _p(s, _u32p), float(sm_scale), _p(q, _f64p),
+    lib().orc_decode_attention(B, flags, n_q, n_kv, _p(s, _u32p), float(sm_scale), _p(q, _f64p),
                                _p(pool, _u8p), _p(staging, _u16p), _p(bt, _i32p), bt.shape[1],
                                _p(sl, _i32p), batch, _p(out, _f64p))
     return out

@@ -43,6 +43,13 @@
 #define ORC_NG 4
 #define ORC_GS 32
 
+/* Ablation switches ([AP3] section 五, 消融): the pages compare the full method
+ * with Hadamard only (no VarN: iters = 0), VarN only (no rotation: R = I),
+ * and VarN along one axis only (token-only, channel-only). */
+#define ORC_NO_ROTATION 1u
+#define ORC_NO_TOKEN_PASS 2u
+#define ORC_NO_CHANNEL_PASS 4u
+
 /* ------------------------------------------------------------------------ */
 /* fp16 grid arithmetic, written from the IEEE-754 binary16 definition:      */
 /* 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; the spacing of   */
@@ -249,15 +256,15 @@ static int usable_variance(double v, double mu)
     return v > 0.0 && isfinite(v) && v > ldexp(mu * mu, -30);
 }
 
-void orc_varn(int B, int iters, const double* Xr, double* Y, double* R, double* C,
+void orc_varn(int B, int iters, uint32_t flags, const double* Xr, double* Y, double* R, double* C,
               double* trace)
 {
     memcpy(Y, Xr, sizeof(double) * (size_t)B * ORC_D);
     for (int t = 0; t < B; t++) R[t] = 1.0;
     for (int c = 0; c < ORC_D; c++) C[c] = 1.0;
     for (int it = 0; it < iters; it++) {
-        /* token axis: every row to variance 1 */
-        for (int t = 0; t < B; t++) {
+        /* token axis: every row to variance 1 (skipped by the channel-only ablation) */
+        for (int t = 0; t < B && !(flags & ORC_NO_TOKEN_PASS); t++) {
             double mu, v;
             row_stats(Y, t, &mu, &v);
             if (!usable_variance(v, mu)) continue;
@@ -274,8 +281,8 @@ void orc_varn(int B, int iters, const double* Xr, double* Y, double* R, double* 
             }
             trace[3 * it + 0] = worst;
         }
-        /* channel axis: every column to variance 1 */
-        for (int c = 0; c < ORC_D; c++) {
+        /* channel axis: every column to variance 1 (skipped by the token-only ablation) */
+        for (int c = 0; c < ORC_D && !(flags & ORC_NO_CHANNEL_PASS); c++) {
             double mu, v;
             col_stats(Y, B, c, &mu, &v);
             if (!usable_variance(v, mu)) continue;
@@ -457,7 +464,7 @@ void orc_unpack(int B, int kind, const uint8_t* in, int32_t* codes, double* s16,
 /* fp64). Any of the detail outputs may be NULL.                             */
 /* ------------------------------------------------------------------------ */
 
-void orc_quantize_block(int B, int iters, int kind, const uint32_t sign_bits[4],
+void orc_quantize_block(int B, int iters, uint32_t flags, int kind, const uint32_t sign_bits[4],
                         const double* X, uint8_t* out,
                         double* Xr_out, double* R_out, double* C_out,
                         double* R16_out, double* C16_out, double* y_out,
@@ -475,8 +482,11 @@ void orc_quantize_block(int B, int iters, int kind, const uint32_t sign_bits[4],
     int32_t* codes = (int32_t*)malloc(sizeof(int32_t) * n);
     double C[ORC_D], C16[ORC_D];
 
-    for (int t = 0; t < B; t++) orc_rotate(X + (size_t)t * ORC_D, sign_bits, Xr + (size_t)t * ORC_D);
-    orc_varn(B, iters, Xr, Y, R, C, trace);
+    for (int t = 0; t < B; t++) {
+        if (flags & ORC_NO_ROTATION) memcpy(Xr + (size_t)t * ORC_D, X + (size_t)t * ORC_D, sizeof(double) * ORC_D);
+        else orc_rotate(X + (size_t)t * ORC_D, sign_bits, Xr + (size_t)t * ORC_D);
+    }
+    orc_varn(B, iters, flags, Xr, Y, R, C, trace);
     for (int t = 0; t < B; t++) R16[t] = orc_round_factor(R[t]);
     for (int c = 0; c < ORC_D; c++) C16[c] = orc_round_factor(C[c]);
     for (int t = 0; t < B; t++)
@@ -505,13 +515,13 @@ void orc_quantize_block(int B, int iters, int kind, const uint32_t sign_bits[4],
 }
 
 /* Many independent head-blocks: X [n][B][128] -> out [n][head_block_bytes]. */
-void orc_quantize_blocks(int64_t n, int B, int iters, int kind, const uint32_t sign_bits[4],
+void orc_quantize_blocks(int64_t n, int B, int iters, uint32_t flags, int kind, const uint32_t sign_bits[4],
                          const double* X, uint8_t* out)
 {
     size_t hb = orc_head_block_bytes(B);
     #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < n; i++)
-        orc_quantize_block(B, iters, kind, sign_bits, X + (size_t)i * B * ORC_D, out + (size_t)i * hb,
+        orc_quantize_block(B, iters, flags, kind, sign_bits, X + (size_t)i * B * ORC_D, out + (size_t)i * hb,
                            NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL);
 }
 
@@ -521,7 +531,7 @@ void orc_quantize_blocks(int64_t n, int B, int iters, int kind, const uint32_t s
 /* out: [B][128]; rotated != 0 keeps the rotated space.                      */
 /* ------------------------------------------------------------------------ */
 
-void orc_decode_block(int B, int kind, const uint32_t sign_bits[4], const uint8_t* in,
+void orc_decode_block(int B, uint32_t flags, int kind, const uint32_t sign_bits[4], const uint8_t* in,
                       int rotated, double* out)
 {
     size_t n = (size_t)B * ORC_D;
@@ -537,19 +547,19 @@ void orc_decode_block(int B, int kind, const uint32_t sign_bits[4], const uint8_
             double yh = codes[t * ORC_D + c] * s16[t * ORC_NG + g] + z16[t * ORC_NG + g];
             xr[c] = yh * R16[t] * C16[c];
         }
-        if (rotated) memcpy(out + (size_t)t * ORC_D, xr, sizeof(xr));
+        if (rotated || (flags & ORC_NO_ROTATION)) memcpy(out + (size_t)t * ORC_D, xr, sizeof(xr));
         else orc_unrotate(xr, sign_bits, out + (size_t)t * ORC_D);
     }
     free(codes); free(s16); free(z16); free(R16);
 }
 
-void orc_decode_blocks(int64_t n, int B, int kind, const uint32_t sign_bits[4],
+void orc_decode_blocks(int64_t n, int B, uint32_t flags, int kind, const uint32_t sign_bits[4],
                        const uint8_t* in, int rotated, double* out)
 {
     size_t hb = orc_head_block_bytes(B);
     #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < n; i++)
-        orc_decode_block(B, kind, sign_bits, in + (size_t)i * hb, rotated, out + (size_t)i * B * ORC_D);
+        orc_decode_block(B, flags, kind, sign_bits, in + (size_t)i * hb, rotated, out + (size_t)i * B * ORC_D);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -612,7 +622,7 @@ void orc_attention_rotated(const double* q, const double* K, const double* V, in
 /* out: fp64 [batch][n_q][128]. Units run in parallel (OpenMP).              */
 /* ------------------------------------------------------------------------ */
 
-void orc_decode_attention(int B, int n_q, int n_kv, const uint32_t sign_bits[4], double sm_scale,
+void orc_decode_attention(int B, uint32_t flags, int n_q, int n_kv, const uint32_t sign_bits[4], double sm_scale,
                           const double* q, const uint8_t* pool, const uint16_t* staging,
                           const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                           int batch, double* out)
@@ -631,8 +641,8 @@ void orc_decode_attention(int B, int n_q, int n_kv, const uint32_t sign_bits[4],
         for (int64_t j = 0; j < nfull; j++) {
             int64_t p = block_table[(int64_t)b * max_blocks + j];
             const uint8_t* base = pool + (size_t)p * block_bytes + (size_t)(2 * h) * hb;
-            orc_decode_block(B, 0, sign_bits, base, 0, K + (size_t)j * B * ORC_D);
-            orc_decode_block(B, 1, sign_bits, base + hb, 0, V + (size_t)j * B * ORC_D);
+            orc_decode_block(B, flags, 0, sign_bits, base, 0, K + (size_t)j * B * ORC_D);
+            orc_decode_block(B, flags, 1, sign_bits, base + hb, 0, V + (size_t)j * B * ORC_D);
         }
         for (int64_t r = 0; r < tail; r++) {
             const uint16_t* sk = staging + ((((size_t)b * n_kv + h) * 2 + 0) * B + r) * ORC_D;

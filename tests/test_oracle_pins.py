@@ -410,3 +410,98 @@ def test_decode_attention_pages_and_tail():
             for j in range(G):
                 want = oracle.attention(q[b, h * G + j], Kc, Vc, 1 / math.sqrt(D))
                 np.testing.assert_allclose(out[b, h * G + j], want, atol=1e-12)
+
+
+# ---------------------------------------------------------------- ablation switches
+
+def _largest_f16_at_most(m):
+    h = np.float16(m)
+    if float(h) > m:
+        h = np.nextafter(h, np.float16(-np.inf))
+    return float(h)
+
+
+def test_no_rotation_no_varn_is_plain_group_quantisation():
+    """With the rotation switched off and 0 VarN iterations the block is plain
+    asymmetric 2-bit group quantisation of the raw values (R = C = 1)."""
+    X = _block(70, 32)
+    r = oracle.quantize_block(X, 0, oracle.KIND_K, [0, 0, 0, 0], flags=oracle.NO_ROTATION)
+    assert np.array_equal(r["Xr"], X) and np.array_equal(r["y"], X)
+    assert np.all(r["R16"] == 1.0) and np.all(r["C16"] == 1.0)
+    for t in range(32):
+        for g in range(4):
+            grp = X[t, 32 * g:32 * g + 32]
+            assert r["z16"][t, g] == _largest_f16_at_most(grp.min())
+            # nearest of the four levels (exact ties never occur on this data)
+            lv = r["z16"][t, g] + r["s16"][t, g] * np.arange(4)
+            want = np.abs(grp[:, None] - lv[None, :]).argmin(axis=1)
+            assert np.array_equal(r["codes"][t, 32 * g:32 * g + 32], want)
+    # decoding never rotates back: both spaces coincide
+    a = oracle.decode_blocks(r["bytes"], 32, 0, [0, 0, 0, 0], rotated=True, flags=oracle.NO_ROTATION)
+    b = oracle.decode_blocks(r["bytes"], 32, 0, [0, 0, 0, 0], rotated=False, flags=oracle.NO_ROTATION)
+    assert np.array_equal(a, b)
+    assert np.all(np.abs(b[0] - X) <= r["s16"].repeat(32, axis=1) / 2 * (1 + 1e-15))
+
+
+def test_hadamard_only_keeps_unit_factors():
+    sb = synth.sign_bits(71)
+    X = _block(71, 64)
+    r = oracle.quantize_block(X, 0, oracle.KIND_V, sb)
+    np.testing.assert_allclose(r["Xr"], oracle.rotate(X, sb), rtol=0, atol=0)
+    assert np.all(r["R"] == 1.0) and np.all(r["C"] == 1.0)
+    assert np.array_equal(r["y"], r["Xr"])
+
+
+@pytest.mark.parametrize("iters", [1, 3])
+def test_token_only_varn_is_the_row_spread(iters):
+    """Channel pass off: C stays 1 and each R_t is the population standard
+    deviation of its rotated row (repeating the pass changes nothing)."""
+    sb = synth.sign_bits(72)
+    X = _block(72, 32)
+    r = oracle.quantize_block(X, iters, oracle.KIND_K, sb, flags=oracle.NO_CHANNEL_PASS)
+    assert np.all(r["C"] == 1.0)
+    np.testing.assert_allclose(r["R"], r["Xr"].std(axis=1), rtol=1e-12)
+
+
+@pytest.mark.parametrize("iters", [1, 3])
+def test_channel_only_varn_is_the_column_spread(iters):
+    sb = synth.sign_bits(73)
+    X = _block(73, 64)
+    r = oracle.quantize_block(X, iters, oracle.KIND_K, sb, flags=oracle.NO_TOKEN_PASS)
+    assert np.all(r["R"] == 1.0)
+    np.testing.assert_allclose(r["C"], r["Xr"].std(axis=0), rtol=1e-12)
+
+
+def test_varn_without_rotation_normalises_the_raw_block():
+    """Rotation off, both passes on: the factors restore the raw block and the
+    last (channel) pass leaves unit column variances."""
+    X = _block(74, 32)
+    Y, R, C, _ = oracle.varn(X, 3, oracle.NO_ROTATION)
+    np.testing.assert_allclose(Y * R[:, None] * C[None, :], X, rtol=1e-12)
+    np.testing.assert_allclose(Y.var(axis=0), 1.0, rtol=1e-12)
+    r = oracle.quantize_block(X, 3, oracle.KIND_K, synth.sign_bits(74), flags=oracle.NO_ROTATION)
+    assert np.array_equal(r["Xr"], X)
+    np.testing.assert_allclose(r["R"], R, rtol=0)
+
+
+def test_decode_attention_without_rotation_equals_plain_attention_over_decoded_keys():
+    B, n_q, n_kv = 32, 4, 1
+    sb = synth.sign_bits(75)
+    g = synth.make_gen(75)
+    K = synth.kv_values(g, 1, 1, 2 * B, 1.0, 2, 10.0)[0, 0].double().numpy()
+    V = synth.kv_values(g, 1, 1, 2 * B, 1.0, 2, 10.0)[0, 0].double().numpy()
+    q = synth.queries(g, 1, n_q).double().numpy()
+    hb = oracle.head_block_bytes(B)
+    pool = np.zeros((2, 1, 2, hb), dtype=np.uint8)
+    f = oracle.NO_ROTATION | oracle.NO_CHANNEL_PASS
+    for j in range(2):
+        pool[j, 0, 0] = oracle.quantize_blocks(K[None, j * B:(j + 1) * B], 2, 0, sb, flags=f)[0]
+        pool[j, 0, 1] = oracle.quantize_blocks(V[None, j * B:(j + 1) * B], 2, 1, sb, flags=f)[0]
+    out = oracle.decode_attention(B, n_q, n_kv, sb, 0.1, q, pool, np.zeros((1, 1, 2, B, D), np.uint16),
+                                  np.array([[1, 0]], np.int32), np.array([2 * B], np.int32), flags=f)
+    Kd = np.concatenate([oracle.decode_blocks(pool[j, 0, 0], B, 0, sb, False, flags=f)[0] for j in (1, 0)])
+    Vd = np.concatenate([oracle.decode_blocks(pool[j, 0, 1], B, 1, sb, False, flags=f)[0] for j in (1, 0)])
+    for h in range(n_q):
+        s = 0.1 * Kd @ q[0, h]
+        p = np.exp(s - s.max())
+        np.testing.assert_allclose(out[0, h], p @ Vd / p.sum(), rtol=1e-12, atol=1e-12)
