@@ -41,6 +41,9 @@ def parse():
     p.add_argument("--layers", type=int, default=None, help="(testing only) fewer layers")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-bf16", action="store_true")
+    p.add_argument("--ablation", action="store_true",
+                   help="instead of the step: error of each ablation (Hadamard only, VarN only, one VarN "
+                        "axis) against the bf16 cache on the Llama-3.1-8B layer, one JSON line per variant")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
                         "lengths), 2-bit vs bf16-cache decode attention, one JSON line per point")
@@ -303,6 +306,7 @@ def run_gpu(args, rank, world):
                    "l2": "no flush: per-step cache 16.3 GB >> 129 MB L2",
                    "parallelism": f"replicas x{world} (each rank its own {batch} sequences; no collective "
                                   "on the data path)"},
+        "decode_step_tokens_per_s": round(world * batch / (ms_per_step * 1e-3), 1),
         "decode_attn": {"GB_per_s": round(achieved, 1), "us_per_layer": round(attn_launch_ms * 1e3, 2),
                         "algorithmic_bytes_per_layer": int(attn_launch_bytes),
                         "frac_of_hbm_peak": round(achieved / peak, 4),
@@ -392,6 +396,43 @@ def bf16_comparison(kv, w, device):
     return {"GB_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1), "us_per_layer": round(ms * 1e3, 2),
             "tokens_per_s_per_layer": round(batch / (ms * 1e-3), 1),
             "bytes_per_layer": int(nbytes), "note": "same shape, bf16 pages, fp32 arithmetic"}
+
+
+def bulk_quantize(kv, w, device, peak):
+    """kvarn_quantize_block in prefill mode: every 64-token block of one
+    layer's K (64 sequences x 8 kv heads x 8192 tokens, bf16, 1.07 GB in)
+    quantised in one call into a contiguous scratch pool."""
+    import torch
+    import synth
+    B, n_kv, batch, L = w.block, w.n_kv, w.batch, w.ctx
+    cfg = kv.make_config(w.n_q, n_kv, B, w.iters, synth.sign_bits(3))
+    g = synth.make_gen(11, device)
+    src = synth.kv_values(g, batch, n_kv, L, w.sigma_m, w.n_out, w.out_factor, device).to(torch.bfloat16)
+    n = batch * n_kv * (L // B)
+    hb = kv.head_block_bytes(cfg)
+    dst = torch.empty(n * hb, dtype=torch.uint8, device=device)
+    ws = kv.alloc_workspace(cfg, 0, 0, device)
+    for _ in range(3):
+        kv.quantize_block(cfg, 0, src, dst, ws, n_head_blocks=n)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kv.quantize_block(cfg, 0, src, dst, ws, n_head_blocks=n)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    assert kv.read_error(ws) == 0
+    ms = statistics.median(ts)
+    rows = n * B
+    nbytes = rows * D * 2 + n * hb
+    del src, dst
+    return {"head_rows_per_s": round(rows / (ms * 1e-3), 1), "GB_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "us_per_call": round(ms * 1e3, 1),
+            "head_blocks": n, "bytes": int(nbytes),
+            "note": "one call over a layer's K: 256 B in + 54 B out per (token, kv head) row; "
+                    "bound by instruction issue, not HBM"}
 
 
 # ---------------------------------------------------------------------------- oracle (CPU)
@@ -565,10 +606,81 @@ def run_sweep(args):
                               "speedup_2bit_vs_bf16": round(ms16 / ms2, 2)}), flush=True)
 
 
+# ---------------------------------------------------------------------------- ablation
+
+ABLATIONS = (  # (name, flags, iters): the pages' ablation list, plus the two ends
+    ("kvarn (full)", 0, 3),
+    ("hadamard only", 0, 0),
+    ("varn only (no rotation)", 1, 3),
+    ("varn token axis only", 4, 3),
+    ("varn channel axis only", 2, 3),
+    ("plain group 2-bit", 1, 0),
+)
+
+
+def run_ablation(args):
+    """Attention-output and reconstruction error of each ablation against the
+    bf16 cache holding the same tokens, on the Llama-3.1-8B layer workload
+    (batch 16, 4096 tokens, block 32), one JSON line per variant."""
+    import numpy as np
+    import torch
+    import bit_kv_cache_08_gb300 as kv
+    import synth
+    kv.build()
+    dev = "cuda"
+    w = synth.LLAMA8B_LAYER
+    B, n_kv, n_q, batch, L = w.block, w.n_kv, w.n_q, w.batch, w.ctx
+    nb = L // B
+    g = synth.make_gen(w.seed, dev)
+    K = synth.kv_values(g, batch, n_kv, L, w.sigma_m, w.n_out, w.out_factor, dev).to(torch.bfloat16)
+    V = synth.kv_values(g, batch, n_kv, L, w.sigma_m, w.n_out, w.out_factor, dev).to(torch.bfloat16)
+    q = synth.queries(g, batch, n_q, dev).to(torch.bfloat16)
+    bt = torch.arange(batch * nb, dtype=torch.int32, device=dev).view(batch, nb)
+    lens = torch.full((batch,), L, dtype=torch.int32, device=dev)
+    sb = synth.sign_bits(w.seed)
+    # the bf16 reference: same tokens, plain pages
+    kvp = torch.stack([K.view(batch, n_kv, nb, B, D), V.view(batch, n_kv, nb, B, D)], dim=3)   # [b][h][j][2][B][D]
+    kvp = kvp.permute(0, 2, 1, 3, 4, 5).reshape(batch * nb, n_kv, 2, B, D).contiguous()
+    cfg0 = kv.make_config(n_q, n_kv, B, 3, sb)
+    ref = torch.empty(batch, n_q, D, device=dev)
+    kv.decode_attn_bf16(cfg0, q, kvp, bt, lens, ref, kv.alloc_workspace(cfg0, batch, nb, dev))
+    del kvp
+    for name, flags, iters in ABLATIONS:
+        cfg = kv.make_config(n_q, n_kv, B, iters, sb, flags=flags)
+        pool = kv.alloc_pool(cfg, batch * nb, dev)
+        staging = kv.alloc_staging(cfg, batch, dev)
+        ws = kv.alloc_workspace(cfg, batch, nb, dev)
+        hb, bb = kv.head_block_bytes(cfg), kv.block_bytes(cfg)
+        rec = []
+        for kind, T in ((0, K), (1, V)):
+            offs = (bt[:, None, :].long() * bb + (2 * torch.arange(n_kv, device=dev)[None, :, None] + kind) * hb)
+            kv.quantize_block(cfg, kind, T.contiguous(), pool, ws, dst_offsets=offs.reshape(-1).contiguous(),
+                              n_head_blocks=batch * n_kv * nb)
+            deq = torch.empty(batch * n_kv * nb, B, D, device=dev)
+            kv.dequantize(cfg, kind, pool, deq, rotated=False, src_offsets=offs.reshape(-1).contiguous())
+            x = T.float().reshape(-1, B, D)
+            rec.append(float(((deq - x) ** 2).sum() / (x ** 2).sum()))
+        out = torch.empty(batch, n_q, D, device=dev)
+        kv.decode_attn(cfg, q, pool, staging, bt, lens, out, ws)
+        torch.cuda.synchronize()
+        assert kv.read_error(ws) == 0
+        d = out - ref
+        cos = torch.nn.functional.cosine_similarity(out.reshape(-1, D), ref.reshape(-1, D), dim=1)
+        print(json.dumps({"ablation": name, "flags": flags, "varn_iters": iters, "workload": w.name,
+                          "attn_rel_l2_vs_bf16": round(float(d.norm() / ref.norm()), 5),
+                          "attn_mean_cosine_vs_bf16": round(float(cos.mean()), 5),
+                          "k_rel_mse": round(rec[0], 5), "v_rel_mse": round(rec[1], 5)}), flush=True)
+        del pool, staging, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.ablation:
+        run_ablation(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -593,6 +705,7 @@ def main():
         del state
         torch.cuda.empty_cache()
         res["bf16_cache_comparison"] = bf16_comparison(objs[0], w, torch.cuda.current_device())
+        res["quantize_bulk"] = bulk_quantize(objs[0], w, torch.cuda.current_device(), res["roofline"]["peak"])
     if rank == 0 and not args.no_cpu_baseline:
         seqs = CPU_SAMPLE_SEQS
         secs, nbytes, threads = cpu_sample_step(cpu_sample_setup(w, seqs))

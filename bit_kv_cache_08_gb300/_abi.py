@@ -24,6 +24,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, -1, -2, -3, -
 DEVERR_BLOCK_ID, DEVERR_POSITION, DEVERR_NONFINITE, DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 BF16, FP32 = 0, 1
 KIND_K, KIND_V = 0, 1
+FLAG_NO_ROTATION, FLAG_NO_TOKEN_PASS, FLAG_NO_CHANNEL_PASS = 0x1, 0x2, 0x4
 
 
 class KVarNError(RuntimeError):
@@ -37,13 +38,14 @@ class Config(ctypes.Structure):
                 ("group_size", ctypes.c_int32), ("bits", ctypes.c_int32),
                 ("varn_iters", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("sm_scale", ctypes.c_float),
-                ("sign_bits", ctypes.c_uint32 * 4)]
+                ("sign_bits", ctypes.c_uint32 * 4), ("flags", ctypes.c_uint32)]
 
 
 def make_config(n_q_heads: int, n_kv_heads: int, block_size: int, varn_iters: int,
                 sign_bits: Sequence[int], sm_scale: float = 0.0, head_dim: int = 128,
-                group_size: int = 32, bits: int = 2) -> Config:
+                group_size: int = 32, bits: int = 2, flags: int = 0) -> Config:
     c = Config()
+    c.flags = flags
     c.head_dim, c.block_size, c.group_size, c.bits = head_dim, block_size, group_size, bits
     c.varn_iters, c.n_q_heads, c.n_kv_heads, c.sm_scale = varn_iters, n_q_heads, n_kv_heads, sm_scale
     for i in range(4):

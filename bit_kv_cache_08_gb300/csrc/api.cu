@@ -38,7 +38,9 @@ int check_config(const kvarn_config* cfg, kvarn_config* out) {
     if (!cfg) return KVARN_ERR_INVALID_ARG;
     if (cfg->head_dim != 128 || cfg->group_size != 32 || cfg->bits != 2) return KVARN_ERR_UNSUPPORTED;
     if (cfg->block_size != 32 && cfg->block_size != 64) return KVARN_ERR_UNSUPPORTED;
-    if (cfg->varn_iters < 1 || cfg->varn_iters > 8) return KVARN_ERR_INVALID_ARG;
+    if (cfg->varn_iters < 0 || cfg->varn_iters > 8) return KVARN_ERR_INVALID_ARG;
+    if (cfg->flags & ~(KVARN_FLAG_NO_ROTATION | KVARN_FLAG_NO_TOKEN_PASS | KVARN_FLAG_NO_CHANNEL_PASS))
+        return KVARN_ERR_INVALID_ARG;
     if (cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads) return KVARN_ERR_INVALID_ARG;
     if (cfg->n_q_heads % cfg->n_kv_heads != 0) return KVARN_ERR_INVALID_ARG;
     if (cfg->n_q_heads / cfg->n_kv_heads > kMaxGroup) return KVARN_ERR_UNSUPPORTED;
@@ -169,6 +171,7 @@ int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, c
         !aligned(workspace, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return KVARN_ERR_INVALID_ARG;
     if ((int64_t)max_blocks_per_seq * c.block_size > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
+    if (n_pool_blocks > 0x7fffffff || kvarn_block_bytes(&c) > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
     const size_t need = ws_bytes(c, batch);
     if (need == 0) return KVARN_ERR_CUDA;
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;

@@ -70,12 +70,15 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     uint32_t* err = a.err;
     const float sm_scale = a.sm_scale;
     const uint32_t sb0 = a.sb[0], sb1 = a.sb[1], sb2 = a.sb[2], sb3 = a.sb[3];
+    const bool rotate_q = !(a.flags & KVARN_FLAG_NO_ROTATION);
 
     const SplitArgs sp{a.seq_lens, a.batch, n_kv, max_blocks, B, 0};
     Cursor cc;
     cc.b = cc.h = cc.j = 0;
     const int64_t W = split_locate(sp, 0, lane, cc.b, cc.h, cc.j);
-    const int64_t s_beg = (int64_t)w * W / a.nw, s_end = (int64_t)(w + 1) * W / a.nw;
+    const int64_t nwe = split_active_warps(W, a.nw);   // every active warp gets >= 1 block
+    if (w >= nwe) return;
+    const int64_t s_beg = (int64_t)w * W / nwe, s_end = (int64_t)(w + 1) * W / nwe;
     if (s_beg >= s_end) return;
     split_locate(sp, s_beg, lane, cc.b, cc.h, cc.j);
     cc.nb = split_nblocks(sp, cc.b);
@@ -133,15 +136,16 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         for (int j = 0; j < G; ++j) {
             float v[4];
             load_q4(qptr, q_dtype, (int64_t)cc.b * n_q + (int64_t)cc.h * G + j, lane, v);
+            if (rotate_q) {   // q_rot = H (sigma . q) / sqrt(128), as the cache was rotated
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] *= sgn4[k];
-            fwht128(v, lane);
+                for (int k = 0; k < 4; ++k) v[k] *= sgn4[k];
+                fwht128(v, lane);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD;
+            }
             float amax = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                v[k] *= kInvSqrtD;
-                amax = fmaxf(amax, fabsf(v[k]));
-            }
+            for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(v[k]));
             amax = warp_max(amax);
             const int e = (amax > 0.f && isfinite(amax)) ? ceil_log2(amax) : 0;
             const float sc = exp2i(12 - e);
@@ -557,6 +561,7 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.G = cfg.n_q_heads / cfg.n_kv_heads;
     a.nw = nw;
     a.sm_scale = cfg.sm_scale;
+    a.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)batch * a.n_q + 3) / 4);
     if (cfg.block_size == 32) {

@@ -2,36 +2,76 @@
 // the comparison point for the 2-bit path, with the same balanced split-K
 // partition and merge, no rotation and no staging.
 //
-// The split unit is a 16-token chunk of a page (4 KB of K and 4 KB of V),
-// streamed into a 3-stage shared-memory ring with 1-D bulk copies. Lane l
-// owns channels 4l..4l+3; the 16 x G partial dot products of a chunk are
-// summed across lanes with a transposing butterfly (each of 5 levels halves
-// the values a lane carries), which leaves lane l with the scores of token
-// l/2 for heads 2(l%2) and 2(l%2)+1. All arithmetic is fp32.
+// The split unit is a 16-token chunk of a page (4 KB of K and 4 KB of V).
+// Each lane copies one 256-byte row (lanes 0-15 K, 16-31 V) with a 1-D bulk
+// copy into a 3-stage shared-memory ring whose rows are padded to 272 bytes,
+// so that ldmatrix reads of 8 rows hit 32 distinct banks. Both contractions
+// run on mma.sync m16n8k16 (bf16 in, f32 accumulate):
+//   QK  A = K chunk (16 tokens x 16 channels per k-step, ldmatrix),
+//       B = q as bf16 hi | lo per head (exact for a bf16 query);
+//   PV  A = V^T (16 channels x 16 tokens per m-tile, ldmatrix.trans),
+//       B = p as bf16 hi | lo per head, so p keeps ~16 bits.
+// Accumulator columns are (head, hi | lo); the online softmax runs per chunk
+// in the log2 domain and rescales the PV accumulators in place. Rows past the
+// sequence end are zero-filled instead of copied (0 * garbage could be NaN).
 #include "attn_common.cuh"
 
 namespace kvarn {
 
 constexpr int kChunk = 16;
 constexpr int kBfStages = 3;
-constexpr int kChunkBytes = kChunk * kD * 2;   // one of K or V
+constexpr int kRowPitch = kD * 2 + 16;                 // 272 bytes
+constexpr int kStageBytes = 2 * kChunk * kRowPitch;    // K rows then V rows
+
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm_x4_trans(const void* p, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_addr(p)));
+}
+
+// (hi, lo) bf16 pairs of two floats: hi = RN(v), lo = RN(v - hi)
+__device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
 
 template <int B>
 __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
     constexpr int CPB = B / kChunk;   // chunks per page
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBfStages * 2 * kChunkBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBfStages * kStageBytes);
     const int lane = threadIdx.x;
+    const int gq = lane >> 2, tq = lane & 3;
     const int w = blockIdx.x;
     const int max_pages = a.max_blocks / CPB;
+    const int G = a.G;
 
     // positions are 16-token chunks; a partial last chunk counts
     const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, kChunk, 1};
     Cursor cc;
     cc.b = cc.h = cc.j = 0;
     const int64_t W = split_locate(sp, 0, lane, cc.b, cc.h, cc.j);
-    const int64_t s_beg = (int64_t)w * W / a.nw, s_end = (int64_t)(w + 1) * W / a.nw;
+    const int64_t nwe = split_active_warps(W, a.nw);   // every active warp gets >= 1 block
+    if (w >= nwe) return;
+    const int64_t s_beg = (int64_t)w * W / nwe, s_end = (int64_t)(w + 1) * W / nwe;
     if (s_beg >= s_end) return;
     split_locate(sp, s_beg, lane, cc.b, cc.h, cc.j);
     cc.nb = split_nblocks(sp, cc.b);
@@ -43,18 +83,27 @@ __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
     }
     __syncwarp();
 
+    // every lane moves one row: lanes 0-15 K, 16-31 V; rows past the end are zeroed
     auto issue = [&](int stage) {
         const int page = ic.j / CPB, sub = ic.j % CPB;
         int64_t phys = a.block_table[(int64_t)ic.b * max_pages + page];
         const bool ok = phys >= 0 && phys < a.n_pool_blocks;
         if (!ok) phys = 0;
-        if (lane == 0) {
-            const uint8_t* kp = a.pool + phys * a.block_bytes + (int64_t)(2 * ic.h) * B * kD * 2 +
-                                (int64_t)sub * kChunkBytes;
-            mbar_arrive_expect_tx(&bars[stage], 2 * kChunkBytes);
-            bulk_g2s(stages + stage * 2 * kChunkBytes, kp, kChunkBytes, &bars[stage]);
-            bulk_g2s(stages + stage * 2 * kChunkBytes + kChunkBytes, kp + (int64_t)B * kD * 2, kChunkBytes,
-                     &bars[stage]);
+        const int nv = min(kChunk, a.seq_lens[ic.b] - ic.j * kChunk);
+        const int kind = lane >> 4, row = lane & 15;
+        uint8_t* dst = stages + stage * kStageBytes + (kind * kChunk + row) * kRowPitch;
+        if (row >= nv) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int i = 0; i < kD * 2 / 16; ++i) d4[i] = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (lane == 0) mbar_arrive_expect_tx(&bars[stage], 2 * nv * kD * 2);
+        __syncwarp();
+        if (row < nv) {
+            const uint8_t* src = a.pool + phys * a.block_bytes + (int64_t)(2 * ic.h + kind) * B * kD * 2 +
+                                 (int64_t)(sub * kChunk + row) * kD * 2;
+            bulk_g2s(dst, src, kD * 2, &bars[stage]);
         }
         split_advance(sp, ic);
         return ok;
@@ -66,37 +115,64 @@ __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
             if (issue(s)) okmask |= 1u << s;
     }
 
-    float qv[4][4], O[4][4], m_run[4], l_run[4];
+    const int hb = gq >> 1, part = gq & 1;   // this lane's B column: (head, hi | lo)
+    const float qs = a.sm_scale * kLog2e;
+    uint32_t qb[16];                          // QK B fragments, k-steps 0..7
+    float O[8][4];                            // PV accumulators: channels 16mt + gq (+8), head tq hi | lo
+    float m_run = -INFINITY, l_part = 0.f;
+
     auto unit_setup = [&]() {
-        const float qs = a.sm_scale * kLog2e;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            float v[4] = {0.f, 0.f, 0.f, 0.f};
-            if (h < a.G) load_q4(a.q, a.q_dtype, (int64_t)cc.b * a.n_q + (int64_t)cc.h * a.G + h, lane, v);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                qv[h][k] = v[k] * qs;
-                O[h][k] = 0.f;
+        for (int i = 0; i < 16; ++i) {
+            const int c = 16 * (i >> 1) + 8 * (i & 1) + 2 * tq;
+            float v0 = 0.f, v1 = 0.f;
+            if (hb < G) {
+                const int64_t row = (int64_t)cc.b * a.n_q + (int64_t)cc.h * G + hb;
+                if (a.q_dtype == KVARN_FP32) {
+                    const float2 f = *reinterpret_cast<const float2*>(static_cast<const float*>(a.q) + row * kD + c);
+                    v0 = f.x; v1 = f.y;
+                } else {
+                    const uint32_t u = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(a.q) + row * kD + c);
+                    v0 = __uint_as_float(u << 16);
+                    v1 = __uint_as_float(u & 0xffff0000u);
+                }
             }
-            m_run[h] = -INFINITY;
-            l_run[h] = 0.f;
+            uint32_t hi, lo;
+            split_bf16x2(v0, v1, hi, lo);
+            qb[i] = part ? lo : hi;
         }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
+        m_run = -INFINITY;
+        l_part = 0.f;
     };
     auto unit_flush = [&]() {
-        const int64_t slot = (int64_t)cc.b * a.n_kv + cc.h + w;
-        for (int h = 0; h < a.G; ++h) {
-            float* base = a.partials + (slot * a.G + h) * kPartialStride;
-            if (lane == 0) {
-                base[0] = m_run[h];
-                base[1] = l_run[h];
+        float l = l_part;
+        l += __shfl_xor_sync(kFull, l, 4);
+        l += __shfl_xor_sync(kFull, l, 8);
+        l += __shfl_xor_sync(kFull, l, 16);
+        if (tq < G) {
+            const int64_t slot = (int64_t)cc.b * a.n_kv + cc.h + w;
+            float* base = a.partials + (slot * G + tq) * kPartialStride;
+            if (gq == 0) {
+                base[0] = m_run;
+                base[1] = l;
             }
-            reinterpret_cast<float4*>(base + 4)[lane] = make_float4(O[h][0], O[h][1], O[h][2], O[h][3]);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                base[4 + 16 * mt + gq] = O[mt][0] + O[mt][1];
+                base[4 + 16 * mt + gq + 8] = O[mt][2] + O[mt][3];
+            }
         }
     };
 
     unit_setup();
     int stage = 0;
     uint32_t phase = 0;
+    // ldmatrix row addresses: lane supplies row (lane & 7) of matrix (lane >> 3)
+    const int mi = lane >> 3, mr = lane & 7;
+    const int k_row = 8 * (mi & 1) + mr, k_col = 8 * (mi >> 1);   // QK A: rows = tokens
+    const int v_row = 8 * (mi >> 1) + mr, v_col = 8 * (mi & 1);   // PV A (trans): rows = tokens
     for (int64_t x = s_beg; x < s_end; ++x) {
         if (!mbar_wait_bounded(&bars[stage], phase, kWaitLimit)) {
             if (lane == 0) raise_error(a.err, KVARN_DEVERR_WAIT_TIMEOUT);
@@ -111,83 +187,48 @@ __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
         if (!valid && lane == 0) raise_error(a.err, KVARN_DEVERR_BLOCK_ID);
         const int nvalid = min(kChunk, a.seq_lens[cc.b] - cc.j * kChunk);
         if (valid) {
-            const uint8_t* Kc = stages + stage * 2 * kChunkBytes;
-            const uint8_t* Vc = Kc + kChunkBytes;
-            float v[64];   // [token][head] partial dots
+            const uint8_t* Kc = stages + stage * kStageBytes;
+            const uint8_t* Vc = Kc + kChunk * kRowPitch;
+            // ---- scores: tokens gq and gq + 8, head tq (hi + lo columns)
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int t = 0; t < kChunk; ++t) {
-                const uint2 ku = *reinterpret_cast<const uint2*>(Kc + t * kD * 2 + 8 * lane);
-                const float k0 = __uint_as_float(ku.x << 16), k1 = __uint_as_float(ku.x & 0xffff0000u);
-                const float k2 = __uint_as_float(ku.y << 16), k3 = __uint_as_float(ku.y & 0xffff0000u);
-#pragma unroll
-                for (int h = 0; h < 4; ++h)
-                    v[4 * t + h] = fmaf(qv[h][3], k3, fmaf(qv[h][2], k2, fmaf(qv[h][1], k1, qv[h][0] * k0)));
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(Kc + k_row * kRowPitch + (16 * ks + k_col) * 2, a0, a1, a2, a3);
+                mma16816_bf16(sacc, a0, a1, a2, a3, qb[2 * ks], qb[2 * ks + 1]);
             }
-            // transposing butterfly: lane ends with entries 2*lane, 2*lane+1
+            float s0 = (sacc[0] + sacc[1]) * qs, s1 = (sacc[2] + sacc[3]) * qs;
+            if (gq >= nvalid) s0 = -INFINITY;
+            if (gq + 8 >= nvalid) s1 = -INFINITY;
+            float bm = fmaxf(s0, s1);
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+            const float m_new = fmaxf(m_run, bm);
+            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+            const float p0 = (m_new == -INFINITY) ? 0.f : exp2f(s0 - m_new);
+            const float p1 = (m_new == -INFINITY) ? 0.f : exp2f(s1 - m_new);
+            l_part = l_part * alpha + (p0 + p1);
+            m_run = m_new;
+            if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
-            for (int lvl = 0, m = 16, half = 32; lvl < 5; ++lvl, m >>= 1, half >>= 1) {
-                const bool up = (lane & m) != 0;
-#pragma unroll
-                for (int i = 0; i < half; ++i) {
-                    const float send = up ? v[i] : v[i + half];
-                    const float keep = up ? v[i + half] : v[i];
-                    v[i] = keep + __shfl_xor_sync(kFull, send, m);
+                for (int mt = 0; mt < 8; ++mt) {
+                    O[mt][0] *= alpha; O[mt][1] *= alpha; O[mt][2] *= alpha; O[mt][3] *= alpha;
                 }
             }
-            const int tok = lane >> 1, hp = 2 * (lane & 1);   // heads hp, hp+1
-            float s0 = (tok < nvalid) ? v[0] : -INFINITY;
-            float s1 = (tok < nvalid) ? v[1] : -INFINITY;
-            float b0 = s0, b1 = s1;
+            // ---- PV B fragments: p of tokens 2tq, 2tq+1 (b0) and 2tq+8, 2tq+9 (b1), head hb
+            const int sA = 8 * tq + hb, sB = 8 * tq + 4 + hb;
+            const float pa0 = __shfl_sync(kFull, p0, sA), pa1 = __shfl_sync(kFull, p0, sB);
+            const float pb0 = __shfl_sync(kFull, p1, sA), pb1 = __shfl_sync(kFull, p1, sB);
+            uint32_t h0, l0, h1, l1;
+            split_bf16x2(pa0, pa1, h0, l0);
+            split_bf16x2(pb0, pb1, h1, l1);
+            const uint32_t b0 = part ? l0 : h0, b1 = part ? l1 : h1;
 #pragma unroll
-            for (int mm = 2; mm <= 16; mm <<= 1) {
-                b0 = fmaxf(b0, __shfl_xor_sync(kFull, b0, mm));
-                b1 = fmaxf(b1, __shfl_xor_sync(kFull, b1, mm));
-            }
-            float mn[2], p[2];
-            const float mo0 = (hp == 0) ? m_run[0] : m_run[2];
-            const float mo1 = (hp == 0) ? m_run[1] : m_run[3];
-            mn[0] = fmaxf(mo0, b0);
-            mn[1] = fmaxf(mo1, b1);
-            p[0] = (mn[0] == -INFINITY) ? 0.f : exp2f(s0 - mn[0]);
-            p[1] = (mn[1] == -INFINITY) ? 0.f : exp2f(s1 - mn[1]);
-            float ps0 = p[0], ps1 = p[1];
-#pragma unroll
-            for (int mm = 2; mm <= 16; mm <<= 1) {
-                ps0 += __shfl_xor_sync(kFull, ps0, mm);
-                ps1 += __shfl_xor_sync(kFull, ps1, mm);
-            }
-            // every lane: new max and chunk sum of all four heads
-            float mnew[4], psum[4];
-            mnew[0] = __shfl_sync(kFull, mn[0], 0);
-            mnew[1] = __shfl_sync(kFull, mn[1], 0);
-            mnew[2] = __shfl_sync(kFull, mn[0], 1);
-            mnew[3] = __shfl_sync(kFull, mn[1], 1);
-            psum[0] = __shfl_sync(kFull, ps0, 0);
-            psum[1] = __shfl_sync(kFull, ps1, 0);
-            psum[2] = __shfl_sync(kFull, ps0, 1);
-            psum[3] = __shfl_sync(kFull, ps1, 1);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float al = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mnew[h]);
-                l_run[h] = l_run[h] * al + psum[h];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) O[h][k] *= al;
-                m_run[h] = mnew[h];
-            }
-#pragma unroll
-            for (int t = 0; t < kChunk; ++t) {
-                if (t >= nvalid) break;   // rows past the length may hold anything
-                const uint2 vu = *reinterpret_cast<const uint2*>(Vc + t * kD * 2 + 8 * lane);
-                const float v0 = __uint_as_float(vu.x << 16), v1 = __uint_as_float(vu.x & 0xffff0000u);
-                const float v2 = __uint_as_float(vu.y << 16), v3 = __uint_as_float(vu.y & 0xffff0000u);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float ph = __shfl_sync(kFull, p[h & 1], 2 * t + (h >> 1));
-                    O[h][0] = fmaf(ph, v0, O[h][0]);
-                    O[h][1] = fmaf(ph, v1, O[h][1]);
-                    O[h][2] = fmaf(ph, v2, O[h][2]);
-                    O[h][3] = fmaf(ph, v3, O[h][3]);
-                }
+            for (int mt = 0; mt < 8; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_trans(Vc + v_row * kRowPitch + (16 * mt + v_col) * 2, a0, a1, a2, a3);
+                mma16816_bf16(O[mt], a0, a1, a2, a3, b0, b1);
             }
         }
         __syncwarp();
@@ -210,7 +251,7 @@ __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
     }
 }
 
-size_t attn_bf16_smem_bytes() { return (size_t)kBfStages * 2 * kChunkBytes + 64; }
+size_t attn_bf16_smem_bytes() { return (size_t)kBfStages * kStageBytes + 64; }
 
 int attn_bf16_grid_warps(int block_size, int device) {
     static int cache[2][64];
@@ -252,6 +293,7 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
     a.G = cfg.n_q_heads / cfg.n_kv_heads;
     a.nw = nw;
     a.sm_scale = cfg.sm_scale;
+    a.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)batch * a.n_q + 3) / 4);
     if (cfg.block_size == 32)

@@ -25,6 +25,7 @@ struct AttnArgs {
     int n_q, n_kv, G;
     int nw;
     float sm_scale;
+    uint32_t flags;   // KVARN_FLAG_*: the cache's ablation switches
     uint32_t sb[4];
 };
 
@@ -111,24 +112,34 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     const int nb = split_nblocks(sp, b);
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (nb > 0) {
+        const int64_t nwe = split_active_warps(W, a.nw);
         const int64_t Su = before * a.n_kv + (int64_t)h * nb;
         const int64_t u = (int64_t)b * a.n_kv + h;
-        const int64_t w0 = split_last_warp_at(Su, W, a.nw), w1 = split_last_warp_at(Su + nb - 1, W, a.nw);
-        for (int64_t ww = w0; ww <= w1; ++ww) {
-            const float* base = a.partials + ((u + ww) * a.G + jq) * kPartialStride;
-            const float pm = base[0], pl = base[1];
-            const float4 pa = reinterpret_cast<const float4*>(base + 4)[lane];
-            const float mn = fmaxf(m, pm);
-            const float fa = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-            const float fb = (pm == -INFINITY) ? 0.f : exp2f(pm - mn);
-            l = l * fa + pl * fb;
-            acc[0] = acc[0] * fa + pa.x * fb;
-            acc[1] = acc[1] * fa + pa.y * fb;
-            acc[2] = acc[2] * fa + pa.z * fb;
-            acc[3] = acc[3] * fa + pa.w * fb;
-            m = mn;
+        const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);
+        const int np = (int)(w1 - w0 + 1);                          // this unit's partials
+        const float* p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
+        const int64_t pstride = (int64_t)a.G * kPartialStride;     // next warp's partial of the unit
+        // the common maximum and the weighted sum of l, lanes over partials
+        float mx = -INFINITY;
+        for (int i = lane; i < np; i += 32) mx = fmaxf(mx, p0[i * pstride]);
+        m = warp_max(mx);
+        if (m != -INFINITY) {
+            float ls = 0.f;
+            for (int i = lane; i < np; i += 32) ls += p0[i * pstride + 1] * exp2f(p0[i * pstride] - m);
+            l = warp_sum(ls);
+            // every lane its 4 channels over all partials (independent loads)
+#pragma unroll 4
+            for (int i = 0; i < np; ++i) {
+                const float* bp = p0 + i * pstride;
+                const float wgt = exp2f(bp[0] - m);
+                const float4 pa = reinterpret_cast<const float4*>(bp + 4)[lane];
+                acc[0] = fmaf(wgt, pa.x, acc[0]);
+                acc[1] = fmaf(wgt, pa.y, acc[1]);
+                acc[2] = fmaf(wgt, pa.z, acc[2]);
+                acc[3] = fmaf(wgt, pa.w, acc[3]);
+            }
         }
-        if (ROT) {
+        if (ROT && !(a.flags & KVARN_FLAG_NO_ROTATION)) {
             // rotate back: x = sigma . H(acc) / sqrt(128)
             fwht128(acc, lane);
 #pragma unroll

@@ -74,6 +74,7 @@ extern "C" int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q,
     if (c.sm_scale == 0.0f) c.sm_scale = 1.0f / sqrtf(128.0f);
     if (q_dtype != KVARN_BF16 && q_dtype != KVARN_FP32) return KVARN_ERR_INVALID_ARG;
     if (batch < 0 || max_blocks_per_seq < 0 || n_pool_blocks < 1) return KVARN_ERR_INVALID_ARG;
+    if (n_pool_blocks > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
     if (batch == 0) return KVARN_OK;
     if (!q || !pool || !staging || !block_table || !seq_lens || !out) return KVARN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(pool) || !aligned16(staging) || !aligned16(out) ||

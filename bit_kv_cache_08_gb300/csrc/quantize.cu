@@ -20,7 +20,9 @@
 //              divide-and-accumulate iteration reaches, without keeping the
 //              normalised tile. Token pass: two-pass mean/variance by warp
 //              reduction; channel pass: per-warp partial sums through shared memory
-//   factors    fp16 round-to-nearest of the clamped factors
+//   factors    sqrt(v) as v * rsqrt(v) (a few fp32 ulps; the factors only feed
+//              statistics and an fp16 rounding), then fp16 round-to-nearest of
+//              the clamped factors
 //   quantise   y = x_rot * (1/R16) * (1/C16) (correctly rounded reciprocals;
 //              a few fp32 ulps from the quotient), per (token, 32-channel group):
 //              z = fp16 round-down of the
@@ -39,13 +41,55 @@ template <int B> constexpr int quant_threads() { return 32 * quant_warps<B>(); }
 template <int B>
 struct QuantSmem {
     alignas(16) uint8_t image[head_block_bytes(B)];   // exact global layout
-    alignas(16) float part_a[quant_warps<B>()][kD];
-    alignas(16) float part_b[quant_warps<B>()][kD];
+    alignas(16) float part[quant_warps<B>()][kD + 4]; // per-warp column partial sums (padded rows)
+    alignas(16) float tot[2][kD];                     // column totals (double-buffered)
 };
+
+// Sums over the tile's rows of one value per (row, channel), given each
+// thread's partial over its warp's rows for channels 4 lane .. 4 lane + 3.
+// Warp w reduces channels [w*CPW, (w+1)*CPW) over all warps (4 shared loads
+// per thread plus a shuffle tree), then every thread reads back its 4 totals.
+// `buf` alternates between calls so that one barrier per call suffices.
+template <int B>
+__device__ __forceinline__ float4 column_totals(QuantSmem<B>& q, const float (&cs)[4], int warp, int lane,
+                                                int buf) {
+    constexpr int NW = quant_warps<B>(), CPW = kD / NW, SUB = 32 / CPW;   // SUB warp subsets of 4 warps
+    *reinterpret_cast<float4*>(&q.part[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+    __syncthreads();
+    const int c = warp * CPW + (lane % CPW), sub = lane / CPW;
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < NW / SUB; ++k) t += q.part[sub * (NW / SUB) + k][c];
+#pragma unroll
+    for (int m = CPW; m < 32; m <<= 1) t += __shfl_xor_sync(kFull, t, m);
+    if (sub == 0) q.tot[buf][c] = t;
+    __syncthreads();
+    return *reinterpret_cast<const float4*>(&q.tot[buf][4 * lane]);
+}
+
+// Row sums of four rows at once (v[i]: this lane's partial of row i): a
+// transposing butterfly leaves lane l with the total of row 2*bit4(l) +
+// bit3(l), then four shuffles hand every lane all four totals.
+__device__ __forceinline__ void row_totals4(float (&v)[4], int lane) {
+    const bool u16 = lane & 16, u8 = lane & 8;
+    float k0 = u16 ? v[2] : v[0], k1 = u16 ? v[3] : v[1];
+    const float s0 = u16 ? v[0] : v[2], s1 = u16 ? v[1] : v[3];
+    k0 += __shfl_xor_sync(kFull, s0, 16);
+    k1 += __shfl_xor_sync(kFull, s1, 16);
+    float k = u8 ? k1 : k0;
+    const float s = u8 ? k0 : k1;
+    k += __shfl_xor_sync(kFull, s, 8);
+    k += __shfl_xor_sync(kFull, k, 4);
+    k += __shfl_xor_sync(kFull, k, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __shfl_sync(kFull, k, 16 * (i >> 1) + 8 * (i & 1));
+}
 
 struct QuantParams {
     int kind;          // 0 = K record order, 1 = V record order
     int iters;
+    uint32_t flags;    // KVARN_FLAG_* ablation switches
     uint32_t sb[4];    // rotation signs
 };
 
@@ -83,10 +127,11 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
     uint16_t* R_sec = reinterpret_cast<uint16_t*>(q.image + off_R(B));
     uint16_t* C_sec = reinterpret_cast<uint16_t*>(q.image + off_C(B));
 
-    // ---- rotation: x_rot = H (sigma . x) / sqrt(128)
+    // ---- rotation: x_rot = H (sigma . x) / sqrt(128) (identity in the no-rotation ablation)
     uint32_t sw = p.sb[lane >> 3] >> (4 * (lane & 7));    // this lane's 4 sign bits
+    const bool rotate = !(p.flags & KVARN_FLAG_NO_ROTATION);
 #pragma unroll
-    for (int i = 0; i < RPW; ++i) {
+    for (int i = 0; i < RPW && rotate; ++i) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) x[i][k] = ((sw >> k) & 1u) ? -x[i][k] : x[i][k];
         fwht128(x[i], lane);
@@ -98,56 +143,63 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
     float Rf[RPW], rR[RPW], Cf[4] = {1.f, 1.f, 1.f, 1.f}, rCf[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
     for (int i = 0; i < RPW; ++i) { Rf[i] = 1.f; rR[i] = 1.f; }
+    static_assert(RPW == 4, "row_totals4 reduces four rows");
+    int buf = 0;
     for (int it = 0; it < p.iters; ++it) {
+        // token pass: R_t = population std over channels of x_rot[t][c] / C_c
+        if (!(p.flags & KVARN_FLAG_NO_TOKEN_PASS)) {
+            float u[RPW][4], mu[RPW], var[RPW];
 #pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-            float u[4];
+            for (int i = 0; i < RPW; ++i) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) u[k] = x[i][k] * rCf[k];
-            float mu = warp_sum(u[0] + u[1] + u[2] + u[3]) * (1.0f / kD);
-            float d0 = u[0] - mu, d1 = u[1] - mu, d2 = u[2] - mu, d3 = u[3] - mu;
-            float var = warp_sum(d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3) * (1.0f / kD);
-            if (usable_variance(var, mu)) {
-                Rf[i] = sqrtf(var);
-                rR[i] = __frcp_rn(Rf[i]);
+                for (int k = 0; k < 4; ++k) u[i][k] = x[i][k] * rCf[k];
+                mu[i] = (u[i][0] + u[i][1]) + (u[i][2] + u[i][3]);
+            }
+            row_totals4(mu, lane);
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                mu[i] *= (1.0f / kD);
+                float d0 = u[i][0] - mu[i], d1 = u[i][1] - mu[i], d2 = u[i][2] - mu[i], d3 = u[i][3] - mu[i];
+                var[i] = (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+            }
+            row_totals4(var, lane);
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const float v = var[i] * (1.0f / kD);
+                if (usable_variance(v, mu[i])) {
+                    rR[i] = rsqrtf(v);        // within 2 ulp; the factor is rounded to fp16 below
+                    Rf[i] = v * rR[i];
+                }
             }
         }
+        if (p.flags & KVARN_FLAG_NO_CHANNEL_PASS) continue;   // (uniform over the CTA)
+        // channel pass: C_c = population std over tokens of x_rot[t][c] / R_t
         float cs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < RPW; ++i)
 #pragma unroll
             for (int k = 0; k < 4; ++k) cs[k] += x[i][k] * rR[i];
-        *reinterpret_cast<float4*>(&q.part_a[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
-        __syncthreads();
-        float mu[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4 m4 = column_totals<B>(q, cs, warp, lane, buf);
+        buf ^= 1;
+        const float cmu[4] = {m4.x * (1.0f / B), m4.y * (1.0f / B), m4.z * (1.0f / B), m4.w * (1.0f / B)};
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            float4 v = *reinterpret_cast<const float4*>(&q.part_a[w][4 * lane]);
-            mu[0] += v.x; mu[1] += v.y; mu[2] += v.z; mu[3] += v.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) { mu[k] *= (1.0f / B); cs[k] = 0.f; }
+        for (int k = 0; k < 4; ++k) cs[k] = 0.f;
 #pragma unroll
         for (int i = 0; i < RPW; ++i)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                float d = x[i][k] * rR[i] - mu[k];
+                const float d = x[i][k] * rR[i] - cmu[k];
                 cs[k] += d * d;
             }
-        *reinterpret_cast<float4*>(&q.part_b[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
-        __syncthreads();
-        float var[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            float4 v = *reinterpret_cast<const float4*>(&q.part_b[w][4 * lane]);
-            var[0] += v.x; var[1] += v.y; var[2] += v.z; var[3] += v.w;
-        }
+        const float4 v4 = column_totals<B>(q, cs, warp, lane, buf);
+        buf ^= 1;
+        const float cvar[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            float vk = var[k] * (1.0f / B);
-            if (usable_variance(vk, mu[k])) {
-                Cf[k] = sqrtf(vk);
-                rCf[k] = __frcp_rn(Cf[k]);
+            const float vk = cvar[k] * (1.0f / B);
+            if (usable_variance(vk, cmu[k])) {
+                rCf[k] = rsqrtf(vk);
+                Cf[k] = vk * rCf[k];
             }
         }
     }
@@ -353,7 +405,7 @@ __global__ void __launch_bounds__(256) dequantize_kernel(
             const float code = (float)((words[word] >> bit) & 3u);
             v[k] = fmaf(code, s, z) * R * h2f(C_sec[c]);
         }
-        if (!rotated) {
+        if (!rotated && !(p.flags & KVARN_FLAG_NO_ROTATION)) {
             fwht128(v, lane);
 #pragma unroll
             for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD * sign_of(p.sb, 4 * lane + k);
@@ -367,6 +419,7 @@ static QuantParams make_params(const kvarn_config& cfg, int kind) {
     QuantParams p;
     p.kind = kind;
     p.iters = cfg.varn_iters;
+    p.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) p.sb[i] = cfg.sign_bits[i];
     return p;
 }

@@ -1,9 +1,10 @@
 // split.cuh -- balanced split-K partition shared by the decode-attention
 // kernels. The (sequence, kv head) units are laid end to end, block by block
-// (sequence-major, then head, then block); warp w of nw takes global blocks
-// [floor(w*W/nw), floor((w+1)*W/nw)). A unit's partial from warp w lives in
-// slot (unit + w), which is unique because consecutive units share at most
-// one warp.
+// (sequence-major, then head, then block); warp w of the nw active warps
+// (nw = min(resident warps, W)) takes global blocks [floor(w*W/nw),
+// floor((w+1)*W/nw)), at least one. A unit's partial from warp w lives in slot
+// (unit + w), which is unique because a later unit's warps never come before
+// an earlier unit's; the warps of one unit are consecutive.
 #pragma once
 #include "common.cuh"
 
@@ -88,6 +89,13 @@ __device__ __forceinline__ void split_prefix(const SplitArgs& s, int b, int lane
         total += warp_sum_i64(nb);
         before += warp_sum_i64(bb < b ? nb : 0);
     }
+}
+
+// Warps that take part in a split of W blocks over at most nw warps: all of
+// them, but never more than there are blocks, so that every active warp owns
+// at least one block and a unit's partials sit in consecutive slots.
+__host__ __device__ __forceinline__ int64_t split_active_warps(int64_t W, int64_t nw) {
+    return W < nw ? W : nw;
 }
 
 // Largest w in [0, nw) with floor(w*W/nw) <= x.

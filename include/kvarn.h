@@ -96,12 +96,28 @@ typedef struct kvarn_config {
     int32_t block_size;     /* tokens per block B: 32 or 64 */
     int32_t group_size;     /* channels per quantisation group: must be 32 */
     int32_t bits;           /* must be 2 */
-    int32_t varn_iters;     /* VarN iterations (token pass then channel pass): 1..8 */
+    int32_t varn_iters;     /* VarN iterations (token pass then channel pass): 0..8 */
     int32_t n_q_heads;      /* query heads */
     int32_t n_kv_heads;     /* kv heads; n_q_heads / n_kv_heads in 1..4 */
     float sm_scale;         /* softmax scale; 0 means 1/sqrt(head_dim) */
     uint32_t sign_bits[4];  /* rotation signs: bit c set => channel c negated */
+    uint32_t flags;         /* 0 for the method; KVARN_FLAG_* bits select an ablation */
 } kvarn_config;
+
+/*
+ * Ablation switches (section 五 of the method page, its ablation list: the
+ * full method against Hadamard only, VarN only, and VarN along one axis).
+ * They change what is stored, so a cache must be read with the flags it was
+ * written with. Hadamard only = flags 0 with varn_iters 0.
+ *   KVARN_FLAG_NO_ROTATION      no Hadamard rotation (R = I): keys, values and
+ *                               queries stay in the original space and the
+ *                               output is not rotated back
+ *   KVARN_FLAG_NO_TOKEN_PASS    VarN without its token-axis pass (R_t = 1)
+ *   KVARN_FLAG_NO_CHANNEL_PASS  VarN without its channel-axis pass (C_c = 1)
+ */
+#define KVARN_FLAG_NO_ROTATION 0x1u
+#define KVARN_FLAG_NO_TOKEN_PASS 0x2u
+#define KVARN_FLAG_NO_CHANNEL_PASS 0x4u
 
 /* Library version string, e.g. "kvarn 0.1 sm_103a". */
 const char* kvarn_version(void);
@@ -185,7 +201,8 @@ int kvarn_append(const kvarn_config* cfg, void* pool, int64_t n_pool_blocks, voi
  * kvarn_workspace_bytes(cfg, batch, max_blocks_per_seq) bytes, 16-byte
  * aligned, passed as workspace_bytes. The work is split evenly over the
  * GPU's resident warps (split-K over each sequence's blocks) and merged by a
- * second kernel on the same stream. Device faults: KVARN_DEVERR_BLOCK_ID,
+ * second kernel on the same stream. n_pool_blocks must be below 2^31
+ * (KVARN_ERR_INVALID_ARG otherwise). Device faults: KVARN_DEVERR_BLOCK_ID,
  * KVARN_DEVERR_POSITION, KVARN_DEVERR_WAIT_TIMEOUT.
  */
 int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,

@@ -42,14 +42,14 @@ def f16_neighbours(v: float):
 
 
 def staged_quantize_parity(X: np.ndarray, gpu_bytes: np.ndarray, B: int, iters: int, kind: int,
-                           sign_bits) -> Counter:
+                           sign_bits, flags: int = 0) -> Counter:
     """X: [n][B][128] float64 inputs exactly as the GPU read them; gpu_bytes:
     [n][head_block_bytes] uint8. Raises AssertionError on a violation."""
     st = Counter()
     X = np.asarray(X, dtype=np.float64)
     n = X.shape[0]
     for i in range(n):
-        ref = oracle.quantize_block(X[i], iters, kind, sign_bits)
+        ref = oracle.quantize_block(X[i], iters, kind, sign_bits, flags=flags)
         f = oracle.unpack(B, kind, gpu_bytes[i])
         # ---- factors
         raw = np.concatenate([ref["R"], ref["C"]])
@@ -178,4 +178,4 @@ def oracle_attention(cache: PagedCache, q: torch.Tensor, seq_lens, sign_bits, sm
     pool_np = cache.pool.cpu().numpy() if pool_np is None else pool_np
     return oracle.decode_attention(cfg.block_size, cfg.n_q_heads, cfg.n_kv_heads, sign_bits, sm_scale, qn,
                                    pool_np, stg, np.ascontiguousarray(cache.block_table_np[seqs]),
-                                   np.asarray(seq_lens, dtype=np.int32)[seqs])
+                                   np.asarray(seq_lens, dtype=np.int32)[seqs], flags=int(cfg.flags))

@@ -64,3 +64,13 @@ def test_invalid_arguments_are_rejected_before_any_launch():
     bad = _cfg(varn_iters=0)
     assert L.kvarn_dequantize(ctypes.byref(bad), 0, None, None, 1, 0, None, None) == INV
     assert kv.status_string(-4) == "workspace too small"
+
+
+def test_ablation_flags_and_zero_iterations_are_validated():
+    L = kv.lib()
+    assert kv.head_block_bytes(_cfg(varn_iters=0)) == 1856                  # Hadamard only
+    assert kv.head_block_bytes(_cfg(flags=kv.FLAG_NO_ROTATION | kv.FLAG_NO_TOKEN_PASS)) == 1856
+    for bad in (_cfg(varn_iters=-1), _cfg(varn_iters=9), _cfg(flags=8)):
+        assert kv.head_block_bytes(bad) == 0
+        assert L.kvarn_quantize_block(ctypes.byref(bad), 0, None, 0, 1, 4096, 128, None, None, None,
+                                      None) == kv._abi.ERR_INVALID_ARG

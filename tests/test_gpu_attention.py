@@ -138,11 +138,13 @@ def test_bf16_cache_kernel(kvlib):
         q = synth.queries(g, batch, n_q).cuda()
         perm = np.random.default_rng(B).permutation(batch * max_blocks).astype(np.int32)
         bt = perm.reshape(batch, max_blocks)
-        pool = torch.zeros(batch * max_blocks, n_kv, 2, B, D, dtype=torch.bfloat16)
+        # rows past each sequence's length hold NaN: the kernel must never let them in
+        pool = torch.full((batch * max_blocks, n_kv, 2, B, D), float("nan"), dtype=torch.bfloat16)
         for b in range(batch):
             for j in range(max_blocks):
-                pool[bt[b, j], :, 0] = K[b, :, j * B:(j + 1) * B]
-                pool[bt[b, j], :, 1] = V[b, :, j * B:(j + 1) * B]
+                n = min(B, max(0, lens[b] - j * B))
+                pool[bt[b, j], :, 0, :n] = K[b, :, j * B:j * B + n]
+                pool[bt[b, j], :, 1, :n] = V[b, :, j * B:j * B + n]
         out = torch.empty(batch, n_q, D, device="cuda")
         ws = kv.alloc_workspace(cfg, batch, max_blocks)
         kv.decode_attn_bf16(cfg, q, pool.cuda(), torch.from_numpy(bt).cuda(),
@@ -157,3 +159,62 @@ def test_bf16_cache_kernel(kvlib):
                 ref = oracle.attention(qd[b, j], Kd[b, j // G, :lens[b]], Vd[b, j // G, :lens[b]],
                                        1 / math.sqrt(D))
                 attn_close(got[b, j], ref)
+
+
+@pytest.mark.parametrize("B,iters", [(32, 3), (64, 2)])
+def test_small_call_after_large_on_one_workspace(kvlib, B, iters):
+    """A workload with fewer blocks than resident warps, run on a workspace a
+    large call has just filled with partials: the merge must read only the
+    partials of warps that own blocks of each unit (stale slots of the
+    earlier call must not leak in), for the 2-bit and the bf16 kernel."""
+    kv = kvlib
+    n_q, n_kv = 32, 8
+    sb = synth.sign_bits(7 + B)
+    cfg = kv.make_config(n_q, n_kv, B, iters, sb)
+    g = synth.make_gen(900 + B)
+    big_batch, big_len = 16, 64 * B       # 16 * 8 * 64 blocks: more than the resident warps
+    small_lens = [3 * B + 5]
+    ws = kv.alloc_workspace(cfg, big_batch, 64)
+    # ---- large call: fills every partial slot with its own data
+    Kb = synth.kv_values(g, big_batch, n_kv, big_len, 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    Vb = synth.kv_values(g, big_batch, n_kv, big_len, 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    big = PagedCache(kv, cfg, big_batch, 64, perm_seed=1)
+    big.prefill(Kb, Vb, [big_len] * big_batch)
+    del Kb, Vb
+    qb = synth.queries(g, big_batch, n_q).to(torch.bfloat16).cuda()
+    out_b = torch.empty(big_batch, n_q, D, device="cuda")
+    kv.decode_attn(cfg, qb, big.pool, big.staging, big.block_table,
+                   torch.full((big_batch,), big_len, dtype=torch.int32, device="cuda"), out_b, ws)
+    # ---- small call on the same workspace
+    Ks = synth.kv_values(g, 1, n_kv, small_lens[0], 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    Vs = synth.kv_values(g, 1, n_kv, small_lens[0], 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    small = PagedCache(kv, cfg, 1, 4, perm_seed=2)
+    small.prefill(Ks, Vs, small_lens)
+    qs = synth.queries(g, 1, n_q).to(torch.bfloat16).cuda()
+    out_s = torch.full((1, n_q, D), float("nan"), device="cuda")
+    kv.decode_attn(cfg, qs, small.pool, small.staging, small.block_table,
+                   torch.tensor(small_lens, dtype=torch.int32, device="cuda"), out_s, ws)
+    torch.cuda.synchronize()
+    assert kv.read_error(ws) == 0
+    attn_close(out_s.cpu().double().numpy(), oracle_attention(small, qs, small_lens, sb))
+    # ---- the bf16 kernel on the same workspace, after another large call
+    kvp_big = torch.randn(big_batch * 64, n_kv, 2, B, D, device="cuda").to(torch.bfloat16)
+    btb = torch.arange(big_batch * 64, dtype=torch.int32, device="cuda").view(big_batch, 64)
+    kv.decode_attn_bf16(cfg, qb, kvp_big, btb,
+                        torch.full((big_batch,), big_len, dtype=torch.int32, device="cuda"), out_b, ws)
+    L = small_lens[0]
+    nb = (L + B - 1) // B
+    kvp = torch.zeros(nb, n_kv, 2, B, D, dtype=torch.bfloat16)
+    for j in range(nb):
+        n = min(B, L - j * B)
+        kvp[j, :, 0, :n] = Ks[0, :, j * B:j * B + n].cpu()
+        kvp[j, :, 1, :n] = Vs[0, :, j * B:j * B + n].cpu()
+    kv.decode_attn_bf16(cfg, qs, kvp.cuda(), torch.arange(nb, dtype=torch.int32, device="cuda").view(1, nb),
+                        torch.tensor(small_lens, dtype=torch.int32, device="cuda"), out_s, ws)
+    torch.cuda.synchronize()
+    assert kv.read_error(ws) == 0
+    got = out_s.cpu().double().numpy()
+    Kd, Vd, qd = Ks.double().cpu().numpy(), Vs.double().cpu().numpy(), qs.double().cpu().numpy()
+    for j in range(n_q):
+        ref = oracle.attention(qd[0, j], Kd[0, j // 4, :L], Vd[0, j // 4, :L], 1 / math.sqrt(D))
+        attn_close(got[0, j], ref)
