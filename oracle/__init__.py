@@ -90,6 +90,8 @@ def lib():
                 "orc_attention_rotated": (None, [_f64p, _f64p, _f64p, _i64, _d, _u32p, _f64p]),
                 "orc_decode_attention": (None, [_i, ctypes.c_uint32, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
                                                 _i32p, _i, _i32p, _i, _f64p]),
+                "orc_error_split": (None, [_f64p, _f64p, _f64p]),
+                "orc_error_decomposition": (None, [_i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p]),
                 "orc_normalise": (None, [_i, _f64p, _f64p, _f64p, _f64p]),
                 "orc_group_params_all": (None, [_i, _f64p, _f64p, _f64p, _f64p, _f64p]),
                 "orc_codes_given": (None, [_i, _f64p, _f64p, _f64p, _i32p, _f64p]),
@@ -342,6 +344,30 @@ def decode_attention(B, n_q, n_kv, sign_bits, sm_scale, q, pool, staging, block_
     lib().orc_decode_attention(B, flags, n_q, n_kv, _p(s, _u32p), float(sm_scale), _p(q, _f64p),
                                _p(pool, _u8p), _p(staging, _u16p), _p(bt, _i32p), bt.shape[1],
                                _p(sl, _i32p), batch, _p(out, _f64p))
+    return out
+
+
+# --------------------------------------------------------------------------
+# error decomposition (magnitude / direction)
+# --------------------------------------------------------------------------
+
+def error_split(x, xh) -> np.ndarray:
+    """(|x|, |x^|, |E_M|, |E_D|) of one token vector and its quantised version."""
+    x, xh = _f64(x).reshape(D), _f64(xh).reshape(D)
+    out = np.empty(4)
+    lib().orc_error_split(_p(x, _f64p), _p(xh, _f64p), _p(out, _f64p))
+    return out
+
+
+def error_decomposition(X, packed, B: int, kind: int, sign_bits, flags: int = 0) -> np.ndarray:
+    """X: [n][B][128] values before quantisation, packed: [n][bytes] -> [n][B][4]."""
+    X = _f64(X).reshape(-1, B, D)
+    pk = np.ascontiguousarray(packed, dtype=np.uint8).reshape(X.shape[0], -1)
+    out = np.empty((X.shape[0], B, 4))
+    s = _signs(sign_bits)
+    for i in range(X.shape[0]):
+        lib().orc_error_decomposition(B, flags, kind, _p(s, _u32p), _p(X[i], _f64p), _p(pk[i], _u8p),
+                                      _p(out[i], _f64p))
     return out
 
 

@@ -662,6 +662,58 @@ void orc_decode_attention(int B, uint32_t flags, int n_q, int n_kv, const uint32
 }
 
 /* ------------------------------------------------------------------------ */
+/* Error decomposition  [AP3] section 二: a token vector x and its quantised  */
+/* version x^ = x + eps; eps = E_M + E_D with the magnitude part             */
+/*   E_M = (|x^| - |x|) x / |x|                                              */
+/* and the direction part                                                     */
+/*   E_D = |x^| (x^ / |x^| - x / |x|).                                        */
+/* out = (|x|, |x^|, |E_M|, |E_D|). Reading: for x = 0 the direction x/|x| is */
+/* undefined and all of eps (= x^) is counted as magnitude error; for x^ = 0  */
+/* the formula itself gives E_M = -x, E_D = 0.                               */
+/* ------------------------------------------------------------------------ */
+
+void orc_error_split(const double* x, const double* xh, double* out)
+{
+    double nx = 0.0, nh = 0.0;
+    for (int c = 0; c < ORC_D; c++) {
+        nx += x[c] * x[c];
+        nh += xh[c] * xh[c];
+    }
+    nx = sqrt(nx);
+    nh = sqrt(nh);
+    out[0] = nx;
+    out[1] = nh;
+    if (nx == 0.0) {
+        out[2] = nh;
+        out[3] = 0.0;
+        return;
+    }
+    out[2] = fabs(nh - nx);
+    if (nh == 0.0) {
+        out[3] = 0.0;
+        return;
+    }
+    double d = 0.0;
+    for (int c = 0; c < ORC_D; c++) {
+        double u = xh[c] / nh - x[c] / nx;
+        d += u * u;
+    }
+    out[3] = nh * sqrt(d);
+}
+
+/* Per token of a head-block: X [B][128] the values before quantisation,
+ * packed the head-block's bytes; out [B][4] as orc_error_split. */
+void orc_error_decomposition(int B, uint32_t flags, int kind, const uint32_t sign_bits[4],
+                             const double* X, const uint8_t* packed, double* out)
+{
+    double* xh = (double*)malloc(sizeof(double) * (size_t)B * ORC_D);
+    orc_decode_block(B, flags, kind, sign_bits, packed, 0, xh);
+    for (int t = 0; t < B; t++)
+        orc_error_split(X + (size_t)t * ORC_D, xh + (size_t)t * ORC_D, out + 4 * t);
+    free(xh);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Staged hand-off helpers for parity: each stage is recomputed from the      */
 /* other side's already validated rounded values, so one boundary case      */
 /* cannot cascade into later stages.                                         */

@@ -505,3 +505,46 @@ def test_decode_attention_without_rotation_equals_plain_attention_over_decoded_k
         s = 0.1 * Kd @ q[0, h]
         p = np.exp(s - s.max())
         np.testing.assert_allclose(out[0, h], p @ Vd / p.sum(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- error decomposition
+
+def test_error_split_closed_forms():
+    """Magnitude / direction split of the quantisation error on vectors whose
+    answer is known by hand."""
+    rng = np.random.default_rng(80)
+    x = rng.standard_normal(D)
+    n = np.linalg.norm(x)
+    np.testing.assert_allclose(oracle.error_split(x, x), [n, n, 0, 0], atol=1e-12)
+    # pure scaling is all magnitude error: |E_M| = |k - 1| |x|
+    np.testing.assert_allclose(oracle.error_split(x, 2.5 * x), [n, 2.5 * n, 1.5 * n, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.error_split(x, 0.25 * x), [n, 0.25 * n, 0.75 * n, 0], rtol=1e-12,
+                               atol=1e-12)
+    # a rotation by 90 degrees at equal length is all direction error: |E_D| = sqrt(2) |x|
+    e = np.zeros(D); e[3] = 2.0
+    f = np.zeros(D); f[17] = 2.0
+    np.testing.assert_allclose(oracle.error_split(e, f), [2, 2, 0, 2 * math.sqrt(2)], rtol=1e-12)
+    # opposite direction, 3x the length: |E_M| = 2|x|, |E_D| = 3|x| * 2
+    np.testing.assert_allclose(oracle.error_split(e, -3 * e), [2, 6, 4, 12], rtol=1e-12)
+    # the degenerate ends of the reading
+    np.testing.assert_allclose(oracle.error_split(np.zeros(D), f), [0, 2, 2, 0])
+    np.testing.assert_allclose(oracle.error_split(e, np.zeros(D)), [2, 0, 2, 0])
+
+
+def test_error_split_parts_add_up_to_the_error():
+    """|E_M + E_D| = |x^ - x| and the triangle inequality, on quantised data."""
+    sb = synth.sign_bits(81)
+    X = _block(81, 32)
+    r = oracle.quantize_block(X, 3, oracle.KIND_K, sb)
+    Xh = oracle.decode_blocks(r["bytes"], 32, 0, sb, rotated=False)[0]
+    out = oracle.error_decomposition(X[None], r["bytes"][None], 32, 0, sb)[0]
+    for t in range(32):
+        nx, nh, em, ed = out[t]
+        assert nx == pytest.approx(np.linalg.norm(X[t]), rel=1e-12)
+        assert nh == pytest.approx(np.linalg.norm(Xh[t]), rel=1e-12)
+        err = np.linalg.norm(Xh[t] - X[t])
+        # E_M is parallel to x and E_D = x^ - |x^| x/|x|, so |E_M + E_D|^2 follows from
+        # the law of cosines on x^ and x: both sides computed independently here
+        cos = X[t] @ Xh[t] / (nx * nh)
+        assert ed == pytest.approx(nh * math.sqrt(max(0.0, 2 - 2 * cos)), rel=1e-6, abs=1e-12)
+        assert em <= err * (1 + 1e-12) and ed <= err + em + 1e-12 and err <= em + ed + 1e-12
