@@ -279,6 +279,24 @@ def run_gpu(args, rank, world):
     assert kv.read_error(ws) == 0, "device error during the timed steps"
     clocks = clk.summary()
 
+    # the same step captured once as a CUDA graph and replayed (no per-launch host work)
+    graph_ms = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        graph_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, device)
+        del graph
+    except RuntimeError as e:   # capture unsupported here: report, do not fall back silently
+        graph_ms = f"capture failed: {e}"
     attn_bytes, app_bytes, attn_launch_bytes, app_launch_bytes = algorithmic_bytes(w, layers)
     ms_per_step = total_ms / args.steps
     value = whole_job_gbs(attn_bytes + app_bytes, world, ms_per_step)
@@ -307,6 +325,9 @@ def run_gpu(args, rank, world):
                    "parallelism": f"replicas x{world} (each rank its own {batch} sequences; no collective "
                                   "on the data path)"},
         "decode_step_tokens_per_s": round(world * batch / (ms_per_step * 1e-3), 1),
+        "cuda_graph_step": ({"ms_per_step": round(graph_ms, 4),
+                             "GB_per_s": round(whole_job_gbs(attn_bytes + app_bytes, world, graph_ms), 2)}
+                            if isinstance(graph_ms, float) else graph_ms),
         "decode_attn": {"GB_per_s": round(achieved, 1), "us_per_layer": round(attn_launch_ms * 1e3, 2),
                         "algorithmic_bytes_per_layer": int(attn_launch_bytes),
                         "frac_of_hbm_peak": round(achieved / peak, 4),
@@ -651,7 +672,7 @@ def run_ablation(args):
         staging = kv.alloc_staging(cfg, batch, dev)
         ws = kv.alloc_workspace(cfg, batch, nb, dev)
         hb, bb = kv.head_block_bytes(cfg), kv.block_bytes(cfg)
-        rec = []
+        rec, split = [], []
         for kind, T in ((0, K), (1, V)):
             offs = (bt[:, None, :].long() * bb + (2 * torch.arange(n_kv, device=dev)[None, :, None] + kind) * hb)
             kv.quantize_block(cfg, kind, T.contiguous(), pool, ws, dst_offsets=offs.reshape(-1).contiguous(),
@@ -660,6 +681,13 @@ def run_ablation(args):
             kv.dequantize(cfg, kind, pool, deq, rotated=False, src_offsets=offs.reshape(-1).contiguous())
             x = T.float().reshape(-1, B, D)
             rec.append(float(((deq - x) ** 2).sum() / (x ** 2).sum()))
+            es = torch.empty(batch * n_kv * nb, B, 4, device=dev)
+            kv.error_decomposition(cfg, kind, T.contiguous(), pool, es, packed_offsets=offs.reshape(-1).contiguous())
+            es = es.reshape(-1, 4)
+            top = es[:, 0] >= torch.quantile(es[:, 0], 0.9)
+            split.append({"em_over_ed_energy": round(float((es[:, 2] ** 2).sum() / (es[:, 3] ** 2).sum()), 4),
+                          "em_dominant_frac": round(float((es[:, 2] > es[:, 3]).float().mean()), 4),
+                          "em_dominant_frac_top_norm_decile": round(float((es[top, 2] > es[top, 3]).float().mean()), 4)})
         out = torch.empty(batch, n_q, D, device=dev)
         kv.decode_attn(cfg, q, pool, staging, bt, lens, out, ws)
         torch.cuda.synchronize()
@@ -669,7 +697,8 @@ def run_ablation(args):
         print(json.dumps({"ablation": name, "flags": flags, "varn_iters": iters, "workload": w.name,
                           "attn_rel_l2_vs_bf16": round(float(d.norm() / ref.norm()), 5),
                           "attn_mean_cosine_vs_bf16": round(float(cos.mean()), 5),
-                          "k_rel_mse": round(rec[0], 5), "v_rel_mse": round(rec[1], 5)}), flush=True)
+                          "k_rel_mse": round(rec[0], 5), "v_rel_mse": round(rec[1], 5),
+                          "error_split_k": split[0], "error_split_v": split[1]}), flush=True)
         del pool, staging, ws
         torch.cuda.empty_cache()
 

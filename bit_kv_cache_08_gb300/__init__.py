@@ -9,7 +9,7 @@ from ._abi import (BF16, FP32, KIND_K, KIND_V, DEVERR_BLOCK_ID, DEVERR_NONFINITE
                    FLAG_NO_CHANNEL_PASS, FLAG_NO_ROTATION, FLAG_NO_TOKEN_PASS,
                    DEVERR_POSITION, DEVERR_WAIT_TIMEOUT, Config, KVarNError, alloc_pool,
                    alloc_staging, alloc_workspace, append, block_bytes, clear_error, decode_attn,
-                   decode_attn_bf16, decode_attn_noalloc, dequantize, head_block_bytes, header_symbols, lib, make_config,
+                   decode_attn_bf16, decode_attn_noalloc, dequantize, error_decomposition, head_block_bytes, header_symbols, lib, make_config,
                    quantize_block, read_error, staging_bytes, status_string, version,
                    workspace_bytes)
 from .build import build  # noqa: F401

