@@ -43,9 +43,18 @@
 
 namespace kvarn {
 
+// 2^x by the MUFU instruction (relative error ~2^-22; results below 2^-126,
+// i.e. softmax weights that cannot move an fp32 sum, flush to 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- the split-K kernel
 template <int B, int S>
 __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
+    wait_prior_grids();
     constexpr int HB = head_block_bytes(B);
     constexpr int NSB = B / 32;
     extern __shared__ __align__(16) uint8_t smem[];
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
             const float m_new = fmaxf(m_run, bm);
-            const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+            const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
             float pR[NSB][4], psum = 0.f, pmax = 0.f;
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 const float Rv[4] = {R01.x, R01.y, R23.x, R23.y};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float p = (m_new == -INFINITY) ? 0.f : exp2f(sc[sb][i] - m_new);
+                    const float p = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[sb][i] - m_new);
                     psum += p;
                     pR[sb][i] = p * Rv[i];
                     pmax = fmaxf(pmax, pR[sb][i]);
@@ -566,14 +575,15 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)batch * a.n_q + 3) / 4);
+    cudaError_t e;
     if (cfg.block_size == 32) {
-        decode_attn_2bit_kernel<32, stages_for<32>()><<<nw, 32, attn_smem_bytes<32>(), st>>>(a);
-        merge_kernel<32, true><<<mgrid, 128, 0, st>>>(a);
+        e = launch_pdl(decode_attn_2bit_kernel<32, stages_for<32>()>, nw, 32, attn_smem_bytes<32>(), st, a);
+        if (e == cudaSuccess) e = launch_pdl(merge_kernel<32, true>, mgrid, 128, 0, st, a);
     } else {
-        decode_attn_2bit_kernel<64, stages_for<64>()><<<nw, 32, attn_smem_bytes<64>(), st>>>(a);
-        merge_kernel<64, true><<<mgrid, 128, 0, st>>>(a);
+        e = launch_pdl(decode_attn_2bit_kernel<64, stages_for<64>()>, nw, 32, attn_smem_bytes<64>(), st, a);
+        if (e == cudaSuccess) e = launch_pdl(merge_kernel<64, true>, mgrid, 128, 0, st, a);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace kvarn

@@ -54,6 +54,7 @@ __device__ __forceinline__ void split_bf16x2(float v0, float v1, uint32_t& hi, u
 
 template <int B>
 __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
+    wait_prior_grids();
     constexpr int CPB = B / kChunk;   // chunks per page
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;
@@ -296,12 +297,13 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
     a.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)batch * a.n_q + 3) / 4);
+    cudaError_t e;
     if (cfg.block_size == 32)
-        decode_attn_bf16_kernel<32><<<nw, 32, attn_bf16_smem_bytes(), st>>>(a);
+        e = launch_pdl(decode_attn_bf16_kernel<32>, nw, 32, attn_bf16_smem_bytes(), st, a);
     else
-        decode_attn_bf16_kernel<64><<<nw, 32, attn_bf16_smem_bytes(), st>>>(a);
-    merge_kernel<kChunk, false><<<mgrid, 128, 0, st>>>(a);
-    return cudaGetLastError();
+        e = launch_pdl(decode_attn_bf16_kernel<64>, nw, 32, attn_bf16_smem_bytes(), st, a);
+    if (e == cudaSuccess) e = launch_pdl(merge_kernel<kChunk, false>, mgrid, 128, 0, st, a);
+    return e;
 }
 
 }  // namespace kvarn

@@ -93,6 +93,7 @@ __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t row,
 // the bf16 cache (ROT = false) has every token in its pages.
 template <int B, bool ROT>
 __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
+    wait_prior_grids();
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (gw >= (int64_t)a.batch * a.n_q) return;

@@ -76,6 +76,30 @@ __device__ __forceinline__ void fwht128(float (&v)[4], int lane) {
     }
 }
 
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch: every kernel of this library is launched with
+// programmatic stream serialization and begins with a wait on the grids ahead
+// of it in the stream. Its CTAs may then be scheduled while the previous
+// kernel drains, and its memory accesses still see everything that kernel
+// wrote (the wait returns once those grids have completed and flushed).
+__device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = grid;
+    c.blockDim = block;
+    c.dynamicSmemBytes = smem;
+    c.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    c.attrs = at;
+    c.numAttrs = 1;
+    return cudaLaunchKernelEx(&c, kernel, args...);
+}
+
 // ---------------------------------------------------------------- fp16 helpers
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __device__ __forceinline__ uint16_t f2h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }

@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(quant_threads<B>()) quantize_blocks_kernel(
     const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
     uint8_t* __restrict__ dst_base, const int64_t* __restrict__ dst_offsets, QuantParams p,
     uint32_t* err) {
+    wait_prior_grids();
     __shared__ QuantSmem<B> q;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(quant_threads<B>()) append_kernel(
     uint16_t* __restrict__ staging, const int32_t* __restrict__ block_table, int max_blocks,
     const int32_t* __restrict__ pos_arr, const uint16_t* __restrict__ k_new,
     const uint16_t* __restrict__ v_new, int n_kv, QuantParams p, uint32_t* err) {
+    wait_prior_grids();
     __shared__ QuantSmem<B> q;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
@@ -407,6 +409,7 @@ template <int B>
 __global__ void __launch_bounds__(256) dequantize_kernel(
     const uint8_t* __restrict__ src_base, const int64_t* __restrict__ src_offsets, int kind,
     int rotated, QuantParams p, float* __restrict__ out) {
+    wait_prior_grids();
     __shared__ alignas(16) uint8_t img[head_block_bytes(B)];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
@@ -436,6 +439,7 @@ __global__ void __launch_bounds__(256) error_split_kernel(
     const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
     const uint8_t* __restrict__ packed_base, const int64_t* __restrict__ packed_offsets, int kind,
     QuantParams p, float* __restrict__ out) {
+    wait_prior_grids();
     __shared__ alignas(16) uint8_t img[head_block_bytes(B)];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
@@ -493,12 +497,10 @@ cudaError_t launch_quantize_blocks(const kvarn_config& cfg, int kind, const void
                                    cudaStream_t st) {
     QuantParams p = make_params(cfg, kind);
     if (cfg.block_size == 32)
-        quantize_blocks_kernel<32><<<(unsigned)n, quant_threads<32>(), 0, st>>>(src, dtype, block_stride, token_stride,
-                                                                (uint8_t*)dst_base, dst_offsets, p, err);
-    else
-        quantize_blocks_kernel<64><<<(unsigned)n, quant_threads<64>(), 0, st>>>(src, dtype, block_stride, token_stride,
-                                                                (uint8_t*)dst_base, dst_offsets, p, err);
-    return cudaGetLastError();
+        return launch_pdl(quantize_blocks_kernel<32>, (unsigned)n, quant_threads<32>(), 0, st, src, dtype,
+                          block_stride, token_stride, (uint8_t*)dst_base, dst_offsets, p, err);
+    return launch_pdl(quantize_blocks_kernel<64>, (unsigned)n, quant_threads<64>(), 0, st, src, dtype,
+                      block_stride, token_stride, (uint8_t*)dst_base, dst_offsets, p, err);
 }
 
 cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_blocks,
@@ -506,18 +508,14 @@ cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_bl
                           int max_blocks, const int32_t* pos, const void* k_new, const void* v_new,
                           int batch, uint32_t* err, cudaStream_t st) {
     QuantParams p = make_params(cfg, 0);
-    dim3 grid(batch, cfg.n_kv_heads, 2);
+    const dim3 grid(batch, cfg.n_kv_heads, 2);
     if (cfg.block_size == 32)
-        append_kernel<32><<<grid, quant_threads<32>(), 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
-                                                (uint16_t*)staging, block_table, max_blocks, pos,
-                                                (const uint16_t*)k_new, (const uint16_t*)v_new,
-                                                cfg.n_kv_heads, p, err);
-    else
-        append_kernel<64><<<grid, quant_threads<64>(), 0, st>>>((uint8_t*)pool, n_pool_blocks, block_bytes,
-                                                (uint16_t*)staging, block_table, max_blocks, pos,
-                                                (const uint16_t*)k_new, (const uint16_t*)v_new,
-                                                cfg.n_kv_heads, p, err);
-    return cudaGetLastError();
+        return launch_pdl(append_kernel<32>, grid, quant_threads<32>(), 0, st, (uint8_t*)pool, n_pool_blocks,
+                          block_bytes, (uint16_t*)staging, block_table, max_blocks, pos, (const uint16_t*)k_new,
+                          (const uint16_t*)v_new, cfg.n_kv_heads, p, err);
+    return launch_pdl(append_kernel<64>, grid, quant_threads<64>(), 0, st, (uint8_t*)pool, n_pool_blocks,
+                      block_bytes, (uint16_t*)staging, block_table, max_blocks, pos, (const uint16_t*)k_new,
+                      (const uint16_t*)v_new, cfg.n_kv_heads, p, err);
 }
 
 cudaError_t launch_error_split(const kvarn_config& cfg, int kind, const void* src, int dtype, int64_t n,
@@ -525,14 +523,10 @@ cudaError_t launch_error_split(const kvarn_config& cfg, int kind, const void* sr
                                const int64_t* packed_offsets, float* out, cudaStream_t st) {
     QuantParams p = make_params(cfg, kind);
     if (cfg.block_size == 32)
-        error_split_kernel<32><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
-                                                            (const uint8_t*)packed_base, packed_offsets, kind, p,
-                                                            out);
-    else
-        error_split_kernel<64><<<(unsigned)n, 256, 0, st>>>(src, dtype, block_stride, token_stride,
-                                                            (const uint8_t*)packed_base, packed_offsets, kind, p,
-                                                            out);
-    return cudaGetLastError();
+        return launch_pdl(error_split_kernel<32>, (unsigned)n, 256, 0, st, src, dtype, block_stride, token_stride,
+                          (const uint8_t*)packed_base, packed_offsets, kind, p, out);
+    return launch_pdl(error_split_kernel<64>, (unsigned)n, 256, 0, st, src, dtype, block_stride, token_stride,
+                      (const uint8_t*)packed_base, packed_offsets, kind, p, out);
 }
 
 cudaError_t launch_dequantize(const kvarn_config& cfg, int kind, const void* src_base,
@@ -540,12 +534,10 @@ cudaError_t launch_dequantize(const kvarn_config& cfg, int kind, const void* src
                               cudaStream_t st) {
     QuantParams p = make_params(cfg, kind);
     if (cfg.block_size == 32)
-        dequantize_kernel<32><<<(unsigned)n, 256, 0, st>>>((const uint8_t*)src_base, src_offsets, kind,
-                                                           rotated, p, out);
-    else
-        dequantize_kernel<64><<<(unsigned)n, 256, 0, st>>>((const uint8_t*)src_base, src_offsets, kind,
-                                                           rotated, p, out);
-    return cudaGetLastError();
+        return launch_pdl(dequantize_kernel<32>, (unsigned)n, 256, 0, st, (const uint8_t*)src_base, src_offsets,
+                          kind, rotated, p, out);
+    return launch_pdl(dequantize_kernel<64>, (unsigned)n, 256, 0, st, (const uint8_t*)src_base, src_offsets,
+                      kind, rotated, p, out);
 }
 
 }  // namespace kvarn
