@@ -353,12 +353,10 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             }
             l_part = l_part * alpha + psum;
             m_run = m_new;
-            if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    O[mt][0] *= alpha;
-                    O[mt][1] *= alpha;
-                }
+            for (int mt = 0; mt < 8; ++mt) {   // (unconditional: cheaper than testing alpha == 1)
+                O[mt][0] *= alpha;
+                O[mt][1] *= alpha;
             }
             pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 4));
             pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 8));

@@ -128,8 +128,9 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
             float ls = 0.f;
             for (int i = lane; i < np; i += 32) ls += p0[i * pstride + 1] * exp2f(p0[i * pstride] - m);
             l = warp_sum(ls);
-            // every lane its 4 channels over all partials (independent loads)
-#pragma unroll 4
+            // every lane its 4 channels over all partials (independent loads; a
+            // deep unroll keeps many in flight when one unit has hundreds of partials)
+#pragma unroll 16
             for (int i = 0; i < np; ++i) {
                 const float* bp = p0 + i * pstride;
                 const float wgt = exp2f(bp[0] - m);
@@ -147,30 +148,60 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
             for (int k = 0; k < 4; ++k) acc[k] *= kInvSqrtD * sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + k);
         }
     }
-    const int ntail = ROT ? L - nb * B : 0;
+    const int ntail = ROT ? L - nb * B : 0;   // < B <= 64 raw rows in staging
     if (ntail > 0) {
         float qv[4];
         load_q4(a.q, a.q_dtype, gw, lane, qv);
         const float qs = a.sm_scale * kLog2e;
         const uint16_t* kst = a.staging + (((int64_t)b * a.n_kv + h) * 2 + 0) * B * kD;
         const uint16_t* vst = kst + B * kD;
-        for (int r = 0; r < ntail; ++r) {
-            const uint2 ku = reinterpret_cast<const uint2*>(kst + r * kD)[lane];
-            float d = qv[0] * __uint_as_float(ku.x << 16);
-            d = fmaf(qv[1], __uint_as_float(ku.x & 0xffff0000u), d);
-            d = fmaf(qv[2], __uint_as_float(ku.y << 16), d);
-            d = fmaf(qv[3], __uint_as_float(ku.y & 0xffff0000u), d);
-            const float sc = warp_sum(d) * qs;
-            const float mn = fmaxf(m, sc);
-            const float fa = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-            const float p = exp2f(sc - mn);
-            const uint2 vu = reinterpret_cast<const uint2*>(vst + r * kD)[lane];
-            acc[0] = acc[0] * fa + p * __uint_as_float(vu.x << 16);
-            acc[1] = acc[1] * fa + p * __uint_as_float(vu.x & 0xffff0000u);
-            acc[2] = acc[2] * fa + p * __uint_as_float(vu.y << 16);
-            acc[3] = acc[3] * fa + p * __uint_as_float(vu.y & 0xffff0000u);
-            l = l * fa + p;
-            m = mn;
+        // scores of all tail rows, 8 rows at a time with independent loads; row r's
+        // score ends on lane r % 32, slot r / 32
+        float mine[2] = {-INFINITY, -INFINITY};
+        for (int r0 = 0; r0 < ntail; r0 += 8) {
+            float d[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                d[k] = 0.f;
+                if (r0 + k < ntail) {
+                    const uint2 ku = reinterpret_cast<const uint2*>(kst + (r0 + k) * kD)[lane];
+                    d[k] = qv[0] * __uint_as_float(ku.x << 16);
+                    d[k] = fmaf(qv[1], __uint_as_float(ku.x & 0xffff0000u), d[k]);
+                    d[k] = fmaf(qv[2], __uint_as_float(ku.y << 16), d[k]);
+                    d[k] = fmaf(qv[3], __uint_as_float(ku.y & 0xffff0000u), d[k]);
+                }
+            }
+#pragma unroll
+            for (int mm = 16; mm >= 1; mm >>= 1)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d[k] += __shfl_xor_sync(kFull, d[k], mm);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int r = r0 + k;
+                if (r < ntail && lane == (r & 31)) mine[r >> 5] = d[k] * qs;
+            }
+        }
+        const float mt = warp_max(fmaxf(mine[0], mine[1]));
+        const float mn = fmaxf(m, mt);                      // finite: ntail > 0
+        const float fa = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+        const float p0 = exp2f(mine[0] - mn), p1 = exp2f(mine[1] - mn);   // 0 for empty slots
+        l = l * fa + warp_sum(p0 + p1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] *= fa;
+        m = mn;
+        for (int r0 = 0; r0 < ntail; r0 += 8) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int r = r0 + k;
+                if (r < ntail) {
+                    const float p = __shfl_sync(kFull, (r < 32) ? p0 : p1, r & 31);
+                    const uint2 vu = reinterpret_cast<const uint2*>(vst + r * kD)[lane];
+                    acc[0] = fmaf(p, __uint_as_float(vu.x << 16), acc[0]);
+                    acc[1] = fmaf(p, __uint_as_float(vu.x & 0xffff0000u), acc[1]);
+                    acc[2] = fmaf(p, __uint_as_float(vu.y << 16), acc[2]);
+                    acc[3] = fmaf(p, __uint_as_float(vu.y & 0xffff0000u), acc[3]);
+                }
+            }
         }
     }
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
