@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
     Cursor cc;
     cc.b = cc.h = cc.j = 0;
     const int64_t W = split_locate(sp, 0, lane, cc.b, cc.h, cc.j);
-    const int64_t nwe = split_active_warps(W, a.nw);   // every active warp gets >= 1 block
+    const int64_t nwe = split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, 0.f);   // >= 1 chunk per warp
     if (w >= nwe) return;
     const int64_t s_beg = (int64_t)w * W / nwe, s_end = (int64_t)(w + 1) * W / nwe;
     if (s_beg >= s_end) return;

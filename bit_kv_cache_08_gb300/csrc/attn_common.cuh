@@ -7,6 +7,10 @@
 namespace kvarn {
 
 constexpr uint32_t kWaitLimit = 1u << 22;
+// Cost of one 2-bit block per token of block size, in units of merging one
+// partial; see split_active_warps. Chosen from batch-1 timings of the
+// Llama-shaped sweep (1K-128K tokens), where 2-4 blocks per warp beat one.
+constexpr float kSplitRatio2bit = 0.5f;
 
 struct AttnArgs {
     const void* q;
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     const int nb = split_nblocks(sp, b);
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (nb > 0) {
-        const int64_t nwe = split_active_warps(W, a.nw);
+        const int64_t nwe = split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, ROT ? kSplitRatio2bit * B : 0.f);
         const int64_t Su = before * a.n_kv + (int64_t)h * nb;
         const int64_t u = (int64_t)b * a.n_kv + h;
         const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);

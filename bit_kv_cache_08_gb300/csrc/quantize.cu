@@ -67,23 +67,34 @@ __device__ __forceinline__ float4 column_totals(QuantSmem<B>& q, const float (&c
     return *reinterpret_cast<const float4*>(&q.tot[buf][4 * lane]);
 }
 
-// Row sums of four rows at once (v[i]: this lane's partial of row i): a
-// transposing butterfly leaves lane l with the total of row 2*bit4(l) +
-// bit3(l), then four shuffles hand every lane all four totals.
-__device__ __forceinline__ void row_totals4(float (&v)[4], int lane) {
-    const bool u16 = lane & 16, u8 = lane & 8;
-    float k0 = u16 ? v[2] : v[0], k1 = u16 ? v[3] : v[1];
-    const float s0 = u16 ? v[0] : v[2], s1 = u16 ? v[1] : v[3];
-    k0 += __shfl_xor_sync(kFull, s0, 16);
-    k1 += __shfl_xor_sync(kFull, s1, 16);
-    float k = u8 ? k1 : k0;
-    const float s = u8 ? k0 : k1;
-    k += __shfl_xor_sync(kFull, s, 8);
+// Row sums of a warp's rows at once (v[i]: this lane's partial of row i): a
+// transposing butterfly leaves each lane with the total of one row (selected
+// by its top lane bits), then one shuffle per row hands every lane all totals.
+template <int RPW>
+__device__ __forceinline__ void row_totals(float (&v)[RPW], int lane) {
+    static_assert(RPW == 2 || RPW == 4, "two or four rows per warp");
+    float k;
+    if constexpr (RPW == 4) {
+        const bool u16 = lane & 16, u8 = lane & 8;
+        float k0 = u16 ? v[2] : v[0], k1 = u16 ? v[3] : v[1];
+        const float s0 = u16 ? v[0] : v[2], s1 = u16 ? v[1] : v[3];
+        k0 += __shfl_xor_sync(kFull, s0, 16);
+        k1 += __shfl_xor_sync(kFull, s1, 16);
+        k = u8 ? k1 : k0;
+        const float s = u8 ? k0 : k1;
+        k += __shfl_xor_sync(kFull, s, 8);
+    } else {
+        const bool u16 = lane & 16;
+        k = u16 ? v[1] : v[0];
+        const float s = u16 ? v[0] : v[1];
+        k += __shfl_xor_sync(kFull, s, 16);
+        k += __shfl_xor_sync(kFull, k, 8);
+    }
     k += __shfl_xor_sync(kFull, k, 4);
     k += __shfl_xor_sync(kFull, k, 2);
     k += __shfl_xor_sync(kFull, k, 1);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __shfl_sync(kFull, k, 16 * (i >> 1) + 8 * (i & 1));
+    for (int i = 0; i < RPW; ++i) v[i] = __shfl_sync(kFull, k, (32 / RPW) * i);
 }
 
 struct QuantParams {
@@ -143,7 +154,6 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
     float Rf[RPW], rR[RPW], Cf[4] = {1.f, 1.f, 1.f, 1.f}, rCf[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
     for (int i = 0; i < RPW; ++i) { Rf[i] = 1.f; rR[i] = 1.f; }
-    static_assert(RPW == 4, "row_totals4 reduces four rows");
     int buf = 0;
     for (int it = 0; it < p.iters; ++it) {
         // token pass: R_t = population std over channels of x_rot[t][c] / C_c
@@ -155,14 +165,14 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
                 for (int k = 0; k < 4; ++k) u[i][k] = x[i][k] * rCf[k];
                 mu[i] = (u[i][0] + u[i][1]) + (u[i][2] + u[i][3]);
             }
-            row_totals4(mu, lane);
+            row_totals<RPW>(mu, lane);
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
                 mu[i] *= (1.0f / kD);
                 float d0 = u[i][0] - mu[i], d1 = u[i][1] - mu[i], d2 = u[i][2] - mu[i], d3 = u[i][3] - mu[i];
                 var[i] = (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
             }
-            row_totals4(var, lane);
+            row_totals<RPW>(var, lane);
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
                 const float v = var[i] * (1.0f / kD);

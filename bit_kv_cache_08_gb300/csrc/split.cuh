@@ -91,11 +91,23 @@ __device__ __forceinline__ void split_prefix(const SplitArgs& s, int b, int lane
     }
 }
 
-// Warps that take part in a split of W blocks over at most nw warps: all of
-// them, but never more than there are blocks, so that every active warp owns
-// at least one block and a unit's partials sit in consecutive slots.
-__host__ __device__ __forceinline__ int64_t split_active_warps(int64_t W, int64_t nw) {
-    return W < nw ? W : nw;
+// Warps that take part in a split of W blocks (units = sequences x kv heads)
+// over at most nw warps. Never more than there are blocks, so that every
+// active warp owns at least one block and a unit's partials sit in
+// consecutive slots. With ratio > 0, also at most sqrt(ratio * W * units):
+// a warp's time grows with its blocks (W / n) while the merge of a unit
+// grows with its partials (n / units); their sum is least near
+// n = sqrt(ratio * W * units), ratio being the cost of a block over that of
+// merging one partial. This only bites when few long units would otherwise
+// be cut into hundreds of single-block partials (batch 1, long contexts).
+__host__ __device__ __forceinline__ int64_t split_active_warps(int64_t W, int64_t nw, int64_t units,
+                                                               float ratio) {
+    int64_t n = W < nw ? W : nw;
+    if (ratio > 0.f) {
+        const int64_t c = (int64_t)sqrtf(ratio * (float)W * (float)units);
+        if (c < n) n = c > 1 ? c : 1;
+    }
+    return n;
 }
 
 // Largest w in [0, nw) with floor(w*W/nw) <= x.
