@@ -124,25 +124,51 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
         const int np = (int)(w1 - w0 + 1);                          // this unit's partials
         const float* p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
         const int64_t pstride = (int64_t)a.G * kPartialStride;     // next warp's partial of the unit
-        // the common maximum and the weighted sum of l, lanes over partials
-        float mx = -INFINITY;
-        for (int i = lane; i < np; i += 32) mx = fmaxf(mx, p0[i * pstride]);
-        m = warp_max(mx);
-        if (m != -INFINITY) {
-            float ls = 0.f;
-            for (int i = lane; i < np; i += 32) ls += p0[i * pstride + 1] * exp2f(p0[i * pstride] - m);
-            l = warp_sum(ls);
-            // every lane its 4 channels over all partials (independent loads; a
-            // deep unroll keeps many in flight when one unit has hundreds of partials)
+        if (np <= 16) {
+            // one round trip: lane i holds partial i's (m, l); every lane loads its
+            // 4 channels of all partials at once, then weighs them
+            const float pm = lane < np ? p0[lane * pstride] : -INFINITY;
+            const float pl = lane < np ? p0[lane * pstride + 1] : 0.f;
+            float4 pa[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i < np) pa[i] = reinterpret_cast<const float4*>(p0 + i * pstride + 4)[lane];
+            m = warp_max(pm);
+            if (m != -INFINITY) {
+                const float wl = lane < np ? exp2f(pm - m) : 0.f;
+                l = warp_sum(pl * wl);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (i < np) {
+                        const float wgt = __shfl_sync(kFull, wl, i);
+                        acc[0] = fmaf(wgt, pa[i].x, acc[0]);
+                        acc[1] = fmaf(wgt, pa[i].y, acc[1]);
+                        acc[2] = fmaf(wgt, pa[i].z, acc[2]);
+                        acc[3] = fmaf(wgt, pa[i].w, acc[3]);
+                    }
+                }
+            }
+        } else {
+            // the common maximum and the weighted sum of l, lanes over partials
+            float mx = -INFINITY;
+            for (int i = lane; i < np; i += 32) mx = fmaxf(mx, p0[i * pstride]);
+            m = warp_max(mx);
+            if (m != -INFINITY) {
+                float ls = 0.f;
+                for (int i = lane; i < np; i += 32) ls += p0[i * pstride + 1] * exp2f(p0[i * pstride] - m);
+                l = warp_sum(ls);
+                // every lane its 4 channels over all partials (independent loads; a
+                // deep unroll keeps many in flight when one unit has hundreds of partials)
 #pragma unroll 16
-            for (int i = 0; i < np; ++i) {
-                const float* bp = p0 + i * pstride;
-                const float wgt = exp2f(bp[0] - m);
-                const float4 pa = reinterpret_cast<const float4*>(bp + 4)[lane];
-                acc[0] = fmaf(wgt, pa.x, acc[0]);
-                acc[1] = fmaf(wgt, pa.y, acc[1]);
-                acc[2] = fmaf(wgt, pa.z, acc[2]);
-                acc[3] = fmaf(wgt, pa.w, acc[3]);
+                for (int i = 0; i < np; ++i) {
+                    const float* bp = p0 + i * pstride;
+                    const float wgt = exp2f(bp[0] - m);
+                    const float4 pa = reinterpret_cast<const float4*>(bp + 4)[lane];
+                    acc[0] = fmaf(wgt, pa.x, acc[0]);
+                    acc[1] = fmaf(wgt, pa.y, acc[1]);
+                    acc[2] = fmaf(wgt, pa.z, acc[2]);
+                    acc[3] = fmaf(wgt, pa.w, acc[3]);
+                }
             }
         }
         if (ROT && !(a.flags & KVARN_FLAG_NO_ROTATION)) {

@@ -83,6 +83,7 @@ __device__ __forceinline__ void split_prefix(const SplitArgs& s, int b, int lane
                                     int64_t& total) {
     before = 0;
     total = 0;
+#pragma unroll 4
     for (int b0 = 0; b0 < s.batch; b0 += 32) {
         const int bb = b0 + lane;
         const int64_t nb = (bb < s.batch) ? (int64_t)split_nblocks(s, bb) : 0;
