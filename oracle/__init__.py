@@ -73,28 +73,28 @@ def lib():
                 "orc_unrotate": (None, [_f64p, _u32p, _f64p]),
                 "orc_varn": (None, [_i, _i, ctypes.c_uint32, _f64p, _f64p, _f64p, _f64p, _f64p]),
                 "orc_round_factor": (_d, [_d]),
-                "orc_group_params": (None, [_f64p, _i, _f64p, _f64p, _f64p, _f64p]),
-                "orc_code": (_i, [_d, _d, _d]),
-                "orc_step_for": (_d, [_d, _d]),
-                "orc_code_position": (None, [_i, _i, _i, _i32p, _i32p]),
-                "orc_head_block_bytes": (ctypes.c_size_t, [_i]),
-                "orc_pack": (None, [_i, _i, _i32p, _f64p, _f64p, _f64p, _f64p, _u8p]),
-                "orc_unpack": (None, [_i, _i, _u8p, _i32p, _f64p, _f64p, _f64p, _f64p]),
-                "orc_quantize_block": (None, [_i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p, _f64p,
+                "orc_group_params": (None, [_f64p, _i, _i, _f64p, _f64p, _f64p, _f64p]),
+                "orc_code": (_i, [_d, _d, _d, _i]),
+                "orc_step_for": (_d, [_d, _d, _i]),
+                "orc_code_position": (None, [_i, _i, _i, _i, _i32p, _i32p]),
+                "orc_head_block_bytes": (ctypes.c_size_t, [_i, _i]),
+                "orc_pack": (None, [_i, _i, _i, _i32p, _f64p, _f64p, _f64p, _f64p, _u8p]),
+                "orc_unpack": (None, [_i, _i, _i, _u8p, _i32p, _f64p, _f64p, _f64p, _f64p]),
+                "orc_quantize_block": (None, [_i, _i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p, _f64p,
                                               _f64p, _f64p, _f64p, _f64p, _f64p, _f64p,
                                               _i32p, _f64p]),
-                "orc_quantize_blocks": (None, [_i64, _i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p]),
-                "orc_decode_block": (None, [_i, ctypes.c_uint32, _i, _u32p, _u8p, _i, _f64p]),
-                "orc_decode_blocks": (None, [_i64, _i, ctypes.c_uint32, _i, _u32p, _u8p, _i, _f64p]),
+                "orc_quantize_blocks": (None, [_i64, _i, _i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p]),
+                "orc_decode_block": (None, [_i, _i, ctypes.c_uint32, _i, _u32p, _u8p, _i, _f64p]),
+                "orc_decode_blocks": (None, [_i64, _i, _i, ctypes.c_uint32, _i, _u32p, _u8p, _i, _f64p]),
                 "orc_attention": (None, [_f64p, _f64p, _f64p, _i64, _d, _f64p]),
                 "orc_attention_rotated": (None, [_f64p, _f64p, _f64p, _i64, _d, _u32p, _f64p]),
-                "orc_decode_attention": (None, [_i, ctypes.c_uint32, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
+                "orc_decode_attention": (None, [_i, _i, ctypes.c_uint32, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
                                                 _i32p, _i, _i32p, _i, _f64p]),
                 "orc_error_split": (None, [_f64p, _f64p, _f64p]),
-                "orc_error_decomposition": (None, [_i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p]),
+                "orc_error_decomposition": (None, [_i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p]),
                 "orc_normalise": (None, [_i, _f64p, _f64p, _f64p, _f64p]),
-                "orc_group_params_all": (None, [_i, _f64p, _f64p, _f64p, _f64p, _f64p]),
-                "orc_codes_given": (None, [_i, _f64p, _f64p, _f64p, _i32p, _f64p]),
+                "orc_group_params_all": (None, [_i, _i, _f64p, _f64p, _f64p, _f64p, _f64p]),
+                "orc_codes_given": (None, [_i, _i, _f64p, _f64p, _f64p, _i32p, _f64p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -129,8 +129,8 @@ def sigma(sign_bits) -> np.ndarray:
     return np.where(bits == 1, -1.0, 1.0)
 
 
-def head_block_bytes(B: int) -> int:
-    return int(lib().orc_head_block_bytes(B))
+def head_block_bytes(B: int, bits: int = 2) -> int:
+    return int(lib().orc_head_block_bytes(B, bits))
 
 
 # --------------------------------------------------------------------------
@@ -216,65 +216,65 @@ def round_factor(f: float) -> float:
     return lib().orc_round_factor(float(f))
 
 
-def group_params(y):
+def group_params(y, bits: int = 2):
     y = _f64(y)
     z = ctypes.c_double()
     s = ctypes.c_double()
     m = ctypes.c_double()
     M = ctypes.c_double()
-    lib().orc_group_params(_p(y, _f64p), y.size, ctypes.byref(z), ctypes.byref(s),
+    lib().orc_group_params(_p(y, _f64p), y.size, (1 << bits) - 1, ctypes.byref(z), ctypes.byref(s),
                            ctypes.byref(m), ctypes.byref(M))
     return z.value, s.value, m.value, M.value
 
 
-def step_for(z16: float, M: float) -> float:
-    """Least fp16 s >= 0 with z16 + 3 s >= M."""
-    return lib().orc_step_for(float(z16), float(M))
+def step_for(z16: float, M: float, bits: int = 2) -> float:
+    """Least fp16 s >= 0 with z16 + (2^bits - 1) s >= M."""
+    return lib().orc_step_for(float(z16), float(M), (1 << bits) - 1)
 
 
-def code(y: float, z16: float, s16: float) -> int:
-    return int(lib().orc_code(float(y), float(z16), float(s16)))
+def code(y: float, z16: float, s16: float, bits: int = 2) -> int:
+    return int(lib().orc_code(float(y), float(z16), float(s16), (1 << bits) - 1))
 
 
-def code_position(kind: int, t: int, c: int):
+def code_position(kind: int, t: int, c: int, bits: int = 2):
     w = ctypes.c_int32()
     b = ctypes.c_int32()
-    lib().orc_code_position(kind, t, c, ctypes.byref(w), ctypes.byref(b))
+    lib().orc_code_position(kind, bits, t, c, ctypes.byref(w), ctypes.byref(b))
     return w.value, b.value
 
 
-def pack(B, kind, codes, s16, z16, R16, C16) -> np.ndarray:
+def pack(B, kind, codes, s16, z16, R16, C16, bits: int = 2) -> np.ndarray:
     codes = np.ascontiguousarray(codes, dtype=np.int32).reshape(B, D)
     s16, z16 = _f64(s16).reshape(B, NG), _f64(z16).reshape(B, NG)
     R16, C16 = _f64(R16).reshape(B), _f64(C16).reshape(D)
-    out = np.zeros(head_block_bytes(B), dtype=np.uint8)
-    lib().orc_pack(B, kind, _p(codes, _i32p), _p(s16, _f64p), _p(z16, _f64p), _p(R16, _f64p),
+    out = np.zeros(head_block_bytes(B, bits), dtype=np.uint8)
+    lib().orc_pack(B, bits, kind, _p(codes, _i32p), _p(s16, _f64p), _p(z16, _f64p), _p(R16, _f64p),
                    _p(C16, _f64p), _p(out, _u8p))
     return out
 
 
-def unpack(B, kind, hb_bytes):
+def unpack(B, kind, hb_bytes, bits: int = 2):
     hb = np.ascontiguousarray(hb_bytes, dtype=np.uint8).reshape(-1)
     codes = np.empty((B, D), dtype=np.int32)
     s16 = np.empty((B, NG))
     z16 = np.empty((B, NG))
     R16 = np.empty(B)
     C16 = np.empty(D)
-    lib().orc_unpack(B, kind, _p(hb, _u8p), _p(codes, _i32p), _p(s16, _f64p), _p(z16, _f64p),
+    lib().orc_unpack(B, bits, kind, _p(hb, _u8p), _p(codes, _i32p), _p(s16, _f64p), _p(z16, _f64p),
                      _p(R16, _f64p), _p(C16, _f64p))
     return dict(codes=codes, s16=s16, z16=z16, R16=R16, C16=C16)
 
 
-def quantize_block(X, iters: int, kind: int, sign_bits, flags: int = 0) -> dict:
+def quantize_block(X, iters: int, kind: int, sign_bits, flags: int = 0, bits: int = 2) -> dict:
     """All intermediate results of one head-block (X: [B][128] values)."""
     X = _f64(X)
     B = X.shape[0]
     s = _signs(sign_bits)
-    r = dict(bytes=np.zeros(head_block_bytes(B), dtype=np.uint8), Xr=np.empty((B, D)),
+    r = dict(bytes=np.zeros(head_block_bytes(B, bits), dtype=np.uint8), Xr=np.empty((B, D)),
              R=np.empty(B), C=np.empty(D), R16=np.empty(B), C16=np.empty(D),
              y=np.empty((B, D)), z16=np.empty((B, NG)), s16=np.empty((B, NG)),
              codes=np.empty((B, D), dtype=np.int32), trace=np.empty((max(iters, 1), 3)))
-    lib().orc_quantize_block(B, iters, flags, kind, _p(s, _u32p), _p(X, _f64p), _p(r["bytes"], _u8p),
+    lib().orc_quantize_block(B, bits, iters, flags, kind, _p(s, _u32p), _p(X, _f64p), _p(r["bytes"], _u8p),
                              _p(r["Xr"], _f64p), _p(r["R"], _f64p), _p(r["C"], _f64p),
                              _p(r["R16"], _f64p), _p(r["C16"], _f64p), _p(r["y"], _f64p),
                              _p(r["z16"], _f64p), _p(r["s16"], _f64p), _p(r["codes"], _i32p),
@@ -283,23 +283,24 @@ def quantize_block(X, iters: int, kind: int, sign_bits, flags: int = 0) -> dict:
     return r
 
 
-def quantize_blocks(X, iters: int, kind: int, sign_bits, flags: int = 0) -> np.ndarray:
+def quantize_blocks(X, iters: int, kind: int, sign_bits, flags: int = 0, bits: int = 2) -> np.ndarray:
     """X: [n][B][128] -> packed bytes [n][head_block_bytes(B)]."""
     X = _f64(X)
     n, B = X.shape[0], X.shape[1]
-    out = np.zeros((n, head_block_bytes(B)), dtype=np.uint8)
+    out = np.zeros((n, head_block_bytes(B, bits)), dtype=np.uint8)
     s = _signs(sign_bits)
-    lib().orc_quantize_blocks(n, B, iters, flags, kind, _p(s, _u32p), _p(X, _f64p), _p(out, _u8p))
+    lib().orc_quantize_blocks(n, B, bits, iters, flags, kind, _p(s, _u32p), _p(X, _f64p), _p(out, _u8p))
     return out
 
 
-def decode_blocks(hb_bytes, B: int, kind: int, sign_bits, rotated: bool, flags: int = 0) -> np.ndarray:
+def decode_blocks(hb_bytes, B: int, kind: int, sign_bits, rotated: bool, flags: int = 0,
+                  bits: int = 2) -> np.ndarray:
     """Packed head-blocks [n][bytes] -> values [n][B][128]."""
-    hb = np.ascontiguousarray(hb_bytes, dtype=np.uint8).reshape(-1, head_block_bytes(B))
+    hb = np.ascontiguousarray(hb_bytes, dtype=np.uint8).reshape(-1, head_block_bytes(B, bits))
     n = hb.shape[0]
     out = np.empty((n, B, D))
     s = _signs(sign_bits)
-    lib().orc_decode_blocks(n, B, flags, kind, _p(s, _u32p), _p(hb, _u8p), 1 if rotated else 0,
+    lib().orc_decode_blocks(n, B, bits, flags, kind, _p(s, _u32p), _p(hb, _u8p), 1 if rotated else 0,
                             _p(out, _f64p))
     return out
 
@@ -326,7 +327,7 @@ def attention_rotated(q, K, V, sm_scale: float, sign_bits) -> np.ndarray:
 
 
 def decode_attention(B, n_q, n_kv, sign_bits, sm_scale, q, pool, staging, block_table,
-                     seq_lens, flags: int = 0) -> np.ndarray:
+                     seq_lens, flags: int = 0, bits: int = 2) -> np.ndarray:
     """Attention of every (sequence, query head) over the paged 2-bit cache.
 
     q: [batch][n_q][128] values; pool: raw bytes of the physical blocks;
@@ -341,7 +342,7 @@ def decode_attention(B, n_q, n_kv, sign_bits, sm_scale, q, pool, staging, block_
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32).reshape(batch)
     out = np.zeros((batch, n_q, D))
     s = _signs(sign_bits)
-    lib().orc_decode_attention(B, flags, n_q, n_kv, _p(s, _u32p), float(sm_scale), _p(q, _f64p),
+    lib().orc_decode_attention(B, bits, flags, n_q, n_kv, _p(s, _u32p), float(sm_scale), _p(q, _f64p),
                                _p(pool, _u8p), _p(staging, _u16p), _p(bt, _i32p), bt.shape[1],
                                _p(sl, _i32p), batch, _p(out, _f64p))
     return out
@@ -359,14 +360,14 @@ def error_split(x, xh) -> np.ndarray:
     return out
 
 
-def error_decomposition(X, packed, B: int, kind: int, sign_bits, flags: int = 0) -> np.ndarray:
+def error_decomposition(X, packed, B: int, kind: int, sign_bits, flags: int = 0, bits: int = 2) -> np.ndarray:
     """X: [n][B][128] values before quantisation, packed: [n][bytes] -> [n][B][4]."""
     X = _f64(X).reshape(-1, B, D)
     pk = np.ascontiguousarray(packed, dtype=np.uint8).reshape(X.shape[0], -1)
     out = np.empty((X.shape[0], B, 4))
     s = _signs(sign_bits)
     for i in range(X.shape[0]):
-        lib().orc_error_decomposition(B, flags, kind, _p(s, _u32p), _p(X[i], _f64p), _p(pk[i], _u8p),
+        lib().orc_error_decomposition(B, bits, flags, kind, _p(s, _u32p), _p(X[i], _f64p), _p(pk[i], _u8p),
                                       _p(out[i], _f64p))
     return out
 
@@ -384,21 +385,21 @@ def normalise(Xr, R16, C16) -> np.ndarray:
     return y
 
 
-def group_params_all(y):
+def group_params_all(y, bits: int = 2):
     y = _f64(y)
     B = y.shape[0]
     z, s, m, M = (np.empty((B, NG)) for _ in range(4))
-    lib().orc_group_params_all(B, _p(y, _f64p), _p(z, _f64p), _p(s, _f64p), _p(m, _f64p),
+    lib().orc_group_params_all(B, bits, _p(y, _f64p), _p(z, _f64p), _p(s, _f64p), _p(m, _f64p),
                                _p(M, _f64p))
     return z, s, m, M
 
 
-def codes_given(y, z16, s16):
+def codes_given(y, z16, s16, bits: int = 2):
     y = _f64(y)
     B = y.shape[0]
     z16, s16 = _f64(z16).reshape(B, NG), _f64(s16).reshape(B, NG)
     codes = np.empty((B, D), dtype=np.int32)
     dist = np.empty((B, D))
-    lib().orc_codes_given(B, _p(y, _f64p), _p(z16, _f64p), _p(s16, _f64p), _p(codes, _i32p),
+    lib().orc_codes_given(B, bits, _p(y, _f64p), _p(z16, _f64p), _p(s16, _f64p), _p(codes, _i32p),
                           _p(dist, _f64p))
     return codes, dist

@@ -27,12 +27,13 @@
  * matrix is built explicitly by Sylvester doubling and multiplied in full.
  *
  * Packed head-block format (the written contract both paths implement):
- *   B tokens x 128 channels, B in {32, 64}, 4 channel groups of 32.
- *   bytes [0, 32B)          2-bit codes, 32-byte records (layout per kind)
- *   bytes [32B, 40B)        s  : fp16 [4][B]  (group-major)
- *   bytes [40B, 48B)        z  : fp16 [4][B]
- *   bytes [48B, 50B)        R  : fp16 [B]     (per-token factor)
- *   bytes [50B, 50B+256)    C  : fp16 [128]   (per-channel factor)
+ *   B tokens x 128 channels, B in {32, 64}, 4 channel groups of 32, codes of
+ *   `bits` in {2, 4} bits (X = 16 B bits bytes of codes):
+ *   bytes [0, X)            codes, records of 8*bits bytes (layout per kind)
+ *   bytes [X, X+8B)         s  : fp16 [4][B]  (group-major)
+ *   bytes [X+8B, X+16B)     z  : fp16 [4][B]
+ *   bytes [X+16B, X+18B)    R  : fp16 [B]     (per-token factor)
+ *   bytes [X+18B, X+18B+256) C : fp16 [128]   (per-channel factor)
  */
 #include <math.h>
 #include <stdint.h>
@@ -319,30 +320,32 @@ double orc_round_factor(double f)
 }
 
 /* ------------------------------------------------------------------------ */
-/* 2-bit asymmetric round-to-nearest over 32-channel groups (reading R-8,    */
-/* R-9). For the group's values with minimum m and maximum M:                */
+/* Asymmetric round-to-nearest over 32-channel groups with L = 2^bits - 1     */
+/* steps (reading R-8, R-9; L = 3 for the method's 2 bits, 15 for the 4-bit  */
+/* width). For the group's values with minimum m and maximum M:              */
 /*   z = largest fp16 <= m (clamped to +-65504)                              */
-/*   s = smallest fp16 >= 0 with z + 3 s >= M (clamped to 65504)             */
-/*   code = clamp(round-half-even((y - z) / s), 0, 3); all 0 when s = 0      */
+/*   s = smallest fp16 >= 0 with z + L s >= M (clamped to 65504)             */
+/*   code = clamp(round-half-even((y - z) / s), 0, L); all 0 when s = 0      */
 /* ------------------------------------------------------------------------ */
 
-/* least fp16 s >= 0 with z16 + 3 s >= M (clamped to 65504); 0 when z16 >= M */
-double orc_step_for(double z16, double M)
+/* least fp16 s >= 0 with z16 + L s >= M (clamped to 65504); 0 when z16 >= M */
+double orc_step_for(double z16, double M, int levels)
 {
     if (z16 >= M) return 0.0;
-    double s = orc_f16_ru((M - z16) / 3.0);
+    const double L = (double)levels;
+    double s = orc_f16_ru((M - z16) / L);
     if (s > 65504.0) s = 65504.0;
     /* the division above rounds in fp64: settle the exact minimum by
-     * comparing z + 3 s against M (exact in fp64 for fp16 operands) */
-    while (s > 0.0 && s < 65504.0 && z16 + 3.0 * s < M) s = f16_next_pos(s);
+     * comparing z + L s against M (exact in fp64 for fp16 operands) */
+    while (s > 0.0 && s < 65504.0 && z16 + L * s < M) s = f16_next_pos(s);
     while (s > 0.0) {
         double p = f16_prev_pos(s);
-        if (z16 + 3.0 * p >= M) s = p; else break;
+        if (z16 + L * p >= M) s = p; else break;
     }
     return s;
 }
 
-void orc_group_params(const double* y, int n, double* z16, double* s16,
+void orc_group_params(const double* y, int n, int levels, double* z16, double* s16,
                       double* m_out, double* M_out)
 {
     double m = y[0], M = y[0];
@@ -353,77 +356,95 @@ void orc_group_params(const double* y, int n, double* z16, double* s16,
     double mc = m < -65504.0 ? -65504.0 : (m > 65504.0 ? 65504.0 : m);
     double z = orc_f16_rd(mc);
     *z16 = z;
-    *s16 = orc_step_for(z, M);
+    *s16 = orc_step_for(z, M, levels);
     if (m_out) *m_out = m;
     if (M_out) *M_out = M;
 }
 
-int orc_code(double y, double z16, double s16)
+int orc_code(double y, double z16, double s16, int levels)
 {
     if (s16 == 0.0) return 0;
     double u = nearbyint((y - z16) / s16);    /* default mode: ties to even */
     if (u < 0) u = 0;
-    if (u > 3) u = 3;
+    if (u > levels) u = levels;
     return (int)u;
 }
 
 /* ------------------------------------------------------------------------ */
 /* Code positions in the packed head-block (the written format contract).    */
-/* Records of 32 bytes; record r = 32*sb + l with sb = t / 32 and a lane      */
-/* l = 4a + b; each record holds 8 little-endian 32-bit words.               */
+/* Records of 8*bits bytes; record r = 32*sb + l with sb = t / 32 and a lane  */
+/* l = 4a + b; each record holds 2*bits little-endian 32-bit words.          */
+/* 2 bits:                                                                   */
 /*   kind 0 (K): a = (t%32)/4, i = t%4, g = c/32, b = (c%32)/8, e = c%8;      */
 /*               word 2i + g/2, bit 2*(4*(g%2) + e/2) + 16*(e%2)             */
 /*   kind 1 (V): b = (t%32)/8, d = t%8, g = c/32, a = (c%32)/4, f = c%4;      */
 /*               word 2g + f/2, bit 2*(4*(d/4) + 2*((d%4)/2) + f%2)+16*(d%2) */
+/* 4 bits (the same lane assignment, one word per (token, group) for K and    */
+/* per (group, channel) for V):                                              */
+/*   kind 0 (K): word 4i + g, bit 4*(e/2) + 16*(e%2)                         */
+/*   kind 1 (V): word 4g + f, bit 4*(d/2) + 16*(d%2)                         */
 /* ------------------------------------------------------------------------ */
 
-void orc_code_position(int kind, int t, int c, int* word_index, int* bit)
+void orc_code_position(int kind, int bits, int t, int c, int* word_index, int* bit)
 {
     int sb = t / 32, g = c / ORC_GS;
     if (kind == 0) {
         int a = (t % 32) / 4, i = t % 4, b = (c % 32) / 8, e = c % 8;
         int rec = 32 * sb + 4 * a + b;
-        *word_index = rec * 8 + 2 * i + g / 2;
-        *bit = 2 * (4 * (g % 2) + e / 2) + 16 * (e % 2);
+        if (bits == 4) {
+            *word_index = rec * 16 + 4 * i + g;
+            *bit = 4 * (e / 2) + 16 * (e % 2);
+        } else {
+            *word_index = rec * 8 + 2 * i + g / 2;
+            *bit = 2 * (4 * (g % 2) + e / 2) + 16 * (e % 2);
+        }
     } else {
         int b = (t % 32) / 8, d = t % 8, a = (c % 32) / 4, f = c % 4;
         int rec = 32 * sb + 4 * a + b;
-        *word_index = rec * 8 + 2 * g + f / 2;
-        *bit = 2 * (4 * (d / 4) + 2 * ((d % 4) / 2) + f % 2) + 16 * (d % 2);
+        if (bits == 4) {
+            *word_index = rec * 16 + 4 * g + f;
+            *bit = 4 * (d / 2) + 16 * (d % 2);
+        } else {
+            *word_index = rec * 8 + 2 * g + f / 2;
+            *bit = 2 * (4 * (d / 4) + 2 * ((d % 4) / 2) + f % 2) + 16 * (d % 2);
+        }
     }
 }
 
-size_t orc_head_block_bytes(int B) { return (size_t)B * 50 + 256; }
+static size_t codes_bytes(int B, int bits) { return (size_t)16 * B * bits; }
+size_t orc_head_block_bytes(int B, int bits) { return codes_bytes(B, bits) + (size_t)18 * B + 256; }
 
 static void put_u16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
 static uint16_t get_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 
 /* Write one head-block from its fields. codes: [B][128] ints 0..3;
  * s16, z16: [B][4] fp16-grid values; R16: [B]; C16: [128]. */
-void orc_pack(int B, int kind, const int32_t* codes, const double* s16, const double* z16,
+void orc_pack(int B, int bits, int kind, const int32_t* codes, const double* s16, const double* z16,
               const double* R16, const double* C16, uint8_t* out)
 {
-    size_t nbytes = orc_head_block_bytes(B);
+    size_t nbytes = orc_head_block_bytes(B, bits);
+    const int nwords = 4 * B * bits;
+    const uint32_t mask = (1u << bits) - 1u;
     memset(out, 0, nbytes);
-    uint32_t* words = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)B * 8);
-    memset(words, 0, sizeof(uint32_t) * (size_t)B * 8);
+    uint32_t* words = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)nwords);
+    memset(words, 0, sizeof(uint32_t) * (size_t)nwords);
     for (int t = 0; t < B; t++)
         for (int c = 0; c < ORC_D; c++) {
             int w, bit;
-            orc_code_position(kind, t, c, &w, &bit);
-            words[w] |= ((uint32_t)(codes[t * ORC_D + c] & 3)) << bit;
+            orc_code_position(kind, bits, t, c, &w, &bit);
+            words[w] |= ((uint32_t)codes[t * ORC_D + c] & mask) << bit;
         }
-    for (int w = 0; w < B * 8; w++) {
+    for (int w = 0; w < nwords; w++) {
         out[4 * w + 0] = (uint8_t)(words[w] & 0xFF);
         out[4 * w + 1] = (uint8_t)((words[w] >> 8) & 0xFF);
         out[4 * w + 2] = (uint8_t)((words[w] >> 16) & 0xFF);
         out[4 * w + 3] = (uint8_t)((words[w] >> 24) & 0xFF);
     }
     free(words);
-    uint8_t* sp = out + 32 * B;
-    uint8_t* zp = out + 40 * B;
-    uint8_t* rp = out + 48 * B;
-    uint8_t* cp = out + 50 * B;
+    uint8_t* sp = out + codes_bytes(B, bits);
+    uint8_t* zp = sp + 8 * B;
+    uint8_t* rp = zp + 8 * B;
+    uint8_t* cp = rp + 2 * B;
     for (int g = 0; g < ORC_NG; g++)
         for (int t = 0; t < B; t++) {
             put_u16(sp + 2 * (g * B + t), orc_f16_bits(s16[t * ORC_NG + g]));
@@ -434,21 +455,22 @@ void orc_pack(int B, int kind, const int32_t* codes, const double* s16, const do
 }
 
 /* Read the fields back from a head-block (the inverse of orc_pack). */
-void orc_unpack(int B, int kind, const uint8_t* in, int32_t* codes, double* s16,
+void orc_unpack(int B, int bits, int kind, const uint8_t* in, int32_t* codes, double* s16,
                 double* z16, double* R16, double* C16)
 {
+    const uint32_t mask = (1u << bits) - 1u;
     for (int t = 0; t < B; t++)
         for (int c = 0; c < ORC_D; c++) {
             int w, bit;
-            orc_code_position(kind, t, c, &w, &bit);
+            orc_code_position(kind, bits, t, c, &w, &bit);
             uint32_t word = (uint32_t)in[4 * w] | ((uint32_t)in[4 * w + 1] << 8) |
                             ((uint32_t)in[4 * w + 2] << 16) | ((uint32_t)in[4 * w + 3] << 24);
-            codes[t * ORC_D + c] = (int32_t)((word >> bit) & 3u);
+            codes[t * ORC_D + c] = (int32_t)((word >> bit) & mask);
         }
-    const uint8_t* sp = in + 32 * B;
-    const uint8_t* zp = in + 40 * B;
-    const uint8_t* rp = in + 48 * B;
-    const uint8_t* cp = in + 50 * B;
+    const uint8_t* sp = in + codes_bytes(B, bits);
+    const uint8_t* zp = sp + 8 * B;
+    const uint8_t* rp = zp + 8 * B;
+    const uint8_t* cp = rp + 2 * B;
     for (int g = 0; g < ORC_NG; g++)
         for (int t = 0; t < B; t++) {
             s16[t * ORC_NG + g] = orc_f16_value(get_u16(sp + 2 * (g * B + t)));
@@ -464,7 +486,7 @@ void orc_unpack(int B, int kind, const uint8_t* in, int32_t* codes, double* s16,
 /* fp64). Any of the detail outputs may be NULL.                             */
 /* ------------------------------------------------------------------------ */
 
-void orc_quantize_block(int B, int iters, uint32_t flags, int kind, const uint32_t sign_bits[4],
+void orc_quantize_block(int B, int bits, int iters, uint32_t flags, int kind, const uint32_t sign_bits[4],
                         const double* X, uint8_t* out,
                         double* Xr_out, double* R_out, double* C_out,
                         double* R16_out, double* C16_out, double* y_out,
@@ -495,12 +517,12 @@ void orc_quantize_block(int B, int iters, uint32_t flags, int kind, const uint32
     for (int t = 0; t < B; t++)
         for (int g = 0; g < ORC_NG; g++) {
             const double* yg = y + t * ORC_D + g * ORC_GS;
-            orc_group_params(yg, ORC_GS, &z16[t * ORC_NG + g], &s16[t * ORC_NG + g], NULL, NULL);
+            orc_group_params(yg, ORC_GS, (1 << bits) - 1, &z16[t * ORC_NG + g], &s16[t * ORC_NG + g], NULL, NULL);
             for (int k = 0; k < ORC_GS; k++)
                 codes[t * ORC_D + g * ORC_GS + k] =
-                    orc_code(yg[k], z16[t * ORC_NG + g], s16[t * ORC_NG + g]);
+                    orc_code(yg[k], z16[t * ORC_NG + g], s16[t * ORC_NG + g], (1 << bits) - 1);
         }
-    if (out) orc_pack(B, kind, codes, s16, z16, R16, C16, out);
+    if (out) orc_pack(B, bits, kind, codes, s16, z16, R16, C16, out);
 
     if (Xr_out) memcpy(Xr_out, Xr, sizeof(double) * n);
     if (R_out) memcpy(R_out, R, sizeof(double) * B);
@@ -515,13 +537,13 @@ void orc_quantize_block(int B, int iters, uint32_t flags, int kind, const uint32
 }
 
 /* Many independent head-blocks: X [n][B][128] -> out [n][head_block_bytes]. */
-void orc_quantize_blocks(int64_t n, int B, int iters, uint32_t flags, int kind, const uint32_t sign_bits[4],
+void orc_quantize_blocks(int64_t n, int B, int bits, int iters, uint32_t flags, int kind, const uint32_t sign_bits[4],
                          const double* X, uint8_t* out)
 {
-    size_t hb = orc_head_block_bytes(B);
+    size_t hb = orc_head_block_bytes(B, bits);
     #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < n; i++)
-        orc_quantize_block(B, iters, flags, kind, sign_bits, X + (size_t)i * B * ORC_D, out + (size_t)i * hb,
+        orc_quantize_block(B, bits, iters, flags, kind, sign_bits, X + (size_t)i * B * ORC_D, out + (size_t)i * hb,
                            NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL);
 }
 
@@ -531,7 +553,7 @@ void orc_quantize_blocks(int64_t n, int B, int iters, uint32_t flags, int kind, 
 /* out: [B][128]; rotated != 0 keeps the rotated space.                      */
 /* ------------------------------------------------------------------------ */
 
-void orc_decode_block(int B, uint32_t flags, int kind, const uint32_t sign_bits[4], const uint8_t* in,
+void orc_decode_block(int B, int bits, uint32_t flags, int kind, const uint32_t sign_bits[4], const uint8_t* in,
                       int rotated, double* out)
 {
     size_t n = (size_t)B * ORC_D;
@@ -540,7 +562,7 @@ void orc_decode_block(int B, uint32_t flags, int kind, const uint32_t sign_bits[
     double* z16 = (double*)malloc(sizeof(double) * B * ORC_NG);
     double* R16 = (double*)malloc(sizeof(double) * B);
     double C16[ORC_D], xr[ORC_D];
-    orc_unpack(B, kind, in, codes, s16, z16, R16, C16);
+    orc_unpack(B, bits, kind, in, codes, s16, z16, R16, C16);
     for (int t = 0; t < B; t++) {
         for (int c = 0; c < ORC_D; c++) {
             int g = c / ORC_GS;
@@ -553,13 +575,13 @@ void orc_decode_block(int B, uint32_t flags, int kind, const uint32_t sign_bits[
     free(codes); free(s16); free(z16); free(R16);
 }
 
-void orc_decode_blocks(int64_t n, int B, uint32_t flags, int kind, const uint32_t sign_bits[4],
+void orc_decode_blocks(int64_t n, int B, int bits, uint32_t flags, int kind, const uint32_t sign_bits[4],
                        const uint8_t* in, int rotated, double* out)
 {
-    size_t hb = orc_head_block_bytes(B);
+    size_t hb = orc_head_block_bytes(B, bits);
     #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t i = 0; i < n; i++)
-        orc_decode_block(B, flags, kind, sign_bits, in + (size_t)i * hb, rotated, out + (size_t)i * B * ORC_D);
+        orc_decode_block(B, bits, flags, kind, sign_bits, in + (size_t)i * hb, rotated, out + (size_t)i * B * ORC_D);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -622,12 +644,12 @@ void orc_attention_rotated(const double* q, const double* K, const double* V, in
 /* out: fp64 [batch][n_q][128]. Units run in parallel (OpenMP).              */
 /* ------------------------------------------------------------------------ */
 
-void orc_decode_attention(int B, uint32_t flags, int n_q, int n_kv, const uint32_t sign_bits[4], double sm_scale,
+void orc_decode_attention(int B, int bits, uint32_t flags, int n_q, int n_kv, const uint32_t sign_bits[4], double sm_scale,
                           const double* q, const uint8_t* pool, const uint16_t* staging,
                           const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                           int batch, double* out)
 {
-    size_t hb = orc_head_block_bytes(B);
+    size_t hb = orc_head_block_bytes(B, bits);
     size_t block_bytes = (size_t)n_kv * 2 * hb;
     int G = n_q / n_kv;
     #pragma omp parallel for schedule(dynamic, 1)
@@ -641,8 +663,8 @@ void orc_decode_attention(int B, uint32_t flags, int n_q, int n_kv, const uint32
         for (int64_t j = 0; j < nfull; j++) {
             int64_t p = block_table[(int64_t)b * max_blocks + j];
             const uint8_t* base = pool + (size_t)p * block_bytes + (size_t)(2 * h) * hb;
-            orc_decode_block(B, flags, 0, sign_bits, base, 0, K + (size_t)j * B * ORC_D);
-            orc_decode_block(B, flags, 1, sign_bits, base + hb, 0, V + (size_t)j * B * ORC_D);
+            orc_decode_block(B, bits, flags, 0, sign_bits, base, 0, K + (size_t)j * B * ORC_D);
+            orc_decode_block(B, bits, flags, 1, sign_bits, base + hb, 0, V + (size_t)j * B * ORC_D);
         }
         for (int64_t r = 0; r < tail; r++) {
             const uint16_t* sk = staging + ((((size_t)b * n_kv + h) * 2 + 0) * B + r) * ORC_D;
@@ -703,11 +725,11 @@ void orc_error_split(const double* x, const double* xh, double* out)
 
 /* Per token of a head-block: X [B][128] the values before quantisation,
  * packed the head-block's bytes; out [B][4] as orc_error_split. */
-void orc_error_decomposition(int B, uint32_t flags, int kind, const uint32_t sign_bits[4],
+void orc_error_decomposition(int B, int bits, uint32_t flags, int kind, const uint32_t sign_bits[4],
                              const double* X, const uint8_t* packed, double* out)
 {
     double* xh = (double*)malloc(sizeof(double) * (size_t)B * ORC_D);
-    orc_decode_block(B, flags, kind, sign_bits, packed, 0, xh);
+    orc_decode_block(B, bits, flags, kind, sign_bits, packed, 0, xh);
     for (int t = 0; t < B; t++)
         orc_error_split(X + (size_t)t * ORC_D, xh + (size_t)t * ORC_D, out + 4 * t);
     free(xh);
@@ -728,17 +750,17 @@ void orc_normalise(int B, const double* Xr, const double* R16, const double* C16
 }
 
 /* per (token, group): z16, s16 from y, plus the group's min and max */
-void orc_group_params_all(int B, const double* y, double* z16, double* s16, double* m, double* M)
+void orc_group_params_all(int B, int bits, const double* y, double* z16, double* s16, double* m, double* M)
 {
     for (int t = 0; t < B; t++)
         for (int g = 0; g < ORC_NG; g++)
-            orc_group_params(y + t * ORC_D + g * ORC_GS, ORC_GS, &z16[t * ORC_NG + g],
+            orc_group_params(y + t * ORC_D + g * ORC_GS, ORC_GS, (1 << bits) - 1, &z16[t * ORC_NG + g],
                              &s16[t * ORC_NG + g], &m[t * ORC_NG + g], &M[t * ORC_NG + g]);
 }
 
 /* codes from y with given z16, s16; dist[t][c] = distance from y to the
  * nearest decision boundary z + (k + 1/2) s, k = 0..2 (inf when s = 0) */
-void orc_codes_given(int B, const double* y, const double* z16, const double* s16,
+void orc_codes_given(int B, int bits, const double* y, const double* z16, const double* s16,
                      int32_t* codes, double* dist)
 {
     for (int t = 0; t < B; t++)
@@ -746,10 +768,10 @@ void orc_codes_given(int B, const double* y, const double* z16, const double* s1
             int g = c / ORC_GS;
             double z = z16[t * ORC_NG + g], s = s16[t * ORC_NG + g];
             double yv = y[t * ORC_D + c];
-            codes[t * ORC_D + c] = orc_code(yv, z, s);
+            codes[t * ORC_D + c] = orc_code(yv, z, s, (1 << bits) - 1);
             double best = INFINITY;
             if (s > 0.0)
-                for (int k = 0; k < 3; k++) {
+                for (int k = 0; k < (1 << bits) - 1; k++) {
                     double bd = fabs(yv - (z + (k + 0.5) * s));
                     if (bd < best) best = bd;
                 }

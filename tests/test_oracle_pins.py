@@ -548,3 +548,77 @@ def test_error_split_parts_add_up_to_the_error():
         cos = X[t] @ Xh[t] / (nx * nh)
         assert ed == pytest.approx(nh * math.sqrt(max(0.0, 2 - 2 * cos)), rel=1e-6, abs=1e-12)
         assert em <= err * (1 + 1e-12) and ed <= err + em + 1e-12 and err <= em + ed + 1e-12
+
+
+# ---------------------------------------------------------------- 4-bit width
+
+def test_pack_4bit_matches_hand_derived_bytes():
+    gold = _golden()
+    B = 32
+    s, z = np.ones((B, 4)), -2.0 * np.ones((B, 4))
+    R, C = 0.5 * np.ones(B), 2.0 * np.ones(D)
+    kcodes = np.tile(np.arange(D) % 16, (B, 1))
+    vcodes = np.tile((np.arange(B) % 16)[:, None], (1, D))
+    kb = oracle.pack(B, oracle.KIND_K, kcodes, s, z, R, C, bits=4)
+    vb = oracle.pack(B, oracle.KIND_V, vcodes, s, z, R, C, bits=4)
+    for key, buf in (("K4 c%16", kb), ("V4 t%16", vb)):
+        w0 = bytes.fromhex(gold[f"{key} record0 word"].replace(" ", ""))
+        w1 = bytes.fromhex(gold[f"{key} record1 word"].replace(" ", ""))
+        assert buf[:64].tobytes() == w0 * 16 and buf[64:128].tobytes() == w1 * 16
+    offs = dict(zip(*[iter(gold["section offsets 4-bit B=32"].split())] * 2))
+    assert kb[int(offs["s"]):int(offs["s"]) + 2].tobytes().hex(" ") == gold["s bytes"]
+    assert kb[int(offs["C"]):int(offs["C"]) + 2].tobytes().hex(" ") == gold["C bytes"]
+    assert len(kb) == int(offs["total"]) == oracle.head_block_bytes(32, 4)
+    offs64 = dict(zip(*[iter(gold["section offsets 4-bit B=64"].split())] * 2))
+    assert oracle.head_block_bytes(64, 4) == int(offs64["total"])
+
+
+def test_4bit_positions_are_a_bijection_and_pack_round_trips():
+    for B in (32, 64):
+        for kind in (0, 1):
+            seen = {oracle.code_position(kind, t, c, bits=4) for t in range(B) for c in range(D)}
+            assert len(seen) == B * D
+            assert all(b % 4 == 0 and 0 <= b < 32 for _, b in seen)
+            assert max(w for w, _ in seen) == 4 * B * 4 - 1
+            rng = np.random.default_rng(40 + B + kind)
+            codes = rng.integers(0, 16, (B, D))
+            f16 = lambda a: a.astype(np.float16).astype(np.float64)
+            s, z = f16(np.abs(rng.standard_normal((B, 4)))), f16(rng.standard_normal((B, 4)))
+            R, C = f16(np.abs(rng.standard_normal(B)) + 1), f16(np.abs(rng.standard_normal(D)) + 1)
+            f = oracle.unpack(B, kind, oracle.pack(B, kind, codes, s, z, R, C, bits=4), bits=4)
+            assert np.array_equal(f["codes"], codes)
+            assert np.array_equal(f["s16"], s) and np.array_equal(f["R16"], R) and np.array_equal(f["C16"], C)
+
+
+def test_4bit_group_params_and_codes_are_brute_force():
+    grid = _all_f16_nonneg()
+    full = np.concatenate([-grid[::-1], grid])
+    rng = np.random.default_rng(41)
+    for _ in range(40):
+        y = rng.standard_normal(32) * np.exp(rng.uniform(-6, 6)) + rng.uniform(-3, 3)
+        z, s, m, M = oracle.group_params(y, bits=4)
+        assert z == full[full <= m].max()
+        assert s == grid[z + 15.0 * grid >= M].min()          # 15 steps cover the group
+        lv = z + s * np.arange(16)
+        for v in y:
+            d = np.abs(v - lv)
+            want = np.flatnonzero(d == d.min())
+            want = want[0] if len(want) == 1 else [k for k in want if k % 2 == 0][0]
+            assert oracle.code(v, z, s, bits=4) == want
+            assert abs(v - lv[oracle.code(v, z, s, bits=4)]) <= s / 2 * (1 + 1e-15)
+
+
+def test_4bit_block_is_within_half_step_and_finer_than_2bit():
+    sb = synth.sign_bits(42)
+    X = _block(42, 64)
+    errs = {}
+    for bits in (2, 4):
+        r = oracle.quantize_block(X, 2, oracle.KIND_K, sb, bits=bits)
+        rot = oracle.decode_blocks(r["bytes"], 64, 0, sb, rotated=True, bits=bits)[0]
+        bound = (r["s16"].repeat(32, axis=1) / 2) * r["R16"][:, None] * r["C16"][None, :]
+        assert np.all(np.abs(rot - r["Xr"]) <= bound * (1 + 1e-9) + 1e-300)
+        assert r["codes"].max() <= (1 << bits) - 1
+        unrot = oracle.decode_blocks(r["bytes"], 64, 0, sb, rotated=False, bits=bits)[0]
+        errs[bits] = np.linalg.norm(unrot - X) / np.linalg.norm(X)
+    # the same factors, 15 steps per group instead of 3: roughly 5x finer
+    assert errs[4] < errs[2] / 3
