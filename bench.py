@@ -46,7 +46,7 @@ def parse():
                         "axis) against the bf16 cache on the Llama-3.1-8B layer, one JSON line per variant")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
-                        "lengths), 2-bit vs bf16-cache decode attention, one JSON line per point")
+                        "lengths), 2-bit and 4-bit vs bf16-cache decode attention, one JSON line per point")
     return p.parse_args()
 
 
@@ -572,7 +572,6 @@ def run_sweep(args):
             lens = np.array(w.seq_lens, dtype=np.int64)
             nbs = (lens + B - 1) // B
             max_blocks = int(nbs.max())
-            cfg = kv.make_config(n_q, n_kv, B, w.iters, synth.sign_bits(w.seed))
             g = synth.make_gen(w.seed + batch + ctx, dev)
             n_phys = int(nbs.sum())
             perm = np.random.default_rng([batch, ctx]).permutation(n_phys).astype(np.int32)
@@ -585,31 +584,39 @@ def run_sweep(args):
             sl = torch.from_numpy(lens.astype(np.int32)).to(dev)
             q = synth.queries(g, batch, n_q, dev).to(torch.bfloat16)
             out = torch.empty(batch, n_q, D, device=dev)
-            ws = kv.alloc_workspace(cfg, batch, max_blocks, dev)
             big = ctx * batch >= 1 << 22
             reps = 5 if big else 30
-            # 2-bit cache: valid packed head-blocks (512 quantised K and V tiles repeated)
-            hb = kv.head_block_bytes(cfg)
-            tile = torch.empty(2, 256, hb, dtype=torch.uint8, device=dev)
-            for kind in (0, 1):
-                x = synth.kv_values(g, 1, 256, B, w.sigma_m, w.n_out, w.out_factor, dev)[0].to(torch.bfloat16)
-                kv.quantize_block(cfg, kind, x.contiguous(), tile[kind], kv.alloc_workspace(cfg, 0, 0, dev))
-            pool = kv.alloc_pool(cfg, n_phys, dev).view(n_phys, n_kv, 2, hb)
-            for c0 in range(0, n_phys, 1 << 15):
-                c1 = min(n_phys, c0 + (1 << 15))
-                idx = (torch.arange(c0 * n_kv, c1 * n_kv, device=dev) % 256).view(c1 - c0, n_kv)
-                pool[c0:c1, :, 0] = tile[0][idx]
-                pool[c0:c1, :, 1] = tile[1][idx]
-            pool = pool.view(n_phys, -1)
-            staging = kv.alloc_staging(cfg, batch, dev)
-            staging.normal_(generator=g)
             full = (lens // B) * B
-            b2 = float((full * n_kv * (2 * (32 + 16 + 2) + 2 * 256 / B)).sum()
-                       + ((lens - full) * n_kv * 512).sum() + batch * n_q * 768 + nbs.sum() * 4)
-            ms2 = _time_events(lambda: kv.decode_attn(cfg, q, pool, staging, bt, sl, out, ws), reps, flush)
-            assert kv.read_error(ws) == 0
-            del pool, staging
-            torch.cuda.empty_cache()
+            packed = {}
+            for bits in (2, 4):
+                cfg = kv.make_config(n_q, n_kv, B, w.iters, synth.sign_bits(w.seed), bits=bits)
+                ws = kv.alloc_workspace(cfg, batch, max_blocks, dev)
+                # packed cache: valid head-blocks (512 quantised K and V tiles repeated)
+                hb = kv.head_block_bytes(cfg)
+                tile = torch.empty(2, 256, hb, dtype=torch.uint8, device=dev)
+                for kind in (0, 1):
+                    x = synth.kv_values(g, 1, 256, B, w.sigma_m, w.n_out, w.out_factor, dev)[0].to(torch.bfloat16)
+                    kv.quantize_block(cfg, kind, x.contiguous(), tile[kind], kv.alloc_workspace(cfg, 0, 0, dev))
+                pool = kv.alloc_pool(cfg, n_phys, dev).view(n_phys, n_kv, 2, hb)
+                for c0 in range(0, n_phys, 1 << 15):
+                    c1 = min(n_phys, c0 + (1 << 15))
+                    idx = (torch.arange(c0 * n_kv, c1 * n_kv, device=dev) % 256).view(c1 - c0, n_kv)
+                    pool[c0:c1, :, 0] = tile[0][idx]
+                    pool[c0:c1, :, 1] = tile[1][idx]
+                pool = pool.view(n_phys, -1)
+                staging = kv.alloc_staging(cfg, batch, dev)
+                staging.normal_(generator=g)
+                nbytes = float((full * n_kv * (2 * (16 * bits + 16 + 2) + 2 * 256 / B)).sum()
+                               + ((lens - full) * n_kv * 512).sum() + batch * n_q * 768 + nbs.sum() * 4)
+                ms = _time_events(lambda: kv.decode_attn(cfg, q, pool, staging, bt, sl, out, ws), reps, flush)
+                assert kv.read_error(ws) == 0
+                packed[bits] = (ms, nbytes)
+                del pool, staging
+                torch.cuda.empty_cache()
+            ms2, b2 = packed[2]
+            ms4, b4 = packed[4]
+            cfg = kv.make_config(n_q, n_kv, B, w.iters, synth.sign_bits(w.seed))
+            ws = kv.alloc_workspace(cfg, batch, max_blocks, dev)
             kvp = torch.empty(n_phys, n_kv, 2, B, D, dtype=torch.bfloat16, device=dev)
             kvp.normal_(generator=g)
             b16 = float((lens * n_kv * 512).sum() + batch * n_q * 768 + nbs.sum() * 4)
@@ -622,20 +629,25 @@ def run_sweep(args):
                               "timing": "CUDA events, median of launches each queued behind a 1 GiB L2-flushing write",
                               "2bit": {"us": round(ms2 * 1e3, 2), "GB_per_s": round(b2 / ms2 / 1e6, 1),
                                        "tokens_per_s": round(batch / ms2 * 1e3, 1), "bytes": int(b2)},
+                              "4bit": {"us": round(ms4 * 1e3, 2), "GB_per_s": round(b4 / ms4 / 1e6, 1),
+                                       "tokens_per_s": round(batch / ms4 * 1e3, 1), "bytes": int(b4)},
                               "bf16": {"us": round(ms16 * 1e3, 2), "GB_per_s": round(b16 / ms16 / 1e6, 1),
                                        "tokens_per_s": round(batch / ms16 * 1e3, 1), "bytes": int(b16)},
-                              "speedup_2bit_vs_bf16": round(ms16 / ms2, 2)}), flush=True)
+                              "speedup_2bit_vs_bf16": round(ms16 / ms2, 2),
+                              "speedup_4bit_vs_bf16": round(ms16 / ms4, 2)}), flush=True)
 
 
 # ---------------------------------------------------------------------------- ablation
 
-ABLATIONS = (  # (name, flags, iters): the pages' ablation list, plus the two ends
-    ("kvarn (full)", 0, 3),
-    ("hadamard only", 0, 0),
-    ("varn only (no rotation)", 1, 3),
-    ("varn token axis only", 4, 3),
-    ("varn channel axis only", 2, 3),
-    ("plain group 2-bit", 1, 0),
+ABLATIONS = (  # (name, flags, iters, bits): the pages' ablation list, plus the two ends and 4-bit codes
+    ("kvarn (full)", 0, 3, 2),
+    ("hadamard only", 0, 0, 2),
+    ("varn only (no rotation)", 1, 3, 2),
+    ("varn token axis only", 4, 3, 2),
+    ("varn channel axis only", 2, 3, 2),
+    ("plain group 2-bit", 1, 0, 2),
+    ("kvarn 4-bit", 0, 3, 4),
+    ("plain group 4-bit", 1, 0, 4),
 )
 
 
@@ -666,8 +678,8 @@ def run_ablation(args):
     ref = torch.empty(batch, n_q, D, device=dev)
     kv.decode_attn_bf16(cfg0, q, kvp, bt, lens, ref, kv.alloc_workspace(cfg0, batch, nb, dev))
     del kvp
-    for name, flags, iters in ABLATIONS:
-        cfg = kv.make_config(n_q, n_kv, B, iters, sb, flags=flags)
+    for name, flags, iters, bits in ABLATIONS:
+        cfg = kv.make_config(n_q, n_kv, B, iters, sb, flags=flags, bits=bits)
         pool = kv.alloc_pool(cfg, batch * nb, dev)
         staging = kv.alloc_staging(cfg, batch, dev)
         ws = kv.alloc_workspace(cfg, batch, nb, dev)
@@ -682,7 +694,8 @@ def run_ablation(args):
             x = T.float().reshape(-1, B, D)
             rec.append(float(((deq - x) ** 2).sum() / (x ** 2).sum()))
             es = torch.empty(batch * n_kv * nb, B, 4, device=dev)
-            kv.error_decomposition(cfg, kind, T.contiguous(), pool, es, packed_offsets=offs.reshape(-1).contiguous())
+            kv.error_decomposition(cfg, kind, T.contiguous(), pool, es, packed_offsets=offs.reshape(-1).contiguous(),
+                                   n_head_blocks=batch * n_kv * nb)
             es = es.reshape(-1, 4)
             top = es[:, 0] >= torch.quantile(es[:, 0], 0.9)
             split.append({"em_over_ed_energy": round(float((es[:, 2] ** 2).sum() / (es[:, 3] ** 2).sum()), 4),
@@ -694,7 +707,7 @@ def run_ablation(args):
         assert kv.read_error(ws) == 0
         d = out - ref
         cos = torch.nn.functional.cosine_similarity(out.reshape(-1, D), ref.reshape(-1, D), dim=1)
-        print(json.dumps({"ablation": name, "flags": flags, "varn_iters": iters, "workload": w.name,
+        print(json.dumps({"ablation": name, "flags": flags, "varn_iters": iters, "bits": bits, "workload": w.name,
                           "attn_rel_l2_vs_bf16": round(float(d.norm() / ref.norm()), 5),
                           "attn_mean_cosine_vs_bf16": round(float(cos.mean()), 5),
                           "k_rel_mse": round(rec[0], 5), "v_rel_mse": round(rec[1], 5),

@@ -177,16 +177,39 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
+def _blocks_in(src: torch.Tensor, cfg: Config, n_head_blocks: Optional[int], block_stride: Optional[int],
+               token_stride: int):
+    """(n, block stride) for a source of head-blocks read from src's first
+    element at the given strides (elements); n defaults to every whole block a
+    contiguous src holds. Raises if block n-1 would read past src's storage."""
+    B = cfg.block_size
+    explicit = block_stride is not None or token_stride != 128
+    if not explicit and not src.is_contiguous():
+        raise ValueError("src must be contiguous unless its strides are given")
+    bstride = B * 128 if block_stride is None else block_stride
+    if n_head_blocks is None:
+        if explicit:
+            raise ValueError("n_head_blocks is required with explicit strides")
+        n = src.numel() // (B * 128)
+    else:
+        n = n_head_blocks
+    room = src.untyped_storage().nbytes() // src.element_size() - src.storage_offset()
+    if n > 0 and (n - 1) * bstride + (B - 1) * token_stride + 128 > room:
+        raise ValueError("src holds fewer elements than n_head_blocks blocks at these strides")
+    return n, bstride
+
+
 def quantize_block(cfg: Config, kind: int, src: torch.Tensor, dst_base: torch.Tensor,
                    workspace: torch.Tensor, dst_offsets: Optional[torch.Tensor] = None,
                    n_head_blocks: Optional[int] = None, block_stride: Optional[int] = None,
                    token_stride: int = 128):
-    """src: [n][B][128] (bf16|fp32) unless strides are given; dst_base: uint8 buffer."""
+    """src: contiguous bf16|fp32 values, head-block i at element i * block_stride
+    (default B * 128) with token rows token_stride apart; n_head_blocks defaults
+    to the whole blocks src holds. dst_base: uint8 buffer."""
     _need_cuda(dst_base, "dst_base", torch.uint8)
     if not src.is_cuda:
         raise ValueError("src must be a CUDA tensor")
-    n = src.shape[0] if n_head_blocks is None else n_head_blocks
-    bstride = cfg.block_size * 128 if block_stride is None else block_stride
+    n, bstride = _blocks_in(src, cfg, n_head_blocks, block_stride, token_stride)
     if dst_offsets is not None:
         _need_cuda(dst_offsets, "dst_offsets", torch.int64)
     _check(lib().kvarn_quantize_block(ctypes.byref(cfg), kind, _ptr(src), _dtype_code(src), n, bstride,
@@ -272,14 +295,18 @@ def dequantize(cfg: Config, kind: int, src_base: torch.Tensor, out: torch.Tensor
 def error_decomposition(cfg: Config, kind: int, src: torch.Tensor, packed_base: torch.Tensor, out: torch.Tensor,
                         packed_offsets: Optional[torch.Tensor] = None, n_head_blocks: Optional[int] = None,
                         block_stride: Optional[int] = None, token_stride: int = 128):
-    """src: [n][B][128] values before quantisation; out: fp32 [n][B][4] =
-    (|x|, |x^|, |E_M|, |E_D|) per token."""
+    """src: the n head-blocks' values before quantisation, block i at element
+    i * block_stride (default B * 128), token rows token_stride apart; out:
+    fp32 [n][B][4] = (|x|, |x^|, |E_M|, |E_D|) per token. n defaults to
+    out.shape[0]."""
     _need_cuda(packed_base, "packed_base", torch.uint8)
     _need_cuda(out, "out", torch.float32)
     if not src.is_cuda:
         raise ValueError("src must be a CUDA tensor")
-    n = src.shape[0] if n_head_blocks is None else n_head_blocks
-    bstride = cfg.block_size * 128 if block_stride is None else block_stride
+    n, bstride = _blocks_in(src, cfg, out.shape[0] if n_head_blocks is None else n_head_blocks, block_stride,
+                            token_stride)
+    if out.numel() < n * cfg.block_size * 4:
+        raise ValueError("out holds fewer than n_head_blocks x B x 4 values")
     if packed_offsets is not None:
         _need_cuda(packed_offsets, "packed_offsets", torch.int64)
     _check(lib().kvarn_error_decomposition(ctypes.byref(cfg), kind, _ptr(src), _dtype_code(src), n, bstride,

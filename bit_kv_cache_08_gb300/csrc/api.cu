@@ -24,7 +24,7 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
                                     int64_t n_pool_blocks, const int32_t* block_table, int max_blocks,
                                     const int32_t* seq_lens, int batch, float* out, void* workspace, int nw,
                                     cudaStream_t st);
-int attn_grid_warps(int block_size, int device);
+int attn_grid_warps(int block_size, int bits, int device);
 int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
 
@@ -39,7 +39,8 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Validates cfg and returns a copy with defaults applied (sm_scale).
 int check_config(const kvarn_config* cfg, kvarn_config* out) {
     if (!cfg) return KVARN_ERR_INVALID_ARG;
-    if (cfg->head_dim != 128 || cfg->group_size != 32 || cfg->bits != 2) return KVARN_ERR_UNSUPPORTED;
+    if (cfg->head_dim != 128 || cfg->group_size != 32 || (cfg->bits != 2 && cfg->bits != 4))
+        return KVARN_ERR_UNSUPPORTED;
     if (cfg->block_size != 32 && cfg->block_size != 64) return KVARN_ERR_UNSUPPORTED;
     if (cfg->varn_iters < 0 || cfg->varn_iters > 8) return KVARN_ERR_INVALID_ARG;
     if (cfg->flags & ~(KVARN_FLAG_NO_ROTATION | KVARN_FLAG_NO_TOKEN_PASS | KVARN_FLAG_NO_CHANNEL_PASS))
@@ -59,17 +60,17 @@ int current_device() {
     return d;
 }
 
-int resident_warps(int block_size) {
+int resident_warps(int block_size, int bits) {
     const int d = current_device();
     if (d < 0) return 0;
-    const int a = attn_grid_warps(block_size, d);
+    const int a = attn_grid_warps(block_size, bits, d);
     const int b = attn_bf16_grid_warps(block_size, d);
     return a > b ? a : b;
 }
 
 size_t ws_bytes(const kvarn_config& c, int32_t batch) {
     if (batch <= 0) return kWsHeader;
-    const int nw = resident_warps(c.block_size);
+    const int nw = resident_warps(c.block_size, c.bits);
     if (nw <= 0) return 0;
     const size_t G = (size_t)(c.n_q_heads / c.n_kv_heads);
     const size_t slots = (size_t)batch * c.n_kv_heads + (size_t)nw;
@@ -98,13 +99,13 @@ const char* kvarn_status_string(int status) {
 size_t kvarn_head_block_bytes(const kvarn_config* cfg) {
     kvarn_config c;
     if (check_config(cfg, &c) != KVARN_OK) return 0;
-    return (size_t)head_block_bytes(c.block_size);
+    return (size_t)head_block_bytes(c.block_size, c.bits);
 }
 
 size_t kvarn_block_bytes(const kvarn_config* cfg) {
     kvarn_config c;
     if (check_config(cfg, &c) != KVARN_OK) return 0;
-    return (size_t)c.n_kv_heads * 2 * head_block_bytes(c.block_size);
+    return (size_t)c.n_kv_heads * 2 * head_block_bytes(c.block_size, c.bits);
 }
 
 size_t kvarn_staging_bytes(const kvarn_config* cfg, int32_t max_seqs) {
@@ -178,7 +179,7 @@ int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, c
     const size_t need = ws_bytes(c, batch);
     if (need == 0) return KVARN_ERR_CUDA;
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;
-    const int nw = attn_grid_warps(c.block_size, current_device());
+    const int nw = attn_grid_warps(c.block_size, c.bits, current_device());
     if (nw <= 0) return KVARN_ERR_CUDA;
     return cuda_status(launch_decode_attn(c, q, q_dtype, pool, n_pool_blocks, (int64_t)kvarn_block_bytes(&c),
                                           staging, block_table, max_blocks_per_seq, seq_lens, batch, out, workspace,

@@ -39,6 +39,9 @@
 // Operand order inside each MMA (which token is row r, which channel is
 // k-slot j) is chosen so that the packed record order gives every lane its
 // operands directly; the writer packs codes in that order.
+// 4-bit codes (BITS = 4) take the same path: a lane's record is 64 bytes,
+// a = 1 + code/16 (code in fraction bits 6..9 of 1.0), and every factor 4
+// above becomes 16 (code * s + z = 16 s (a - 1) + z).
 #include "attn_common.cuh"
 
 namespace kvarn {
@@ -52,10 +55,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------- the split-K kernel
-template <int B, int S>
+template <int B, int BITS, int S>
 __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
+    static_assert(BITS == 2 || BITS == 4, "2- or 4-bit codes");
     wait_prior_grids();
-    constexpr int HB = head_block_bytes(B);
+    constexpr int HB = head_block_bytes(B, BITS);
+    constexpr int RW = 4 * BITS;             // 32-bit words per lane record
+    constexpr float kLevels = 1 << BITS;     // code = 2^BITS (a - 1)
     constexpr int NSB = B / 32;
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                              // S x (K, V)
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 
     // per-unit state
     uint32_t Qh[16], Ql[16];   // q_rot*2^(12-e) as fp16 hi | lo (lo kept only by the lo-column lanes)
-    float kmul = 0.f;          // 4 * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
+    float kmul = 0.f;          // 2^BITS * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
     float m_run = -INFINITY, l_part = 0.f;
     float O[8][2];             // rotated output, channels 32g + 4gq + 2m + rh, head tq
     const float sgn4[4] = {sign_of4(sb0, sb1, sb2, sb3, 4 * lane), sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 1),
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             const float sc = exp2i(12 - e);
             *reinterpret_cast<float4*>(&qsm[j * kD + 4 * lane]) =
                 make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
-            if (j == tq) kmul = 4.0f * exp2i(e - 12) * sm_scale * kLog2e;
+            if (j == tq) kmul = kLevels * exp2i(e - 12) * sm_scale * kLog2e;
         }
         __syncwarp();
 #pragma unroll
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         if (!valid && lane == 0) raise_error(err, KVARN_DEVERR_BLOCK_ID);
 
         if (valid) {
-            const uint16_t* KC = reinterpret_cast<const uint16_t*>(Kb + off_C(B));
+            const uint16_t* KC = reinterpret_cast<const uint16_t*>(Kb + off_C(B, BITS));
             // ---- per-block power of two bringing max C to (1/2, 1]
             float cmax;
             {
@@ -260,41 +266,54 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 mma16816(d, kOnes, kOnes, kOnes, kOnes, bq[4 * g + 2], bq[4 * g + 3]);
                 const float qg = d[0] + d[1];
                 Qneg[g] = -qg;
-                Qq[g] = 0.25f * qg;
+                Qq[g] = qg * (1.0f / kLevels);
             }
-            const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B));
-            const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B));
-            const uint16_t* KR = reinterpret_cast<const uint16_t*>(Kb + off_R(B));
-            const uint16_t* Vs = reinterpret_cast<const uint16_t*>(Vb + off_s(B));
-            const uint16_t* Vz = reinterpret_cast<const uint16_t*>(Vb + off_z(B));
-            const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B));
+            const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, BITS));
+            const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B, BITS));
+            const uint16_t* KR = reinterpret_cast<const uint16_t*>(Kb + off_R(B, BITS));
+            const uint16_t* Vs = reinterpret_cast<const uint16_t*>(Vb + off_s(B, BITS));
+            const uint16_t* Vz = reinterpret_cast<const uint16_t*>(Vb + off_z(B, BITS));
+            const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B, BITS));
 
             // ---------------- QK for every 32-token sub-block
             float sc[NSB][4];
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
-                uint32_t kw[8], kw8[8];
+                uint32_t kw[RW], kw8[RW];
                 {
-                    const uint4* rec = reinterpret_cast<const uint4*>(Kb) + 2 * (32 * sb + lane);
-                    const uint4 r0 = rec[0], r1 = rec[1];
-                    kw[0] = r0.x; kw[1] = r0.y; kw[2] = r0.z; kw[3] = r0.w;
-                    kw[4] = r1.x; kw[5] = r1.y; kw[6] = r1.z; kw[7] = r1.w;
+                    const uint4* rec = reinterpret_cast<const uint4*>(Kb) + (RW / 4) * (32 * sb + lane);
+#pragma unroll
+                    for (int r = 0; r < RW / 4; ++r) {
+                        const uint4 rr = rec[r];
+                        kw[4 * r] = rr.x; kw[4 * r + 1] = rr.y; kw[4 * r + 2] = rr.z; kw[4 * r + 3] = rr.w;
+                    }
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) kw8[k] = kw[k] >> 8;
+                for (int k = 0; k < RW; ++k) kw8[k] = kw[k] >> 8;
                 float acc[4][2][4];   // chains start from (-Q'_g, 0) per row
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const uint32_t b0 = bq[4 * g + 2 * kk], b1 = bq[4 * g + 2 * kk + 1];
-                        const int j = 4 * (g & 1) + 2 * kk;
 #pragma unroll
                         for (int mt = 0; mt < 2; ++mt) {
-                            const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
-                            const uint32_t a0 = code_pair(kw[i0], kw8[i0], j), a1 = code_pair(kw[i1], kw8[i1], j);
-                            const uint32_t a2 = code_pair(kw[i0], kw8[i0], j + 1);
-                            const uint32_t a3 = code_pair(kw[i1], kw8[i1], j + 1);
+                            uint32_t a0, a1, a2, a3;
+                            if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
+                                const int j = 4 * (g & 1) + 2 * kk;
+                                const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
+                                a0 = code_pair(kw[i0], kw8[i0], j);
+                                a1 = code_pair(kw[i1], kw8[i1], j);
+                                a2 = code_pair(kw[i0], kw8[i0], j + 1);
+                                a3 = code_pair(kw[i1], kw8[i1], j + 1);
+                            } else {           // word 4i + g, field e/2
+                                const int j = 2 * kk;
+                                const int i0 = 4 * (2 * mt) + g, i1 = 4 * (2 * mt + 1) + g;
+                                a0 = code_quad(kw[i0], kw8[i0], j);
+                                a1 = code_quad(kw[i1], kw8[i1], j);
+                                a2 = code_quad(kw[i0], kw8[i0], j + 1);
+                                a3 = code_quad(kw[i1], kw8[i1], j + 1);
+                            }
                             if (kk == 0)
                                 mma16816_from(acc[g][mt], a0, a1, a2, a3, b0, b1, Qneg[g], 0.f);
                             else
@@ -442,43 +461,55 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                     mma16816(Dz, pa[0], 0u, pa[1], 0u, z4.x, z4.y);
                     mma16816(Dz, pa[2], 0u, pa[3], 0u, z4.z, z4.w);
                 }
-                uint32_t vw[8], vw8[8];
+                uint32_t vw[RW], vw8[RW];
                 {
-                    const uint4* rec = reinterpret_cast<const uint4*>(Vb) + 2 * (32 * sb + lane);
-                    const uint4 r0 = rec[0], r1 = rec[1];
-                    vw[0] = r0.x; vw[1] = r0.y; vw[2] = r0.z; vw[3] = r0.w;
-                    vw[4] = r1.x; vw[5] = r1.y; vw[6] = r1.z; vw[7] = r1.w;
+                    const uint4* rec = reinterpret_cast<const uint4*>(Vb) + (RW / 4) * (32 * sb + lane);
+#pragma unroll
+                    for (int r = 0; r < RW / 4; ++r) {
+                        const uint4 rr = rec[r];
+                        vw[4 * r] = rr.x; vw[4 * r + 1] = rr.y; vw[4 * r + 2] = rr.z; vw[4 * r + 3] = rr.w;
+                    }
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) vw8[k] = vw[k] >> 8;
+                for (int k = 0; k < RW; ++k) vw8[k] = vw[k] >> 8;
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     const int g = mt >> 1, m = mt & 1;
-                    const uint32_t wd = vw[2 * g + m], wd8 = vw8[2 * g + m];
+                    if (BITS == 2) {   // word 2g + f/2, pair 4(d/4) + 2((d%4)/2) + f%2
+                        const uint32_t wd = vw[2 * g + m], wd8 = vw8[2 * g + m];
 #pragma unroll
-                    for (int kt = 0; kt < 2; ++kt)
-                        mma16816(Ob[mt], code_pair(wd, wd8, 4 * kt + 0), code_pair(wd, wd8, 4 * kt + 1),
-                                 code_pair(wd, wd8, 4 * kt + 2), code_pair(wd, wd8, 4 * kt + 3),
-                                 bv[g][2 * kt], bv[g][2 * kt + 1]);
+                        for (int kt = 0; kt < 2; ++kt)
+                            mma16816(Ob[mt], code_pair(wd, wd8, 4 * kt + 0), code_pair(wd, wd8, 4 * kt + 1),
+                                     code_pair(wd, wd8, 4 * kt + 2), code_pair(wd, wd8, 4 * kt + 3),
+                                     bv[g][2 * kt], bv[g][2 * kt + 1]);
+                    } else {           // word 4g + f, field d/2
+                        const int w0 = 4 * g + 2 * m, w1 = w0 + 1;
+#pragma unroll
+                        for (int kt = 0; kt < 2; ++kt)
+                            mma16816(Ob[mt], code_quad(vw[w0], vw8[w0], 2 * kt), code_quad(vw[w1], vw8[w1], 2 * kt),
+                                     code_quad(vw[w0], vw8[w0], 2 * kt + 1), code_quad(vw[w1], vw8[w1], 2 * kt + 1),
+                                     bv[g][2 * kt], bv[g][2 * kt + 1]);
+                    }
                 }
             }
             __syncwarp();   // pex is rewritten by the next block
-            // zs[h][g] = z-sum - 4 s-sum, hi + lo rows; delivered to the lanes of head tq
+            // zs[h][g] = z-sum - 2^BITS s-sum, hi + lo rows; delivered to the lanes of head tq
             float zq[4];
             {
                 const float v0 = Dz[0] + __shfl_xor_sync(kFull, Dz[0], 4);
                 const float v1 = Dz[1] + __shfl_xor_sync(kFull, Dz[1], 4);
-                const float zA = v0 - 4.0f * __shfl_xor_sync(kFull, v0, 2);   // valid where tq < 2:
-                const float zB = v1 - 4.0f * __shfl_xor_sync(kFull, v1, 2);   // groups 2tq, 2tq+1 of head gq/2
-                zq[0] = 0.25f * __shfl_sync(kFull, zA, 8 * tq);
-                zq[1] = 0.25f * __shfl_sync(kFull, zB, 8 * tq);
-                zq[2] = 0.25f * __shfl_sync(kFull, zA, 8 * tq + 1);
-                zq[3] = 0.25f * __shfl_sync(kFull, zB, 8 * tq + 1);
+                const float zA = v0 - kLevels * __shfl_xor_sync(kFull, v0, 2);   // valid where tq < 2:
+                const float zB = v1 - kLevels * __shfl_xor_sync(kFull, v1, 2);   // groups 2tq, 2tq+1 of head gq/2
+                constexpr float kInv = 1.0f / kLevels;
+                zq[0] = kInv * __shfl_sync(kFull, zA, 8 * tq);
+                zq[1] = kInv * __shfl_sync(kFull, zB, 8 * tq);
+                zq[2] = kInv * __shfl_sync(kFull, zA, 8 * tq + 1);
+                zq[3] = kInv * __shfl_sync(kFull, zB, 8 * tq + 1);
             }
-            // ---------------- O += 4 C_c / lam * (Ob + zs / 4)
+            // ---------------- O += 2^BITS C_c / lam * (Ob + zs / 2^BITS)
             {
-                const float il4 = 4.0f / lam;
-                const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B));
+                const float il4 = kLevels / lam;
+                const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const uint2 c2 = *reinterpret_cast<const uint2*>(VC + 32 * g + 4 * gq);
@@ -519,32 +550,44 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 }
 
 // ---------------------------------------------------------------- host side
-template <int B>
+template <int B, int BITS>
 constexpr int stages_for() { return B == 32 ? 4 : 2; }
 
-template <int B>
+template <int B, int BITS>
 size_t attn_smem_bytes() {
-    return (size_t)stages_for<B>() * 2 * head_block_bytes(B) + 64 + 4 * kD * sizeof(float) + 2 * 4 * B * sizeof(uint16_t);
+    return (size_t)stages_for<B, BITS>() * 2 * head_block_bytes(B, BITS) + 64 + 4 * kD * sizeof(float) +
+           2 * 4 * B * sizeof(uint16_t);
 }
 
-// Resident warps of the split-K kernel on `device` (cached per device).
-int attn_grid_warps(int block_size, int device) {
-    static int cache[2][64];
-    const int bi = block_size == 32 ? 0 : 1;
+template <int B, int BITS>
+struct AttnKernel {
+    static constexpr int kB = B;
+    static constexpr auto fn = decode_attn_2bit_kernel<B, BITS, stages_for<B, BITS>()>;
+    static size_t smem() { return attn_smem_bytes<B, BITS>(); }
+};
+
+template <typename F>
+auto with_attn_kernel(int block_size, int bits, F&& f) {
+    if (block_size == 32) return bits == 4 ? f(AttnKernel<32, 4>{}) : f(AttnKernel<32, 2>{});
+    return bits == 4 ? f(AttnKernel<64, 4>{}) : f(AttnKernel<64, 2>{});
+}
+
+// Resident warps of the split-K kernel for (block size, code width) on
+// `device` (cached per device).
+int attn_grid_warps(int block_size, int bits, int device) {
+    static int cache[2][2][64];
+    const int bi = block_size == 32 ? 0 : 1, wi = bits == 4 ? 1 : 0;
     if (device < 0 || device >= 64) return 0;
-    if (cache[bi][device] > 0) return cache[bi][device];
+    if (cache[bi][wi][device] > 0) return cache[bi][wi][device];
     int sms = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-    cudaError_t e;
-    if (block_size == 32)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_attn_2bit_kernel<32, stages_for<32>()>, 32,
-                                                          attn_smem_bytes<32>());
-    else
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_attn_2bit_kernel<64, stages_for<64>()>, 32,
-                                                          attn_smem_bytes<64>());
+    const cudaError_t e = with_attn_kernel(block_size, bits, [&](auto k) {
+        using K = decltype(k);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, K::fn, 32, K::smem());
+    });
     if (e != cudaSuccess || per_sm <= 0) return 0;
-    cache[bi][device] = sms * per_sm;
-    return cache[bi][device];
+    cache[bi][wi][device] = sms * per_sm;
+    return cache[bi][wi][device];
 }
 
 cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
@@ -573,15 +616,12 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)batch * a.n_q + 3) / 4);
-    cudaError_t e;
-    if (cfg.block_size == 32) {
-        e = launch_pdl(decode_attn_2bit_kernel<32, stages_for<32>()>, nw, 32, attn_smem_bytes<32>(), st, a);
-        if (e == cudaSuccess) e = launch_pdl(merge_kernel<32, true>, mgrid, 128, 0, st, a);
-    } else {
-        e = launch_pdl(decode_attn_2bit_kernel<64, stages_for<64>()>, nw, 32, attn_smem_bytes<64>(), st, a);
-        if (e == cudaSuccess) e = launch_pdl(merge_kernel<64, true>, mgrid, 128, 0, st, a);
-    }
-    return e;
+    return with_attn_kernel(cfg.block_size, cfg.bits, [&](auto k) {
+        using K = decltype(k);
+        cudaError_t e = launch_pdl(K::fn, nw, 32, K::smem(), st, a);
+        if (e == cudaSuccess) e = launch_pdl(merge_kernel<K::kB, true>, mgrid, 128, 0, st, a);
+        return e;
+    });
 }
 
 }  // namespace kvarn

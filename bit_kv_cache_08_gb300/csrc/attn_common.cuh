@@ -61,6 +61,13 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int j) {
     const uint32_t x = (j < 4) ? w * (1u << (8 - 2 * j)) : (j == 4 ? w : w8 * (1u << (16 - 2 * j)));
     return (x & 0x03000300u) | 0x3C003C00u;
 }
+// The 4-bit analogue: field j (0..3) of each half of w (bits 4j..4j+3 and
+// 16+4j..) moved to fp16 mantissa bits 6..9 and or-ed with 1.0, giving the
+// exact fp16x2 (1 + code_lo/16, 1 + code_hi/16); w8 = w >> 8 as above.
+__device__ __forceinline__ uint32_t code_quad(uint32_t w, uint32_t w8, int j) {
+    const uint32_t x = (j < 2) ? w * (1u << (6 - 4 * j)) : w8 * (1u << (14 - 4 * j));
+    return (x & 0x03C003C0u) | 0x3C003C00u;
+}
 
 // 2^k as a float for k in [-126, 127]
 __device__ __forceinline__ float exp2i(int k) {

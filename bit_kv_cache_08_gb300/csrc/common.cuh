@@ -19,11 +19,13 @@ constexpr float kF16Max = 65504.0f;
 constexpr float kF16MinNormal = 6.103515625e-05f;   // 2^-14
 constexpr uint32_t kFull = 0xffffffffu;
 
-__host__ __device__ constexpr int head_block_bytes(int B) { return 50 * B + 256; }
-__host__ __device__ constexpr int off_s(int B) { return 32 * B; }
-__host__ __device__ constexpr int off_z(int B) { return 40 * B; }
-__host__ __device__ constexpr int off_R(int B) { return 48 * B; }
-__host__ __device__ constexpr int off_C(int B) { return 50 * B; }
+// Head-block sections for codes of `bits` bits: codes (16 B bits bytes), then
+// s, z (fp16 [4][B] each), R (fp16 [B]), C (fp16 [128]).
+__host__ __device__ constexpr int off_s(int B, int bits) { return 16 * bits * B; }
+__host__ __device__ constexpr int off_z(int B, int bits) { return off_s(B, bits) + 8 * B; }
+__host__ __device__ constexpr int off_R(int B, int bits) { return off_s(B, bits) + 16 * B; }
+__host__ __device__ constexpr int off_C(int B, int bits) { return off_s(B, bits) + 18 * B; }
+__host__ __device__ constexpr int head_block_bytes(int B, int bits) { return off_C(B, bits) + 256; }
 
 // Workspace header: the first uint32 is the sticky device error word.
 constexpr size_t kWsHeader = 256;

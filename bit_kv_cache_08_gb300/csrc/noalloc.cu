@@ -23,7 +23,7 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
                                float* out, void* workspace, int nw, cudaStream_t st);
-int attn_grid_warps(int block_size, int device);
+int attn_grid_warps(int block_size, int bits, int device);
 int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
 
@@ -63,11 +63,12 @@ extern "C" int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q,
                                          const int32_t* seq_lens, int32_t batch, float* out,
                                          uint32_t* error_word, void* stream) {
     if (!cfg) return KVARN_ERR_INVALID_ARG;
-    if (cfg->head_dim != 128 || cfg->group_size != 32 || cfg->bits != 2 ||
+    if (cfg->head_dim != 128 || cfg->group_size != 32 || (cfg->bits != 2 && cfg->bits != 4) ||
         (cfg->block_size != 32 && cfg->block_size != 64))
         return KVARN_ERR_UNSUPPORTED;
-    if (cfg->varn_iters < 1 || cfg->varn_iters > 8 || cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads ||
-        cfg->n_q_heads % cfg->n_kv_heads != 0 || !(cfg->sm_scale >= 0.0f) || isinf(cfg->sm_scale))
+    if (cfg->varn_iters < 0 || cfg->varn_iters > 8 || cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads ||
+        cfg->n_q_heads % cfg->n_kv_heads != 0 || !(cfg->sm_scale >= 0.0f) || isinf(cfg->sm_scale) ||
+        (cfg->flags & ~(KVARN_FLAG_NO_ROTATION | KVARN_FLAG_NO_TOKEN_PASS | KVARN_FLAG_NO_CHANNEL_PASS)))
         return KVARN_ERR_INVALID_ARG;
     if (cfg->n_q_heads / cfg->n_kv_heads > 4) return KVARN_ERR_UNSUPPORTED;
     kvarn_config c = *cfg;
@@ -85,7 +86,7 @@ extern "C" int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q,
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVARN_ERR_CUDA;
-    const int nw = attn_grid_warps(c.block_size, dev);
+    const int nw = attn_grid_warps(c.block_size, c.bits, dev);
     const int nw_any = nw > attn_bf16_grid_warps(c.block_size, dev) ? nw : attn_bf16_grid_warps(c.block_size, dev);
     if (nw <= 0 || nw_any <= 0) return KVARN_ERR_CUDA;
     // same size rule as kvarn_workspace_bytes; beyond the fixed array: refuse
@@ -99,7 +100,7 @@ extern "C" int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q,
     cudaStream_t st = (cudaStream_t)stream;
     // the error word is the only part of the scratch that must start at zero
     if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st) != cudaSuccess) return KVARN_ERR_CUDA;
-    const int64_t block_bytes = (int64_t)c.n_kv_heads * 2 * head_block_bytes(c.block_size);
+    const int64_t block_bytes = (int64_t)c.n_kv_heads * 2 * head_block_bytes(c.block_size, c.bits);
     if (launch_decode_attn(c, q, q_dtype, pool, n_pool_blocks, block_bytes, staging, block_table,
                            max_blocks_per_seq, seq_lens, batch, out, scratch, nw, st) != cudaSuccess)
         return KVARN_ERR_CUDA;

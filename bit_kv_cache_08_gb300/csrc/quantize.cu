@@ -26,8 +26,10 @@
 //   quantise   y = x_rot * (1/R16) * (1/C16) (correctly rounded reciprocals;
 //              a few fp32 ulps from the quotient), per (token, 32-channel group):
 //              z = fp16 round-down of the
-//              minimum, s = least fp16 with z + 3s >= maximum (directed-rounding
-//              candidate plus one exact check), code = nearest level, ties even
+//              minimum, s = least fp16 with z + L s >= maximum, L = 2^bits - 1
+//              (directed-rounding candidate plus one exact check), code = nearest
+//              level, ties even (3 compares at 2 bits, a 4-step binary search
+//              over the 15 boundaries at 4 bits)
 //   pack       codes OR-ed into the shared-memory image of the head-block in
 //              the attention kernel's record order, then 16-byte stores.
 #include "common.cuh"
@@ -38,9 +40,9 @@ constexpr int kRowsPerWarp = 4;
 template <int B> constexpr int quant_warps() { return B / kRowsPerWarp; }
 template <int B> constexpr int quant_threads() { return 32 * quant_warps<B>(); }
 
-template <int B>
+template <int B, int BITS>
 struct QuantSmem {
-    alignas(16) uint8_t image[head_block_bytes(B)];   // exact global layout
+    alignas(16) uint8_t image[head_block_bytes(B, BITS)];   // exact global layout
     alignas(16) float part[quant_warps<B>()][kD + 4]; // per-warp column partial sums (padded rows)
     alignas(16) float tot[2][kD];                     // column totals (double-buffered)
 };
@@ -50,8 +52,8 @@ struct QuantSmem {
 // Warp w reduces channels [w*CPW, (w+1)*CPW) over all warps (4 shared loads
 // per thread plus a shuffle tree), then every thread reads back its 4 totals.
 // `buf` alternates between calls so that one barrier per call suffices.
-template <int B>
-__device__ __forceinline__ float4 column_totals(QuantSmem<B>& q, const float (&cs)[4], int warp, int lane,
+template <int B, int BITS>
+__device__ __forceinline__ float4 column_totals(QuantSmem<B, BITS>& q, const float (&cs)[4], int warp, int lane,
                                                 int buf) {
     constexpr int NW = quant_warps<B>(), CPW = kD / NW, SUB = 32 / CPW;   // SUB warp subsets of 4 warps
     *reinterpret_cast<float4*>(&q.part[warp][4 * lane]) = make_float4(cs[0], cs[1], cs[2], cs[3]);
@@ -110,11 +112,16 @@ __device__ __forceinline__ bool usable_variance(float v, float mu) {
     return v > 0.f && isfinite(v) && v > 0x1p-30f * (mu * mu);
 }
 
-// Least fp16 s >= 0 with z + 3 s >= M, for fp16 z <= M (all exact comparisons).
+// Least fp16 s >= 0 with z + L s >= M (L = 2^bits - 1 steps), for fp16 z <= M
+// (all exact comparisons).
+template <int L>
 __device__ __forceinline__ float step_for(float zf, float M) {
+    static_assert(L == 3 || L == 15, "2- or 4-bit codes");
     if (zf >= M) return 0.0f;
-    // >= exact (M - z)/3: every step rounds up, 0x1.555556p-2f = RU(1/3)
-    float t = __fmul_ru(__fsub_ru(M, zf), 0x1.555556p-2f);
+    // >= exact (M - z)/L: every step rounds up; RU(1/3) = 0x1.555556p-2f,
+    // RU(1/15) = 0x1.111112p-4f
+    constexpr float kInvL = L == 3 ? 0x1.555556p-2f : 0x1.111112p-4f;
+    float t = __fmul_ru(__fsub_ru(M, zf), kInvL);
     __half s = __float2half_ru(t);                         // >= exact minimum
     float sf = __half2float(s);
     if (!(sf <= kF16Max)) { s = __float2half_rn(kF16Max); sf = kF16Max; }
@@ -122,21 +129,21 @@ __device__ __forceinline__ float step_for(float zf, float M) {
     uint16_t bits = __half_as_ushort(s);
     if (bits > 0) {
         float pf = __half2float(__ushort_as_half((uint16_t)(bits - 1)));
-        if (__fadd_rd(zf, 3.0f * pf) >= M) sf = pf;         // rd-sum >= M <=> exact sum >= M
+        if (__fadd_rd(zf, (float)L * pf) >= M) sf = pf;     // L pf exact; rd-sum >= M <=> exact sum >= M
     }
     return sf;
 }
 
 // Quantise the tile held in x (rows of this warp) into q.image.
-template <int B>
-__device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p, QuantSmem<B>& q,
+template <int B, int BITS>
+__device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p, QuantSmem<B, BITS>& q,
                               int warp, int lane) {
     constexpr int RPW = kRowsPerWarp, NW = quant_warps<B>();
     uint32_t* words = reinterpret_cast<uint32_t*>(q.image);
-    uint16_t* s_sec = reinterpret_cast<uint16_t*>(q.image + off_s(B));
-    uint16_t* z_sec = reinterpret_cast<uint16_t*>(q.image + off_z(B));
-    uint16_t* R_sec = reinterpret_cast<uint16_t*>(q.image + off_R(B));
-    uint16_t* C_sec = reinterpret_cast<uint16_t*>(q.image + off_C(B));
+    uint16_t* s_sec = reinterpret_cast<uint16_t*>(q.image + off_s(B, BITS));
+    uint16_t* z_sec = reinterpret_cast<uint16_t*>(q.image + off_z(B, BITS));
+    uint16_t* R_sec = reinterpret_cast<uint16_t*>(q.image + off_R(B, BITS));
+    uint16_t* C_sec = reinterpret_cast<uint16_t*>(q.image + off_C(B, BITS));
 
     // ---- rotation: x_rot = H (sigma . x) / sqrt(128) (identity in the no-rotation ablation)
     uint32_t sw = p.sb[lane >> 3] >> (4 * (lane & 7));    // this lane's 4 sign bits
@@ -189,7 +196,7 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
         for (int i = 0; i < RPW; ++i)
 #pragma unroll
             for (int k = 0; k < 4; ++k) cs[k] += x[i][k] * rR[i];
-        const float4 m4 = column_totals<B>(q, cs, warp, lane, buf);
+        const float4 m4 = column_totals<B, BITS>(q, cs, warp, lane, buf);
         buf ^= 1;
         const float cmu[4] = {m4.x * (1.0f / B), m4.y * (1.0f / B), m4.z * (1.0f / B), m4.w * (1.0f / B)};
 #pragma unroll
@@ -201,7 +208,7 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
                 const float d = x[i][k] * rR[i] - cmu[k];
                 cs[k] += d * d;
             }
-        const float4 v4 = column_totals<B>(q, cs, warp, lane, buf);
+        const float4 v4 = column_totals<B, BITS>(q, cs, warp, lane, buf);
         buf ^= 1;
         const float cvar[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
@@ -239,19 +246,50 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
         }
         const __half zh = __float2half_rd(fminf(fmaxf(mn, -kF16Max), kF16Max));
         const float zf = __half2float(zh);
-        const float sf = step_for(zf, mx);
+        const float sf = step_for<(1 << BITS) - 1>(zf, mx);
         uint32_t code[4];
         if (sf == 0.0f) {
             code[0] = code[1] = code[2] = code[3] = 0u;
-        } else {
+        } else if (BITS == 2) {
             const float b0 = zf + 0.5f * sf, b1 = zf + 1.5f * sf, b2 = zf + 2.5f * sf;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 code[k] = (uint32_t)(yq[k] > b0) + (uint32_t)(yq[k] >= b1) + (uint32_t)(yq[k] > b2);
+        } else {
+            // binary search over the 15 boundaries z + (c - 1/2) s (each one fma,
+            // rounded once like the 2-bit ones); a tie goes to the even level, so
+            // the candidate steps 8, 4, 2 (even candidates) test >=, step 1 tests >
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t c = 0;
+#pragma unroll
+                for (int st = 8; st >= 1; st >>= 1) {
+                    const float b = fmaf((float)(c + st) - 0.5f, sf, zf);
+                    const bool up = (st == 1) ? (yq[k] > b) : (yq[k] >= b);
+                    c = up ? c + st : c;
+                }
+                code[k] = c;
+            }
         }
         // ---- pack into the record order of this kind
         const int sb = t >> 5;
-        if (p.kind == KVARN_KIND_K) {
+        if (BITS == 4) {
+            if (p.kind == KVARN_KIND_K) {   // word 4i + g, bit 4(e/2) + 16(e%2)
+                const int a = (t & 31) >> 2, ii = t & 3, bq = (lane & 7) >> 1, eh = lane & 1;
+                uint32_t contrib = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = 4 * eh + k;
+                    contrib |= code[k] << (4 * (e >> 1) + 16 * (e & 1));
+                }
+                atomicOr(&words[(32 * sb + 4 * a + bq) * 16 + 4 * ii + g], contrib);
+            } else {                        // word 4g + f, bit 4(d/2) + 16(d%2)
+                const int a = lane & 7, bq = (t & 31) >> 3, d = t & 7;
+                const int rec = 32 * sb + 4 * a + bq, bit = 4 * (d >> 1) + 16 * (d & 1);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) atomicOr(&words[rec * 16 + 4 * g + k], code[k] << bit);
+            }
+        } else if (p.kind == KVARN_KIND_K) {
             const int a = (t & 31) >> 2, ii = t & 3, bq = (lane & 7) >> 1, eh = lane & 1;
             const int word = (32 * sb + 4 * a + bq) * 8 + 2 * ii + (g >> 1);
             uint32_t contrib = 0;
@@ -281,17 +319,17 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
     __syncthreads();
 }
 
-template <int B>
-__device__ __forceinline__ void zero_code_words(QuantSmem<B>& q, int tid) {
+template <int B, int BITS>
+__device__ __forceinline__ void zero_code_words(QuantSmem<B, BITS>& q, int tid) {
     uint32_t* words = reinterpret_cast<uint32_t*>(q.image);
-    for (int i = tid; i < B * 8; i += quant_threads<B>()) words[i] = 0u;
+    for (int i = tid; i < B * 4 * BITS; i += quant_threads<B>()) words[i] = 0u;
 }
 
-template <int B>
-__device__ __forceinline__ void store_image(const QuantSmem<B>& q, uint8_t* dst, int tid) {
+template <int B, int BITS>
+__device__ __forceinline__ void store_image(const QuantSmem<B, BITS>& q, uint8_t* dst, int tid) {
     const uint4* src = reinterpret_cast<const uint4*>(q.image);
     uint4* d = reinterpret_cast<uint4*>(dst);
-    for (int i = tid; i < head_block_bytes(B) / 16; i += quant_threads<B>()) d[i] = src[i];
+    for (int i = tid; i < head_block_bytes(B, BITS) / 16; i += quant_threads<B>()) d[i] = src[i];
 }
 
 __device__ __forceinline__ void load4(const void* src, int dtype, int64_t elem_off, float (&v)[4]) {
@@ -308,16 +346,16 @@ __device__ __forceinline__ void load4(const void* src, int dtype, int64_t elem_o
 }
 
 // ---------------------------------------------------------------- bulk quantise
-template <int B>
+template <int B, int BITS>
 __global__ void __launch_bounds__(quant_threads<B>()) quantize_blocks_kernel(
     const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
     uint8_t* __restrict__ dst_base, const int64_t* __restrict__ dst_offsets, QuantParams p,
     uint32_t* err) {
     wait_prior_grids();
-    __shared__ QuantSmem<B> q;
+    __shared__ QuantSmem<B, BITS> q;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
-    zero_code_words<B>(q, tid);
+    zero_code_words<B, BITS>(q, tid);
     float x[kRowsPerWarp][4];
     bool bad = false;
 #pragma unroll
@@ -328,21 +366,21 @@ __global__ void __launch_bounds__(quant_threads<B>()) quantize_blocks_kernel(
         for (int k = 0; k < 4; ++k) bad |= !isfinite(x[i][k]);
     }
     if (__syncthreads_or(bad) && tid == 0) raise_error(err, KVARN_DEVERR_NONFINITE);
-    quantize_tile<B>(x, p, q, warp, lane);
-    const int64_t off = dst_offsets ? dst_offsets[n] : n * (int64_t)head_block_bytes(B);
-    store_image<B>(q, dst_base + off, tid);
+    quantize_tile<B, BITS>(x, p, q, warp, lane);
+    const int64_t off = dst_offsets ? dst_offsets[n] : n * (int64_t)head_block_bytes(B, BITS);
+    store_image<B, BITS>(q, dst_base + off, tid);
 }
 
 // ---------------------------------------------------------------- fused append
 // grid (batch, n_kv, 2): one CTA per (sequence, kv head, K|V).
-template <int B>
+template <int B, int BITS>
 __global__ void __launch_bounds__(quant_threads<B>()) append_kernel(
     uint8_t* __restrict__ pool, int64_t n_pool_blocks, int64_t block_bytes,
     uint16_t* __restrict__ staging, const int32_t* __restrict__ block_table, int max_blocks,
     const int32_t* __restrict__ pos_arr, const uint16_t* __restrict__ k_new,
     const uint16_t* __restrict__ v_new, int n_kv, QuantParams p, uint32_t* err) {
     wait_prior_grids();
-    __shared__ QuantSmem<B> q;
+    __shared__ QuantSmem<B, BITS> q;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
     const int pos = pos_arr[b];
@@ -363,7 +401,7 @@ __global__ void __launch_bounds__(quant_threads<B>()) append_kernel(
         return;
     }
     p.kind = kv;
-    zero_code_words<B>(q, tid);
+    zero_code_words<B, BITS>(q, tid);
     float x[kRowsPerWarp][4];
     bool bad = false;
 #pragma unroll
@@ -375,20 +413,20 @@ __global__ void __launch_bounds__(quant_threads<B>()) append_kernel(
         for (int k = 0; k < 4; ++k) bad |= !isfinite(x[i][k]);
     }
     if (__syncthreads_or(bad) && tid == 0) raise_error(err, KVARN_DEVERR_NONFINITE);
-    quantize_tile<B>(x, p, q, warp, lane);
-    store_image<B>(q, pool + phys * block_bytes + (int64_t)(2 * h + kv) * head_block_bytes(B), tid);
+    quantize_tile<B, BITS>(x, p, q, warp, lane);
+    store_image<B, BITS>(q, pool + phys * block_bytes + (int64_t)(2 * h + kv) * head_block_bytes(B, BITS), tid);
 }
 
 // ---------------------------------------------------------------- dequantise
 // Token row t of a head-block image in shared memory: this lane's 4 channels
 // 4 lane .. 4 lane + 3 of (code*s + z)*R*C (rotated space).
-template <int B>
+template <int B, int BITS>
 __device__ __forceinline__ void dequant_row4(const uint8_t* img, int kind, int t, int lane, float (&v)[4]) {
     const uint32_t* words = reinterpret_cast<const uint32_t*>(img);
-    const uint16_t* s_sec = reinterpret_cast<const uint16_t*>(img + off_s(B));
-    const uint16_t* z_sec = reinterpret_cast<const uint16_t*>(img + off_z(B));
-    const uint16_t* R_sec = reinterpret_cast<const uint16_t*>(img + off_R(B));
-    const uint16_t* C_sec = reinterpret_cast<const uint16_t*>(img + off_C(B));
+    const uint16_t* s_sec = reinterpret_cast<const uint16_t*>(img + off_s(B, BITS));
+    const uint16_t* z_sec = reinterpret_cast<const uint16_t*>(img + off_z(B, BITS));
+    const uint16_t* R_sec = reinterpret_cast<const uint16_t*>(img + off_R(B, BITS));
+    const uint16_t* C_sec = reinterpret_cast<const uint16_t*>(img + off_C(B, BITS));
     const int g = lane >> 3, sb = t >> 5;
     const float s = h2f(s_sec[g * B + t]), z = h2f(z_sec[g * B + t]), R = h2f(R_sec[t]);
 #pragma unroll
@@ -397,39 +435,49 @@ __device__ __forceinline__ void dequant_row4(const uint8_t* img, int kind, int t
         int word, bit;
         if (kind == KVARN_KIND_K) {
             const int a = (t & 31) >> 2, ii = t & 3, bq = (c & 31) >> 3, e = c & 7;
-            word = (32 * sb + 4 * a + bq) * 8 + 2 * ii + (g >> 1);
-            bit = 2 * (4 * (g & 1) + (e >> 1)) + 16 * (e & 1);
+            if (BITS == 4) {
+                word = (32 * sb + 4 * a + bq) * 16 + 4 * ii + g;
+                bit = 4 * (e >> 1) + 16 * (e & 1);
+            } else {
+                word = (32 * sb + 4 * a + bq) * 8 + 2 * ii + (g >> 1);
+                bit = 2 * (4 * (g & 1) + (e >> 1)) + 16 * (e & 1);
+            }
         } else {
             const int bq = (t & 31) >> 3, d = t & 7, a = (c & 31) >> 2, f = c & 3;
-            word = (32 * sb + 4 * a + bq) * 8 + 2 * g + (f >> 1);
-            bit = 2 * (4 * (d >> 2) + 2 * ((d & 3) >> 1) + (f & 1)) + 16 * (d & 1);
+            if (BITS == 4) {
+                word = (32 * sb + 4 * a + bq) * 16 + 4 * g + f;
+                bit = 4 * (d >> 1) + 16 * (d & 1);
+            } else {
+                word = (32 * sb + 4 * a + bq) * 8 + 2 * g + (f >> 1);
+                bit = 2 * (4 * (d >> 2) + 2 * ((d & 3) >> 1) + (f & 1)) + 16 * (d & 1);
+            }
         }
-        const float code = (float)((words[word] >> bit) & 3u);
+        const float code = (float)((words[word] >> bit) & ((1u << BITS) - 1u));
         v[k] = fmaf(code, s, z) * R * h2f(C_sec[c]);
     }
 }
 
-template <int B>
+template <int B, int BITS>
 __device__ __forceinline__ void load_image(uint8_t* img, const uint8_t* src, int tid) {
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    for (int i = tid; i < head_block_bytes(B) / 16; i += 256) reinterpret_cast<uint4*>(img)[i] = s4[i];
+    for (int i = tid; i < head_block_bytes(B, BITS) / 16; i += 256) reinterpret_cast<uint4*>(img)[i] = s4[i];
 }
 
-template <int B>
+template <int B, int BITS>
 __global__ void __launch_bounds__(256) dequantize_kernel(
     const uint8_t* __restrict__ src_base, const int64_t* __restrict__ src_offsets, int kind,
     int rotated, QuantParams p, float* __restrict__ out) {
     wait_prior_grids();
-    __shared__ alignas(16) uint8_t img[head_block_bytes(B)];
+    __shared__ alignas(16) uint8_t img[head_block_bytes(B, BITS)];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
-    const int64_t off = src_offsets ? src_offsets[n] : n * (int64_t)head_block_bytes(B);
-    load_image<B>(img, src_base + off, tid);
+    const int64_t off = src_offsets ? src_offsets[n] : n * (int64_t)head_block_bytes(B, BITS);
+    load_image<B, BITS>(img, src_base + off, tid);
     __syncthreads();
     for (int i = 0; i < B / 8; ++i) {
         const int t = warp * (B / 8) + i;
         float v[4];
-        dequant_row4<B>(img, kind, t, lane, v);
+        dequant_row4<B, BITS>(img, kind, t, lane, v);
         if (!rotated && !(p.flags & KVARN_FLAG_NO_ROTATION)) {
             fwht128(v, lane);
 #pragma unroll
@@ -444,17 +492,17 @@ __global__ void __launch_bounds__(256) dequantize_kernel(
 // E_D = |x^| (x^/|x^| - x/|x|), x the values before quantisation and x^ the
 // dequantised ones. Norms and the angle do not change under the rotation, so
 // both are taken in the rotated space (x rotated like the quantiser does).
-template <int B>
+template <int B, int BITS>
 __global__ void __launch_bounds__(256) error_split_kernel(
     const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
     const uint8_t* __restrict__ packed_base, const int64_t* __restrict__ packed_offsets, int kind,
     QuantParams p, float* __restrict__ out) {
     wait_prior_grids();
-    __shared__ alignas(16) uint8_t img[head_block_bytes(B)];
+    __shared__ alignas(16) uint8_t img[head_block_bytes(B, BITS)];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = blockIdx.x;
-    const int64_t off = packed_offsets ? packed_offsets[n] : n * (int64_t)head_block_bytes(B);
-    load_image<B>(img, packed_base + off, tid);
+    const int64_t off = packed_offsets ? packed_offsets[n] : n * (int64_t)head_block_bytes(B, BITS);
+    load_image<B, BITS>(img, packed_base + off, tid);
     __syncthreads();
     const uint32_t sw = p.sb[lane >> 3] >> (4 * (lane & 7));
     for (int i = 0; i < B / 8; ++i) {
@@ -468,7 +516,7 @@ __global__ void __launch_bounds__(256) error_split_kernel(
 #pragma unroll
             for (int k = 0; k < 4; ++k) x[k] *= kInvSqrtD;
         }
-        dequant_row4<B>(img, kind, t, lane, xh);
+        dequant_row4<B, BITS>(img, kind, t, lane, xh);
         const float nx = sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]));
         const float nh = sqrtf(warp_sum(xh[0] * xh[0] + xh[1] * xh[1] + xh[2] * xh[2] + xh[3] * xh[3]));
         float em, ed = 0.f;
@@ -501,16 +549,24 @@ static QuantParams make_params(const kvarn_config& cfg, int kind) {
     return p;
 }
 
+// The (block size, code width) instantiation for a config: f(int_constant<B>, int_constant<BITS>).
+template <int V> struct ic { static constexpr int value = V; };
+template <typename F>
+cudaError_t dispatch(const kvarn_config& cfg, F&& f) {
+    if (cfg.block_size == 32) return cfg.bits == 4 ? f(ic<32>{}, ic<4>{}) : f(ic<32>{}, ic<2>{});
+    return cfg.bits == 4 ? f(ic<64>{}, ic<4>{}) : f(ic<64>{}, ic<2>{});
+}
+
 cudaError_t launch_quantize_blocks(const kvarn_config& cfg, int kind, const void* src, int dtype,
                                    int64_t n, int64_t block_stride, int64_t token_stride,
                                    void* dst_base, const int64_t* dst_offsets, uint32_t* err,
                                    cudaStream_t st) {
     QuantParams p = make_params(cfg, kind);
-    if (cfg.block_size == 32)
-        return launch_pdl(quantize_blocks_kernel<32>, (unsigned)n, quant_threads<32>(), 0, st, src, dtype,
+    return dispatch(cfg, [&](auto b, auto w) {
+        constexpr int B = decltype(b)::value, BITS = decltype(w)::value;
+        return launch_pdl(quantize_blocks_kernel<B, BITS>, (unsigned)n, quant_threads<B>(), 0, st, src, dtype,
                           block_stride, token_stride, (uint8_t*)dst_base, dst_offsets, p, err);
-    return launch_pdl(quantize_blocks_kernel<64>, (unsigned)n, quant_threads<64>(), 0, st, src, dtype,
-                      block_stride, token_stride, (uint8_t*)dst_base, dst_offsets, p, err);
+    });
 }
 
 cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_blocks,
@@ -519,35 +575,34 @@ cudaError_t launch_append(const kvarn_config& cfg, void* pool, int64_t n_pool_bl
                           int batch, uint32_t* err, cudaStream_t st) {
     QuantParams p = make_params(cfg, 0);
     const dim3 grid(batch, cfg.n_kv_heads, 2);
-    if (cfg.block_size == 32)
-        return launch_pdl(append_kernel<32>, grid, quant_threads<32>(), 0, st, (uint8_t*)pool, n_pool_blocks,
+    return dispatch(cfg, [&](auto b, auto w) {
+        constexpr int B = decltype(b)::value, BITS = decltype(w)::value;
+        return launch_pdl(append_kernel<B, BITS>, grid, quant_threads<B>(), 0, st, (uint8_t*)pool, n_pool_blocks,
                           block_bytes, (uint16_t*)staging, block_table, max_blocks, pos, (const uint16_t*)k_new,
                           (const uint16_t*)v_new, cfg.n_kv_heads, p, err);
-    return launch_pdl(append_kernel<64>, grid, quant_threads<64>(), 0, st, (uint8_t*)pool, n_pool_blocks,
-                      block_bytes, (uint16_t*)staging, block_table, max_blocks, pos, (const uint16_t*)k_new,
-                      (const uint16_t*)v_new, cfg.n_kv_heads, p, err);
+    });
 }
 
 cudaError_t launch_error_split(const kvarn_config& cfg, int kind, const void* src, int dtype, int64_t n,
                                int64_t block_stride, int64_t token_stride, const void* packed_base,
                                const int64_t* packed_offsets, float* out, cudaStream_t st) {
     QuantParams p = make_params(cfg, kind);
-    if (cfg.block_size == 32)
-        return launch_pdl(error_split_kernel<32>, (unsigned)n, 256, 0, st, src, dtype, block_stride, token_stride,
-                          (const uint8_t*)packed_base, packed_offsets, kind, p, out);
-    return launch_pdl(error_split_kernel<64>, (unsigned)n, 256, 0, st, src, dtype, block_stride, token_stride,
-                      (const uint8_t*)packed_base, packed_offsets, kind, p, out);
+    return dispatch(cfg, [&](auto b, auto w) {
+        constexpr int B = decltype(b)::value, BITS = decltype(w)::value;
+        return launch_pdl(error_split_kernel<B, BITS>, (unsigned)n, 256, 0, st, src, dtype, block_stride,
+                          token_stride, (const uint8_t*)packed_base, packed_offsets, kind, p, out);
+    });
 }
 
 cudaError_t launch_dequantize(const kvarn_config& cfg, int kind, const void* src_base,
                               const int64_t* src_offsets, int64_t n, int rotated, float* out,
                               cudaStream_t st) {
     QuantParams p = make_params(cfg, kind);
-    if (cfg.block_size == 32)
-        return launch_pdl(dequantize_kernel<32>, (unsigned)n, 256, 0, st, (const uint8_t*)src_base, src_offsets,
-                          kind, rotated, p, out);
-    return launch_pdl(dequantize_kernel<64>, (unsigned)n, 256, 0, st, (const uint8_t*)src_base, src_offsets,
-                      kind, rotated, p, out);
+    return dispatch(cfg, [&](auto b, auto w) {
+        constexpr int B = decltype(b)::value, BITS = decltype(w)::value;
+        return launch_pdl(dequantize_kernel<B, BITS>, (unsigned)n, 256, 0, st, (const uint8_t*)src_base,
+                          src_offsets, kind, rotated, p, out);
+    });
 }
 
 }  // namespace kvarn

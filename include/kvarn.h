@@ -1,5 +1,6 @@
 /*
- * kvarn.h -- C ABI of the GB300 (sm_103a) KVarN 2-bit KV-cache library.
+ * kvarn.h -- C ABI of the GB300 (sm_103a) KVarN 2-bit KV-cache library
+ * (4-bit codes as an option of the same format).
  *
  * KVarN stores the K and V caches at 2 bits per element without calibration
  * data: each block of tokens is rotated by a randomised Hadamard matrix over
@@ -39,24 +40,27 @@
  *
  * Data layouts (little-endian; fp16/bf16 are IEEE binary16 / bfloat16)
  *   Head-block: one (physical block, kv head, K or V): B tokens x 128
- *   channels, packed as
- *     [0, 32B)        2-bit codes, in 32-byte records (order below)
- *     [32B, 40B)      s: fp16 [4][B]   per (group, token) step
- *     [40B, 48B)      z: fp16 [4][B]   per (group, token) zero (lowest level)
- *     [48B, 50B)      R: fp16 [B]      per-token factor
- *     [50B, 50B+256)  C: fp16 [128]    per-channel factor
- *   = 1856 bytes (B = 32) or 3456 bytes (B = 64). The value of element
- *   (t, c) in the rotated space is (code * s[g][t] + z[g][t]) * R[t] * C[c]
- *   with g = c / 32. Code records: record r = 32*sb + 4a + b (sb = t / 32)
- *   holds 8 little-endian 32-bit words; a code sits at bit position p of
- *   word w of its record:
+ *   channels with `bits` (2 or 4) bits per code, packed as (X = 16*bits*B)
+ *     [0, X)             codes, in 8*bits-byte records (order below)
+ *     [X, X+8B)          s: fp16 [4][B]   per (group, token) step
+ *     [X+8B, X+16B)      z: fp16 [4][B]   per (group, token) zero (lowest level)
+ *     [X+16B, X+18B)     R: fp16 [B]      per-token factor
+ *     [X+18B, X+18B+256) C: fp16 [128]    per-channel factor
+ *   = 1856 / 3456 bytes for 2 bits at B = 32 / 64, 2880 / 5504 for 4 bits.
+ *   The value of element (t, c) in the rotated space is
+ *   (code * s[g][t] + z[g][t]) * R[t] * C[c] with g = c / 32 and code in
+ *   0 .. 2^bits - 1. Code records: record r = 32*sb + 4a + b (sb = t / 32)
+ *   holds 2*bits little-endian 32-bit words; a code sits at bit position p
+ *   of word w of its record:
  *     kind K: a = (t%32)/4, i = t%4, g = c/32, b = (c%32)/8, e = c%8;
- *             w = 2i + g/2, p = 2*(4*(g%2) + e/2) + 16*(e%2)
+ *             2 bits: w = 2i + g/2, p = 2*(4*(g%2) + e/2) + 16*(e%2)
+ *             4 bits: w = 4i + g,   p = 4*(e/2) + 16*(e%2)
  *     kind V: b = (t%32)/8, d = t%8, g = c/32, a = (c%32)/4, f = c%4;
- *             w = 2g + f/2, p = 2*(4*(d/4) + 2*((d%4)/2) + f%2) + 16*(d%2)
- *   (each lane of the attention kernel's warp reads exactly one 32-byte
- *   record per 32 tokens and turns it into tensor-core operands with one
- *   shift and one mask per pair of codes).
+ *             2 bits: w = 2g + f/2, p = 2*(4*(d/4) + 2*((d%4)/2) + f%2) + 16*(d%2)
+ *             4 bits: w = 4g + f,   p = 4*(d/2) + 16*(d%2)
+ *   (each lane of the attention kernel's warp reads exactly one record per
+ *   32 tokens and turns it into tensor-core operands with one shift and one
+ *   mask per pair of codes).
  *   Pool: physical block p holds its head-blocks at
  *     pool + p*kvarn_block_bytes + (2*h + kind)*kvarn_head_block_bytes,
  *   kind 0 = K, 1 = V. pool must be 16-byte aligned.
@@ -95,7 +99,7 @@ typedef struct kvarn_config {
     int32_t head_dim;       /* must be 128 */
     int32_t block_size;     /* tokens per block B: 32 or 64 */
     int32_t group_size;     /* channels per quantisation group: must be 32 */
-    int32_t bits;           /* must be 2 */
+    int32_t bits;           /* bits per code: 2 (the method) or 4 */
     int32_t varn_iters;     /* VarN iterations (token pass then channel pass): 0..8 */
     int32_t n_q_heads;      /* query heads */
     int32_t n_kv_heads;     /* kv heads; n_q_heads / n_kv_heads in 1..4 */
@@ -125,7 +129,8 @@ const char* kvarn_version(void);
 /* Human-readable text for a kvarn_status value. */
 const char* kvarn_status_string(int status);
 
-/* Bytes of one packed head-block: 50*B + 256. 0 for an invalid config. */
+/* Bytes of one packed head-block: (16*bits + 18)*B + 256 (50*B + 256 at 2
+ * bits). 0 for an invalid config. */
 size_t kvarn_head_block_bytes(const kvarn_config* cfg);
 
 /* Bytes of one physical block: n_kv_heads * 2 * kvarn_head_block_bytes. */
@@ -153,8 +158,8 @@ size_t kvarn_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max
  *   src_dtype: KVARN_BF16 or KVARN_FP32; device)
  * rotates each token by H diag(sigma)/sqrt(128), runs varn_iters passes of
  * token-axis then channel-axis variance normalisation, rounds the factors to
- * fp16, quantises each (token, 32-channel group) to 2 bits with an fp16
- * step and zero, and writes one packed head-block of `kind` layout to
+ * fp16, quantises each (token, 32-channel group) to `bits` bits
+ * (2^bits - 1 steps) with an fp16 step and zero, and writes one packed head-block of `kind` layout to
  *   dst_base + dst_offsets[n]   (bytes; device int64 array, NULL means
  *                               n * kvarn_head_block_bytes)
  * dst_base + offset must be 16-byte aligned. workspace: >= 256 bytes of

@@ -9,7 +9,8 @@ already-validated rounded values so one boundary case cannot cascade):
   z16/s16  recomputed by the oracle from its fp64 rotated values and the GPU's
            R16, C16: equal, or the pre-rounding value lies within 1e-5 of an
            fp16 value, relative to the group's own scale: max(|m|, M - m) for
-           the zero (group minimum m, maximum M), (M - z)/3 for the step (counted);
+           the zero (group minimum m, maximum M), (M - z)/L for the step, L =
+           2^bits - 1 (counted);
   codes    recomputed from that y with the GPU's z16, s16: equal, or y lies
            within 1e-6 * max(1, |b|) of a decision boundary b (counted; the
            count over a test's whole population must stay <= 1e-6 of its codes,
@@ -42,15 +43,15 @@ def f16_neighbours(v: float):
 
 
 def staged_quantize_parity(X: np.ndarray, gpu_bytes: np.ndarray, B: int, iters: int, kind: int,
-                           sign_bits, flags: int = 0) -> Counter:
+                           sign_bits, flags: int = 0, bits: int = 2) -> Counter:
     """X: [n][B][128] float64 inputs exactly as the GPU read them; gpu_bytes:
     [n][head_block_bytes] uint8. Raises AssertionError on a violation."""
     st = Counter()
     X = np.asarray(X, dtype=np.float64)
     n = X.shape[0]
     for i in range(n):
-        ref = oracle.quantize_block(X[i], iters, kind, sign_bits, flags=flags)
-        f = oracle.unpack(B, kind, gpu_bytes[i])
+        ref = oracle.quantize_block(X[i], iters, kind, sign_bits, flags=flags, bits=bits)
+        f = oracle.unpack(B, kind, gpu_bytes[i], bits=bits)
         # ---- factors
         raw = np.concatenate([ref["R"], ref["C"]])
         got = np.concatenate([f["R16"], f["C16"]])
@@ -66,7 +67,7 @@ def staged_quantize_parity(X: np.ndarray, gpu_bytes: np.ndarray, B: int, iters: 
         st["factors"] += raw.size
         # ---- group zero and step from the GPU's factors
         y = oracle.normalise(ref["Xr"], f["R16"], f["C16"])
-        z_o, _, m, M = oracle.group_params_all(y)
+        z_o, _, m, M = oracle.group_params_all(y, bits=bits)
         zb = np.nonzero(f["z16"] != z_o)
         if zb[0].size:
             mc = np.clip(m[zb], -65504, 65504)
@@ -75,16 +76,17 @@ def staged_quantize_parity(X: np.ndarray, gpu_bytes: np.ndarray, B: int, iters: 
             assert np.all(near <= 1e-5 * scale), (
                 f"block {i}: z16 mismatch gpu {f['z16'][zb]} oracle {z_o[zb]} min {m[zb]} max {M[zb]}")
             st["zero_excused"] += zb[0].size
-        s_o = np.array([[oracle.step_for(f["z16"][t, g], M[t, g]) for g in range(4)] for t in range(B)])
+        s_o = np.array([[oracle.step_for(f["z16"][t, g], M[t, g], bits=bits) for g in range(4)]
+                        for t in range(B)])
         sb_ = np.nonzero(f["s16"] != s_o)
         if sb_[0].size:
-            pre = (M[sb_] - f["z16"][sb_]) / 3.0
+            pre = (M[sb_] - f["z16"][sb_]) / ((1 << bits) - 1)
             assert np.all(f16_near_grid(pre, 1e-5)), (
                 f"block {i}: s16 mismatch gpu {f['s16'][sb_]} oracle {s_o[sb_]} pre {pre}")
             st["step_excused"] += sb_[0].size
         st["groups"] += B * 4
         # ---- codes from y with the GPU's z16, s16
-        codes, dist = oracle.codes_given(y, f["z16"], f["s16"])
+        codes, dist = oracle.codes_given(y, f["z16"], f["s16"], bits=bits)
         cb = np.nonzero(codes != f["codes"])
         if cb[0].size:
             window = 1e-6 * np.maximum(1.0, np.abs(y[cb]))
@@ -115,7 +117,7 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 
 
 class PagedCache:
-    """A 2-bit paged cache built through the C ABI.
+    """A packed paged cache (the config's code width) built through the C ABI.
 
     block_table[b][j] is a physical block id (a seeded permutation when
     perm_seed is given); staging holds the raw tail rows.
@@ -178,4 +180,5 @@ def oracle_attention(cache: PagedCache, q: torch.Tensor, seq_lens, sign_bits, sm
     pool_np = cache.pool.cpu().numpy() if pool_np is None else pool_np
     return oracle.decode_attention(cfg.block_size, cfg.n_q_heads, cfg.n_kv_heads, sign_bits, sm_scale, qn,
                                    pool_np, stg, np.ascontiguousarray(cache.block_table_np[seqs]),
-                                   np.asarray(seq_lens, dtype=np.int32)[seqs], flags=int(cfg.flags))
+                                   np.asarray(seq_lens, dtype=np.int32)[seqs], flags=int(cfg.flags),
+                                   bits=int(cfg.bits))

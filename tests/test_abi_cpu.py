@@ -6,6 +6,7 @@ import ctypes
 import pytest
 
 import bit_kv_cache_08_gb300 as kv
+import oracle
 import synth
 
 
@@ -37,7 +38,16 @@ def test_sizes_match_the_format():
     assert kv.workspace_bytes(c32, 0, 0) == 256
 
 
-@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 16), ("bits", 4),
+def test_four_bit_sizes_match_the_oracle_format():
+    """4-bit codes: records of 64 bytes, then the same s, z, R, C sections."""
+    for B in (32, 64):
+        c = _cfg(block_size=B, bits=4)
+        assert kv.head_block_bytes(c) == 82 * B + 256 == oracle.head_block_bytes(B, bits=4)
+        assert kv.block_bytes(c) == 8 * 2 * (82 * B + 256)
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 16), ("bits", 3),
+                                         ("bits", 1), ("bits", 8),
                                          ("group_size", 64), ("n_q_heads", 48)])
 def test_unsupported_configs_are_rejected(field, value):
     c = _cfg()
@@ -74,3 +84,23 @@ def test_ablation_flags_and_zero_iterations_are_validated():
         assert kv.head_block_bytes(bad) == 0
         assert L.kvarn_quantize_block(ctypes.byref(bad), 0, None, 0, 1, 4096, 128, None, None, None,
                                       None) == kv._abi.ERR_INVALID_ARG
+
+
+def test_source_extent_checks_in_the_binding():
+    """The binding counts whole blocks of a contiguous source and refuses a
+    block count or strides that would read past the source's storage."""
+    import torch
+    c = _cfg()
+    src = torch.zeros(2, 2, 64, 128, dtype=torch.bfloat16)
+    assert kv._abi._blocks_in(src, c, None, None, 128) == (8, 32 * 128)
+    with pytest.raises(ValueError):
+        kv._abi._blocks_in(src, c, 9, None, 128)
+    with pytest.raises(ValueError):
+        kv._abi._blocks_in(src, c, None, 64 * 128, 128)          # strides need an explicit count
+    inter = torch.zeros(3, 32, 2, 128)                             # [n][B][2][128], V rows interleaved
+    view = inter[:, :, 1]
+    assert kv._abi._blocks_in(view, c, 3, 32 * 256, 256) == (3, 32 * 256)
+    with pytest.raises(ValueError):
+        kv._abi._blocks_in(view, c, 4, 32 * 256, 256)
+    with pytest.raises(ValueError):
+        kv._abi._blocks_in(view, c, None, None, 128)               # non-contiguous without strides
