@@ -90,6 +90,8 @@ def lib():
                 "orc_attention_rotated": (None, [_f64p, _f64p, _f64p, _i64, _d, _u32p, _f64p]),
                 "orc_decode_attention": (None, [_i, _i, ctypes.c_uint32, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
                                                 _i32p, _i, _i32p, _i, _f64p]),
+                "orc_prefill_attention": (None, [_i, _i, ctypes.c_uint32, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
+                                                 _i32p, _i, _i32p, _i, _i, _f64p]),
                 "orc_error_split": (None, [_f64p, _f64p, _f64p]),
                 "orc_error_decomposition": (None, [_i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p]),
                 "orc_normalise": (None, [_i, _f64p, _f64p, _f64p, _f64p]),
@@ -345,6 +347,26 @@ def decode_attention(B, n_q, n_kv, sign_bits, sm_scale, q, pool, staging, block_
     lib().orc_decode_attention(B, bits, flags, n_q, n_kv, _p(s, _u32p), float(sm_scale), _p(q, _f64p),
                                _p(pool, _u8p), _p(staging, _u16p), _p(bt, _i32p), bt.shape[1],
                                _p(sl, _i32p), batch, _p(out, _f64p))
+    return out
+
+
+def prefill_attention(B, n_q, n_kv, sign_bits, sm_scale, q, pool, staging, block_table,
+                      seq_lens, flags: int = 0, bits: int = 2) -> np.ndarray:
+    """Chunked prefill attention over the paged cache: q is [batch][chunk][n_q][128];
+    query row r of sequence b sits at position seq_lens[b] - chunk + r and sees
+    the tokens up to it, read from the cache as it stands (zeros for a row at a
+    negative position). Returns [batch][chunk][n_q][128]."""
+    q = _f64(q)
+    batch, chunk = q.shape[0], q.shape[1]
+    pool = np.ascontiguousarray(pool, dtype=np.uint8).reshape(-1)
+    staging = np.ascontiguousarray(staging, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32).reshape(batch)
+    out = np.zeros((batch, chunk, n_q, D))
+    s = _signs(sign_bits)
+    lib().orc_prefill_attention(B, bits, flags, n_q, n_kv, _p(s, _u32p), float(sm_scale), _p(q, _f64p),
+                                _p(pool, _u8p), _p(staging, _u16p), _p(bt, _i32p), bt.shape[1],
+                                _p(sl, _i32p), batch, chunk, _p(out, _f64p))
     return out
 
 

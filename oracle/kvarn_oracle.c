@@ -684,6 +684,59 @@ void orc_decode_attention(int B, int bits, uint32_t flags, int n_q, int n_kv, co
 }
 
 /* ------------------------------------------------------------------------ */
+/* Chunked prefill attention over the same paged cache (reading R-24).       */
+/* Each sequence b holds L = seq_lens[b] tokens after its last `chunk` tokens  */
+/* were appended; query row r of the chunk sits at position p = L - chunk + r */
+/* and attends to tokens 0..p, every token read from the cache as it stands  */
+/* (complete blocks decoded, the open tail raw bf16). A row with p < 0 sees  */
+/* no token and gives zeros. q: fp64 [batch][chunk][n_q][128]; out likewise. */
+/* ------------------------------------------------------------------------ */
+
+void orc_prefill_attention(int B, int bits, uint32_t flags, int n_q, int n_kv, const uint32_t sign_bits[4],
+                           double sm_scale, const double* q, const uint8_t* pool, const uint16_t* staging,
+                           const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
+                           int chunk, double* out)
+{
+    size_t hb = orc_head_block_bytes(B, bits);
+    size_t block_bytes = (size_t)n_kv * 2 * hb;
+    int G = n_q / n_kv;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int unit = 0; unit < batch * n_kv; unit++) {
+        int b = unit / n_kv, h = unit % n_kv;
+        int64_t L = seq_lens[b];
+        int64_t nfull = L / B;
+        int64_t tail = L % B;
+        double* K = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * ORC_D);
+        double* V = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * ORC_D);
+        /* the cache as it stands: decoded complete blocks, then the raw tail */
+        for (int64_t j = 0; j < nfull; j++) {
+            int64_t p = block_table[(int64_t)b * max_blocks + j];
+            const uint8_t* base = pool + (size_t)p * block_bytes + (size_t)(2 * h) * hb;
+            orc_decode_block(B, bits, flags, 0, sign_bits, base, 0, K + (size_t)j * B * ORC_D);
+            orc_decode_block(B, bits, flags, 1, sign_bits, base + hb, 0, V + (size_t)j * B * ORC_D);
+        }
+        for (int64_t r = 0; r < tail; r++) {
+            const uint16_t* sk = staging + ((((size_t)b * n_kv + h) * 2 + 0) * B + r) * ORC_D;
+            const uint16_t* sv = staging + ((((size_t)b * n_kv + h) * 2 + 1) * B + r) * ORC_D;
+            for (int c = 0; c < ORC_D; c++) {
+                K[(nfull * B + r) * ORC_D + c] = orc_bf16_value(sk[c]);
+                V[(nfull * B + r) * ORC_D + c] = orc_bf16_value(sv[c]);
+            }
+        }
+        /* causal: row r sees the first p + 1 tokens */
+        for (int r = 0; r < chunk; r++) {
+            int64_t visible = L - chunk + r + 1;
+            for (int j = 0; j < G; j++) {
+                int hq = h * G + j;
+                size_t row = (((size_t)b * chunk + r) * n_q + hq) * ORC_D;
+                orc_attention(q + row, K, V, visible, sm_scale, out + row);   /* zeros when visible <= 0 */
+            }
+        }
+        free(K); free(V);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Error decomposition  [AP3] section 二: a token vector x and its quantised  */
 /* version x^ = x + eps; eps = E_M + E_D with the magnitude part             */
 /*   E_M = (|x^| - |x|) x / |x|                                              */

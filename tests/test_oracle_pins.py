@@ -622,3 +622,88 @@ def test_4bit_block_is_within_half_step_and_finer_than_2bit():
         errs[bits] = np.linalg.norm(unrot - X) / np.linalg.norm(X)
     # the same factors, 15 steps per group instead of 3: roughly 5x finer
     assert errs[4] < errs[2] / 3
+
+
+# ---------------------------------------------------------------- chunked prefill attention
+
+def _paged_cache(B, n_kv, batch, lens, max_blocks, K, V, sb, iters=3, bits=2):
+    """Pool (permuted blocks) and staging holding K, V ([batch][n_kv][L][128]
+    bf16 tensors) for the given lengths, built with the oracle's quantiser."""
+    perm = np.random.default_rng(batch + max_blocks).permutation(batch * max_blocks).astype(np.int32)
+    bt = perm.reshape(batch, max_blocks)
+    hb = oracle.head_block_bytes(B, bits)
+    pool = np.zeros((batch * max_blocks, n_kv, 2, hb), dtype=np.uint8)
+    staging = np.zeros((batch, n_kv, 2, B, D), dtype=np.uint16)
+    for b in range(batch):
+        for h in range(n_kv):
+            nfull = lens[b] // B
+            for kind, T in ((0, K), (1, V)):
+                for j in range(nfull):
+                    vals = T[b, h, j * B:(j + 1) * B].double().numpy()
+                    pool[bt[b, j], h, kind] = oracle.quantize_blocks(vals[None], iters, kind, sb, bits=bits)[0]
+                tail = lens[b] - nfull * B
+                staging[b, h, kind, :tail] = T[b, h, nfull * B:lens[b]].view(torch.int16).numpy()
+    return pool, staging, bt
+
+
+def test_prefill_chunk_of_one_is_decode_attention():
+    """A chunk of one query per sequence is the decode step over the same cache."""
+    B, n_q, n_kv, batch = 32, 4, 2, 3
+    sb = synth.sign_bits(90)
+    g = synth.make_gen(90)
+    lens = [70, 32, 17]
+    K = synth.kv_values(g, batch, n_kv, 96, 1.0, 2, 10.0).to(torch.bfloat16)
+    V = synth.kv_values(g, batch, n_kv, 96, 1.0, 2, 10.0).to(torch.bfloat16)
+    q = synth.queries(g, batch, n_q).double().numpy()
+    pool, staging, bt = _paged_cache(B, n_kv, batch, lens, 3, K, V, sb)
+    sl = np.array(lens, np.int32)
+    dec = oracle.decode_attention(B, n_q, n_kv, sb, 0.2, q, pool, staging, bt, sl)
+    pre = oracle.prefill_attention(B, n_q, n_kv, sb, 0.2, q[:, None], pool, staging, bt, sl)
+    assert np.array_equal(pre[:, 0], dec)
+
+
+def test_prefill_identical_keys_average_the_visible_values():
+    """All keys equal (zero keys: every score 0) -> each row is the plain mean
+    of the values it may see: the first p + 1 tokens, decoded or raw."""
+    B, n_q, n_kv, batch, chunk = 32, 2, 1, 2, 40
+    sb = synth.sign_bits(91)
+    g = synth.make_gen(91)
+    lens = [75, 30]                      # the second has rows at negative positions
+    K = torch.zeros(batch, n_kv, 96, D, dtype=torch.bfloat16)
+    V = synth.kv_values(g, batch, n_kv, 96, 1.0, 2, 10.0).to(torch.bfloat16)
+    pool, staging, bt = _paged_cache(B, n_kv, batch, lens, 3, K, V, sb)
+    q = synth.queries(g, batch * chunk, n_q).double().numpy().reshape(batch, chunk, n_q, D)
+    out = oracle.prefill_attention(B, n_q, n_kv, sb, 0.3, q, pool, staging, bt, np.array(lens, np.int32))
+    for b in range(batch):
+        nfull = lens[b] // B
+        rows = [oracle.decode_blocks(pool[bt[b, j], 0, 1], B, 1, sb, False)[0] for j in range(nfull)]
+        rows.append(V[b, 0, nfull * B:lens[b]].double().numpy())
+        Vc = np.concatenate(rows)
+        for r in range(chunk):
+            p = lens[b] - chunk + r
+            want = Vc[:p + 1].mean(axis=0) if p >= 0 else np.zeros(D)
+            for h in range(n_q):
+                np.testing.assert_allclose(out[b, r, h], want, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_is_causal():
+    """Changing the raw tail row of position p0 (K and V) leaves every row
+    before p0 as it was and changes the rows at or after it (a small softmax
+    scale keeps every visible token's weight well above zero)."""
+    B, n_q, n_kv, batch, chunk = 32, 4, 2, 1, 24
+    sb = synth.sign_bits(92)
+    g = synth.make_gen(92)
+    L = 2 * B + 20                       # 20 raw rows; the chunk spans a complete block and the tail
+    K = synth.kv_values(g, batch, n_kv, L, 1.0, 2, 10.0).to(torch.bfloat16)
+    V = synth.kv_values(g, batch, n_kv, L, 1.0, 2, 10.0).to(torch.bfloat16)
+    pool, staging, bt = _paged_cache(B, n_kv, batch, [L], 3, K, V, sb)
+    q = synth.queries(g, chunk, n_q).double().numpy().reshape(1, chunk, n_q, D)
+    sl = np.array([L], np.int32)
+    base = oracle.prefill_attention(B, n_q, n_kv, sb, 0.01, q, pool, staging, bt, sl)
+    p0 = 2 * B + 10
+    st2 = staging.copy()
+    st2[0, :, :, p0 - 2 * B] = torch.full((n_kv, 2, D), 3.0, dtype=torch.bfloat16).view(torch.int16).numpy()
+    moved = oracle.prefill_attention(B, n_q, n_kv, sb, 0.01, q, pool, st2, bt, sl)
+    r0 = p0 - (L - chunk)
+    assert np.array_equal(moved[0, :r0], base[0, :r0])
+    assert np.all(np.abs(moved[0, r0:] - base[0, r0:]).max(axis=(1, 2)) > 1e-3)
