@@ -44,6 +44,9 @@ def parse():
     p.add_argument("--ablation", action="store_true",
                    help="instead of the step: error of each ablation (Hadamard only, VarN only, one VarN "
                         "axis) against the bf16 cache on the Llama-3.1-8B layer, one JSON line per variant")
+    p.add_argument("--prefill", action="store_true",
+                   help="instead of the step: chunked prefill attention over the Llama-3.1-8B layer "
+                        "(batch 16 x 4096 cached tokens) for several chunk lengths, one JSON line each")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
                         "lengths), 2-bit and 4-bit vs bf16-cache decode attention, one JSON line per point")
@@ -637,6 +640,59 @@ def run_sweep(args):
                               "speedup_4bit_vs_bf16": round(ms16 / ms4, 2)}), flush=True)
 
 
+# ---------------------------------------------------------------------------- chunked prefill
+
+PREFILL_CHUNKS = (1, 4, 16, 64)
+
+
+def run_prefill(args):
+    """kvarn_prefill_attn on the Llama-3.1-8B layer: every sequence holds 4096
+    tokens, the last `chunk` of them are the chunk's queries. Each launch is
+    timed alone after a 1 GiB L2-flushing write (median). Reported: query rows
+    per second and the cache bytes of one pass over the visible cache per
+    launch, divided by its time (every row re-reads its prefix; the repeats
+    come from L2)."""
+    import torch
+    import bit_kv_cache_08_gb300 as kv
+    import synth
+    kv.build()
+    dev = "cuda"
+    w = synth.LLAMA8B_LAYER
+    B, n_kv, n_q, batch, L = w.block, w.n_kv, w.n_q, w.batch, w.ctx
+    nb = L // B
+    sb = synth.sign_bits(w.seed)
+    cfg = kv.make_config(n_q, n_kv, B, w.iters, sb)
+    g = synth.make_gen(w.seed, dev)
+    bt = torch.arange(batch * nb, dtype=torch.int32, device=dev).view(batch, nb)
+    pool = kv.alloc_pool(cfg, batch * nb, dev)
+    staging = kv.alloc_staging(cfg, batch, dev)
+    ws0 = kv.alloc_workspace(cfg, 0, 0, dev)
+    hb, bb = kv.head_block_bytes(cfg), kv.block_bytes(cfg)
+    for kind in (0, 1):
+        T = synth.kv_values(g, batch, n_kv, L, w.sigma_m, w.n_out, w.out_factor, dev).to(torch.bfloat16)
+        offs = (bt[:, None, :].long() * bb + (2 * torch.arange(n_kv, device=dev)[None, :, None] + kind) * hb)
+        kv.quantize_block(cfg, kind, T.contiguous(), pool, ws0, dst_offsets=offs.reshape(-1).contiguous(),
+                          n_head_blocks=batch * n_kv * nb)
+        del T
+    lens = torch.full((batch,), L, dtype=torch.int32, device=dev)
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    cache_bytes = batch * nb * bb            # every (kv head, K, V) head-block once
+    for chunk in PREFILL_CHUNKS:
+        q = synth.queries(g, batch * chunk, n_q, dev).reshape(batch, chunk, n_q, D).to(torch.bfloat16)
+        out = torch.empty(batch, chunk, n_q, D, device=dev)
+        ws = kv.alloc_workspace(cfg, batch * chunk, nb, dev)
+        for _ in range(3):
+            kv.prefill_attn(cfg, q, pool, staging, bt, lens, out, ws)
+        ms = _time_events(lambda: kv.prefill_attn(cfg, q, pool, staging, bt, lens, out, ws), 10, flush)
+        assert kv.read_error(ws) == 0
+        print(json.dumps({"prefill_chunk": chunk, "workload": w.name, "batch": batch, "cached_tokens": L,
+                          "us": round(ms * 1e3, 1), "query_rows_per_s": round(batch * chunk / ms * 1e3, 1),
+                          "cache_GB_per_s_one_pass": round(cache_bytes / ms / 1e6, 1),
+                          "timing": "CUDA events, median of 10 launches each after a 1 GiB L2-flushing write"}),
+              flush=True)
+        del q, out, ws
+
+
 # ---------------------------------------------------------------------------- ablation
 
 ABLATIONS = (  # (name, flags, iters, bits): the pages' ablation list, plus the two ends and 4-bit codes
@@ -723,6 +779,9 @@ def main():
         return
     if args.ablation:
         run_ablation(args)
+        return
+    if args.prefill:
+        run_prefill(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -69,6 +69,8 @@ _SIGS = {
     "kvarn_append": (ctypes.c_int, [_cfgp, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
     "kvarn_decode_attn": (ctypes.c_int, [_cfgp, _vp, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
                                          _sz, _vp]),
+    "kvarn_prefill_attn": (ctypes.c_int, [_cfgp, _vp, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32, _i32, _vp,
+                                          _vp, _sz, _vp]),
     "kvarn_dequantize": (ctypes.c_int, [_cfgp, _i32, _vp, _vp, _i64, _i32, _vp, _vp]),
     "kvarn_decode_attn_bf16": (ctypes.c_int, [_cfgp, _vp, _i32, _vp, _i64, _vp, _i32, _vp, _i32, _vp, _vp,
                                               _sz, _vp]),
@@ -245,6 +247,26 @@ def decode_attn(cfg: Config, q: torch.Tensor, pool: torch.Tensor, staging: torch
                                    _ptr(staging), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                    q.shape[0], _ptr(out), _ptr(workspace), workspace.numel(), _stream()),
            "kvarn_decode_attn")
+
+
+def prefill_attn(cfg: Config, q: torch.Tensor, pool: torch.Tensor, staging: torch.Tensor,
+                 block_table: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor):
+    """q: [batch][chunk][n_q][128] (bf16|fp32) queries of each sequence's last
+    chunk tokens; out: fp32 [batch][chunk][n_q][128]."""
+    _need_cuda(q, "q")
+    _need_cuda(pool, "pool", torch.uint8)
+    _need_cuda(staging, "staging", torch.bfloat16)
+    _need_cuda(block_table, "block_table", torch.int32)
+    _need_cuda(seq_lens, "seq_lens", torch.int32)
+    _need_cuda(out, "out", torch.float32)
+    _need_cuda(workspace, "workspace", torch.uint8)
+    if q.dim() != 4 or out.shape != q.shape:
+        raise ValueError("q and out must be [batch][chunk][n_q][128]")
+    _check(lib().kvarn_prefill_attn(ctypes.byref(cfg), _ptr(q), _dtype_code(q), _ptr(pool), pool.shape[0],
+                                    _ptr(staging), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                    q.shape[0], q.shape[1], _ptr(out), _ptr(workspace), workspace.numel(),
+                                    _stream()),
+           "kvarn_prefill_attn")
 
 
 def decode_attn_bf16(cfg: Config, q: torch.Tensor, kv_pool: torch.Tensor, block_table: torch.Tensor,

@@ -19,12 +19,12 @@ cudaError_t launch_error_split(const kvarn_config& cfg, int kind, const void* sr
 cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
-                               float* out, void* workspace, int nw, cudaStream_t st);
+                               int chunk, float* out, void* workspace, int nw, cudaStream_t st);
 cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int q_dtype, const void* kv_pool,
                                     int64_t n_pool_blocks, const int32_t* block_table, int max_blocks,
                                     const int32_t* seq_lens, int batch, float* out, void* workspace, int nw,
                                     cudaStream_t st);
-int attn_grid_warps(int block_size, int bits, int device);
+int attn_grid_warps(int block_size, int bits, bool prefill, int device);
 int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
 
@@ -63,9 +63,10 @@ int current_device() {
 int resident_warps(int block_size, int bits) {
     const int d = current_device();
     if (d < 0) return 0;
-    const int a = attn_grid_warps(block_size, bits, d);
+    const int a = attn_grid_warps(block_size, bits, false, d), p = attn_grid_warps(block_size, bits, true, d);
     const int b = attn_bf16_grid_warps(block_size, d);
-    return a > b ? a : b;
+    const int m = a > p ? a : p;
+    return m > b ? m : b;
 }
 
 size_t ws_bytes(const kvarn_config& c, int32_t batch) {
@@ -160,15 +161,19 @@ int kvarn_append(const kvarn_config* cfg, void* pool, int64_t n_pool_blocks, voi
                                      (cudaStream_t)stream));
 }
 
-int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,
-                      int64_t n_pool_blocks, const void* staging, const int32_t* block_table,
-                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, float* out,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+// Decode (chunk = 1) and chunked prefill share one split-K launch: every query
+// row of a chunk is a virtual sequence with its own causal prefix.
+int packed_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool, int64_t n_pool_blocks,
+                const void* staging, const int32_t* block_table, int32_t max_blocks_per_seq,
+                const int32_t* seq_lens, int32_t batch, int32_t chunk, float* out, void* workspace,
+                size_t workspace_bytes, void* stream) {
     kvarn_config c;
     int r = check_config(cfg, &c);
     if (r != KVARN_OK) return r;
     if (q_dtype != KVARN_BF16 && q_dtype != KVARN_FP32) return KVARN_ERR_INVALID_ARG;
-    if (batch < 0 || max_blocks_per_seq < 0 || n_pool_blocks < 1) return KVARN_ERR_INVALID_ARG;
+    if (batch < 0 || chunk < 1 || max_blocks_per_seq < 0 || n_pool_blocks < 1) return KVARN_ERR_INVALID_ARG;
+    if ((int64_t)batch * chunk > 0x7fffffff / c.n_q_heads) return KVARN_ERR_INVALID_ARG;
     if (batch == 0) return KVARN_OK;
     if (!q || !pool || !staging || !block_table || !seq_lens || !out || !workspace) return KVARN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(staging, 16) || !aligned(out, 16) ||
@@ -176,14 +181,31 @@ int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, c
         return KVARN_ERR_INVALID_ARG;
     if ((int64_t)max_blocks_per_seq * c.block_size > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
     if (n_pool_blocks > 0x7fffffff || kvarn_block_bytes(&c) > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
-    const size_t need = ws_bytes(c, batch);
+    const size_t need = ws_bytes(c, batch * chunk);
     if (need == 0) return KVARN_ERR_CUDA;
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;
-    const int nw = attn_grid_warps(c.block_size, c.bits, current_device());
+    const int nw = attn_grid_warps(c.block_size, c.bits, chunk > 1, current_device());
     if (nw <= 0) return KVARN_ERR_CUDA;
     return cuda_status(launch_decode_attn(c, q, q_dtype, pool, n_pool_blocks, (int64_t)kvarn_block_bytes(&c),
-                                          staging, block_table, max_blocks_per_seq, seq_lens, batch, out, workspace,
-                                          nw, (cudaStream_t)stream));
+                                          staging, block_table, max_blocks_per_seq, seq_lens, batch, chunk, out,
+                                          workspace, nw, (cudaStream_t)stream));
+}
+}  // namespace
+
+int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,
+                      int64_t n_pool_blocks, const void* staging, const int32_t* block_table,
+                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, float* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    return packed_attn(cfg, q, q_dtype, pool, n_pool_blocks, staging, block_table, max_blocks_per_seq, seq_lens,
+                       batch, 1, out, workspace, workspace_bytes, stream);
+}
+
+int kvarn_prefill_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,
+                       int64_t n_pool_blocks, const void* staging, const int32_t* block_table,
+                       int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, int32_t chunk,
+                       float* out, void* workspace, size_t workspace_bytes, void* stream) {
+    return packed_attn(cfg, q, q_dtype, pool, n_pool_blocks, staging, block_table, max_blocks_per_seq, seq_lens,
+                       batch, chunk, out, workspace, workspace_bytes, stream);
 }
 
 int kvarn_dequantize(const kvarn_config* cfg, int32_t kind, const void* src_base, const int64_t* src_offsets,

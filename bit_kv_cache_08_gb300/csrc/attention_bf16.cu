@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(32) decode_attn_bf16_kernel(AttnArgs a) {
     const int G = a.G;
 
     // positions are 16-token chunks; a partial last chunk counts
-    const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, kChunk, 1};
+    const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, kChunk, 1, 1};
     Cursor cc;
     cc.b = cc.h = cc.j = 0;
     const int64_t W = split_locate(sp, 0, lane, cc.b, cc.h, cc.j);
@@ -289,6 +289,7 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
     a.block_bytes = (int64_t)cfg.n_kv_heads * 2 * cfg.block_size * kD * 2;
     a.max_blocks = max_blocks * (cfg.block_size / kChunk);   // in 16-token chunks
     a.batch = batch;
+    a.chunk = 1;
     a.n_q = cfg.n_q_heads;
     a.n_kv = cfg.n_kv_heads;
     a.G = cfg.n_q_heads / cfg.n_kv_heads;

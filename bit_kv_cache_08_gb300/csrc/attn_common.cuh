@@ -28,6 +28,7 @@ struct AttnArgs {
     int batch;
     int n_q, n_kv, G;
     int nw;
+    int chunk;        // query rows per sequence (1: decode); batch counts batch * chunk rows
     float sm_scale;
     uint32_t flags;   // KVARN_FLAG_*: the cache's ablation switches
     uint32_t sb[4];
@@ -108,16 +109,17 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (gw >= (int64_t)a.batch * a.n_q) return;
-    const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);
+    const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);   // b: a (virtual) row sequence
     const int h = hq / a.G, jq = hq % a.G;
-    const int L = a.seq_lens[b];
+    const int rb = a.chunk == 1 ? b : b / a.chunk;              // its real sequence
+    const int L = a.seq_lens[rb];
     float* out = a.out + gw * kD;
     if (L < 0 || L > a.max_blocks * B) {
         if (lane == 0) raise_error(a.err, KVARN_DEVERR_POSITION);
         reinterpret_cast<float4*>(out)[lane] = make_float4(NAN, NAN, NAN, NAN);
         return;
     }
-    const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1};
+    const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1, a.chunk};
     int64_t before, total;
     split_prefix(sp, b, lane, before, total);
     const int64_t W = total * a.n_kv;
@@ -185,12 +187,13 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
             for (int k = 0; k < 4; ++k) acc[k] *= kInvSqrtD * sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + k);
         }
     }
-    const int ntail = ROT ? L - nb * B : 0;   // < B <= 64 raw rows in staging
+    // raw rows in staging (< B <= 64): the visible tokens past the pool blocks
+    const int ntail = ROT ? max(0, split_visible(sp, b, L) - nb * B) : 0;
     if (ntail > 0) {
         float qv[4];
         load_q4(a.q, a.q_dtype, gw, lane, qv);
         const float qs = a.sm_scale * kLog2e;
-        const uint16_t* kst = a.staging + (((int64_t)b * a.n_kv + h) * 2 + 0) * B * kD;
+        const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
         const uint16_t* vst = kst + B * kD;
         // scores of all tail rows, 8 rows at a time with independent loads; row r's
         // score ends on lane r % 32, slot r / 32

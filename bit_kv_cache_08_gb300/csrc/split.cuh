@@ -1,5 +1,7 @@
 // split.cuh -- balanced split-K partition shared by the decode-attention
-// kernels. The (sequence, kv head) units are laid end to end, block by block
+// kernels (and by chunked prefill, where every query row of a chunk is a
+// virtual sequence of its own: virtual v = b * chunk + r sees the causal
+// prefix of real sequence b). The (sequence, kv head) units are laid end to end, block by block
 // (sequence-major, then head, then block); warp w of the nw active warps
 // (nw = min(resident warps, W)) takes global blocks [floor(w*W/nw),
 // floor((w+1)*W/nw)), at least one. A unit's partial from warp w lives in slot
@@ -19,12 +21,27 @@ struct SplitArgs {
     int max_blocks;
     int B;
     int ceil_blocks;   // 1: a partial last block counts (bf16 pages); 0: full blocks only
+    int chunk;         // query rows per real sequence (1: decode); batch counts virtual sequences
 };
 
-__device__ __forceinline__ int split_nblocks(const SplitArgs& s, int b) {
-    const int L = s.seq_lens[b];
+// Tokens virtual sequence v may see: the causal prefix 0 .. L - chunk + r of
+// its real sequence (L itself when chunk = 1); <= 0 sees nothing.
+__device__ __forceinline__ int split_visible(const SplitArgs& s, int v, int L) {
+    if (s.chunk == 1) return L;
+    const int b = v / s.chunk;
+    return L - s.chunk + 1 + (v - b * s.chunk);
+}
+
+// Pool blocks a (virtual) sequence reads: its complete blocks (all blocks for
+// bf16 pages), cut at the last one holding a visible token.
+__device__ __forceinline__ int split_nblocks(const SplitArgs& s, int v) {
+    const int L = s.seq_lens[s.chunk == 1 ? v : v / s.chunk];
     if (L < 0 || L > s.max_blocks * s.B) return 0;   // flagged by the merge kernel
-    return s.ceil_blocks ? (L + s.B - 1) / s.B : L / s.B;
+    const int full = s.ceil_blocks ? (L + s.B - 1) / s.B : L / s.B;
+    if (s.chunk == 1) return full;
+    const int vis = split_visible(s, v, L);
+    const int cap = vis > 0 ? (vis + s.B - 1) / s.B : 0;
+    return cap < full ? cap : full;
 }
 
 // Warp-cooperative: returns W (total blocks over all units); if x < W, sets

@@ -216,6 +216,31 @@ int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, c
                       float* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kvarn_prefill_attn -- chunked prefill attention over the same packed cache
+ * (the pages describe only the decode step; this is its causal extension,
+ * with the query multiplied by the same Hadamard matrix, section 三 3.1).
+ *
+ * The last `chunk` tokens of every sequence have already been appended
+ * (kvarn_append / kvarn_quantize_block); q: device [batch][chunk][n_q][128]
+ * (q_dtype KVARN_BF16 or KVARN_FP32) holds their queries. Query row r of
+ * sequence b sits at position p = seq_lens[b] - chunk + r and, for query
+ * head j (kv head j / (n_q / n_kv)),
+ *   out[b][r][j][:] = sum_{t <= p} softmax_t(sm_scale * q.k_t) v_t
+ * with every token read from the cache as it stands: tokens below
+ * floor(L/B)*B dequantised from the pool, the rest raw bf16 from staging. A
+ * row with p < 0 (seq_lens[b] < chunk) gives zeros. out: device fp32
+ * [batch][chunk][n_q][128]. chunk >= 1; chunk = 1 is kvarn_decode_attn.
+ * workspace: at least kvarn_workspace_bytes(cfg, batch * chunk,
+ * max_blocks_per_seq) bytes. Every row is split and merged like a decode
+ * query of its own (the cache is read once per row, mostly from L2). Device
+ * faults as kvarn_decode_attn.
+ */
+int kvarn_prefill_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,
+                       int64_t n_pool_blocks, const void* staging, const int32_t* block_table,
+                       int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, int32_t chunk,
+                       float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kvarn_dequantize -- packed head-blocks back to fp32 values. Passage:
  * section 三 3.2 of the method page (the kept scales restore the data).
  * Reads n_head_blocks head-blocks of `kind` layout at src_base +
