@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvarn.so")
-SOURCES = ["api.cu", "quantize.cu", "attention.cu", "attention_bf16.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quantize.cu", "attention.cu", "attention_bf16.cu", "prefill.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE]

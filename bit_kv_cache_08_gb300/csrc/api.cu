@@ -24,6 +24,11 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
                                     int64_t n_pool_blocks, const int32_t* block_table, int max_blocks,
                                     const int32_t* seq_lens, int batch, float* out, void* workspace, int nw,
                                     cudaStream_t st);
+cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
+                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
+                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
+                                int chunk, float* out, void* workspace, int64_t max_slots, int target_warps,
+                                cudaStream_t st);
 int attn_grid_warps(int block_size, int bits, bool prefill, int device);
 int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
@@ -184,6 +189,13 @@ int packed_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const v
     const size_t need = ws_bytes(c, batch * chunk);
     if (need == 0) return KVARN_ERR_CUDA;
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;
+    if (chunk > 1 && c.bits == 2) {   // rows of a chunk share each block's operands
+        const int rw = resident_warps(c.block_size, c.bits);
+        const int64_t slots = (int64_t)batch * chunk * c.n_kv_heads + rw;   // what ws_bytes sized
+        return cuda_status(launch_prefill_attn(c, q, q_dtype, pool, n_pool_blocks, (int64_t)kvarn_block_bytes(&c),
+                                               staging, block_table, max_blocks_per_seq, seq_lens, batch, chunk,
+                                               out, workspace, slots, rw, (cudaStream_t)stream));
+    }
     const int nw = attn_grid_warps(c.block_size, c.bits, chunk > 1, current_device());
     if (nw <= 0) return KVARN_ERR_CUDA;
     return cuda_status(launch_decode_attn(c, q, q_dtype, pool, n_pool_blocks, (int64_t)kvarn_block_bytes(&c),

@@ -624,6 +624,7 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.max_blocks = max_blocks;
     a.batch = batch * chunk;   // one (virtual) sequence per query row
     a.chunk = chunk;
+    a.single = 0;
     a.n_q = cfg.n_q_heads;
     a.n_kv = cfg.n_kv_heads;
     a.G = cfg.n_q_heads / cfg.n_kv_heads;

@@ -290,6 +290,7 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
     a.max_blocks = max_blocks * (cfg.block_size / kChunk);   // in 16-token chunks
     a.batch = batch;
     a.chunk = 1;
+    a.single = 0;
     a.n_q = cfg.n_q_heads;
     a.n_kv = cfg.n_kv_heads;
     a.G = cfg.n_q_heads / cfg.n_kv_heads;

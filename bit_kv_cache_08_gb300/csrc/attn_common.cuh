@@ -29,6 +29,7 @@ struct AttnArgs {
     int n_q, n_kv, G;
     int nw;
     int chunk;        // query rows per sequence (1: decode); batch counts batch * chunk rows
+    int single;       // > 0: that many partials per (row, kv head) unit u, in slots u * single ..
     float sm_scale;
     uint32_t flags;   // KVARN_FLAG_*: the cache's ablation switches
     uint32_t sb[4];
@@ -120,18 +121,26 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
         return;
     }
     const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1, a.chunk};
-    int64_t before, total;
-    split_prefix(sp, b, lane, before, total);
-    const int64_t W = total * a.n_kv;
     const int nb = split_nblocks(sp, b);
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (nb > 0) {
-        const int64_t nwe = split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, ROT ? kSplitRatio2bit * B : 0.f);
-        const int64_t Su = before * a.n_kv + (int64_t)h * nb;
         const int64_t u = (int64_t)b * a.n_kv + h;
-        const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);
-        const int np = (int)(w1 - w0 + 1);                          // this unit's partials
-        const float* p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
+        int np;                                                     // this unit's partials
+        const float* p0;
+        if (a.single > 0) {
+            np = a.single;
+            p0 = a.partials + (u * a.single * a.G + jq) * kPartialStride;
+        } else {
+            int64_t before, total;
+            split_prefix(sp, b, lane, before, total);
+            const int64_t W = total * a.n_kv;
+            const int64_t nwe =
+                split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, ROT ? kSplitRatio2bit * B : 0.f);
+            const int64_t Su = before * a.n_kv + (int64_t)h * nb;
+            const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);
+            np = (int)(w1 - w0 + 1);
+            p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
+        }
         const int64_t pstride = (int64_t)a.G * kPartialStride;     // next warp's partial of the unit
         if (np <= 16) {
             // one round trip: lane i holds partial i's (m, l); every lane loads its

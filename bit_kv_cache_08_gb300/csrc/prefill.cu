@@ -1,0 +1,529 @@
+// prefill.cu -- chunked prefill attention over the KVarN 2-bit paged cache
+// (sm_103a): the query rows of a chunk share one pass over each cache block.
+//
+// Method: "KVarN：方差归一化让 2-bit KV 缓存扛住长链推理", section 三 3.1 (the
+// query multiplied by the same randomised Hadamard matrix as K and V) and 3.2
+// (the stored scales applied again when the cache is read), extended from the
+// decode step to the rows of a chunk: row r of a chunk of C rows sits at
+// position L - C + r of its sequence and sees tokens 0 .. L - C + r, read from
+// the cache as it stands.
+//
+// One warp owns 8 query vectors of one (sequence, kv head): P = 8 / G chunk
+// rows x G query heads (vector v = row v / G, head v % G). Unlike the decode
+// kernel (keys as MMA rows, the 4 heads of one row as columns), the vectors
+// are the MMA rows and the keys the columns, so every 2-bit code is turned
+// into a tensor-core operand once for all 8 vectors:
+//   QK  A = q' (vector gq in row gq as fp16 hi, row gq + 8 as lo), B = the
+//       K codes as exact fp16 1 + code/4, straight from the lane's record
+//       (n-tile i holds tokens 4n + i of a 32-token sub-block); one
+//       accumulator per 32-channel group started at (-Q'_g, 0)
+//   the score accumulator layout leaves lane (gq, tq) with tokens
+//   8tq .. 8tq + 7 of each sub-block for vector gq, which is exactly the
+//   A-operand layout of the PV product, so P never leaves registers
+//   PV  A = P'_g = p R s_g lam (hi rows, lo rows), B = the V codes
+//       (n = channel, k = token), one group at a time; the block's result
+//       is folded into O with the per-channel factor 4 C / lam at once.
+// K and V head-blocks stream through a shared-memory ring filled by 1-D bulk
+// copies (lane 0) counted on mbarriers with bounded waits. Each vector's
+// (max, sum, 128 rotated accumulators) goes to one workspace partial; the
+// merge kernel adds the raw bf16 tail rows, rotates back once and
+// normalises.
+#include <algorithm>
+
+#include "attn_common.cuh"
+
+namespace kvarn {
+
+namespace {
+
+// d = A B + (c0, c0, c1, c1): rows gq start at c0, rows gq + 8 at c1
+__device__ __forceinline__ void mma16816_rows(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%11,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 8 fp16 at a 16-byte aligned shared address -> 8 floats
+__device__ __forceinline__ void load8h(const uint16_t* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(u32_as_h2(w[k]));
+        v[2 * k] = f.x;
+        v[2 * k + 1] = f.y;
+    }
+}
+
+}  // namespace
+
+constexpr int kPrefillVecs = 8;   // query vectors per warp
+
+template <int B>
+constexpr int prefill_stages() { return B == 32 ? 4 : 2; }
+
+template <int B>
+constexpr size_t prefill_smem_bytes() {
+    return (size_t)prefill_stages<B>() * 2 * head_block_bytes(B, 2) + 64 + 2 * kPrefillVecs * kD * 2 +
+           kPrefillVecs * 4;
+}
+
+template <int B, int S>
+__global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
+    wait_prior_grids();
+    constexpr int HB = head_block_bytes(B, 2);
+    constexpr int NSB = B / 32;
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t* stages = smem;                                                    // S x (K, V)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);           // S mbarriers
+    uint16_t* qh_s = reinterpret_cast<uint16_t*>(smem + S * 2 * HB + 64);      // [8][128] fp16 hi
+    uint16_t* ql_s = qh_s + kPrefillVecs * kD;                                 // [8][128] fp16 lo
+    float* kmul_s = reinterpret_cast<float*>(ql_s + kPrefillVecs * kD);        // [8]
+
+    const int lane = threadIdx.x;
+    const int gq = lane >> 2, tq = lane & 3;
+    constexpr uint32_t kOnes = 0x3C003C00u;
+
+    const int G = a.G, n_kv = a.n_kv, n_q = a.n_q, chunk = a.chunk, max_blocks = a.max_blocks;
+    const int P = kPrefillVecs / G;                       // chunk rows per warp
+    const int tiles = (chunk + P - 1) / P;
+    const int NS = a.single;                              // block ranges per (row tile, kv head)
+    const int64_t w = blockIdx.x;
+    const int split = (int)(w % NS);
+    const int64_t wu = w / NS;
+    const int tile = (int)(wu % tiles);
+    const int h = (int)((wu / tiles) % n_kv);
+    const int b = (int)(wu / tiles / n_kv);
+    if (b >= a.batch) return;
+    const int L = a.seq_lens[b];
+    if (L < 0 || L > max_blocks * B) return;               // flagged by the merge kernel
+    const int r0 = tile * P;
+    const uint8_t* __restrict__ pool = a.pool;
+    uint32_t* err = a.err;
+    const int64_t n_pool_blocks = a.n_pool_blocks, block_bytes = a.block_bytes;
+
+    // this lane's vector (row gq of the MMAs) and the tokens it may see
+    const int my_row = r0 + gq / G;
+    const bool my_ok = gq < P * G && my_row < chunk;
+    const int my_vis = my_ok ? L - chunk + my_row + 1 : 0;
+    // the warp's last row sees the most
+    const int last_row = min(chunk - 1, r0 + P - 1);
+    const int max_vis = L - chunk + last_row + 1;
+    const int nvis = max_vis > 0 ? min(L / B, (max_vis + B - 1) / B) : 0;
+    // this warp's share of those blocks (possibly none: its partial is then empty)
+    const int jb = (int)((int64_t)split * nvis / NS), je = (int)((int64_t)(split + 1) * nvis / NS);
+    const int nblk = je - jb;
+
+    // ---- queries: rotate, scale to 2^12, fp16 hi | lo in shared memory
+    {
+        const bool rotate = !(a.flags & KVARN_FLAG_NO_ROTATION);
+        const float sgn[4] = {sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane),
+                              sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + 1),
+                              sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + 2),
+                              sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + 3)};
+        for (int v = 0; v < kPrefillVecs; ++v) {
+            const int row = r0 + v / G;
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            float km = 0.f;
+            if (v < P * G && row < chunk) {
+                load_q4(a.q, a.q_dtype, ((int64_t)b * chunk + row) * n_q + (int64_t)h * G + v % G, lane, x);
+                if (rotate) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) x[k] *= sgn[k];
+                    fwht128(x, lane);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) x[k] *= kInvSqrtD;
+                }
+                float amax = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) amax = fmaxf(amax, fabsf(x[k]));
+                amax = warp_max(amax);
+                const int e = (amax > 0.f && isfinite(amax)) ? ceil_log2(amax) : 0;
+                const float sc = exp2i(12 - e);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] *= sc;
+                km = 4.0f * exp2i(e - 12) * a.sm_scale * kLog2e;
+            }
+            uint16_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const __half hh = __float2half_rn(x[k]);
+                hi[k] = __half_as_ushort(hh);
+                lo[k] = f2h_rn(x[k] - __half2float(hh));
+            }
+            *reinterpret_cast<uint2*>(qh_s + v * kD + 4 * lane) =
+                make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+            *reinterpret_cast<uint2*>(ql_s + v * kD + 4 * lane) =
+                make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+            if (lane == 0) kmul_s[v] = km;
+        }
+    }
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const float kmul = my_ok ? kmul_s[gq] : 0.f;
+
+    // ---- block ring
+    const int32_t* __restrict__ btab = a.block_table + (int64_t)b * max_blocks;
+    uint32_t okmask = 0;
+    auto issue = [&](int j, int stage) {
+        int64_t phys = btab[jb + j];
+        const bool ok = phys >= 0 && phys < n_pool_blocks;
+        if (!ok) phys = 0;   // read a valid block, result discarded below
+        if (lane == 0) {
+            const uint8_t* src = pool + phys * block_bytes + (int64_t)(2 * h) * HB;
+            mbar_arrive_expect_tx(&bars[stage], 2 * HB);
+            bulk_g2s(stages + stage * 2 * HB, src, 2 * HB, &bars[stage]);
+        }
+        return ok;
+    };
+    for (int s = 0; s < S && s < nblk; ++s)
+        if (issue(s, s)) okmask |= 1u << s;
+
+    float m_run = -INFINITY, l_part = 0.f;
+    float O[4][8];   // vector gq, channels 32g + 8tq + k
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) O[g][k] = 0.f;
+
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < nblk; ++j) {
+        if (!mbar_wait_bounded(&bars[stage], phase, kWaitLimit)) {
+            if (lane == 0) raise_error(err, KVARN_DEVERR_WAIT_TIMEOUT);
+            uint32_t ph = phase;
+            for (int k = 0, st2 = stage; k < S && j + k < nblk; ++k) {
+                mbar_wait_bounded(&bars[st2], ph, kWaitLimit);
+                if (++st2 == S) { st2 = 0; ph ^= 1u; }
+            }
+            return;
+        }
+        const uint8_t* Kb = stages + stage * 2 * HB;
+        const uint8_t* Vb = Kb + HB;
+        const bool valid = (okmask >> stage) & 1u;
+        if (!valid && lane == 0) raise_error(err, KVARN_DEVERR_BLOCK_ID);
+
+        if (valid) {
+            const uint16_t* KC = reinterpret_cast<const uint16_t*>(Kb + off_C(B, 2));
+            // ---- per-block power of two bringing max C to (1/2, 1]
+            float cmax;
+            {
+                const uint2 c2 = *reinterpret_cast<const uint2*>(KC + 4 * lane);
+                const __half2 m2 = __hmax2(u32_as_h2(c2.x), u32_as_h2(c2.y));
+                cmax = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
+            }
+            const int ec = ceil_log2(fmaxf(cmax, kF16MinNormal));
+            const __half2 cinv = __float2half2_rn(exp2i(-ec));
+            const float kmb = kmul * exp2i(ec);
+            // ---- QK A operand for vector gq: q' = q_s * C * 2^-ec, hi (row gq) | lo (row gq + 8)
+            uint32_t qa_h[16], qa_l[16];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint4 c4 = *reinterpret_cast<const uint4*>(KC + 32 * g + 8 * tq);
+                const uint4 h4 = *reinterpret_cast<const uint4*>(qh_s + gq * kD + 32 * g + 8 * tq);
+                const uint4 l4 = *reinterpret_cast<const uint4*>(ql_s + gq * kD + 32 * g + 8 * tq);
+                const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+                const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
+                const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
+                    const __half2 qh = u32_as_h2(hw[e2]);
+                    const __half2 hi = __hmul2(qh, C2);
+                    __half2 lo = __hfma2(qh, C2, __hneg2(hi));
+                    lo = __hfma2(u32_as_h2(lw[e2]), C2, lo);
+                    qa_h[4 * g + e2] = h2_as_u32(hi);
+                    qa_l[4 * g + e2] = h2_as_u32(lo);
+                }
+            }
+            // ---- Q'_g of vector gq: the same A against an all-ones B
+            float Qneg[4], Qq[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(d, qa_h[4 * g], qa_l[4 * g], qa_h[4 * g + 1], qa_l[4 * g + 1], kOnes, kOnes);
+                mma16816(d, qa_h[4 * g + 2], qa_l[4 * g + 2], qa_h[4 * g + 3], qa_l[4 * g + 3], kOnes, kOnes);
+                const float qg = d[0] + d[2];
+                Qneg[g] = -qg;
+                Qq[g] = 0.25f * qg;
+            }
+            const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, 2));
+            const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B, 2));
+            const uint16_t* KR = reinterpret_cast<const uint16_t*>(Kb + off_R(B, 2));
+
+            // ---------------- QK: scores of tokens 32sb + 8tq + {0..7} for vector gq
+            float sc[NSB][8];
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb) {
+                uint32_t kw[8], kw8[8];
+                {
+                    const uint4* rec = reinterpret_cast<const uint4*>(Kb) + 2 * (32 * sb + lane);
+                    const uint4 q0 = rec[0], q1 = rec[1];
+                    kw[0] = q0.x; kw[1] = q0.y; kw[2] = q0.z; kw[3] = q0.w;
+                    kw[4] = q1.x; kw[5] = q1.y; kw[6] = q1.z; kw[7] = q1.w;
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) kw8[k] = kw[k] >> 8;
+                const int t0 = 32 * sb + 8 * tq;
+                float Rv[8];
+                load8h(KR + t0, Rv);
+                float sv[4][8], zv[4][8];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    load8h(Ks + g * B + t0, sv[g]);
+                    load8h(Kz + g * B + t0, zv[g]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {   // n-tile i: tokens 4n + i; this lane's columns 2tq, 2tq + 1
+                    float acc[4][4];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int wi = 2 * i + (g >> 1);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int jj = 4 * (g & 1) + 2 * kk;
+                            const uint32_t b0 = code_pair(kw[wi], kw8[wi], jj);
+                            const uint32_t b1 = code_pair(kw[wi], kw8[wi], jj + 1);
+                            const int qi = 4 * g + 2 * kk;
+                            if (kk == 0)
+                                mma16816_rows(acc[g], qa_h[qi], qa_l[qi], qa_h[qi + 1], qa_l[qi + 1], b0, b1,
+                                              Qneg[g], 0.f);
+                            else
+                                mma16816(acc[g], qa_h[qi], qa_l[qi], qa_h[qi + 1], qa_l[qi + 1], b0, b1);
+                        }
+                    }
+                    // column 2tq: token t0 + i; column 2tq + 1: token t0 + 4 + i
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int tt = i + 4 * c;
+                        float s_ = 0.f;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            s_ = fmaf(sv[g][tt], acc[g][c] + acc[g][2 + c], s_);
+                            s_ = fmaf(zv[g][tt], Qq[g], s_);
+                        }
+                        sc[sb][tt] = s_ * Rv[tt] * kmb;
+                    }
+                }
+            }
+            // causal cut: tokens at or past this vector's visible length
+            const int lim = my_vis - (jb + j) * B;
+            if (__any_sync(kFull, lim < B)) {
+#pragma unroll
+                for (int sb = 0; sb < NSB; ++sb)
+#pragma unroll
+                    for (int tt = 0; tt < 8; ++tt)
+                        if (32 * sb + 8 * tq + tt >= lim) sc[sb][tt] = -INFINITY;
+            }
+
+            // ---------------- online softmax of vector gq (its 4 lanes hold the block)
+            float bm = -INFINITY;
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb)
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) bm = fmaxf(bm, sc[sb][tt]);
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+            const float m_new = fmaxf(m_run, bm);
+            const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
+            const uint16_t* Vs = reinterpret_cast<const uint16_t*>(Vb + off_s(B, 2));
+            const uint16_t* Vz = reinterpret_cast<const uint16_t*>(Vb + off_z(B, 2));
+            const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B, 2));
+            float pR[NSB][8], psum = 0.f, pmax = 0.f;
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb) {
+                float Rv[8];
+                load8h(VR + 32 * sb + 8 * tq, Rv);
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    const float p = (m_new == -INFINITY) ? 0.f : ex2(sc[sb][tt] - m_new);
+                    psum += p;
+                    pR[sb][tt] = p * Rv[tt];
+                    pmax = fmaxf(pmax, pR[sb][tt]);
+                }
+            }
+            l_part = l_part * alpha + psum;
+            m_run = m_new;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) O[g][k] *= alpha;
+            pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 1));
+            pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 2));
+            float smax;
+            if (B == 32) {
+                const uint2 s2 = *reinterpret_cast<const uint2*>(Vs + 4 * lane);
+                const __half2 m2 = __hmax2(u32_as_h2(s2.x), u32_as_h2(s2.y));
+                smax = fmaxf(__low2float(m2), __high2float(m2));
+            } else {
+                const uint4 s4 = *reinterpret_cast<const uint4*>(Vs + 8 * lane);
+                const __half2 m2 = __hmax2(__hmax2(u32_as_h2(s4.x), u32_as_h2(s4.y)),
+                                           __hmax2(u32_as_h2(s4.z), u32_as_h2(s4.w)));
+                smax = fmaxf(__low2float(m2), __high2float(m2));
+            }
+            smax = warp_max(smax);
+            // power of two lam with p R lam <= 2^14 and p R s lam <= 2^12 (fp16 range
+            // of P' and of its hi | lo halves); undone in the update of O
+            float lam = 1.f;
+            if (pmax > 0.f) {
+                int k = 14 - ceil_log2(pmax);
+                if (smax > 0.f) k = min(k, 12 - ceil_log2(pmax * smax));
+                lam = exp2i(k);
+            }
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb)
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) pR[sb][tt] *= lam;
+            const float il4 = 4.0f / lam;
+            const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, 2));
+
+            // ---------------- PV, one 32-channel group at a time
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float Ob[4][4];   // n-tile f: channels 32g + 4n + f
+#pragma unroll
+                for (int f = 0; f < 4; ++f) Ob[f][0] = Ob[f][1] = Ob[f][2] = Ob[f][3] = 0.f;
+                float Ssum = 0.f, Zsum = 0.f;
+#pragma unroll
+                for (int sb = 0; sb < NSB; ++sb) {
+                    float sv[8], zv[8];
+                    load8h(Vs + g * B + 32 * sb + 8 * tq, sv);
+                    load8h(Vz + g * B + 32 * sb + 8 * tq, zv);
+                    const uint32_t* rec = reinterpret_cast<const uint32_t*>(Vb) + 8 * (32 * sb + lane);
+                    const uint32_t vw[2] = {rec[2 * g], rec[2 * g + 1]};
+                    const uint32_t vw8[2] = {vw[0] >> 8, vw[1] >> 8};
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt) {
+                        // A: P'_g of tokens 32sb + 8tq + 4kt + {0, 1 | 2, 3}, hi row gq, lo row gq + 8
+                        float hi[4], lo[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int tt = 4 * kt + u;
+                            const float v = pR[sb][tt] * sv[tt];
+                            hi[u] = __half2float(__float2half_rn(v));
+                            lo[u] = __half2float(__float2half_rn(v - hi[u]));
+                            Ssum += hi[u] + lo[u];
+                            Zsum = fmaf(pR[sb][tt], zv[tt], Zsum);
+                        }
+                        const uint32_t a0 = pack_h2(hi[0], hi[1]), a2 = pack_h2(hi[2], hi[3]);
+                        const uint32_t a1 = pack_h2(lo[0], lo[1]), a3 = pack_h2(lo[2], lo[3]);
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) {
+                            const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
+                            mma16816(Ob[f], a0, a1, a2, a3, code_pair(w, w8, 4 * kt + (f & 1)),
+                                     code_pair(w, w8, 4 * kt + 2 + (f & 1)));
+                        }
+                    }
+                }
+                Ssum += __shfl_xor_sync(kFull, Ssum, 1);
+                Ssum += __shfl_xor_sync(kFull, Ssum, 2);
+                Zsum += __shfl_xor_sync(kFull, Zsum, 1);
+                Zsum += __shfl_xor_sync(kFull, Zsum, 2);
+                const float zq = 0.25f * Zsum - Ssum;
+                // O += 4 C_c / lam * (Ob + Z/4 - S): lane holds channels 32g + 8tq + f (column 2tq)
+                // and 32g + 8tq + 4 + f (column 2tq + 1)
+                float cf[8];
+                load8h(VC + 32 * g + 8 * tq, cf);
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    O[g][f] = fmaf(cf[f] * il4, (Ob[f][0] + Ob[f][2]) + zq, O[g][f]);
+                    O[g][4 + f] = fmaf(cf[4 + f] * il4, (Ob[f][1] + Ob[f][3]) + zq, O[g][4 + f]);
+                }
+            }
+        }
+        // ---- retire the stage and refill it
+        __syncwarp();
+        okmask &= ~(1u << stage);
+        if (j + S < nblk && issue(j + S, stage)) okmask |= 1u << stage;
+        if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+
+    // ---- this vector's partial: (max, sum, rotated accumulators) in its row's slot
+    float l = l_part;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (my_ok) {
+        const int64_t vrow = (int64_t)b * chunk + my_row;
+        float* base = a.partials + (((vrow * n_kv + h) * NS + split) * G + gq % G) * kPartialStride;
+        if (tq == 0) {
+            base[0] = m_run;
+            base[1] = l;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float4* dst = reinterpret_cast<float4*>(base + 4 + 32 * g + 8 * tq);
+            dst[0] = make_float4(O[g][0], O[g][1], O[g][2], O[g][3]);
+            dst[1] = make_float4(O[g][4], O[g][5], O[g][6], O[g][7]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
+                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
+                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
+                                int chunk, float* out, void* workspace, int64_t max_slots, int target_warps,
+                                cudaStream_t st) {
+    AttnArgs a;
+    a.q = q;
+    a.q_dtype = q_dtype;
+    a.pool = (const uint8_t*)pool;
+    a.staging = (const uint16_t*)staging;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.err = (uint32_t*)workspace;
+    a.partials = (float*)((uint8_t*)workspace + kWsHeader);
+    a.out = out;
+    a.n_pool_blocks = n_pool_blocks;
+    a.block_bytes = block_bytes;
+    a.max_blocks = max_blocks;
+    a.batch = batch;   // real sequences here; the merge below runs over the batch * chunk rows
+    a.n_q = cfg.n_q_heads;
+    a.n_kv = cfg.n_kv_heads;
+    a.G = cfg.n_q_heads / cfg.n_kv_heads;
+    a.nw = 0;
+    a.chunk = chunk;
+    a.sm_scale = cfg.sm_scale;
+    a.flags = cfg.flags;
+    for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
+    const int P = kPrefillVecs / a.G;
+    const int64_t tiles = (chunk + P - 1) / P;
+    const int64_t units = (int64_t)batch * a.n_kv * tiles;
+    // split each unit's blocks when there are too few units to fill the GPU; the
+    // partials of a row must fit the workspace slots and one merge round trip (16)
+    const int64_t rows = (int64_t)batch * chunk * a.n_kv;
+    int64_t ns = units > 0 ? (target_warps + units - 1) / units : 1;
+    ns = std::min<int64_t>(ns, std::min<int64_t>(16, rows > 0 ? max_slots / rows : 1));
+    a.single = (int)std::max<int64_t>(ns, 1);
+    const int64_t warps = units * a.single;
+    if (warps > 0x7fffffff) return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (cfg.block_size == 32) {
+        e = launch_pdl(prefill_attn_kernel<32, prefill_stages<32>()>, (unsigned)warps, 32,
+                       prefill_smem_bytes<32>(), st, a);
+    } else {
+        e = launch_pdl(prefill_attn_kernel<64, prefill_stages<64>()>, (unsigned)warps, 32,
+                       prefill_smem_bytes<64>(), st, a);
+    }
+    if (e != cudaSuccess) return e;
+    a.batch = batch * chunk;
+    const unsigned mgrid = (unsigned)(((int64_t)a.batch * a.n_q + 3) / 4);
+    return cfg.block_size == 32 ? launch_pdl(merge_kernel<32, true>, mgrid, 128, 0, st, a)
+                                : launch_pdl(merge_kernel<64, true>, mgrid, 128, 0, st, a);
+}
+
+}  // namespace kvarn
