@@ -692,7 +692,7 @@ def run_prefill(args):
     for chunk in PREFILL_CHUNKS:
         q = synth.queries(g, batch * chunk, n_q, dev).reshape(batch, chunk, n_q, D).to(torch.bfloat16)
         out = torch.empty(batch, chunk, n_q, D, device=dev)
-        ws = kv.alloc_workspace(cfg, batch * chunk, nb, dev)
+        ws = kv.alloc_prefill_workspace(cfg, batch, chunk, nb, dev)
         for _ in range(3):
             kv.prefill_attn(cfg, q, pool, staging, bt, lens, out, ws)
         ms = _time_events(lambda: kv.prefill_attn(cfg, q, pool, staging, bt, lens, out, ws), 10, flush)

@@ -65,6 +65,7 @@ _SIGS = {
     "kvarn_block_bytes": (_sz, [_cfgp]),
     "kvarn_staging_bytes": (_sz, [_cfgp, _i32]),
     "kvarn_workspace_bytes": (_sz, [_cfgp, _i32, _i32]),
+    "kvarn_prefill_workspace_bytes": (_sz, [_cfgp, _i32, _i32, _i32]),
     "kvarn_quantize_block": (ctypes.c_int, [_cfgp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "kvarn_append": (ctypes.c_int, [_cfgp, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
     "kvarn_decode_attn": (ctypes.c_int, [_cfgp, _vp, _i32, _vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
@@ -152,6 +153,18 @@ def workspace_bytes(cfg: Config, batch: int, max_blocks_per_seq: int) -> int:
 
 
 # ------------------------------------------------------------------ buffers
+
+def prefill_workspace_bytes(cfg: Config, batch: int, chunk: int, max_blocks_per_seq: int) -> int:
+    return int(lib().kvarn_prefill_workspace_bytes(ctypes.byref(cfg), batch, chunk, max_blocks_per_seq))
+
+
+def alloc_prefill_workspace(cfg: Config, batch: int, chunk: int, max_blocks_per_seq: int,
+                            device="cuda") -> torch.Tensor:
+    n = prefill_workspace_bytes(cfg, batch, chunk, max_blocks_per_seq)
+    if n == 0:
+        raise ValueError("kvarn_prefill_workspace_bytes: invalid config or sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
 
 def alloc_workspace(cfg: Config, batch: int, max_blocks_per_seq: int, device="cuda") -> torch.Tensor:
     n = workspace_bytes(cfg, batch, max_blocks_per_seq)

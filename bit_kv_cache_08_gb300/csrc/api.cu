@@ -120,6 +120,36 @@ size_t kvarn_staging_bytes(const kvarn_config* cfg, int32_t max_seqs) {
     return (size_t)max_seqs * c.n_kv_heads * 2 * c.block_size * 128 * 2;
 }
 
+// Warps the 2-bit prefill kernel aims for: half the resident warps (measured
+// on the Llama-3.1-8B layer: more block splits than that cost more in partials
+// and merging than they gain in occupancy).
+static int prefill_target_warps(int rw) { return rw / 2 > 1 ? rw / 2 : 1; }
+
+// Row tiles of the 2-bit prefill kernel and the block splits it wants: enough
+// warps to reach the target, at most 16 partials per row.
+static int64_t prefill_ideal_splits(const kvarn_config& c, int64_t batch, int64_t chunk, int rw) {
+    const int G = c.n_q_heads / c.n_kv_heads, P = 8 / G;
+    const int64_t units = batch * c.n_kv_heads * ((chunk + P - 1) / P);
+    if (units <= 0) return 1;
+    const int64_t target = prefill_target_warps(rw);
+    const int64_t ns = (target + units - 1) / units;
+    return ns < 1 ? 1 : (ns > 16 ? 16 : ns);
+}
+
+size_t kvarn_prefill_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t chunk,
+                                     int32_t max_blocks_per_seq) {
+    kvarn_config c;
+    if (check_config(cfg, &c) != KVARN_OK || batch < 0 || chunk < 1 || max_blocks_per_seq < 0) return 0;
+    if ((int64_t)batch * chunk > 0x7fffffff / c.n_q_heads) return 0;
+    const size_t base = ws_bytes(c, batch * chunk);
+    if (base == 0 || batch == 0 || c.bits != 2 || chunk == 1) return base;
+    const int rw = resident_warps(c.block_size, c.bits);
+    const int64_t rows = (int64_t)batch * chunk * c.n_kv_heads;
+    const size_t split = kWsHeader + (size_t)(rows * prefill_ideal_splits(c, batch, chunk, rw)) *
+                                         (size_t)(c.n_q_heads / c.n_kv_heads) * 132 * sizeof(float);
+    return split > base ? split : base;
+}
+
 size_t kvarn_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks_per_seq) {
     kvarn_config c;
     if (check_config(cfg, &c) != KVARN_OK || batch < 0 || max_blocks_per_seq < 0) return 0;
@@ -191,10 +221,13 @@ int packed_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const v
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;
     if (chunk > 1 && c.bits == 2) {   // rows of a chunk share each block's operands
         const int rw = resident_warps(c.block_size, c.bits);
-        const int64_t slots = (int64_t)batch * chunk * c.n_kv_heads + rw;   // what ws_bytes sized
+        // partial slots the caller's workspace holds: the block splits adapt to it
+        const int64_t slots = (int64_t)((workspace_bytes - kWsHeader) /
+                                        ((size_t)(c.n_q_heads / c.n_kv_heads) * 132 * sizeof(float)));
         return cuda_status(launch_prefill_attn(c, q, q_dtype, pool, n_pool_blocks, (int64_t)kvarn_block_bytes(&c),
                                                staging, block_table, max_blocks_per_seq, seq_lens, batch, chunk,
-                                               out, workspace, slots, rw, (cudaStream_t)stream));
+                                               out, workspace, slots, prefill_target_warps(rw),
+                                               (cudaStream_t)stream));
     }
     const int nw = attn_grid_warps(c.block_size, c.bits, chunk > 1, current_device());
     if (nw <= 0) return KVARN_ERR_CUDA;

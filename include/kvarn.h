@@ -148,6 +148,15 @@ size_t kvarn_staging_bytes(const kvarn_config* cfg, int32_t max_seqs);
  * kvarn_quantize_block and kvarn_append need. 0 on a bad config. */
 size_t kvarn_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks_per_seq);
 
+/* Workspace with which kvarn_prefill_attn runs at full speed for this batch
+ * and chunk on the CURRENT device: at least kvarn_workspace_bytes(cfg,
+ * batch * chunk, ...), and room for several partials per row when there are
+ * too few (sequence, kv head, row tile) units to fill the GPU (2-bit caches;
+ * the block split adapts to the workspace actually passed). 0 on a bad
+ * config. */
+size_t kvarn_prefill_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t chunk,
+                                     int32_t max_blocks_per_seq);
+
 /*
  * kvarn_quantize_block -- bulk quantise-on-write of complete head-blocks
  * (prefill). Passage: abstract (rotation then dual-axis normalisation, 2-bit);
@@ -231,9 +240,10 @@ int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, c
  * row with p < 0 (seq_lens[b] < chunk) gives zeros. out: device fp32
  * [batch][chunk][n_q][128]. chunk >= 1; chunk = 1 is kvarn_decode_attn.
  * workspace: at least kvarn_workspace_bytes(cfg, batch * chunk,
- * max_blocks_per_seq) bytes. Every row is split and merged like a decode
- * query of its own (the cache is read once per row, mostly from L2). Device
- * faults as kvarn_decode_attn.
+ * max_blocks_per_seq) bytes (kvarn_prefill_workspace_bytes for full speed). 2-bit caches: one warp scores 8 query vectors
+ * (8 / G rows x G heads) against each block, building each code's
+ * tensor-core operand once for all 8; 4-bit caches: every row runs the
+ * decode kernel's split of its own. Device faults as kvarn_decode_attn.
  */
 int kvarn_prefill_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,
                        int64_t n_pool_blocks, const void* staging, const int32_t* block_table,

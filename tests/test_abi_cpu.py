@@ -38,6 +38,13 @@ def test_sizes_match_the_format():
     assert kv.workspace_bytes(c32, 0, 0) == 256
 
 
+def test_prefill_workspace_query_without_a_device():
+    c = _cfg()
+    assert kv.prefill_workspace_bytes(c, 0, 4, 0) == 256
+    assert kv.prefill_workspace_bytes(c, 2, 0, 4) == 0          # chunk >= 1
+    assert kv.prefill_workspace_bytes(c, -1, 4, 4) == 0
+
+
 def test_four_bit_sizes_match_the_oracle_format():
     """4-bit codes: records of 64 bytes, then the same s, z, R, C sections."""
     for B in (32, 64):

@@ -14,11 +14,13 @@ pytestmark = pytest.mark.gpu
 D = 128
 
 
-def _prefill(kv, cache, q, lens):
+def _prefill(kv, cache, q, lens, split=True):
+    """split: the workspace sized for the full block split (else the minimum)."""
     cfg = cache.cfg
     sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     out = torch.full(q.shape, float("nan"), device="cuda")
-    ws = kv.alloc_workspace(cfg, q.shape[0] * q.shape[1], cache.max_blocks)
+    ws = (kv.alloc_prefill_workspace(cfg, q.shape[0], q.shape[1], cache.max_blocks) if split
+          else kv.alloc_workspace(cfg, q.shape[0] * q.shape[1], cache.max_blocks))
     kv.prefill_attn(cfg, q, cache.pool, cache.staging, cache.block_table, sl, out, ws)
     torch.cuda.synchronize()
     return out.cpu().double().numpy(), kv.read_error(ws)
@@ -97,6 +99,21 @@ def test_prefill_long_chunk_many_partials(kvlib, G):
     got, err = _prefill(kv, cache, q, lens)
     assert err == 0
     attn_close(got, _oracle(cache, q, lens, sb))
+
+
+def test_prefill_minimum_workspace_gives_the_same_rows(kvlib):
+    """The block split adapts to the workspace passed: the minimum workspace
+    (fewer splits) gives the same rows up to rounding."""
+    kv = kvlib
+    B, n_q, n_kv = 32, 8, 2
+    lens = [900, 333]
+    cache, sb, g = _cache(kv, B, 2, 3, n_q, n_kv, lens, 61)
+    q = synth.queries(g, len(lens) * 6, n_q).reshape(len(lens), 6, n_q, D).to(torch.bfloat16).cuda()
+    a, err_a = _prefill(kv, cache, q, lens, split=True)
+    b, err_b = _prefill(kv, cache, q, lens, split=False)
+    assert err_a == 0 and err_b == 0
+    np.testing.assert_allclose(a, b, rtol=1e-5, atol=1e-5)
+    attn_close(b, _oracle(cache, q, lens, sb))
 
 
 def test_prefill_bad_length_is_flagged(kvlib):
