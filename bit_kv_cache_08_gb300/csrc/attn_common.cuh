@@ -99,6 +99,10 @@ __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t row,
     }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- merge kernel
 // One warp per (sequence, query head): LSE-merge the unit's partials. For the
 // 2-bit cache (ROT = true) the merged accumulator is in the rotated space: it
@@ -122,6 +126,17 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     }
     const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1, a.chunk};
     const int nb = split_nblocks(sp, b);
+    // raw rows in staging (< B <= 64): the visible tokens past the pool blocks
+    const int ntail = ROT ? max(0, split_visible(sp, b, L) - nb * B) : 0;
+    if (ntail > 0) {   // start the tail rows on their way to L2 while the partials merge
+        const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
+        for (int r = lane; r < ntail; r += 32) {
+            prefetch_l2(kst + (int64_t)r * kD);
+            prefetch_l2(kst + (int64_t)r * kD + 64);
+            prefetch_l2(kst + (int64_t)(B + r) * kD);
+            prefetch_l2(kst + (int64_t)(B + r) * kD + 64);
+        }
+    }
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (nb > 0) {
         const int64_t u = (int64_t)b * a.n_kv + h;
@@ -196,38 +211,48 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
             for (int k = 0; k < 4; ++k) acc[k] *= kInvSqrtD * sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + k);
         }
     }
-    // raw rows in staging (< B <= 64): the visible tokens past the pool blocks
-    const int ntail = ROT ? max(0, split_visible(sp, b, L) - nb * B) : 0;
     if (ntail > 0) {
-        float qv[4];
-        load_q4(a.q, a.q_dtype, gw, lane, qv);
-        const float qs = a.sm_scale * kLog2e;
+        // this warp's query (unrotated, times sm_scale log2 e) in shared memory, so
+        // that lane r can score tail row r (and r + 32) over all 128 channels
+        // with its loads issued at once
+        __shared__ __align__(16) float q_all[4][kD];
+        float* qsh = q_all[threadIdx.x >> 5];
+        {
+            float qv[4];
+            load_q4(a.q, a.q_dtype, gw, lane, qv);
+            const float qs = a.sm_scale * kLog2e;
+            *reinterpret_cast<float4*>(qsh + 4 * lane) = make_float4(qv[0] * qs, qv[1] * qs, qv[2] * qs, qv[3] * qs);
+        }
+        __syncwarp();
         const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
         const uint16_t* vst = kst + B * kD;
-        // scores of all tail rows, 8 rows at a time with independent loads; row r's
-        // score ends on lane r % 32, slot r / 32
-        float mine[2] = {-INFINITY, -INFINITY};
-        for (int r0 = 0; r0 < ntail; r0 += 8) {
-            float d[8];
+        float mine[2] = {-INFINITY, -INFINITY};   // scores of rows lane, lane + 32
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                d[k] = 0.f;
-                if (r0 + k < ntail) {
-                    const uint2 ku = reinterpret_cast<const uint2*>(kst + (r0 + k) * kD)[lane];
-                    d[k] = qv[0] * __uint_as_float(ku.x << 16);
-                    d[k] = fmaf(qv[1], __uint_as_float(ku.x & 0xffff0000u), d[k]);
-                    d[k] = fmaf(qv[2], __uint_as_float(ku.y << 16), d[k]);
-                    d[k] = fmaf(qv[3], __uint_as_float(ku.y & 0xffff0000u), d[k]);
+        for (int half = 0; half < 2; ++half) {
+            const int r = lane + 32 * half;
+            if (half * 32 < ntail && r < ntail) {
+                const uint4* kr = reinterpret_cast<const uint4*>(kst + (int64_t)r * kD);
+                float d = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < 16; c0 += 8) {
+                uint4 ku[16];
+#pragma unroll
+                for (int c = c0; c < c0 + 8; ++c) ku[c] = kr[c];
+#pragma unroll
+                for (int c = c0; c < c0 + 8; ++c) {
+                    const float4 qa = *reinterpret_cast<const float4*>(qsh + 8 * c);
+                    const float4 qb = *reinterpret_cast<const float4*>(qsh + 8 * c + 4);
+                    d = fmaf(qa.x, __uint_as_float(ku[c].x << 16), d);
+                    d = fmaf(qa.y, __uint_as_float(ku[c].x & 0xffff0000u), d);
+                    d = fmaf(qa.z, __uint_as_float(ku[c].y << 16), d);
+                    d = fmaf(qa.w, __uint_as_float(ku[c].y & 0xffff0000u), d);
+                    d = fmaf(qb.x, __uint_as_float(ku[c].z << 16), d);
+                    d = fmaf(qb.y, __uint_as_float(ku[c].z & 0xffff0000u), d);
+                    d = fmaf(qb.z, __uint_as_float(ku[c].w << 16), d);
+                    d = fmaf(qb.w, __uint_as_float(ku[c].w & 0xffff0000u), d);
                 }
-            }
-#pragma unroll
-            for (int mm = 16; mm >= 1; mm >>= 1)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) d[k] += __shfl_xor_sync(kFull, d[k], mm);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int r = r0 + k;
-                if (r < ntail && lane == (r & 31)) mine[r >> 5] = d[k] * qs;
+                }
+                mine[half] = d;
             }
         }
         const float mt = warp_max(fmaxf(mine[0], mine[1]));
@@ -238,17 +263,21 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] *= fa;
         m = mn;
+        // values: 8 rows per step, their loads independent of each other
         for (int r0 = 0; r0 < ntail; r0 += 8) {
+            uint2 vu[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < ntail) vu[k] = reinterpret_cast<const uint2*>(vst + (int64_t)(r0 + k) * kD)[lane];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int r = r0 + k;
                 if (r < ntail) {
                     const float p = __shfl_sync(kFull, (r < 32) ? p0 : p1, r & 31);
-                    const uint2 vu = reinterpret_cast<const uint2*>(vst + r * kD)[lane];
-                    acc[0] = fmaf(p, __uint_as_float(vu.x << 16), acc[0]);
-                    acc[1] = fmaf(p, __uint_as_float(vu.x & 0xffff0000u), acc[1]);
-                    acc[2] = fmaf(p, __uint_as_float(vu.y << 16), acc[2]);
-                    acc[3] = fmaf(p, __uint_as_float(vu.y & 0xffff0000u), acc[3]);
+                    acc[0] = fmaf(p, __uint_as_float(vu[k].x << 16), acc[0]);
+                    acc[1] = fmaf(p, __uint_as_float(vu[k].x & 0xffff0000u), acc[1]);
+                    acc[2] = fmaf(p, __uint_as_float(vu[k].y << 16), acc[2]);
+                    acc[3] = fmaf(p, __uint_as_float(vu[k].y & 0xffff0000u), acc[3]);
                 }
             }
         }
