@@ -19,7 +19,7 @@ cudaError_t launch_error_split(const kvarn_config& cfg, int kind, const void* sr
 cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
-                               int chunk, float* out, void* workspace, int nw, cudaStream_t st);
+                               float* out, void* workspace, int nw, cudaStream_t st);
 cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int q_dtype, const void* kv_pool,
                                     int64_t n_pool_blocks, const int32_t* block_table, int max_blocks,
                                     const int32_t* seq_lens, int batch, float* out, void* workspace, int nw,
@@ -29,7 +29,7 @@ cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dt
                                 const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
                                 int chunk, float* out, void* workspace, int64_t max_slots, int target_warps,
                                 cudaStream_t st);
-int attn_grid_warps(int block_size, int bits, bool prefill, int device);
+int attn_grid_warps(int block_size, int bits, int device);
 int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
 
@@ -68,10 +68,9 @@ int current_device() {
 int resident_warps(int block_size, int bits) {
     const int d = current_device();
     if (d < 0) return 0;
-    const int a = attn_grid_warps(block_size, bits, false, d), p = attn_grid_warps(block_size, bits, true, d);
+    const int a = attn_grid_warps(block_size, bits, d);
     const int b = attn_bf16_grid_warps(block_size, d);
-    const int m = a > p ? a : p;
-    return m > b ? m : b;
+    return a > b ? a : b;
 }
 
 size_t ws_bytes(const kvarn_config& c, int32_t batch) {
@@ -142,7 +141,7 @@ size_t kvarn_prefill_workspace_bytes(const kvarn_config* cfg, int32_t batch, int
     if (check_config(cfg, &c) != KVARN_OK || batch < 0 || chunk < 1 || max_blocks_per_seq < 0) return 0;
     if ((int64_t)batch * chunk > 0x7fffffff / c.n_q_heads) return 0;
     const size_t base = ws_bytes(c, batch * chunk);
-    if (base == 0 || batch == 0 || c.bits != 2 || chunk == 1) return base;
+    if (base == 0 || batch == 0 || chunk == 1) return base;
     const int rw = resident_warps(c.block_size, c.bits);
     const int64_t rows = (int64_t)batch * chunk * c.n_kv_heads;
     const size_t split = kWsHeader + (size_t)(rows * prefill_ideal_splits(c, batch, chunk, rw)) *
@@ -219,7 +218,7 @@ int packed_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const v
     const size_t need = ws_bytes(c, batch * chunk);
     if (need == 0) return KVARN_ERR_CUDA;
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;
-    if (chunk > 1 && c.bits == 2) {   // rows of a chunk share each block's operands
+    if (chunk > 1) {   // rows of a chunk share each block's operands
         const int rw = resident_warps(c.block_size, c.bits);
         // partial slots the caller's workspace holds: the block splits adapt to it
         const int64_t slots = (int64_t)((workspace_bytes - kWsHeader) /
@@ -229,10 +228,10 @@ int packed_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const v
                                                out, workspace, slots, prefill_target_warps(rw),
                                                (cudaStream_t)stream));
     }
-    const int nw = attn_grid_warps(c.block_size, c.bits, chunk > 1, current_device());
+    const int nw = attn_grid_warps(c.block_size, c.bits, current_device());
     if (nw <= 0) return KVARN_ERR_CUDA;
     return cuda_status(launch_decode_attn(c, q, q_dtype, pool, n_pool_blocks, (int64_t)kvarn_block_bytes(&c),
-                                          staging, block_table, max_blocks_per_seq, seq_lens, batch, chunk, out,
+                                          staging, block_table, max_blocks_per_seq, seq_lens, batch, out,
                                           workspace, nw, (cudaStream_t)stream));
 }
 }  // namespace

@@ -55,7 +55,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------- the split-K kernel
-template <int B, int BITS, int S, bool PREFILL>
+template <int B, int BITS, int S>
 __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     static_assert(BITS == 2 || BITS == 4, "2- or 4-bit codes");
     wait_prior_grids();
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const uint32_t sb0 = a.sb[0], sb1 = a.sb[1], sb2 = a.sb[2], sb3 = a.sb[3];
     const bool rotate_q = !(a.flags & KVARN_FLAG_NO_ROTATION);
 
-    const SplitArgs sp{a.seq_lens, a.batch, n_kv, max_blocks, B, 0, PREFILL ? a.chunk : 1};
+    const SplitArgs sp{a.seq_lens, a.batch, n_kv, max_blocks, B, 0, 1};
     Cursor cc;
     cc.b = cc.h = cc.j = 0;
     const int64_t W = split_locate(sp, 0, lane, cc.b, cc.h, cc.j);
@@ -112,8 +112,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             bt_b = ic.b;
             bt_j0 = ic.j;
             const int jj = bt_j0 + lane;
-            const int64_t row = PREFILL ? bt_b / sp.chunk : bt_b;   // the real sequence's table row
-            bt_val = (jj < max_blocks) ? btab[row * max_blocks + jj] : -1;
+            bt_val = (jj < max_blocks) ? btab[(int64_t)bt_b * max_blocks + jj] : -1;
         }
         int64_t phys = __shfl_sync(kFull, bt_val, ic.j - bt_j0);
         const bool ok = phys >= 0 && phys < n_pool_blocks;
@@ -346,16 +345,6 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sc[sb][i] = s_[i] * Rv[i] * kmb;
             }
-            // causal cut inside the last visible block of a prefill row
-            const int lim = PREFILL ? split_visible(sp, cc.b, sp.seq_lens[cc.b / sp.chunk]) - cc.j * B : B;
-            if (PREFILL && lim < B) {
-#pragma unroll
-                for (int sb = 0; sb < NSB; ++sb)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (32 * sb + 4 * gq + i >= lim) sc[sb][i] = -INFINITY;
-            }
-
             // ---------------- online softmax over the block (head tq: 8 lanes x 4 tokens per sub-block)
             float bm = -INFINITY;
 #pragma unroll
@@ -569,46 +558,41 @@ size_t attn_smem_bytes() {
            2 * 4 * B * sizeof(uint16_t);
 }
 
-template <int B, int BITS, bool PREFILL>
+template <int B, int BITS>
 struct AttnKernel {
     static constexpr int kB = B;
-    static constexpr auto fn = decode_attn_2bit_kernel<B, BITS, stages_for<B, BITS>(), PREFILL>;
+    static constexpr auto fn = decode_attn_2bit_kernel<B, BITS, stages_for<B, BITS>()>;
     static size_t smem() { return attn_smem_bytes<B, BITS>(); }
 };
 
-template <bool PREFILL, typename F>
-auto with_attn_kernel_p(int block_size, int bits, F&& f) {
-    if (block_size == 32) return bits == 4 ? f(AttnKernel<32, 4, PREFILL>{}) : f(AttnKernel<32, 2, PREFILL>{});
-    return bits == 4 ? f(AttnKernel<64, 4, PREFILL>{}) : f(AttnKernel<64, 2, PREFILL>{});
-}
-// The decode kernel (chunk = 1) or its chunked-prefill instantiation.
 template <typename F>
-auto with_attn_kernel(int block_size, int bits, bool prefill, F&& f) {
-    return prefill ? with_attn_kernel_p<true>(block_size, bits, f) : with_attn_kernel_p<false>(block_size, bits, f);
+auto with_attn_kernel(int block_size, int bits, F&& f) {
+    if (block_size == 32) return bits == 4 ? f(AttnKernel<32, 4>{}) : f(AttnKernel<32, 2>{});
+    return bits == 4 ? f(AttnKernel<64, 4>{}) : f(AttnKernel<64, 2>{});
 }
 
-// Resident warps of the split-K kernel for (block size, code width, prefill)
-// on `device` (cached per device).
-int attn_grid_warps(int block_size, int bits, bool prefill, int device) {
-    static int cache[2][2][2][64];
-    const int bi = block_size == 32 ? 0 : 1, wi = bits == 4 ? 1 : 0, pi = prefill ? 1 : 0;
+// Resident warps of the split-K kernel for (block size, code width) on
+// `device` (cached per device).
+int attn_grid_warps(int block_size, int bits, int device) {
+    static int cache[2][2][64];
+    const int bi = block_size == 32 ? 0 : 1, wi = bits == 4 ? 1 : 0;
     if (device < 0 || device >= 64) return 0;
-    if (cache[bi][wi][pi][device] > 0) return cache[bi][wi][pi][device];
+    if (cache[bi][wi][device] > 0) return cache[bi][wi][device];
     int sms = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-    const cudaError_t e = with_attn_kernel(block_size, bits, prefill, [&](auto k) {
+    const cudaError_t e = with_attn_kernel(block_size, bits, [&](auto k) {
         using K = decltype(k);
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, K::fn, 32, K::smem());
     });
     if (e != cudaSuccess || per_sm <= 0) return 0;
-    cache[bi][wi][pi][device] = sms * per_sm;
-    return cache[bi][wi][pi][device];
+    cache[bi][wi][device] = sms * per_sm;
+    return cache[bi][wi][device];
 }
 
 cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
-                               int batch, int chunk, float* out, void* workspace, int nw, cudaStream_t st) {
+                               int batch, float* out, void* workspace, int nw, cudaStream_t st) {
     AttnArgs a;
     a.q = q;
     a.q_dtype = q_dtype;
@@ -622,8 +606,8 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.n_pool_blocks = n_pool_blocks;
     a.block_bytes = block_bytes;
     a.max_blocks = max_blocks;
-    a.batch = batch * chunk;   // one (virtual) sequence per query row
-    a.chunk = chunk;
+    a.batch = batch;
+    a.chunk = 1;
     a.single = 0;
     a.n_q = cfg.n_q_heads;
     a.n_kv = cfg.n_kv_heads;
@@ -633,7 +617,7 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)a.batch * a.n_q + 3) / 4);
-    return with_attn_kernel(cfg.block_size, cfg.bits, chunk > 1, [&](auto k) {
+    return with_attn_kernel(cfg.block_size, cfg.bits, [&](auto k) {
         using K = decltype(k);
         cudaError_t e = launch_pdl(K::fn, nw, 32, K::smem(), st, a);
         if (e == cudaSuccess) e = launch_pdl(merge_kernel<K::kB, true>, mgrid, 128, 0, st, a);

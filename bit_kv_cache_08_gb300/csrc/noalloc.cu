@@ -22,8 +22,8 @@ namespace kvarn {
 cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
-                               int chunk, float* out, void* workspace, int nw, cudaStream_t st);
-int attn_grid_warps(int block_size, int bits, bool prefill, int device);
+                               float* out, void* workspace, int nw, cudaStream_t st);
+int attn_grid_warps(int block_size, int bits, int device);
 int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
 
@@ -86,7 +86,7 @@ extern "C" int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q,
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KVARN_ERR_CUDA;
-    const int nw = attn_grid_warps(c.block_size, c.bits, false, dev);
+    const int nw = attn_grid_warps(c.block_size, c.bits, dev);
     const int nw_any = nw > attn_bf16_grid_warps(c.block_size, dev) ? nw : attn_bf16_grid_warps(c.block_size, dev);
     if (nw <= 0 || nw_any <= 0) return KVARN_ERR_CUDA;
     // same size rule as kvarn_workspace_bytes; beyond the fixed array: refuse
@@ -102,7 +102,7 @@ extern "C" int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q,
     if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st) != cudaSuccess) return KVARN_ERR_CUDA;
     const int64_t block_bytes = (int64_t)c.n_kv_heads * 2 * head_block_bytes(c.block_size, c.bits);
     if (launch_decode_attn(c, q, q_dtype, pool, n_pool_blocks, block_bytes, staging, block_table,
-                           max_blocks_per_seq, seq_lens, batch, 1, out, scratch, nw, st) != cudaSuccess)
+                           max_blocks_per_seq, seq_lens, batch, out, scratch, nw, st) != cudaSuccess)
         return KVARN_ERR_CUDA;
     if (error_word &&
         cudaMemcpyAsync(error_word, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

@@ -1,5 +1,6 @@
-// prefill.cu -- chunked prefill attention over the KVarN 2-bit paged cache
-// (sm_103a): the query rows of a chunk share one pass over each cache block.
+// prefill.cu -- chunked prefill attention over the KVarN paged cache (2- or
+// 4-bit codes; sm_103a): the query rows of a chunk share one pass over each
+// cache block.
 //
 // Method: "KVarN：方差归一化让 2-bit KV 缓存扛住长链推理", section 三 3.1 (the
 // query multiplied by the same randomised Hadamard matrix as K and V) and 3.2
@@ -27,7 +28,8 @@
 // copies (lane 0) counted on mbarriers with bounded waits. Each vector's
 // (max, sum, 128 rotated accumulators) goes to one workspace partial; the
 // merge kernel adds the raw bf16 tail rows, rotates back once and
-// normalises.
+// normalises. 4-bit codes take the same path with 64-byte records and
+// a = 1 + code/16 (every factor 4 above becomes 16).
 #include <algorithm>
 
 #include "attn_common.cuh"
@@ -70,17 +72,20 @@ constexpr int kPrefillVecs = 8;   // query vectors per warp
 template <int B>
 constexpr int prefill_stages() { return B == 32 ? 4 : 2; }
 
-template <int B>
+template <int B, int BITS>
 constexpr size_t prefill_smem_bytes() {
-    return (size_t)prefill_stages<B>() * 2 * head_block_bytes(B, 2) + 64 + 2 * kPrefillVecs * kD * 2 +
+    return (size_t)prefill_stages<B>() * 2 * head_block_bytes(B, BITS) + 64 + 2 * kPrefillVecs * kD * 2 +
            kPrefillVecs * 4;
 }
 
-template <int B, int S>
+template <int B, int BITS, int S>
 __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
+    static_assert(BITS == 2 || BITS == 4, "2- or 4-bit codes");
     wait_prior_grids();
-    constexpr int HB = head_block_bytes(B, 2);
+    constexpr int HB = head_block_bytes(B, BITS);
     constexpr int NSB = B / 32;
+    constexpr int RW = 4 * BITS;              // 32-bit words per lane record
+    constexpr float kLevels = 1 << BITS;      // a = 1 + code / 2^BITS
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                                    // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);           // S mbarriers
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 const float sc = exp2i(12 - e);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) x[k] *= sc;
-                km = 4.0f * exp2i(e - 12) * a.sm_scale * kLog2e;
+                km = kLevels * exp2i(e - 12) * a.sm_scale * kLog2e;
             }
             uint16_t hi[4], lo[4];
 #pragma unroll
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
         if (!valid && lane == 0) raise_error(err, KVARN_DEVERR_BLOCK_ID);
 
         if (valid) {
-            const uint16_t* KC = reinterpret_cast<const uint16_t*>(Kb + off_C(B, 2));
+            const uint16_t* KC = reinterpret_cast<const uint16_t*>(Kb + off_C(B, BITS));
             // ---- per-block power of two bringing max C to (1/2, 1]
             float cmax;
             {
@@ -256,25 +261,27 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 mma16816(d, qa_h[4 * g + 2], qa_l[4 * g + 2], qa_h[4 * g + 3], qa_l[4 * g + 3], kOnes, kOnes);
                 const float qg = d[0] + d[2];
                 Qneg[g] = -qg;
-                Qq[g] = 0.25f * qg;
+                Qq[g] = qg * (1.0f / kLevels);
             }
-            const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, 2));
-            const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B, 2));
-            const uint16_t* KR = reinterpret_cast<const uint16_t*>(Kb + off_R(B, 2));
+            const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, BITS));
+            const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B, BITS));
+            const uint16_t* KR = reinterpret_cast<const uint16_t*>(Kb + off_R(B, BITS));
 
             // ---------------- QK: scores of tokens 32sb + 8tq + {0..7} for vector gq
             float sc[NSB][8];
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
-                uint32_t kw[8], kw8[8];
+                uint32_t kw[RW], kw8[RW];
                 {
-                    const uint4* rec = reinterpret_cast<const uint4*>(Kb) + 2 * (32 * sb + lane);
-                    const uint4 q0 = rec[0], q1 = rec[1];
-                    kw[0] = q0.x; kw[1] = q0.y; kw[2] = q0.z; kw[3] = q0.w;
-                    kw[4] = q1.x; kw[5] = q1.y; kw[6] = q1.z; kw[7] = q1.w;
+                    const uint4* rec = reinterpret_cast<const uint4*>(Kb) + (RW / 4) * (32 * sb + lane);
+#pragma unroll
+                    for (int r = 0; r < RW / 4; ++r) {
+                        const uint4 rr = rec[r];
+                        kw[4 * r] = rr.x; kw[4 * r + 1] = rr.y; kw[4 * r + 2] = rr.z; kw[4 * r + 3] = rr.w;
+                    }
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) kw8[k] = kw[k] >> 8;
+                for (int k = 0; k < RW; ++k) kw8[k] = kw[k] >> 8;
                 const int t0 = 32 * sb + 8 * tq;
                 float Rv[8];
                 load8h(KR + t0, Rv);
@@ -289,12 +296,18 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                     float acc[4][4];
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
-                        const int wi = 2 * i + (g >> 1);
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
-                            const int jj = 4 * (g & 1) + 2 * kk;
-                            const uint32_t b0 = code_pair(kw[wi], kw8[wi], jj);
-                            const uint32_t b1 = code_pair(kw[wi], kw8[wi], jj + 1);
+                            uint32_t b0, b1;
+                            if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
+                                const int wi = 2 * i + (g >> 1), jj = 4 * (g & 1) + 2 * kk;
+                                b0 = code_pair(kw[wi], kw8[wi], jj);
+                                b1 = code_pair(kw[wi], kw8[wi], jj + 1);
+                            } else {           // word 4i + g, field e/2
+                                const int wi = 4 * i + g;
+                                b0 = code_quad(kw[wi], kw8[wi], 2 * kk);
+                                b1 = code_quad(kw[wi], kw8[wi], 2 * kk + 1);
+                            }
                             const int qi = 4 * g + 2 * kk;
                             if (kk == 0)
                                 mma16816_rows(acc[g], qa_h[qi], qa_l[qi], qa_h[qi + 1], qa_l[qi + 1], b0, b1,
@@ -337,9 +350,9 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
             const float m_new = fmaxf(m_run, bm);
             const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
-            const uint16_t* Vs = reinterpret_cast<const uint16_t*>(Vb + off_s(B, 2));
-            const uint16_t* Vz = reinterpret_cast<const uint16_t*>(Vb + off_z(B, 2));
-            const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B, 2));
+            const uint16_t* Vs = reinterpret_cast<const uint16_t*>(Vb + off_s(B, BITS));
+            const uint16_t* Vz = reinterpret_cast<const uint16_t*>(Vb + off_z(B, BITS));
+            const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B, BITS));
             float pR[NSB][8], psum = 0.f, pmax = 0.f;
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
@@ -385,8 +398,8 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
             for (int sb = 0; sb < NSB; ++sb)
 #pragma unroll
                 for (int tt = 0; tt < 8; ++tt) pR[sb][tt] *= lam;
-            const float il4 = 4.0f / lam;
-            const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, 2));
+            const float il4 = kLevels / lam;
+            const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 
             // ---------------- PV, one 32-channel group at a time
 #pragma unroll
@@ -400,9 +413,14 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                     float sv[8], zv[8];
                     load8h(Vs + g * B + 32 * sb + 8 * tq, sv);
                     load8h(Vz + g * B + 32 * sb + 8 * tq, zv);
-                    const uint32_t* rec = reinterpret_cast<const uint32_t*>(Vb) + 8 * (32 * sb + lane);
-                    const uint32_t vw[2] = {rec[2 * g], rec[2 * g + 1]};
-                    const uint32_t vw8[2] = {vw[0] >> 8, vw[1] >> 8};
+                    // this group's record words: 2g + f/2 at 2 bits, 4g + f at 4 bits
+                    const uint32_t* rec = reinterpret_cast<const uint32_t*>(Vb) + RW * (32 * sb + lane);
+                    uint32_t vw[BITS], vw8[BITS];
+#pragma unroll
+                    for (int k = 0; k < BITS; ++k) {
+                        vw[k] = rec[BITS * g + k];
+                        vw8[k] = vw[k] >> 8;
+                    }
 #pragma unroll
                     for (int kt = 0; kt < 2; ++kt) {
                         // A: P'_g of tokens 32sb + 8tq + 4kt + {0, 1 | 2, 3}, hi row gq, lo row gq + 8
@@ -420,9 +438,14 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                         const uint32_t a1 = pack_h2(lo[0], lo[1]), a3 = pack_h2(lo[2], lo[3]);
 #pragma unroll
                         for (int f = 0; f < 4; ++f) {
-                            const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
-                            mma16816(Ob[f], a0, a1, a2, a3, code_pair(w, w8, 4 * kt + (f & 1)),
-                                     code_pair(w, w8, 4 * kt + 2 + (f & 1)));
+                            if (BITS == 2) {   // pair 4(d/4) + 2((d%4)/2) + f%2
+                                const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
+                                mma16816(Ob[f], a0, a1, a2, a3, code_pair(w, w8, 4 * kt + (f & 1)),
+                                         code_pair(w, w8, 4 * kt + 2 + (f & 1)));
+                            } else {           // field d/2
+                                mma16816(Ob[f], a0, a1, a2, a3, code_quad(vw[f], vw8[f], 2 * kt),
+                                         code_quad(vw[f], vw8[f], 2 * kt + 1));
+                            }
                         }
                     }
                 }
@@ -430,8 +453,8 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 Ssum += __shfl_xor_sync(kFull, Ssum, 2);
                 Zsum += __shfl_xor_sync(kFull, Zsum, 1);
                 Zsum += __shfl_xor_sync(kFull, Zsum, 2);
-                const float zq = 0.25f * Zsum - Ssum;
-                // O += 4 C_c / lam * (Ob + Z/4 - S): lane holds channels 32g + 8tq + f (column 2tq)
+                const float zq = Zsum * (1.0f / kLevels) - Ssum;
+                // O += 2^BITS C_c / lam * (Ob + Z/2^BITS - S): lane holds channels 32g + 8tq + f (column 2tq)
                 // and 32g + 8tq + 4 + f (column 2tq + 1)
                 float cf[8];
                 load8h(VC + 32 * g + 8 * tq, cf);
@@ -513,11 +536,15 @@ cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dt
     if (warps > 0x7fffffff) return cudaErrorInvalidValue;
     cudaError_t e;
     if (cfg.block_size == 32) {
-        e = launch_pdl(prefill_attn_kernel<32, prefill_stages<32>()>, (unsigned)warps, 32,
-                       prefill_smem_bytes<32>(), st, a);
+        e = cfg.bits == 4 ? launch_pdl(prefill_attn_kernel<32, 4, prefill_stages<32>()>, (unsigned)warps, 32,
+                                       prefill_smem_bytes<32, 4>(), st, a)
+                          : launch_pdl(prefill_attn_kernel<32, 2, prefill_stages<32>()>, (unsigned)warps, 32,
+                                       prefill_smem_bytes<32, 2>(), st, a);
     } else {
-        e = launch_pdl(prefill_attn_kernel<64, prefill_stages<64>()>, (unsigned)warps, 32,
-                       prefill_smem_bytes<64>(), st, a);
+        e = cfg.bits == 4 ? launch_pdl(prefill_attn_kernel<64, 4, prefill_stages<64>()>, (unsigned)warps, 32,
+                                       prefill_smem_bytes<64, 4>(), st, a)
+                          : launch_pdl(prefill_attn_kernel<64, 2, prefill_stages<64>()>, (unsigned)warps, 32,
+                                       prefill_smem_bytes<64, 2>(), st, a);
     }
     if (e != cudaSuccess) return e;
     a.batch = batch * chunk;
