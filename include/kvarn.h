@@ -240,12 +240,11 @@ int kvarn_decode_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, c
  * row with p < 0 (seq_lens[b] < chunk) gives zeros. out: device fp32
  * [batch][chunk][n_q][128]. chunk >= 1; chunk = 1 is kvarn_decode_attn.
  * workspace: at least kvarn_workspace_bytes(cfg, batch * chunk,
- * max_blocks_per_seq) bytes. One warp scores 8 query vectors (8 / G rows x
- * G heads) against each block, building each code's tensor-core operand
- * once for all 8. Device faults as kvarn_decode_attn.
- * (8 / G rows x G heads) against each block, building each code's
- * tensor-core operand once for all 8; 4-bit caches: every row runs the
- * decode kernel's split of its own. Device faults as kvarn_decode_attn.
+ * max_blocks_per_seq) bytes; kvarn_prefill_workspace_bytes gives the size
+ * with which short chunks split each sequence's blocks over enough warps.
+ * One warp scores 8 query vectors (8 / G rows x G heads) against each
+ * block, building each code's tensor-core operand once for all 8. Device
+ * faults as kvarn_decode_attn.
  */
 int kvarn_prefill_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const void* pool,
                        int64_t n_pool_blocks, const void* staging, const int32_t* block_table,
