@@ -47,7 +47,7 @@ def _cache(kv, B, bits, iters, n_q, n_kv, lens, seed):
     return cache, sb, g
 
 
-@pytest.mark.parametrize("B,bits,iters", [(32, 2, 3), (64, 2, 2), (32, 4, 3)])
+@pytest.mark.parametrize("B,bits,iters", [(32, 2, 3), (64, 2, 2), (32, 4, 3), (64, 4, 2)])
 @pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float32])
 def test_prefill_ragged_chunks_match_oracle(kvlib, B, bits, iters, qdtype):
     """A 40-row chunk over ragged sequences: rows inside complete blocks (the
@@ -85,7 +85,7 @@ def test_prefill_chunk_of_one_matches_decode(kvlib):
     attn_close(pre, ref)
 
 
-@pytest.mark.parametrize("G", [1, 3])
+@pytest.mark.parametrize("G", [1, 2, 3])
 def test_prefill_long_chunk_many_partials(kvlib, G):
     """2048-token sequences, a 96-row chunk: every row is split over several
     warps and merged, with the causal cut in the last visible block."""
