@@ -394,12 +394,47 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 if (smax > 0.f) k = min(k, 12 - ceil_log2(pmax * smax));
                 lam = exp2i(k);
             }
+            // P'' = p R lam per token as fp16 hi | lo pairs (tokens 8tq + 2k, + 1 of
+            // each sub-block): the A operand of the zero-point MMA, and the
+            // factor of every group's P' = P'' s two-product
+            uint32_t ph[NSB][4], pl[NSB][4];
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb)
 #pragma unroll
-                for (int tt = 0; tt < 8; ++tt) pR[sb][tt] *= lam;
+                for (int k = 0; k < 4; ++k) {
+                    const float v0 = pR[sb][2 * k] * lam, v1 = pR[sb][2 * k + 1] * lam;
+                    const __half2 hh = __floats2half2_rn(v0, v1);
+                    const float2 hf = __half22float2(hh);
+                    ph[sb][k] = h2_as_u32(hh);
+                    pl[sb][k] = pack_h2(v0 - hf.x, v1 - hf.y);
+                }
             const float il4 = kLevels / lam;
             const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
+
+            // ---------------- zero-point sums by MMA: A = P'' (hi rows, lo rows), B columns
+            // 0..3 = z of groups 0..3, 4..7 = s of groups 0..3, k = tokens
+            float Dz[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb) {
+                const uint16_t* src = (gq < 4 ? Vz : Vs) + (gq & 3) * B + 32 * sb + 8 * tq;
+                const uint4 zs4 = *reinterpret_cast<const uint4*>(src);
+                mma16816(Dz, ph[sb][0], pl[sb][0], ph[sb][1], pl[sb][1], zs4.x, zs4.y);
+                mma16816(Dz, ph[sb][2], pl[sb][2], ph[sb][3], pl[sb][3], zs4.z, zs4.w);
+            }
+            // this lane: columns 2tq, 2tq + 1 of vector gq (hi + lo rows): tq < 2 holds
+            // Z of groups 2tq, 2tq + 1, tq >= 2 holds S of groups 2tq - 4, 2tq - 3;
+            // zq[g] = Z_g / 2^BITS - S_g for the 4 lanes of vector gq
+            float zq[4];
+            {
+                const float c0 = Dz[0] + Dz[2], c1 = Dz[1] + Dz[3];
+                const float s0 = __shfl_xor_sync(kFull, c0, 2), s1 = __shfl_xor_sync(kFull, c1, 2);
+                const float zA = c0 * (1.0f / kLevels) - s0, zB = c1 * (1.0f / kLevels) - s1;   // valid at tq < 2
+                const int base = lane & ~3;
+                zq[0] = __shfl_sync(kFull, zA, base);
+                zq[1] = __shfl_sync(kFull, zB, base);
+                zq[2] = __shfl_sync(kFull, zA, base + 1);
+                zq[3] = __shfl_sync(kFull, zB, base + 1);
+            }
 
             // ---------------- PV, one 32-channel group at a time
 #pragma unroll
@@ -407,12 +442,21 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 float Ob[4][4];   // n-tile f: channels 32g + 4n + f
 #pragma unroll
                 for (int f = 0; f < 4; ++f) Ob[f][0] = Ob[f][1] = Ob[f][2] = Ob[f][3] = 0.f;
-                float Ssum = 0.f, Zsum = 0.f;
 #pragma unroll
                 for (int sb = 0; sb < NSB; ++sb) {
-                    float sv[8], zv[8];
-                    load8h(Vs + g * B + 32 * sb + 8 * tq, sv);
-                    load8h(Vz + g * B + 32 * sb + 8 * tq, zv);
+                    // P' = P'' s_g as fp16 hi | lo (two-product), tokens 8tq + 2k, + 1
+                    const uint4 s4 = *reinterpret_cast<const uint4*>(Vs + g * B + 32 * sb + 8 * tq);
+                    const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+                    uint32_t Ph[4], Pl[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __half2 s2 = u32_as_h2(sw[k]), hp = u32_as_h2(ph[sb][k]);
+                        const __half2 hi = __hmul2(hp, s2);
+                        __half2 lo = __hfma2(hp, s2, __hneg2(hi));
+                        lo = __hfma2(u32_as_h2(pl[sb][k]), s2, lo);
+                        Ph[k] = h2_as_u32(hi);
+                        Pl[k] = h2_as_u32(lo);
+                    }
                     // this group's record words: 2g + f/2 at 2 bits, 4g + f at 4 bits
                     const uint32_t* rec = reinterpret_cast<const uint32_t*>(Vb) + RW * (32 * sb + lane);
                     uint32_t vw[BITS], vw8[BITS];
@@ -423,19 +467,8 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                     }
 #pragma unroll
                     for (int kt = 0; kt < 2; ++kt) {
-                        // A: P'_g of tokens 32sb + 8tq + 4kt + {0, 1 | 2, 3}, hi row gq, lo row gq + 8
-                        float hi[4], lo[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int tt = 4 * kt + u;
-                            const float v = pR[sb][tt] * sv[tt];
-                            hi[u] = __half2float(__float2half_rn(v));
-                            lo[u] = __half2float(__float2half_rn(v - hi[u]));
-                            Ssum += hi[u] + lo[u];
-                            Zsum = fmaf(pR[sb][tt], zv[tt], Zsum);
-                        }
-                        const uint32_t a0 = pack_h2(hi[0], hi[1]), a2 = pack_h2(hi[2], hi[3]);
-                        const uint32_t a1 = pack_h2(lo[0], lo[1]), a3 = pack_h2(lo[2], lo[3]);
+                        // A: P' of tokens 8tq + 4kt + {0, 1 | 2, 3}, hi row gq, lo row gq + 8
+                        const uint32_t a0 = Ph[2 * kt], a1 = Pl[2 * kt], a2 = Ph[2 * kt + 1], a3 = Pl[2 * kt + 1];
 #pragma unroll
                         for (int f = 0; f < 4; ++f) {
                             if (BITS == 2) {   // pair 4(d/4) + 2((d%4)/2) + f%2
@@ -449,19 +482,14 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                         }
                     }
                 }
-                Ssum += __shfl_xor_sync(kFull, Ssum, 1);
-                Ssum += __shfl_xor_sync(kFull, Ssum, 2);
-                Zsum += __shfl_xor_sync(kFull, Zsum, 1);
-                Zsum += __shfl_xor_sync(kFull, Zsum, 2);
-                const float zq = Zsum * (1.0f / kLevels) - Ssum;
                 // O += 2^BITS C_c / lam * (Ob + Z/2^BITS - S): lane holds channels 32g + 8tq + f (column 2tq)
                 // and 32g + 8tq + 4 + f (column 2tq + 1)
                 float cf[8];
                 load8h(VC + 32 * g + 8 * tq, cf);
 #pragma unroll
                 for (int f = 0; f < 4; ++f) {
-                    O[g][f] = fmaf(cf[f] * il4, (Ob[f][0] + Ob[f][2]) + zq, O[g][f]);
-                    O[g][4 + f] = fmaf(cf[4 + f] * il4, (Ob[f][1] + Ob[f][3]) + zq, O[g][4 + f]);
+                    O[g][f] = fmaf(cf[f] * il4, (Ob[f][0] + Ob[f][2]) + zq[g], O[g][f]);
+                    O[g][4 + f] = fmaf(cf[4 + f] * il4, (Ob[f][1] + Ob[f][3]) + zq[g], O[g][4 + f]);
                 }
             }
         }
