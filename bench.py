@@ -113,9 +113,9 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record():
-    """ncu DRAM bytes per attention launch, valid only for the kernel source it
-    was captured from (profiles/attention_traffic.json)."""
+def _attention_record():
+    """profiles/attention_traffic.json (ncu counters of one attention launch on
+    the Qwen3-4B layer) if it was captured from the current kernel source."""
     path = os.path.join(ROOT, "profiles", "attention_traffic.json")
     if not os.path.exists(path):
         return None
@@ -123,9 +123,31 @@ def traffic_record():
     h = hashlib.sha256()
     for f in ("attention.cu", "attn_common.cuh", "split.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "bit_kv_cache_08_gb300", "csrc", f), "rb").read())
-    if rec.get("source_sha256") != h.hexdigest():
+    return rec if rec.get("source_sha256") == h.hexdigest() else None
+
+
+def traffic_record():
+    """ncu DRAM bytes per attention launch, valid only for the kernel source it
+    was captured from."""
+    rec = _attention_record()
+    return rec.get("bytes_per_launch") if rec else None
+
+
+def issue_context(attn_launch_ms, sm_mhz, sms):
+    """The attention kernel against the instruction-issue ceiling: warp
+    instructions of one split-K launch (ncu, current source only) over the
+    live split + merge time, against 4 issues per SM and cycle at the sampled
+    SM clock."""
+    rec = _attention_record()
+    n = rec.get("split_kernel", {}).get("warp_instr") if rec else None
+    if not n or not sm_mhz or not sms:
         return None
-    return rec.get("bytes_per_launch")
+    achieved = n / (attn_launch_ms * 1e-3)
+    peak = sms * 4 * sm_mhz * 1e6
+    return {"warp_instr_per_launch": int(n), "achieved_warp_instr_per_s": round(achieved / 1e12, 4),
+            "peak_warp_instr_per_s": round(peak / 1e12, 4), "unit": "T warp-instr/s",
+            "frac": round(achieved / peak, 4),
+            "note": "context for the HBM roofline: the kernel is bound by instruction issue"}
 
 
 class ClockSampler:
@@ -358,6 +380,8 @@ def run_gpu(args, rank, world):
         "gpu_launches": args.steps * layers * 3,
         "clocks": clocks,
     }
+    res["issue"] = issue_context(attn_launch_ms, clocks.get("sm_mhz") if isinstance(clocks, dict) else None,
+                                 torch.cuda.get_device_properties(device).multi_processor_count)
     return res, state, (kv, ws, pos, lens, out)
 
 

@@ -123,3 +123,23 @@ def test_prefill_bad_length_is_flagged(kvlib):
     q = synth.queries(g, 4, 4).reshape(1, 4, 4, D).cuda()
     got, err = _prefill(kv, cache, q, [cache.max_blocks * B + 1])
     assert err & kv.DEVERR_POSITION
+
+
+@pytest.mark.parametrize("flags,iters", [(oracle.NO_ROTATION, 3), (0, 0), (oracle.NO_TOKEN_PASS, 2)])
+def test_prefill_with_ablation_switches(kvlib, flags, iters):
+    """A cache written with an ablation switch is read with it: no rotation
+    (queries and output stay unrotated), Hadamard only, one VarN axis."""
+    kv = kvlib
+    B, n_q, n_kv = 32, 8, 2
+    lens = [300, 77]
+    sb = synth.sign_bits(70 + flags)
+    cfg = kv.make_config(n_q, n_kv, B, iters, sb, flags=flags)
+    g = synth.make_gen(71 + flags)
+    K = synth.kv_values(g, len(lens), n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    V = synth.kv_values(g, len(lens), n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    cache = PagedCache(kv, cfg, len(lens), (max(lens) + B - 1) // B + 1, perm_seed=flags)
+    cache.prefill(K, V, lens)
+    q = synth.queries(g, len(lens) * 12, n_q).reshape(len(lens), 12, n_q, D).cuda()
+    got, err = _prefill(kv, cache, q, lens)
+    assert err == 0
+    attn_close(got, _oracle(cache, q, lens, sb))
