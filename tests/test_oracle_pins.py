@@ -662,7 +662,8 @@ def test_prefill_chunk_of_one_is_decode_attention():
     assert np.array_equal(pre[:, 0], dec)
 
 
-def test_prefill_identical_keys_average_the_visible_values():
+@pytest.mark.parametrize("bits", [2, 4])
+def test_prefill_identical_keys_average_the_visible_values(bits):
     """All keys equal (zero keys: every score 0) -> each row is the plain mean
     of the values it may see: the first p + 1 tokens, decoded or raw."""
     B, n_q, n_kv, batch, chunk = 32, 2, 1, 2, 40
@@ -671,12 +672,13 @@ def test_prefill_identical_keys_average_the_visible_values():
     lens = [75, 30]                      # the second has rows at negative positions
     K = torch.zeros(batch, n_kv, 96, D, dtype=torch.bfloat16)
     V = synth.kv_values(g, batch, n_kv, 96, 1.0, 2, 10.0).to(torch.bfloat16)
-    pool, staging, bt = _paged_cache(B, n_kv, batch, lens, 3, K, V, sb)
+    pool, staging, bt = _paged_cache(B, n_kv, batch, lens, 3, K, V, sb, bits=bits)
     q = synth.queries(g, batch * chunk, n_q).double().numpy().reshape(batch, chunk, n_q, D)
-    out = oracle.prefill_attention(B, n_q, n_kv, sb, 0.3, q, pool, staging, bt, np.array(lens, np.int32))
+    out = oracle.prefill_attention(B, n_q, n_kv, sb, 0.3, q, pool, staging, bt, np.array(lens, np.int32),
+                                   bits=bits)
     for b in range(batch):
         nfull = lens[b] // B
-        rows = [oracle.decode_blocks(pool[bt[b, j], 0, 1], B, 1, sb, False)[0] for j in range(nfull)]
+        rows = [oracle.decode_blocks(pool[bt[b, j], 0, 1], B, 1, sb, False, bits=bits)[0] for j in range(nfull)]
         rows.append(V[b, 0, nfull * B:lens[b]].double().numpy())
         Vc = np.concatenate(rows)
         for r in range(chunk):
