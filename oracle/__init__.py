@@ -92,6 +92,7 @@ def lib():
                                                 _i32p, _i, _i32p, _i, _f64p]),
                 "orc_prefill_attention": (None, [_i, _i, ctypes.c_uint32, _i, _i, _u32p, _d, _f64p, _u8p, _u16p,
                                                  _i32p, _i, _i32p, _i, _i, _f64p]),
+                "orc_code_high_position": (None, [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
                 "orc_error_split": (None, [_f64p, _f64p, _f64p]),
                 "orc_error_decomposition": (None, [_i, _i, ctypes.c_uint32, _i, _u32p, _f64p, _u8p, _f64p]),
                 "orc_normalise": (None, [_i, _f64p, _f64p, _f64p, _f64p]),
@@ -242,6 +243,14 @@ def code_position(kind: int, t: int, c: int, bits: int = 2):
     w = ctypes.c_int32()
     b = ctypes.c_int32()
     lib().orc_code_position(kind, bits, t, c, ctypes.byref(w), ctypes.byref(b))
+    return w.value, b.value
+
+
+def code_high_position(kind: int, t: int, c: int):
+    """(word, bit) of the high bit of a 3-bit code (its low two bits sit at
+    code_position(kind, t, c, bits=3))."""
+    w, b = ctypes.c_int(), ctypes.c_int()
+    lib().orc_code_high_position(kind, t, c, ctypes.byref(w), ctypes.byref(b))
     return w.value, b.value
 
 

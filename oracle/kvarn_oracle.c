@@ -28,7 +28,7 @@
  *
  * Packed head-block format (the written contract both paths implement):
  *   B tokens x 128 channels, B in {32, 64}, 4 channel groups of 32, codes of
- *   `bits` in {2, 4} bits (X = 16 B bits bytes of codes):
+ *   `bits` in {2, 3, 4} bits (X = 16 B bits bytes of codes):
  *   bytes [0, X)            codes, records of 8*bits bytes (layout per kind)
  *   bytes [X, X+8B)         s  : fp16 [4][B]  (group-major)
  *   bytes [X+8B, X+16B)     z  : fp16 [4][B]
@@ -321,7 +321,7 @@ double orc_round_factor(double f)
 
 /* ------------------------------------------------------------------------ */
 /* Asymmetric round-to-nearest over 32-channel groups with L = 2^bits - 1     */
-/* steps (reading R-8, R-9; L = 3 for the method's 2 bits, 15 for the 4-bit  */
+/* steps (reading R-8, R-9; L = 3 for the method's 2 bits, 7 / 15 for 3 / 4-bit  */
 /* width). For the group's values with minimum m and maximum M:              */
 /*   z = largest fp16 <= m (clamped to +-65504)                              */
 /*   s = smallest fp16 >= 0 with z + L s >= M (clamped to 65504)             */
@@ -383,10 +383,54 @@ int orc_code(double y, double z16, double s16, int levels)
 /* per (group, channel) for V):                                              */
 /*   kind 0 (K): word 4i + g, bit 4*(e/2) + 16*(e%2)                         */
 /*   kind 1 (V): word 4g + f, bit 4*(d/2) + 16*(d%2)                         */
+/* 3 bits: words 0..7 of the record hold the low two bits of each code at    */
+/* its 2-bit position (word w2, bit 2j + 16h: pair j, half h, as above);     */
+/* words 8..11 hold the high bit at word 8 + w2/2, bit 8*(w2%2) + j + 16h.   */
+/* orc_code_position gives the low field's place, orc_code_high_position    */
+/* the high bit's.                                                           */
 /* ------------------------------------------------------------------------ */
+
+/* 2-bit layout within a record: word w2 (0..7), pair j (0..7), half h. */
+static void pair_position(int kind, int t, int c, int* w2, int* j, int* h)
+{
+    int g = c / ORC_GS;
+    if (kind == 0) {
+        int i = t % 4, e = c % 8;
+        *w2 = 2 * i + g / 2;
+        *j = 4 * (g % 2) + e / 2;
+        *h = e % 2;
+    } else {
+        int d = t % 8, f = c % 4;
+        *w2 = 2 * g + f / 2;
+        *j = 4 * (d / 4) + 2 * ((d % 4) / 2) + f % 2;
+        *h = d % 2;
+    }
+}
+
+static int record_of(int kind, int t, int c)
+{
+    int sb = t / 32;
+    if (kind == 0) return 32 * sb + 4 * ((t % 32) / 4) + (c % 32) / 8;
+    return 32 * sb + 4 * ((c % 32) / 4) + (t % 32) / 8;
+}
+
+void orc_code_high_position(int kind, int t, int c, int* word_index, int* bit)
+{
+    int w2, j, h;
+    pair_position(kind, t, c, &w2, &j, &h);
+    *word_index = record_of(kind, t, c) * 12 + 8 + w2 / 2;
+    *bit = 8 * (w2 % 2) + j + 16 * h;
+}
 
 void orc_code_position(int kind, int bits, int t, int c, int* word_index, int* bit)
 {
+    if (bits == 3) {
+        int w2, j, h;
+        pair_position(kind, t, c, &w2, &j, &h);
+        *word_index = record_of(kind, t, c) * 12 + w2;
+        *bit = 2 * j + 16 * h;
+        return;
+    }
     int sb = t / 32, g = c / ORC_GS;
     if (kind == 0) {
         int a = (t % 32) / 4, i = t % 4, b = (c % 32) / 8, e = c % 8;
@@ -431,8 +475,15 @@ void orc_pack(int B, int bits, int kind, const int32_t* codes, const double* s16
     for (int t = 0; t < B; t++)
         for (int c = 0; c < ORC_D; c++) {
             int w, bit;
+            const uint32_t code = (uint32_t)codes[t * ORC_D + c] & mask;
             orc_code_position(kind, bits, t, c, &w, &bit);
-            words[w] |= ((uint32_t)codes[t * ORC_D + c] & mask) << bit;
+            if (bits == 3) {
+                words[w] |= (code & 3u) << bit;
+                orc_code_high_position(kind, t, c, &w, &bit);
+                words[w] |= (code >> 2) << bit;
+            } else {
+                words[w] |= code << bit;
+            }
         }
     for (int w = 0; w < nwords; w++) {
         out[4 * w + 0] = (uint8_t)(words[w] & 0xFF);
@@ -465,7 +516,15 @@ void orc_unpack(int B, int bits, int kind, const uint8_t* in, int32_t* codes, do
             orc_code_position(kind, bits, t, c, &w, &bit);
             uint32_t word = (uint32_t)in[4 * w] | ((uint32_t)in[4 * w + 1] << 8) |
                             ((uint32_t)in[4 * w + 2] << 16) | ((uint32_t)in[4 * w + 3] << 24);
-            codes[t * ORC_D + c] = (int32_t)((word >> bit) & mask);
+            if (bits == 3) {
+                uint32_t code = (word >> bit) & 3u;
+                orc_code_high_position(kind, t, c, &w, &bit);
+                word = (uint32_t)in[4 * w] | ((uint32_t)in[4 * w + 1] << 8) |
+                       ((uint32_t)in[4 * w + 2] << 16) | ((uint32_t)in[4 * w + 3] << 24);
+                codes[t * ORC_D + c] = (int32_t)(code | (((word >> bit) & 1u) << 2));
+            } else {
+                codes[t * ORC_D + c] = (int32_t)((word >> bit) & mask);
+            }
         }
     const uint8_t* sp = in + codes_bytes(B, bits);
     const uint8_t* zp = sp + 8 * B;

@@ -709,3 +709,81 @@ def test_prefill_is_causal():
     r0 = p0 - (L - chunk)
     assert np.array_equal(moved[0, :r0], base[0, :r0])
     assert np.all(np.abs(moved[0, r0:] - base[0, r0:]).max(axis=(1, 2)) > 1e-3)
+
+
+# ---------------------------------------------------------------- 3-bit width (2-bit plane + 1-bit plane)
+
+def test_pack_3bit_matches_hand_derived_bytes():
+    gold = _golden()
+    B = 32
+    s, z = np.ones((B, 4)), -2.0 * np.ones((B, 4))
+    R, C = 0.5 * np.ones(B), 2.0 * np.ones(D)
+    kcodes = np.tile(np.arange(D) % 8, (B, 1))
+    vcodes = np.tile((np.arange(B) % 8)[:, None], (1, D))
+    kb = oracle.pack(B, oracle.KIND_K, kcodes, s, z, R, C, bits=3)
+    vb = oracle.pack(B, oracle.KIND_V, vcodes, s, z, R, C, bits=3)
+    for key, buf in (("K3 c%8", kb), ("V3 t%8", vb)):
+        lo = bytes.fromhex(gold[f"{key} low word"].replace(" ", ""))
+        hi = bytes.fromhex(gold[f"{key} high word"].replace(" ", ""))
+        for rec in range(32):
+            assert buf[48 * rec:48 * rec + 48].tobytes() == lo * 8 + hi * 4
+    offs = dict(zip(*[iter(gold["section offsets 3-bit B=32"].split())] * 2))
+    assert kb[int(offs["s"]):int(offs["s"]) + 2].tobytes().hex(" ") == gold["s bytes"]
+    assert kb[int(offs["R"]):int(offs["R"]) + 2].tobytes().hex(" ") == gold["R bytes"]
+    assert len(kb) == int(offs["total"]) == oracle.head_block_bytes(32, 3)
+    offs64 = dict(zip(*[iter(gold["section offsets 3-bit B=64"].split())] * 2))
+    assert oracle.head_block_bytes(64, 3) == int(offs64["total"])
+
+
+def test_3bit_positions_cover_every_bit_once_and_pack_round_trips():
+    for B in (32, 64):
+        for kind in (0, 1):
+            used = set()
+            for t in range(B):
+                for c in range(D):
+                    w, b = oracle.code_position(kind, t, c, bits=3)
+                    wh, bh = oracle.code_high_position(kind, t, c)
+                    assert w % 12 < 8 and b % 2 == 0 and wh % 12 >= 8 and w // 12 == wh // 12
+                    for bit in ((w, b), (w, b + 1), (wh, bh)):
+                        assert bit not in used
+                        used.add(bit)
+            assert len(used) == 32 * 4 * B * 3          # every bit of the code section
+            rng = np.random.default_rng(50 + B + kind)
+            codes = rng.integers(0, 8, (B, D))
+            f16 = lambda a: a.astype(np.float16).astype(np.float64)
+            s, z = f16(np.abs(rng.standard_normal((B, 4)))), f16(rng.standard_normal((B, 4)))
+            R, C = f16(np.abs(rng.standard_normal(B)) + 1), f16(np.abs(rng.standard_normal(D)) + 1)
+            f = oracle.unpack(B, kind, oracle.pack(B, kind, codes, s, z, R, C, bits=3), bits=3)
+            assert np.array_equal(f["codes"], codes)
+            assert np.array_equal(f["z16"], z) and np.array_equal(f["C16"], C)
+
+
+def test_3bit_group_params_and_codes_are_brute_force():
+    grid = _all_f16_nonneg()
+    full = np.concatenate([-grid[::-1], grid])
+    rng = np.random.default_rng(51)
+    for _ in range(40):
+        y = rng.standard_normal(32) * np.exp(rng.uniform(-6, 6)) + rng.uniform(-3, 3)
+        z, s, m, M = oracle.group_params(y, bits=3)
+        assert z == full[full <= m].max()
+        assert s == grid[z + 7.0 * grid >= M].min()           # 7 steps cover the group
+        lv = z + s * np.arange(8)
+        for v in y:
+            d = np.abs(v - lv)
+            want = np.flatnonzero(d == d.min())
+            want = want[0] if len(want) == 1 else [k for k in want if k % 2 == 0][0]
+            assert oracle.code(v, z, s, bits=3) == want
+
+
+def test_3bit_block_is_within_half_step_between_2_and_4_bits():
+    sb = synth.sign_bits(52)
+    X = _block(52, 32)
+    errs = {}
+    for bits in (2, 3, 4):
+        r = oracle.quantize_block(X, 3, oracle.KIND_V, sb, bits=bits)
+        rot = oracle.decode_blocks(r["bytes"], 32, 1, sb, rotated=True, bits=bits)[0]
+        bound = (r["s16"].repeat(32, axis=1) / 2) * r["R16"][:, None] * r["C16"][None, :]
+        assert np.all(np.abs(rot - r["Xr"]) <= bound * (1 + 1e-9) + 1e-300)
+        assert r["codes"].max() <= (1 << bits) - 1
+        errs[bits] = np.linalg.norm(rot - r["Xr"])
+    assert errs[4] < errs[3] < errs[2]
