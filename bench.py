@@ -49,7 +49,7 @@ def parse():
                         "(batch 16 x 4096 cached tokens) for several chunk lengths, one JSON line each")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
-                        "lengths), 2-bit and 4-bit vs bf16-cache decode attention, one JSON line per point")
+                        "lengths), 2-, 3- and 4-bit vs bf16-cache decode attention, one JSON line per point")
     return p.parse_args()
 
 
@@ -627,7 +627,7 @@ def run_sweep(args):
             reps = 5 if big else 30
             full = (lens // B) * B
             packed = {}
-            for bits in (2, 4):
+            for bits in (2, 3, 4):
                 cfg = kv.make_config(n_q, n_kv, B, w.iters, synth.sign_bits(w.seed), bits=bits)
                 ws = kv.alloc_workspace(cfg, batch, max_blocks, dev)
                 # packed cache: valid head-blocks (512 quantised K and V tiles repeated)
@@ -653,6 +653,7 @@ def run_sweep(args):
                 del pool, staging
                 torch.cuda.empty_cache()
             ms2, b2 = packed[2]
+            ms3, b3 = packed[3]
             ms4, b4 = packed[4]
             cfg = kv.make_config(n_q, n_kv, B, w.iters, synth.sign_bits(w.seed))
             ws = kv.alloc_workspace(cfg, batch, max_blocks, dev)
@@ -668,11 +669,14 @@ def run_sweep(args):
                               "timing": "CUDA events, median of launches each queued behind a 1 GiB L2-flushing write",
                               "2bit": {"us": round(ms2 * 1e3, 2), "GB_per_s": round(b2 / ms2 / 1e6, 1),
                                        "tokens_per_s": round(batch / ms2 * 1e3, 1), "bytes": int(b2)},
+                              "3bit": {"us": round(ms3 * 1e3, 2), "GB_per_s": round(b3 / ms3 / 1e6, 1),
+                                       "tokens_per_s": round(batch / ms3 * 1e3, 1), "bytes": int(b3)},
                               "4bit": {"us": round(ms4 * 1e3, 2), "GB_per_s": round(b4 / ms4 / 1e6, 1),
                                        "tokens_per_s": round(batch / ms4 * 1e3, 1), "bytes": int(b4)},
                               "bf16": {"us": round(ms16 * 1e3, 2), "GB_per_s": round(b16 / ms16 / 1e6, 1),
                                        "tokens_per_s": round(batch / ms16 * 1e3, 1), "bytes": int(b16)},
                               "speedup_2bit_vs_bf16": round(ms16 / ms2, 2),
+                              "speedup_3bit_vs_bf16": round(ms16 / ms3, 2),
                               "speedup_4bit_vs_bf16": round(ms16 / ms4, 2)}), flush=True)
 
 
@@ -738,6 +742,7 @@ ABLATIONS = (  # (name, flags, iters, bits): the pages' ablation list, plus the 
     ("varn token axis only", 4, 3, 2),
     ("varn channel axis only", 2, 3, 2),
     ("plain group 2-bit", 1, 0, 2),
+    ("kvarn 3-bit", 0, 3, 3),
     ("kvarn 4-bit", 0, 3, 4),
     ("plain group 4-bit", 1, 0, 4),
 )

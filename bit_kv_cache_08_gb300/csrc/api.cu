@@ -44,7 +44,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Validates cfg and returns a copy with defaults applied (sm_scale).
 int check_config(const kvarn_config* cfg, kvarn_config* out) {
     if (!cfg) return KVARN_ERR_INVALID_ARG;
-    if (cfg->head_dim != 128 || cfg->group_size != 32 || (cfg->bits != 2 && cfg->bits != 4))
+    if (cfg->head_dim != 128 || cfg->group_size != 32 || (cfg->bits < 2 || cfg->bits > 4))
         return KVARN_ERR_UNSUPPORTED;
     if (cfg->block_size != 32 && cfg->block_size != 64) return KVARN_ERR_UNSUPPORTED;
     if (cfg->varn_iters < 0 || cfg->varn_iters > 8) return KVARN_ERR_INVALID_ARG;

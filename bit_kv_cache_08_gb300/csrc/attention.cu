@@ -57,7 +57,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // ---------------------------------------------------------------- the split-K kernel
 template <int B, int BITS, int S>
 __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
-    static_assert(BITS == 2 || BITS == 4, "2- or 4-bit codes");
+    static_assert(BITS >= 2 && BITS <= 4, "2-, 3- or 4-bit codes");
     wait_prior_grids();
     constexpr int HB = head_block_bytes(B, BITS);
     constexpr int RW = 4 * BITS;             // 32-bit words per lane record
@@ -306,6 +306,14 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                                 a1 = code_pair(kw[i1], kw8[i1], j);
                                 a2 = code_pair(kw[i0], kw8[i0], j + 1);
                                 a3 = code_pair(kw[i1], kw8[i1], j + 1);
+                            } else if (BITS == 3) {   // 2-bit word 2i + g/2; high bits in word 8 + i
+                                const int j = 4 * (g & 1) + 2 * kk, jh = 8 * (g >> 1) + j;
+                                const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
+                                const int h0 = 8 + 2 * mt, h1 = 8 + 2 * mt + 1;
+                                a0 = code_triple(kw[i0], kw8[i0], kw[h0], kw8[h0], j, jh);
+                                a1 = code_triple(kw[i1], kw8[i1], kw[h1], kw8[h1], j, jh);
+                                a2 = code_triple(kw[i0], kw8[i0], kw[h0], kw8[h0], j + 1, jh + 1);
+                                a3 = code_triple(kw[i1], kw8[i1], kw[h1], kw8[h1], j + 1, jh + 1);
                             } else {           // word 4i + g, field e/2
                                 const int j = 2 * kk;
                                 const int i0 = 4 * (2 * mt) + g, i1 = 4 * (2 * mt + 1) + g;
@@ -481,6 +489,16 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                             mma16816(Ob[mt], code_pair(wd, wd8, 4 * kt + 0), code_pair(wd, wd8, 4 * kt + 1),
                                      code_pair(wd, wd8, 4 * kt + 2), code_pair(wd, wd8, 4 * kt + 3),
                                      bv[g][2 * kt], bv[g][2 * kt + 1]);
+                    } else if (BITS == 3) {   // 2-bit word 2g + f/2; high bits in word 8 + g, bit 8(f/2) + j
+                        const int wl = 2 * g + m, wh = 8 + g;
+#pragma unroll
+                        for (int kt = 0; kt < 2; ++kt)
+                            mma16816(Ob[mt],
+                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 0, 8 * m + 4 * kt + 0),
+                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 1, 8 * m + 4 * kt + 1),
+                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 2, 8 * m + 4 * kt + 2),
+                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 3, 8 * m + 4 * kt + 3),
+                                     bv[g][2 * kt], bv[g][2 * kt + 1]);
                     } else {           // word 4g + f, field d/2
                         const int w0 = 4 * g + 2 * m, w1 = w0 + 1;
 #pragma unroll
@@ -567,15 +585,16 @@ struct AttnKernel {
 
 template <typename F>
 auto with_attn_kernel(int block_size, int bits, F&& f) {
-    if (block_size == 32) return bits == 4 ? f(AttnKernel<32, 4>{}) : f(AttnKernel<32, 2>{});
-    return bits == 4 ? f(AttnKernel<64, 4>{}) : f(AttnKernel<64, 2>{});
+    if (block_size == 32)
+        return bits == 4 ? f(AttnKernel<32, 4>{}) : (bits == 3 ? f(AttnKernel<32, 3>{}) : f(AttnKernel<32, 2>{}));
+    return bits == 4 ? f(AttnKernel<64, 4>{}) : (bits == 3 ? f(AttnKernel<64, 3>{}) : f(AttnKernel<64, 2>{}));
 }
 
 // Resident warps of the split-K kernel for (block size, code width) on
 // `device` (cached per device).
 int attn_grid_warps(int block_size, int bits, int device) {
-    static int cache[2][2][64];
-    const int bi = block_size == 32 ? 0 : 1, wi = bits == 4 ? 1 : 0;
+    static int cache[2][3][64];
+    const int bi = block_size == 32 ? 0 : 1, wi = bits - 2;
     if (device < 0 || device >= 64) return 0;
     if (cache[bi][wi][device] > 0) return cache[bi][wi][device];
     int sms = 0, per_sm = 0;

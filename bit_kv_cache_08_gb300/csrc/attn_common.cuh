@@ -63,6 +63,17 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int j) {
     const uint32_t x = (j < 4) ? w * (1u << (8 - 2 * j)) : (j == 4 ? w : w8 * (1u << (16 - 2 * j)));
     return (x & 0x03000300u) | 0x3C003C00u;
 }
+// The 3-bit analogue: the low two bits of a pair from its 2-bit word w (pair
+// j, w8 = w >> 8) moved to fraction bits 7..8, the high bit from the 1-bit
+// plane word hw (bit jh of each half, hw8 = hw >> 8 for jh >= 8) moved to
+// bit 9, or-ed with 1.0: the exact fp16x2 (1 + code_lo/8, 1 + code_hi/8).
+__device__ __forceinline__ uint32_t code_triple(uint32_t w, uint32_t w8, uint32_t hw, uint32_t hw8, int j,
+                                                int jh) {
+    const uint32_t x2 = (j < 4) ? w * (1u << (7 - 2 * j)) : w8 * (1u << (15 - 2 * j));
+    const uint32_t x1 = (jh < 8) ? hw * (1u << (9 - jh)) : hw8 * (1u << (17 - jh));
+    return (x2 & 0x01800180u) | ((x1 & 0x02000200u) | 0x3C003C00u);
+}
+
 // The 4-bit analogue: field j (0..3) of each half of w (bits 4j..4j+3 and
 // 16+4j..) moved to fp16 mantissa bits 6..9 and or-ed with 1.0, giving the
 // exact fp16x2 (1 + code_lo/16, 1 + code_hi/16); w8 = w >> 8 as above.

@@ -63,7 +63,7 @@ extern "C" int kvarn_decode_attn_noalloc(const kvarn_config* cfg, const void* q,
                                          const int32_t* seq_lens, int32_t batch, float* out,
                                          uint32_t* error_word, void* stream) {
     if (!cfg) return KVARN_ERR_INVALID_ARG;
-    if (cfg->head_dim != 128 || cfg->group_size != 32 || (cfg->bits != 2 && cfg->bits != 4) ||
+    if (cfg->head_dim != 128 || cfg->group_size != 32 || (cfg->bits < 2 || cfg->bits > 4) ||
         (cfg->block_size != 32 && cfg->block_size != 64))
         return KVARN_ERR_UNSUPPORTED;
     if (cfg->varn_iters < 0 || cfg->varn_iters > 8 || cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads ||

@@ -28,8 +28,9 @@
 // copies (lane 0) counted on mbarriers with bounded waits. Each vector's
 // (max, sum, 128 rotated accumulators) goes to one workspace partial; the
 // merge kernel adds the raw bf16 tail rows, rotates back once and
-// normalises. 4-bit codes take the same path with 64-byte records and
-// a = 1 + code/16 (every factor 4 above becomes 16).
+// normalises. 3- and 4-bit codes take the same path with 48- and 64-byte
+// records and a = 1 + code/8 or 1 + code/16 (every factor 4 above becomes 8
+// or 16).
 #include <algorithm>
 
 #include "attn_common.cuh"
@@ -80,7 +81,7 @@ constexpr size_t prefill_smem_bytes() {
 
 template <int B, int BITS, int S>
 __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
-    static_assert(BITS == 2 || BITS == 4, "2- or 4-bit codes");
+    static_assert(BITS >= 2 && BITS <= 4, "2-, 3- or 4-bit codes");
     wait_prior_grids();
     constexpr int HB = head_block_bytes(B, BITS);
     constexpr int NSB = B / 32;
@@ -303,6 +304,11 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                                 const int wi = 2 * i + (g >> 1), jj = 4 * (g & 1) + 2 * kk;
                                 b0 = code_pair(kw[wi], kw8[wi], jj);
                                 b1 = code_pair(kw[wi], kw8[wi], jj + 1);
+                            } else if (BITS == 3) {   // + the high bit: word 8 + i, bit 8(g/2) + pair
+                                const int wi = 2 * i + (g >> 1), jj = 4 * (g & 1) + 2 * kk, wh = 8 + i;
+                                const int jh = 8 * (g >> 1) + jj;
+                                b0 = code_triple(kw[wi], kw8[wi], kw[wh], kw8[wh], jj, jh);
+                                b1 = code_triple(kw[wi], kw8[wi], kw[wh], kw8[wh], jj + 1, jh + 1);
                             } else {           // word 4i + g, field e/2
                                 const int wi = 4 * i + g;
                                 b0 = code_quad(kw[wi], kw8[wi], 2 * kk);
@@ -457,12 +463,14 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                         Ph[k] = h2_as_u32(hi);
                         Pl[k] = h2_as_u32(lo);
                     }
-                    // this group's record words: 2g + f/2 at 2 bits, 4g + f at 4 bits
+                    // this group's record words: 2g + f/2 at 2 bits (and the high-bit
+                    // word 8 + g at 3 bits), 4g + f at 4 bits
                     const uint32_t* rec = reinterpret_cast<const uint32_t*>(Vb) + RW * (32 * sb + lane);
-                    uint32_t vw[BITS], vw8[BITS];
+                    constexpr int NV = BITS == 4 ? 4 : 3;
+                    uint32_t vw[NV], vw8[NV];
 #pragma unroll
-                    for (int k = 0; k < BITS; ++k) {
-                        vw[k] = rec[BITS * g + k];
+                    for (int k = 0; k < NV; ++k) {
+                        vw[k] = BITS == 4 ? rec[4 * g + k] : (k < 2 ? rec[2 * g + k] : rec[8 + g]);
                         vw8[k] = vw[k] >> 8;
                     }
 #pragma unroll
@@ -475,6 +483,11 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                                 const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
                                 mma16816(Ob[f], a0, a1, a2, a3, code_pair(w, w8, 4 * kt + (f & 1)),
                                          code_pair(w, w8, 4 * kt + 2 + (f & 1)));
+                            } else if (BITS == 3) {   // + the high bit at 8(f/2) + pair in word 8 + g
+                                const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
+                                const int j0 = 4 * kt + (f & 1), j1 = j0 + 2, hb = 8 * (f >> 1);
+                                mma16816(Ob[f], a0, a1, a2, a3, code_triple(w, w8, vw[2], vw8[2], j0, hb + j0),
+                                         code_triple(w, w8, vw[2], vw8[2], j1, hb + j1));
                             } else {           // field d/2
                                 mma16816(Ob[f], a0, a1, a2, a3, code_quad(vw[f], vw8[f], 2 * kt),
                                          code_quad(vw[f], vw8[f], 2 * kt + 1));
@@ -563,16 +576,15 @@ cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dt
     const int64_t warps = units * a.single;
     if (warps > 0x7fffffff) return cudaErrorInvalidValue;
     cudaError_t e;
+    auto go = [&](auto kernel, size_t smem) { return launch_pdl(kernel, (unsigned)warps, 32, smem, st, a); };
     if (cfg.block_size == 32) {
-        e = cfg.bits == 4 ? launch_pdl(prefill_attn_kernel<32, 4, prefill_stages<32>()>, (unsigned)warps, 32,
-                                       prefill_smem_bytes<32, 4>(), st, a)
-                          : launch_pdl(prefill_attn_kernel<32, 2, prefill_stages<32>()>, (unsigned)warps, 32,
-                                       prefill_smem_bytes<32, 2>(), st, a);
+        e = cfg.bits == 4   ? go(prefill_attn_kernel<32, 4, prefill_stages<32>()>, prefill_smem_bytes<32, 4>())
+            : cfg.bits == 3 ? go(prefill_attn_kernel<32, 3, prefill_stages<32>()>, prefill_smem_bytes<32, 3>())
+                            : go(prefill_attn_kernel<32, 2, prefill_stages<32>()>, prefill_smem_bytes<32, 2>());
     } else {
-        e = cfg.bits == 4 ? launch_pdl(prefill_attn_kernel<64, 4, prefill_stages<64>()>, (unsigned)warps, 32,
-                                       prefill_smem_bytes<64, 4>(), st, a)
-                          : launch_pdl(prefill_attn_kernel<64, 2, prefill_stages<64>()>, (unsigned)warps, 32,
-                                       prefill_smem_bytes<64, 2>(), st, a);
+        e = cfg.bits == 4   ? go(prefill_attn_kernel<64, 4, prefill_stages<64>()>, prefill_smem_bytes<64, 4>())
+            : cfg.bits == 3 ? go(prefill_attn_kernel<64, 3, prefill_stages<64>()>, prefill_smem_bytes<64, 3>())
+                            : go(prefill_attn_kernel<64, 2, prefill_stages<64>()>, prefill_smem_bytes<64, 2>());
     }
     if (e != cudaSuccess) return e;
     a.batch = batch * chunk;

@@ -116,11 +116,11 @@ __device__ __forceinline__ bool usable_variance(float v, float mu) {
 // (all exact comparisons).
 template <int L>
 __device__ __forceinline__ float step_for(float zf, float M) {
-    static_assert(L == 3 || L == 15, "2- or 4-bit codes");
+    static_assert(L == 3 || L == 7 || L == 15, "2-, 3- or 4-bit codes");
     if (zf >= M) return 0.0f;
     // >= exact (M - z)/L: every step rounds up; RU(1/3) = 0x1.555556p-2f,
-    // RU(1/15) = 0x1.111112p-4f
-    constexpr float kInvL = L == 3 ? 0x1.555556p-2f : 0x1.111112p-4f;
+    // RU(1/7) = 0x1.24924ap-3f, RU(1/15) = 0x1.111112p-4f
+    constexpr float kInvL = L == 3 ? 0x1.555556p-2f : (L == 7 ? 0x1.24924ap-3f : 0x1.111112p-4f);
     float t = __fmul_ru(__fsub_ru(M, zf), kInvL);
     __half s = __float2half_ru(t);                         // >= exact minimum
     float sf = __half2float(s);
@@ -256,14 +256,14 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
             for (int k = 0; k < 4; ++k)
                 code[k] = (uint32_t)(yq[k] > b0) + (uint32_t)(yq[k] >= b1) + (uint32_t)(yq[k] > b2);
         } else {
-            // binary search over the 15 boundaries z + (c - 1/2) s (each one fma,
-            // rounded once like the 2-bit ones); a tie goes to the even level, so
-            // the candidate steps 8, 4, 2 (even candidates) test >=, step 1 tests >
+            // binary search over the 2^BITS - 1 boundaries z + (c - 1/2) s (each one
+            // fma, rounded once like the 2-bit ones); a tie goes to the even level,
+            // so the candidate steps above 1 (even candidates) test >=, step 1 tests >
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 uint32_t c = 0;
 #pragma unroll
-                for (int st = 8; st >= 1; st >>= 1) {
+                for (int st = 1 << (BITS - 1); st >= 1; st >>= 1) {
                     const float b = fmaf((float)(c + st) - 0.5f, sf, zf);
                     const bool up = (st == 1) ? (yq[k] > b) : (yq[k] >= b);
                     c = up ? c + st : c;
@@ -273,7 +273,35 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
         }
         // ---- pack into the record order of this kind
         const int sb = t >> 5;
-        if (BITS == 4) {
+        if (BITS == 3) {
+            // low two bits at the 2-bit positions of a 12-word record, the high bit
+            // in the record's 1-bit plane: word 8 + w2/2, bit 8(w2%2) + j + 16h
+            if (p.kind == KVARN_KIND_K) {   // w2 = 2i + g/2, j = 4(g%2) + e/2, h = e%2
+                const int a = (t & 31) >> 2, ii = t & 3, bq = (lane & 7) >> 1, eh = lane & 1;
+                const int rec = 32 * sb + 4 * a + bq;
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = 4 * eh + k, j = 4 * (g & 1) + (e >> 1), h = e & 1;
+                    lo |= (code[k] & 3u) << (2 * j + 16 * h);
+                    hi |= (code[k] >> 2) << (8 * (g >> 1) + j + 16 * h);
+                }
+                atomicOr(&words[rec * 12 + 2 * ii + (g >> 1)], lo);
+                atomicOr(&words[rec * 12 + 8 + ii], hi);
+            } else {                        // w2 = 2g + f/2, j = 4(d/4) + 2((d%4)/2) + f%2, h = d%2
+                const int a = lane & 7, bq = (t & 31) >> 3, d = t & 7;
+                const int rec = 32 * sb + 4 * a + bq;
+                const int jb = 4 * (d >> 2) + 2 * ((d & 3) >> 1), h = d & 1;
+                uint32_t hi = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) hi |= (code[k] >> 2) << (8 * (k >> 1) + jb + (k & 1) + 16 * h);
+                atomicOr(&words[rec * 12 + 2 * g + 0],
+                         ((code[0] & 3u) << (2 * jb + 16 * h)) | ((code[1] & 3u) << (2 * jb + 2 + 16 * h)));
+                atomicOr(&words[rec * 12 + 2 * g + 1],
+                         ((code[2] & 3u) << (2 * jb + 16 * h)) | ((code[3] & 3u) << (2 * jb + 2 + 16 * h)));
+                atomicOr(&words[rec * 12 + 8 + g], hi);
+            }
+        } else if (BITS == 4) {
             if (p.kind == KVARN_KIND_K) {   // word 4i + g, bit 4(e/2) + 16(e%2)
                 const int a = (t & 31) >> 2, ii = t & 3, bq = (lane & 7) >> 1, eh = lane & 1;
                 uint32_t contrib = 0;
@@ -433,6 +461,26 @@ __device__ __forceinline__ void dequant_row4(const uint8_t* img, int kind, int t
     for (int k = 0; k < 4; ++k) {
         const int c = 4 * lane + k;
         int word, bit;
+        if (BITS == 3) {   // low two bits in the 2-bit layout, the high bit in the 1-bit plane
+            int rec, w2, j, h;
+            if (kind == KVARN_KIND_K) {
+                const int a = (t & 31) >> 2, ii = t & 3, bq = (c & 31) >> 3, e = c & 7;
+                rec = 32 * sb + 4 * a + bq;
+                w2 = 2 * ii + (g >> 1);
+                j = 4 * (g & 1) + (e >> 1);
+                h = e & 1;
+            } else {
+                const int bq = (t & 31) >> 3, d = t & 7, a = (c & 31) >> 2, f = c & 3;
+                rec = 32 * sb + 4 * a + bq;
+                w2 = 2 * g + (f >> 1);
+                j = 4 * (d >> 2) + 2 * ((d & 3) >> 1) + (f & 1);
+                h = d & 1;
+            }
+            const uint32_t lo = (words[rec * 12 + w2] >> (2 * j + 16 * h)) & 3u;
+            const uint32_t hb = (words[rec * 12 + 8 + (w2 >> 1)] >> (8 * (w2 & 1) + j + 16 * h)) & 1u;
+            v[k] = fmaf((float)(lo | (hb << 2)), s, z) * R * h2f(C_sec[c]);
+            continue;
+        }
         if (kind == KVARN_KIND_K) {
             const int a = (t & 31) >> 2, ii = t & 3, bq = (c & 31) >> 3, e = c & 7;
             if (BITS == 4) {
@@ -553,8 +601,9 @@ static QuantParams make_params(const kvarn_config& cfg, int kind) {
 template <int V> struct ic { static constexpr int value = V; };
 template <typename F>
 cudaError_t dispatch(const kvarn_config& cfg, F&& f) {
-    if (cfg.block_size == 32) return cfg.bits == 4 ? f(ic<32>{}, ic<4>{}) : f(ic<32>{}, ic<2>{});
-    return cfg.bits == 4 ? f(ic<64>{}, ic<4>{}) : f(ic<64>{}, ic<2>{});
+    if (cfg.block_size == 32)
+        return cfg.bits == 4 ? f(ic<32>{}, ic<4>{}) : (cfg.bits == 3 ? f(ic<32>{}, ic<3>{}) : f(ic<32>{}, ic<2>{}));
+    return cfg.bits == 4 ? f(ic<64>{}, ic<4>{}) : (cfg.bits == 3 ? f(ic<64>{}, ic<3>{}) : f(ic<64>{}, ic<2>{}));
 }
 
 cudaError_t launch_quantize_blocks(const kvarn_config& cfg, int kind, const void* src, int dtype,

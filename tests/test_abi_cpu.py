@@ -45,15 +45,17 @@ def test_prefill_workspace_query_without_a_device():
     assert kv.prefill_workspace_bytes(c, -1, 4, 4) == 0
 
 
-def test_four_bit_sizes_match_the_oracle_format():
-    """4-bit codes: records of 64 bytes, then the same s, z, R, C sections."""
+def test_wide_code_sizes_match_the_oracle_format():
+    """3- and 4-bit codes: records of 48 / 64 bytes, then the same s, z, R, C sections."""
     for B in (32, 64):
-        c = _cfg(block_size=B, bits=4)
-        assert kv.head_block_bytes(c) == 82 * B + 256 == oracle.head_block_bytes(B, bits=4)
-        assert kv.block_bytes(c) == 8 * 2 * (82 * B + 256)
+        for bits in (3, 4):
+            c = _cfg(block_size=B, bits=bits)
+            hb = (16 * bits + 18) * B + 256
+            assert kv.head_block_bytes(c) == hb == oracle.head_block_bytes(B, bits=bits)
+            assert kv.block_bytes(c) == 8 * 2 * hb
 
 
-@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 16), ("bits", 3),
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("block_size", 16), ("bits", 5),
                                          ("bits", 1), ("bits", 8),
                                          ("group_size", 64), ("n_q_heads", 48)])
 def test_unsupported_configs_are_rejected(field, value):

@@ -1,6 +1,7 @@
-"""The 4-bit code width on the GPU against the fp64 oracle: bulk quantise
-(staged hand-off), dequantise, quantise-on-append, the error split and split-K
-decode attention over a ragged paged cache, each over the GPU's own bytes."""
+"""The 3- and 4-bit code widths on the GPU against the fp64 oracle: bulk
+quantise (staged hand-off), dequantise, quantise-on-append, the error split
+and split-K decode attention over a ragged paged cache, each over the GPU's
+own bytes."""
 import zlib
 from collections import Counter
 
@@ -14,7 +15,11 @@ from kvtest_util import PagedCache, assert_code_flip_rate, attn_close, oracle_at
 
 pytestmark = pytest.mark.gpu
 D = 128
-BITS = 4
+
+
+@pytest.fixture(params=[3, 4], ids=["3bit", "4bit"])
+def BITS(request):
+    return request.param
 
 
 def _quantize(kv, cfg, kind, x):
@@ -31,7 +36,7 @@ def _quantize(kv, cfg, kind, x):
     ("b32-bf16", 32, 3, "bf16", 128),
     ("b64-bf16", 64, 2, "bf16", 64),
 ])
-def test_quantize_matches_oracle_staged(kvlib, name, B, iters, dtype, n):
+def test_quantize_matches_oracle_staged(kvlib, name, B, iters, dtype, n, BITS):
     kv = kvlib
     sb = synth.sign_bits(B + 40)
     cfg = kv.make_config(4, 1, B, iters, sb, bits=BITS)
@@ -47,11 +52,11 @@ def test_quantize_matches_oracle_staged(kvlib, name, B, iters, dtype, n):
         st = staged_quantize_parity(X, got, B, iters, kind, sb, bits=BITS)
         print(name, kind, dict(st))
         total.update(st)
-        assert int(oracle.unpack(B, kind, got[0], bits=BITS)["codes"].max()) <= 15
+        assert int(oracle.unpack(B, kind, got[0], bits=BITS)["codes"].max()) <= (1 << BITS) - 1
     assert_code_flip_rate(total)
 
 
-def test_degenerate_blocks_and_token_scaling(kvlib):
+def test_degenerate_blocks_and_token_scaling(kvlib, BITS):
     """An all-zero block stores zero codes and steps and R = 1; a constant
     block passes the staged check; scaling one token by 8 scales its R by
     exactly 8 and leaves every code and C unchanged."""
@@ -77,7 +82,7 @@ def test_degenerate_blocks_and_token_scaling(kvlib):
 
 
 @pytest.mark.parametrize("B", [32, 64])
-def test_dequantize_matches_oracle_decode(kvlib, B):
+def test_dequantize_matches_oracle_decode(kvlib, B, BITS):
     kv = kvlib
     sb = synth.sign_bits(11 + B)
     cfg = kv.make_config(4, 1, B, 2, sb, bits=BITS)
@@ -95,26 +100,27 @@ def test_dequantize_matches_oracle_decode(kvlib, B):
             assert np.max(np.abs(o - ref) / scale) < 2e-6
 
 
-def test_four_bits_beat_two_bits(kvlib):
-    """On the same rows the 4-bit cache reconstructs with far less error."""
+def test_wider_codes_reconstruct_better(kvlib):
+    """On the same rows every extra bit cuts the reconstruction error (each
+    step count is 2^bits - 1: 3, 7, 15)."""
     kv = kvlib
     B = 32
     sb = synth.sign_bits(5)
     g = synth.make_gen(99)
     x = synth.kv_values(g, 1, 32, B, 1.5, 4, 20.0)[0]
     errs = {}
-    for bits in (2, 4):
+    for bits in (2, 3, 4):
         cfg = kv.make_config(4, 1, B, 3, sb, bits=bits)
         got, _ = _quantize(kv, cfg, 0, x)
         out = torch.empty(32, B, D, dtype=torch.float32, device="cuda")
         kv.dequantize(cfg, 0, torch.from_numpy(got.reshape(-1)).cuda(), out, False)
         xr = out.cpu().double().numpy()
         errs[bits] = np.linalg.norm(xr - x.double().numpy()) / np.linalg.norm(x.double().numpy())
-    assert errs[4] < 0.3 * errs[2], errs
+    assert errs[4] < 0.6 * errs[3] and errs[3] < 0.6 * errs[2], errs
 
 
 @pytest.mark.parametrize("B,iters", [(32, 3), (64, 2)])
-def test_append_token_by_token(kvlib, B, iters):
+def test_append_token_by_token(kvlib, B, iters, BITS):
     kv = kvlib
     n_q, n_kv, batch = 4, 2, 2
     sb = synth.sign_bits(B + 3)
@@ -153,7 +159,7 @@ def test_append_token_by_token(kvlib, B, iters):
 
 
 @pytest.mark.parametrize("B", [32, 64])
-def test_error_split_matches_oracle(kvlib, B):
+def test_error_split_matches_oracle(kvlib, B, BITS):
     kv = kvlib
     sb = synth.sign_bits(610 + B)
     cfg = kv.make_config(4, 1, B, 2, sb, bits=BITS)
@@ -179,7 +185,7 @@ def test_error_split_matches_oracle(kvlib, B):
 
 @pytest.mark.parametrize("B,iters", [(32, 3), (64, 2)])
 @pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float32])
-def test_attention_ragged_paged_with_tails(kvlib, B, iters, qdtype):
+def test_attention_ragged_paged_with_tails(kvlib, B, iters, qdtype, BITS):
     kv = kvlib
     n_q, n_kv = 8, 2
     lens = [0, 1, B - 1, B, B + 1, 3 * B + 7, 700]
@@ -206,7 +212,7 @@ def test_attention_ragged_paged_with_tails(kvlib, B, iters, qdtype):
 
 
 @pytest.mark.parametrize("G", [1, 3, 4])
-def test_attention_group_sizes_and_long_context(kvlib, G):
+def test_attention_group_sizes_and_long_context(kvlib, G, BITS):
     """Several query heads per kv head, 2048 tokens, B = 64: many blocks per
     warp, so the split-K partials and the merge both run."""
     kv = kvlib

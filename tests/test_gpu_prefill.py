@@ -47,7 +47,7 @@ def _cache(kv, B, bits, iters, n_q, n_kv, lens, seed):
     return cache, sb, g
 
 
-@pytest.mark.parametrize("B,bits,iters", [(32, 2, 3), (64, 2, 2), (32, 4, 3), (64, 4, 2)])
+@pytest.mark.parametrize("B,bits,iters", [(32, 2, 3), (64, 2, 2), (32, 3, 3), (64, 3, 2), (32, 4, 3), (64, 4, 2)])
 @pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float32])
 def test_prefill_ragged_chunks_match_oracle(kvlib, B, bits, iters, qdtype):
     """A 40-row chunk over ragged sequences: rows inside complete blocks (the
