@@ -1,6 +1,6 @@
 /*
  * kvarn.h -- C ABI of the GB300 (sm_103a) KVarN 2-bit KV-cache library
- * (4-bit codes as an option of the same format).
+ * (3- and 4-bit codes as options of the same format).
  *
  * KVarN stores the K and V caches at 2 bits per element without calibration
  * data: each block of tokens is rotated by a randomised Hadamard matrix over
@@ -40,13 +40,14 @@
  *
  * Data layouts (little-endian; fp16/bf16 are IEEE binary16 / bfloat16)
  *   Head-block: one (physical block, kv head, K or V): B tokens x 128
- *   channels with `bits` (2 or 4) bits per code, packed as (X = 16*bits*B)
+ *   channels with `bits` (2, 3 or 4) bits per code, packed as (X = 16*bits*B)
  *     [0, X)             codes, in 8*bits-byte records (order below)
  *     [X, X+8B)          s: fp16 [4][B]   per (group, token) step
  *     [X+8B, X+16B)      z: fp16 [4][B]   per (group, token) zero (lowest level)
  *     [X+16B, X+18B)     R: fp16 [B]      per-token factor
  *     [X+18B, X+18B+256) C: fp16 [128]    per-channel factor
- *   = 1856 / 3456 bytes for 2 bits at B = 32 / 64, 2880 / 5504 for 4 bits.
+ *   = 1856 / 3456 bytes for 2 bits at B = 32 / 64, 2368 / 4480 for 3 bits,
+ *   2880 / 5504 for 4 bits.
  *   The value of element (t, c) in the rotated space is
  *   (code * s[g][t] + z[g][t]) * R[t] * C[c] with g = c / 32 and code in
  *   0 .. 2^bits - 1. Code records: record r = 32*sb + 4a + b (sb = t / 32)
@@ -58,6 +59,9 @@
  *     kind V: b = (t%32)/8, d = t%8, g = c/32, a = (c%32)/4, f = c%4;
  *             2 bits: w = 2g + f/2, p = 2*(4*(d/4) + 2*((d%4)/2) + f%2) + 16*(d%2)
  *             4 bits: w = 4g + f,   p = 4*(d/2) + 16*(d%2)
+ *   3 bits: words 0..7 of a 12-word record hold each code's low two bits
+ *           at its 2-bit (w, p); words 8..11 hold its high bit at word
+ *           8 + w/2, bit 8*(w%2) + j + 16*h, where p = 2j + 16h
  *   (each lane of the attention kernel's warp reads exactly one record per
  *   32 tokens and turns it into tensor-core operands with one shift and one
  *   mask per pair of codes).
@@ -99,7 +103,7 @@ typedef struct kvarn_config {
     int32_t head_dim;       /* must be 128 */
     int32_t block_size;     /* tokens per block B: 32 or 64 */
     int32_t group_size;     /* channels per quantisation group: must be 32 */
-    int32_t bits;           /* bits per code: 2 (the method) or 4 */
+    int32_t bits;           /* bits per code: 2 (the method), 3 or 4 */
     int32_t varn_iters;     /* VarN iterations (token pass then channel pass): 0..8 */
     int32_t n_q_heads;      /* query heads */
     int32_t n_kv_heads;     /* kv heads; n_q_heads / n_kv_heads in 1..4 */
