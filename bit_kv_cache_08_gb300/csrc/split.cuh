@@ -1,7 +1,7 @@
 // split.cuh -- balanced split-K partition shared by the decode-attention
-// kernels (and by chunked prefill, where every query row of a chunk is a
-// virtual sequence of its own: virtual v = b * chunk + r sees the causal
-// prefix of real sequence b). The (sequence, kv head) units are laid end to end, block by block
+// kernels, and the per-row block counts the merge uses for chunked prefill
+// (every query row of a chunk is a virtual sequence of its own: virtual
+// v = b * chunk + r sees the causal prefix of real sequence b). The (sequence, kv head) units are laid end to end, block by block
 // (sequence-major, then head, then block); warp w of the nw active warps
 // (nw = min(resident warps, W)) takes global blocks [floor(w*W/nw),
 // floor((w+1)*W/nw)), at least one. A unit's partial from warp w lives in slot
