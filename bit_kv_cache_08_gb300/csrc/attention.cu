@@ -86,6 +86,13 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const float sm_scale = a.sm_scale;
     const uint32_t sb0 = a.sb[0], sb1 = a.sb[1], sb2 = a.sb[2], sb3 = a.sb[3];
     const bool rotate_q = !(a.flags & KVARN_FLAG_NO_ROTATION);
+    // B = 64 (measured): q's hi | lo halves live in shared memory instead of 32
+    // registers and the 2-bit operand shifts run as integer multiplies
+    constexpr bool kLean = B == 64;
+    const uint32_t mulv[4] = {a.mul[0], a.mul[1], a.mul[2], a.mul[3]};
+    auto cpair = [&](uint32_t w, uint32_t w8, int j) {
+        return kLean ? code_pair_m(w, w8, j, mulv) : code_pair(w, w8, j);
+    };
 
     const SplitArgs sp{a.seq_lens, a.batch, n_kv, max_blocks, B, 0, 1};
     Cursor cc;
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     }
 
     // per-unit state
-    uint32_t Qh[16], Ql[16];   // q_rot*2^(12-e) as fp16 hi | lo (lo kept only by the lo-column lanes)
+    uint32_t Qh[kLean ? 1 : 16], Ql[kLean ? 1 : 16];   // q_rot*2^(12-e) as fp16 hi | lo (lo only on lo-column lanes)
     float kmul = 0.f;          // 2^BITS * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
     float m_run = -INFINITY, l_part = 0.f;
     float O[8][2];             // rotated output, channels 32g + 4gq + 2m + rh, head tq
@@ -169,18 +176,43 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             if (j == tq) kmul = kLevels * exp2i(e - 12) * sm_scale * kLog2e;
         }
         __syncwarp();
+        if constexpr (kLean) {
+            // fp16 hi | lo planes [4][128] each, over the fp32 copy (rows of heads >= G zero)
+            float4 qv[4];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int c0 = 32 * (i >> 2) + 8 * tq + 2 * (i & 3);
-            uint32_t hv = 0, lv = 0;
-            if (bcol_ok) {
-                const float v0 = qsm[hbq * kD + c0], v1 = qsm[hbq * kD + c0 + 1];
-                const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-                hv = h2_as_u32(__halves2half2(h0, h1));
-                lv = pack_h2(v0 - __half2float(h0), v1 - __half2float(h1));
+            for (int j = 0; j < 4; ++j)
+                qv[j] = j < G ? *reinterpret_cast<const float4*>(&qsm[j * kD + 4 * lane])
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncwarp();
+            uint16_t* qhp = reinterpret_cast<uint16_t*>(qsm);
+            uint16_t* qlp = qhp + 4 * kD;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float v[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
+                uint32_t hw[2], lw[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const __half h0 = __float2half_rn(v[2 * k]), h1 = __float2half_rn(v[2 * k + 1]);
+                    hw[k] = h2_as_u32(__halves2half2(h0, h1));
+                    lw[k] = pack_h2(v[2 * k] - __half2float(h0), v[2 * k + 1] - __half2float(h1));
+                }
+                *reinterpret_cast<uint2*>(qhp + j * kD + 4 * lane) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(qlp + j * kD + 4 * lane) = make_uint2(lw[0], lw[1]);
             }
-            Qh[i] = hv;
-            Ql[i] = part ? lv : 0u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c0 = 32 * (i >> 2) + 8 * tq + 2 * (i & 3);
+                uint32_t hv = 0, lv = 0;
+                if (bcol_ok) {
+                    const float v0 = qsm[hbq * kD + c0], v1 = qsm[hbq * kD + c0 + 1];
+                    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+                    hv = h2_as_u32(__halves2half2(h0, h1));
+                    lv = pack_h2(v0 - __half2float(h0), v1 - __half2float(h1));
+                }
+                Qh[i] = hv;
+                Ql[i] = part ? lv : 0u;
+            }
         }
         if (!head_ok) kmul = 0.f;
         m_run = -INFINITY;
@@ -246,14 +278,29 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             for (int g = 0; g < 4; ++g) {
                 const uint4 c4 = *reinterpret_cast<const uint4*>(KC + 32 * g + 8 * tq);
                 const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+                uint32_t hw[4], lw[4];
+                if constexpr (kLean) {
+                    const uint16_t* qhp = reinterpret_cast<const uint16_t*>(qsm) + hbq * kD + 8 * tq + 32 * g;
+                    const uint4 h4 = *reinterpret_cast<const uint4*>(qhp);
+                    uint4 l4 = *reinterpret_cast<const uint4*>(qhp + 4 * kD);
+                    if (!part) l4 = make_uint4(0, 0, 0, 0);   // the lo term only on the lo-column lanes
+                    hw[0] = h4.x; hw[1] = h4.y; hw[2] = h4.z; hw[3] = h4.w;
+                    lw[0] = l4.x; lw[1] = l4.y; lw[2] = l4.z; lw[3] = l4.w;
+                } else {
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        hw[e2] = Qh[4 * g + e2];
+                        lw[e2] = Ql[4 * g + e2];
+                    }
+                }
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
                     const int i = 4 * g + e2;
                     const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
-                    const __half2 qh = u32_as_h2(Qh[i]);
+                    const __half2 qh = u32_as_h2(hw[e2]);
                     const __half2 mneg = __hmul2(__hmul2(qh, C2), nmask);   // -RN(qh*C) | 0
                     __half2 r = __hfma2(qh, C2, mneg);
-                    r = __hfma2(u32_as_h2(Ql[i]), C2, r);
+                    r = __hfma2(u32_as_h2(lw[e2]), C2, r);
                     bq[i] = h2_as_u32(r);
                 }
             }
@@ -302,10 +349,10 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                             if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
                                 const int j = 4 * (g & 1) + 2 * kk;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
-                                a0 = code_pair(kw[i0], kw8[i0], j);
-                                a1 = code_pair(kw[i1], kw8[i1], j);
-                                a2 = code_pair(kw[i0], kw8[i0], j + 1);
-                                a3 = code_pair(kw[i1], kw8[i1], j + 1);
+                                a0 = cpair(kw[i0], kw8[i0], j);
+                                a1 = cpair(kw[i1], kw8[i1], j);
+                                a2 = cpair(kw[i0], kw8[i0], j + 1);
+                                a3 = cpair(kw[i1], kw8[i1], j + 1);
                             } else if (BITS == 3) {   // 2-bit word 2i + g/2; high bits in word 8 + i
                                 const int j = 4 * (g & 1) + 2 * kk, jh = 8 * (g >> 1) + j;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
@@ -486,8 +533,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         const uint32_t wd = vw[2 * g + m], wd8 = vw8[2 * g + m];
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt)
-                            mma16816(Ob[mt], code_pair(wd, wd8, 4 * kt + 0), code_pair(wd, wd8, 4 * kt + 1),
-                                     code_pair(wd, wd8, 4 * kt + 2), code_pair(wd, wd8, 4 * kt + 3),
+                            mma16816(Ob[mt], cpair(wd, wd8, 4 * kt + 0), cpair(wd, wd8, 4 * kt + 1),
+                                     cpair(wd, wd8, 4 * kt + 2), cpair(wd, wd8, 4 * kt + 3),
                                      bv[g][2 * kt], bv[g][2 * kt + 1]);
                     } else if (BITS == 3) {   // 2-bit word 2g + f/2; high bits in word 8 + g, bit 8(f/2) + j
                         const int wl = 2 * g + m, wh = 8 + g;
@@ -634,6 +681,10 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.nw = nw;
     a.sm_scale = cfg.sm_scale;
     a.flags = cfg.flags;
+    a.mul[0] = 256;
+    a.mul[1] = 64;
+    a.mul[2] = 16;
+    a.mul[3] = 4;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)a.batch * a.n_q + 3) / 4);
     return with_attn_kernel(cfg.block_size, cfg.bits, [&](auto k) {

@@ -33,6 +33,7 @@ struct AttnArgs {
     float sm_scale;
     uint32_t flags;   // KVARN_FLAG_*: the cache's ablation switches
     uint32_t sb[4];
+    uint32_t mul[4];   // 256, 64, 16, 4, passed at run time (see code_pair_m)
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -63,6 +64,15 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int j) {
     const uint32_t x = (j < 4) ? w * (1u << (8 - 2 * j)) : (j == 4 ? w : w8 * (1u << (16 - 2 * j)));
     return (x & 0x03000300u) | 0x3C003C00u;
 }
+// code_pair with the shifts written as multiplies by powers of two that the
+// compiler cannot see (m = {256, 64, 16, 4} from the kernel arguments): they
+// become integer multiply-adds on the FMA pipe instead of shifts on the ALU
+// pipe, which the LOP3s and the epilogues already keep busy.
+__device__ __forceinline__ uint32_t code_pair_m(uint32_t w, uint32_t w8, int j, const uint32_t (&m)[4]) {
+    const uint32_t x = j < 4 ? w * m[j] : (j == 4 ? w : w8 * m[j - 4]);
+    return (x & 0x03000300u) | 0x3C003C00u;
+}
+
 // The 3-bit analogue: the low two bits of a pair from its 2-bit word w (pair
 // j, w8 = w >> 8) moved to fraction bits 7..8, the high bit from the 1-bit
 // plane word hw (bit jh of each half, hw8 = hw >> 8 for jh >= 8) moved to
