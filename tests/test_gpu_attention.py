@@ -66,9 +66,12 @@ def test_ragged_paged_with_tails(kvlib, B, iters, qdtype):
 
 
 @pytest.mark.parametrize("G", [1, 2, 3, 4])
-def test_group_sizes(kvlib, G):
+@pytest.mark.parametrize("B", [32, 64])
+def test_group_sizes(kvlib, G, B):
+    """G = n_q / n_kv query heads per kv head (empty columns and, at B = 64,
+    empty rows of the shared-memory q planes for G < 4)."""
     kv = kvlib
-    B, n_kv = 32, 2
+    n_kv = 2
     n_q = G * n_kv
     lens = [5 * B + 3, 2 * B]
     sb = synth.sign_bits(G)
