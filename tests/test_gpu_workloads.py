@@ -14,9 +14,9 @@ from kvtest_util import PagedCache, assert_code_flip_rate, attn_close, oracle_at
 pytestmark = pytest.mark.gpu
 
 
-def _layer(kv, w, seed_extra=0, perm=True):
+def _layer(kv, w, seed_extra=0, perm=True, bits=2):
     sb = synth.sign_bits(w.seed)
-    cfg = kv.make_config(w.n_q, w.n_kv, w.block, w.iters, sb)
+    cfg = kv.make_config(w.n_q, w.n_kv, w.block, w.iters, sb, bits=bits)
     g = synth.make_gen(w.seed + seed_extra, "cuda")
     K = synth.kv_values(g, w.batch, w.n_kv, w.ctx, w.sigma_m, w.n_out, w.out_factor, "cuda").to(torch.bfloat16)
     V = synth.kv_values(g, w.batch, w.n_kv, w.ctx, w.sigma_m, w.n_out, w.out_factor, "cuda").to(torch.bfloat16)
@@ -35,7 +35,7 @@ def _layer(kv, w, seed_extra=0, perm=True):
     return sb, cfg, K, V, q, cache, out.cpu().double().numpy()
 
 
-def _check_appended(w, sb, K, V, cache, samples):
+def _check_appended(w, sb, K, V, cache, samples, bits=2):
     B = w.block
     j = w.ctx // B - 1
     total = Counter()
@@ -43,7 +43,7 @@ def _check_appended(w, sb, K, V, cache, samples):
         for kind, T in ((0, K), (1, V)):
             rows = T[b, h, j * B:(j + 1) * B].double().cpu().numpy()
             total.update(staged_quantize_parity(rows[None], cache.head_block(b, h, j, kind)[None], B, w.iters,
-                                                kind, sb))
+                                                kind, sb, bits=bits))
     assert_code_flip_rate(total)
 
 
@@ -56,11 +56,14 @@ def test_llama8b_layer(kvlib):
     print("llama8b layer worst error ratio", worst)
 
 
-def test_qwen3_4b_layer_sampled(kvlib):
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_qwen3_4b_layer_sampled(kvlib, bits):
+    """The 36-layer workload's layer shape at full size (64 x 8192 tokens,
+    B = 64), at every code width."""
     w = synth.QWEN3_4B_CACHE
-    sb, cfg, K, V, q, cache, got = _layer(kvlib, w)
-    _check_appended(w, sb, K, V, cache, [(0, 0), (63, 7)])
+    sb, cfg, K, V, q, cache, got = _layer(kvlib, w, bits=bits)
+    _check_appended(w, sb, K, V, cache, [(0, 0), (63, 7)], bits=bits)
     seqs = [0, 21, 63]
     ref = oracle_attention(cache, q, [w.ctx] * w.batch, sb, seqs=seqs)
     worst = attn_close(got[seqs], ref)
-    print("qwen3-4b layer (sampled) worst error ratio", worst)
+    print(f"qwen3-4b layer {bits}-bit (sampled) worst error ratio", worst)
