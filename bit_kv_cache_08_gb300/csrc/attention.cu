@@ -39,9 +39,15 @@
 // Operand order inside each MMA (which token is row r, which channel is
 // k-slot j) is chosen so that the packed record order gives every lane its
 // operands directly; the writer packs codes in that order.
-// 4-bit codes (BITS = 4) take the same path: a lane's record is 64 bytes,
-// a = 1 + code/16 (code in fraction bits 6..9 of 1.0), and every factor 4
-// above becomes 16 (code * s + z = 16 s (a - 1) + z).
+// 3- and 4-bit codes (BITS = 3, 4) take the same path: a lane's record is
+// 48 or 64 bytes, a = 1 + code/8 or 1 + code/16 (the code in fraction bits
+// 7..9 or 6..9 of 1.0), and every factor 4 above becomes 8 or 16
+// (code * s + z = 2^BITS s (a - 1) + z). The kernel's name keeps the
+// method's width. At B = 64 q's hi | lo halves are read from shared memory
+// per block (32 fewer registers) and the 2-bit operand shifts run as
+// multiplies by powers of two from the kernel arguments (integer
+// multiply-adds on the FMA pipe, which has room, instead of shifts on the
+// ALU pipe, which binds).
 #include "attn_common.cuh"
 
 namespace kvarn {
@@ -66,7 +72,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                              // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);     // S mbarriers
-    float* qsm = reinterpret_cast<float*>(smem + S * 2 * HB + 64);       // [4][128]
+    float* qsm = reinterpret_cast<float*>(smem + S * 2 * HB + 64);       // [4][128] (fp16 hi | lo planes at B = 64)
     uint16_t* pex = reinterpret_cast<uint16_t*>(qsm + 4 * kD);           // [hi|lo][4 heads][B]
 
     const int lane = threadIdx.x;

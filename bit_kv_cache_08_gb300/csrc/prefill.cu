@@ -1,6 +1,6 @@
-// prefill.cu -- chunked prefill attention over the KVarN paged cache (2- or
-// 4-bit codes; sm_103a): the query rows of a chunk share one pass over each
-// cache block.
+// prefill.cu -- chunked prefill attention over the KVarN paged cache (2-, 3-
+// or 4-bit codes; sm_103a): the query rows of a chunk share one pass over
+// each cache block.
 //
 // Method: "KVarN：方差归一化让 2-bit KV 缓存扛住长链推理", section 三 3.1 (the
 // query multiplied by the same randomised Hadamard matrix as K and V) and 3.2
@@ -24,11 +24,16 @@
 //   PV  A = P'_g = p R s_g lam (hi rows, lo rows), B = the V codes
 //       (n = channel, k = token), one group at a time; the block's result
 //       is folded into O with the per-channel factor 4 C / lam at once.
+//       P' is an fp16 two-product of P'' = p R lam (hi | lo once per token)
+//       with the group's steps; the zero-point sums of all groups come from
+//       two MMAs per 32 tokens (B columns z_0..z_3 | s_0..s_3).
 // K and V head-blocks stream through a shared-memory ring filled by 1-D bulk
-// copies (lane 0) counted on mbarriers with bounded waits. Each vector's
-// (max, sum, 128 rotated accumulators) goes to one workspace partial; the
-// merge kernel adds the raw bf16 tail rows, rotates back once and
-// normalises. 3- and 4-bit codes take the same path with 48- and 64-byte
+// copies (lane 0) counted on mbarriers with bounded waits. When there are
+// fewer (sequence, kv head, row tile) units than half the resident warps,
+// each unit's blocks are split over up to 16 warps. Each vector's (max,
+// sum, 128 rotated accumulators) per split goes to one workspace partial;
+// the merge kernel combines a row's partials, adds the raw bf16 tail rows,
+// rotates back once and normalises. 3- and 4-bit codes take the same path with 48- and 64-byte
 // records and a = 1 + code/8 or 1 + code/16 (every factor 4 above becomes 8
 // or 16).
 #include <algorithm>
