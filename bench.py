@@ -113,6 +113,19 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def attention_source_hash():
+    """SHA-256 of the attention kernel's sources with comments and blank lines
+    removed (a comment edit does not change the kernel the counters describe)."""
+    import re
+    h = hashlib.sha256()
+    for f in ("attention.cu", "attn_common.cuh", "split.cuh", "common.cuh"):
+        text = open(os.path.join(ROOT, "bit_kv_cache_08_gb300", "csrc", f), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
+    return h.hexdigest()
+
+
 def _attention_record():
     """profiles/attention_traffic.json (ncu counters of one attention launch on
     the Qwen3-4B layer) if it was captured from the current kernel source."""
@@ -120,10 +133,7 @@ def _attention_record():
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
-    h = hashlib.sha256()
-    for f in ("attention.cu", "attn_common.cuh", "split.cuh", "common.cuh"):
-        h.update(open(os.path.join(ROOT, "bit_kv_cache_08_gb300", "csrc", f), "rb").read())
-    return rec if rec.get("source_sha256") == h.hexdigest() else None
+    return rec if rec.get("source_sha256") == attention_source_hash() else None
 
 
 def traffic_record():
