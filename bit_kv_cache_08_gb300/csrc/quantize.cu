@@ -177,7 +177,9 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
             for (int i = 0; i < RPW; ++i) {
                 mu[i] *= (1.0f / kD);
                 float d0 = u[i][0] - mu[i], d1 = u[i][1] - mu[i], d2 = u[i][2] - mu[i], d3 = u[i][3] - mu[i];
-                var[i] = (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+                // every multiply-add written out as one fma (no contraction left to the
+                // compiler, so the statistics are the same in every kernel and build)
+                var[i] = fmaf(d0, d0, __fmul_rn(d1, d1)) + fmaf(d2, d2, __fmul_rn(d3, d3));
             }
             row_totals<RPW>(var, lane);
 #pragma unroll
@@ -195,7 +197,7 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
 #pragma unroll
         for (int i = 0; i < RPW; ++i)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cs[k] += x[i][k] * rR[i];
+            for (int k = 0; k < 4; ++k) cs[k] = fmaf(x[i][k], rR[i], cs[k]);
         const float4 m4 = column_totals<B, BITS>(q, cs, warp, lane, buf);
         buf ^= 1;
         const float cmu[4] = {m4.x * (1.0f / B), m4.y * (1.0f / B), m4.z * (1.0f / B), m4.w * (1.0f / B)};
@@ -205,8 +207,8 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
         for (int i = 0; i < RPW; ++i)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float d = x[i][k] * rR[i] - cmu[k];
-                cs[k] += d * d;
+                const float d = fmaf(x[i][k], rR[i], -cmu[k]);
+                cs[k] = fmaf(d, d, cs[k]);
             }
         const float4 v4 = column_totals<B, BITS>(q, cs, warp, lane, buf);
         buf ^= 1;
@@ -375,7 +377,7 @@ __device__ __forceinline__ void load4(const void* src, int dtype, int64_t elem_o
 
 // ---------------------------------------------------------------- bulk quantise
 template <int B, int BITS>
-__global__ void __launch_bounds__(quant_threads<B>()) quantize_blocks_kernel(
+__global__ void __launch_bounds__(quant_threads<B>(), 3) quantize_blocks_kernel(
     const void* __restrict__ src, int dtype, int64_t block_stride, int64_t token_stride,
     uint8_t* __restrict__ dst_base, const int64_t* __restrict__ dst_offsets, QuantParams p,
     uint32_t* err) {
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(quant_threads<B>()) quantize_blocks_kernel(
 // ---------------------------------------------------------------- fused append
 // grid (batch, n_kv, 2): one CTA per (sequence, kv head, K|V).
 template <int B, int BITS>
-__global__ void __launch_bounds__(quant_threads<B>()) append_kernel(
+__global__ void __launch_bounds__(quant_threads<B>(), 3) append_kernel(
     uint8_t* __restrict__ pool, int64_t n_pool_blocks, int64_t block_bytes,
     uint16_t* __restrict__ staging, const int32_t* __restrict__ block_table, int max_blocks,
     const int32_t* __restrict__ pos_arr, const uint16_t* __restrict__ k_new,
