@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     uint32_t Qh[kLean ? 1 : 16], Ql[kLean ? 1 : 16];   // q_rot*2^(12-e) as fp16 hi | lo (lo only on lo-column lanes)
     float kmul = 0.f;          // 2^BITS * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
     float m_run = -INFINITY, l_part = 0.f;
-    float O[8][2];             // rotated output, channels 32g + 4gq + 2m + rh, head tq
+    float2 O[8];               // rotated output, channels 32g + 4gq + 2m + {0, 1}, head tq
     const float sgn4[4] = {sign_of4(sb0, sb1, sb2, sb3, 4 * lane), sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 1),
                            sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 2), sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 3)};
     const bool head_ok = tq < G;            // this lane's score / accumulator head
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         m_run = -INFINITY;
         l_part = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = 0.f;
+        for (int mt = 0; mt < 8; ++mt) O[mt] = make_float2(0.f, 0.f);
     };
 
     auto unit_flush = [&]() {
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
             for (int g = 0; g < 4; ++g)   // channels 32g + 4gq + {0,1,2,3}
                 *reinterpret_cast<float4*>(base + 4 + 32 * g + 4 * gq) =
-                    make_float4(O[2 * g][0], O[2 * g][1], O[2 * g + 1][0], O[2 * g + 1][1]);
+                    make_float4(O[2 * g].x, O[2 * g].y, O[2 * g + 1].x, O[2 * g + 1].y);
         }
     };
 
@@ -268,12 +268,26 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 
         if (valid) {
             const uint16_t* KC = reinterpret_cast<const uint16_t*>(Kb + off_C(B, BITS));
-            // ---- per-block power of two bringing max C to (1/2, 1]
-            float cmax;
+            // ---- largest K channel factor (for a per-block power of two bringing
+            // it to (1/2, 1]) and largest V step, in one fp16x2 warp reduction
+            float cmax, smax;
             {
                 const uint2 c2 = *reinterpret_cast<const uint2*>(KC + 4 * lane);
-                const __half2 m2 = __hmax2(u32_as_h2(c2.x), u32_as_h2(c2.y));
-                cmax = warp_max(fmaxf(__low2float(m2), __high2float(m2)));
+                const __half2 mc = __hmax2(u32_as_h2(c2.x), u32_as_h2(c2.y));
+                __half2 ms;
+                if (B == 32) {
+                    const uint2 s2 = *reinterpret_cast<const uint2*>(Vb + off_s(B, BITS) + 8 * lane);
+                    ms = __hmax2(u32_as_h2(s2.x), u32_as_h2(s2.y));
+                } else {
+                    const uint4 s4 = *reinterpret_cast<const uint4*>(Vb + off_s(B, BITS) + 16 * lane);
+                    ms = __hmax2(__hmax2(u32_as_h2(s4.x), u32_as_h2(s4.y)), __hmax2(u32_as_h2(s4.z), u32_as_h2(s4.w)));
+                }
+                __half2 m2 = __hmax2(__lows2half2(mc, ms), __highs2half2(mc, ms));   // (C max, s max)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    m2 = __hmax2(m2, u32_as_h2(__shfl_xor_sync(kFull, h2_as_u32(m2), o)));
+                cmax = __low2float(m2);
+                smax = __high2float(m2);
             }
             const int ec = ceil_log2(fmaxf(cmax, kF16MinNormal));
             const __half2 cinv = __float2half2_rn(exp2i(-ec));
@@ -329,7 +343,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B, BITS));
 
             // ---------------- QK for every 32-token sub-block
-            float sc[NSB][4];
+            float2 sc[NSB][2];   // tokens 32sb + 4gq + 2mt + {0, 1}
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
                 uint32_t kw[RW], kw8[RW];
@@ -381,78 +395,67 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                                 mma16816(acc[g][mt], a0, a1, a2, a3, b0, b1);
                         }
                     }
-                // scores of tokens 32sb + 4gq + i, head tq
+                // scores of tokens 32sb + 4gq + 2mt + {0, 1}, head tq, as fp32 pairs
                 const int t0 = 32 * sb + 4 * gq;
                 const uint2 Rr = *reinterpret_cast<const uint2*>(KR + t0);
-                const float2 R01 = __half22float2(u32_as_h2(Rr.x)), R23 = __half22float2(u32_as_h2(Rr.y));
-                const float Rv[4] = {R01.x, R01.y, R23.x, R23.y};
-                float s_[4] = {0.f, 0.f, 0.f, 0.f};
+                const float2 Rv[2] = {__half22float2(u32_as_h2(Rr.x)), __half22float2(u32_as_h2(Rr.y))};
+                float2 s_[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const uint2 s2 = *reinterpret_cast<const uint2*>(Ks + g * B + t0);
                     const uint2 z2 = *reinterpret_cast<const uint2*>(Kz + g * B + t0);
-                    const float2 s01 = __half22float2(u32_as_h2(s2.x)), s23 = __half22float2(u32_as_h2(s2.y));
-                    const float2 z01 = __half22float2(u32_as_h2(z2.x)), z23 = __half22float2(u32_as_h2(z2.y));
-                    const float sv[4] = {s01.x, s01.y, s23.x, s23.y};
-                    const float zv[4] = {z01.x, z01.y, z23.x, z23.y};
+                    const float2 sv[2] = {__half22float2(u32_as_h2(s2.x)), __half22float2(u32_as_h2(s2.y))};
+                    const float2 zv[2] = {__half22float2(u32_as_h2(z2.x)), __half22float2(u32_as_h2(z2.y))};
+                    const float2 qq = make_float2(Qq[g], Qq[g]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int mt = i >> 1, rh = i & 1;
-                        const float d = acc[g][mt][2 * rh] + acc[g][mt][2 * rh + 1];
-                        s_[i] = fmaf(sv[i], d, s_[i]);
-                        s_[i] = fmaf(zv[i], Qq[g], s_[i]);
+                    for (int mt = 0; mt < 2; ++mt) {   // hi + lo column of rows gq, gq + 8
+                        const float2 d = make_float2(acc[g][mt][0] + acc[g][mt][1], acc[g][mt][2] + acc[g][mt][3]);
+                        s_[mt] = __ffma2_rn(sv[mt], d, s_[mt]);
+                        s_[mt] = __ffma2_rn(zv[mt], qq, s_[mt]);
                     }
                 }
+                const float2 kmb2 = make_float2(kmb, kmb);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) sc[sb][i] = s_[i] * Rv[i] * kmb;
+                for (int mt = 0; mt < 2; ++mt) sc[sb][mt] = __fmul2_rn(__fmul2_rn(s_[mt], Rv[mt]), kmb2);
             }
             // ---------------- online softmax over the block (head tq: 8 lanes x 4 tokens per sub-block)
             float bm = -INFINITY;
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb)
-                bm = fmaxf(bm, fmaxf(fmaxf(sc[sb][0], sc[sb][1]), fmaxf(sc[sb][2], sc[sb][3])));
+                bm = fmaxf(bm, fmaxf(fmaxf(sc[sb][0].x, sc[sb][0].y), fmaxf(sc[sb][1].x, sc[sb][1].y)));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
             const float m_new = fmaxf(m_run, bm);
-            const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run - m_new);
-            float pR[NSB][4], psum = 0.f, pmax = 0.f;
+            const bool none = m_new == -INFINITY;
+            const float alpha = none ? 1.f : fast_exp2(m_run - m_new);
+            const float2 nm2 = make_float2(-m_new, -m_new);
+            float2 pR[NSB][2];
+            float psum = 0.f, pmax = 0.f;
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
                 const uint2 Rr = *reinterpret_cast<const uint2*>(VR + 32 * sb + 4 * gq);
-                const float2 R01 = __half22float2(u32_as_h2(Rr.x)), R23 = __half22float2(u32_as_h2(Rr.y));
-                const float Rv[4] = {R01.x, R01.y, R23.x, R23.y};
+                const float2 Rv[2] = {__half22float2(u32_as_h2(Rr.x)), __half22float2(u32_as_h2(Rr.y))};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float p = (m_new == -INFINITY) ? 0.f : fast_exp2(sc[sb][i] - m_new);
-                    psum += p;
-                    pR[sb][i] = p * Rv[i];
-                    pmax = fmaxf(pmax, pR[sb][i]);
+                for (int mt = 0; mt < 2; ++mt) {
+                    const float2 e = __fadd2_rn(sc[sb][mt], nm2);
+                    const float2 p = none ? make_float2(0.f, 0.f) : make_float2(fast_exp2(e.x), fast_exp2(e.y));
+                    psum += p.x;
+                    psum += p.y;
+                    pR[sb][mt] = __fmul2_rn(p, Rv[mt]);
+                    pmax = fmaxf(pmax, fmaxf(pR[sb][mt].x, pR[sb][mt].y));
                 }
             }
             l_part = l_part * alpha + psum;
             m_run = m_new;
+            {   // (unconditional: cheaper than testing alpha == 1)
+                const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {   // (unconditional: cheaper than testing alpha == 1)
-                O[mt][0] *= alpha;
-                O[mt][1] *= alpha;
+                for (int mt = 0; mt < 8; ++mt) O[mt] = __fmul2_rn(O[mt], al2);
             }
             pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 4));
             pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 8));
             pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 16));
-            // largest V step of the block (all groups and tokens)
-            float smax;
-            if (B == 32) {
-                const uint2 s2 = *reinterpret_cast<const uint2*>(Vs + 4 * lane);
-                const __half2 m2 = __hmax2(u32_as_h2(s2.x), u32_as_h2(s2.y));
-                smax = fmaxf(__low2float(m2), __high2float(m2));
-            } else {
-                const uint4 s4 = *reinterpret_cast<const uint4*>(Vs + 8 * lane);
-                const __half2 m2 = __hmax2(__hmax2(u32_as_h2(s4.x), u32_as_h2(s4.y)),
-                                           __hmax2(u32_as_h2(s4.z), u32_as_h2(s4.w)));
-                smax = fmaxf(__low2float(m2), __high2float(m2));
-            }
-            smax = warp_max(smax);
             // power of two lam so that p*R*lam <= 2^14 and p*R*s*lam <= 2^12 (fp16 range
             // of P' and of its hi | lo halves); undone in the update of O
             float lam = 1.f;
@@ -461,19 +464,22 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 if (smax > 0.f) k = min(k, 12 - ceil_log2(pmax * smax));
                 lam = exp2i(k);
             }
+            const float2 lam2 = make_float2(lam, lam);
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
-                float hi[4], lo[4];
+                uint32_t hw[2], lw[2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float v = pR[sb][i] * lam;
-                    hi[i] = __half2float(__float2half_rn(v));
-                    lo[i] = v - hi[i];
+                for (int mt = 0; mt < 2; ++mt) {
+                    const float2 v = __fmul2_rn(pR[sb][mt], lam2);
+                    const __half2 h = __float22half2_rn(v);
+                    const float2 hf = __half22float2(h);
+                    hw[mt] = h2_as_u32(h);
+                    lw[mt] = h2_as_u32(__float22half2_rn(__fadd2_rn(v, make_float2(-hf.x, -hf.y))));
                 }
                 uint16_t* ph = pex + (0 * 4 + tq) * B + 32 * sb + 4 * gq;
                 uint16_t* pl = pex + (1 * 4 + tq) * B + 32 * sb + 4 * gq;
-                *reinterpret_cast<uint2*>(ph) = make_uint2(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]));
-                *reinterpret_cast<uint2*>(pl) = make_uint2(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]));
+                *reinterpret_cast<uint2*>(ph) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(pl) = make_uint2(lw[0], lw[1]);
             }
             __syncwarp();
 
@@ -579,20 +585,18 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             // ---------------- O += 2^BITS C_c / lam * (Ob + zs / 2^BITS)
             {
                 const float il4 = kLevels / lam;
+                const float2 il42 = make_float2(il4, il4);
                 const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const uint2 c2 = *reinterpret_cast<const uint2*>(VC + 32 * g + 4 * gq);
                     const float2 c01 = __half22float2(u32_as_h2(c2.x)), c23 = __half22float2(u32_as_h2(c2.y));
-                    const float cf[4] = {c01.x, c01.y, c23.x, c23.y};   // channels 32g+4gq+{0..3}
+                    const float2 zq2 = make_float2(zq[g], zq[g]);
 #pragma unroll
-                    for (int m = 0; m < 2; ++m) {
+                    for (int m = 0; m < 2; ++m) {   // channels 32g + 4gq + 2m + {0, 1}
                         const int mt = 2 * g + m;
-#pragma unroll
-                        for (int rh = 0; rh < 2; ++rh) {
-                            const float t = (Ob[mt][2 * rh] + Ob[mt][2 * rh + 1]) + zq[g];
-                            O[mt][rh] = fmaf(cf[2 * m + rh] * il4, t, O[mt][rh]);
-                        }
+                        const float2 t = __fadd2_rn(make_float2(Ob[mt][0] + Ob[mt][1], Ob[mt][2] + Ob[mt][3]), zq2);
+                        O[mt] = __ffma2_rn(__fmul2_rn(m ? c23 : c01, il42), t, O[mt]);
                     }
                 }
             }
