@@ -61,6 +61,10 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------- the split-K kernel
+// Shared memory for q: fp32 [4][128] at B = 32; at B = 64 the fp16 planes hi,
+// -hi, lo ([4][128] each, the first two over the fp32 copy) and a zero line.
+__host__ __device__ constexpr int attn_q_bytes(int B) { return B == 64 ? 3 * 4 * kD * 2 + 2 * kD : 4 * kD * 4; }
+
 template <int B, int BITS, int S>
 __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     static_assert(BITS >= 2 && BITS <= 4, "2-, 3- or 4-bit codes");
@@ -72,8 +76,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                              // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);     // S mbarriers
-    float* qsm = reinterpret_cast<float*>(smem + S * 2 * HB + 64);       // [4][128] (fp16 hi | lo planes at B = 64)
-    uint16_t* pex = reinterpret_cast<uint16_t*>(qsm + 4 * kD);           // [hi|lo][4 heads][B]
+    float* qsm = reinterpret_cast<float*>(smem + S * 2 * HB + 64);       // [4][128] fp32 q (and at B = 64 the fp16 planes below)
+    uint16_t* pex = reinterpret_cast<uint16_t*>(smem + S * 2 * HB + 64 + attn_q_bytes(B));   // [hi|lo][4 heads][B]
 
     const int lane = threadIdx.x;
     const int gq = lane >> 2, tq = lane & 3;   // mma groupID, thread-in-group
@@ -158,6 +162,18 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     // (-1,-1) on the lanes holding a lo column, (0,0) on the hi ones: the
     // two-product's correction term is multiplied by it instead of selected
     const __half2 nmask = part ? __float2half2_rn(-1.f) : __float2half2_rn(0.f);
+    // The same two-products in three operations: t = RN(x * y) negated on the
+    // lo-column lanes, then fma(x_z, y, t) with x_z = x there and 0 on the hi
+    // ones (-RN(xy) + xy exact | RN(xy)), then + lo * y.
+    const __half2 pneg = part ? __float2half2_rn(-1.f) : __float2half2_rn(1.f);
+    const __half2 pone = part ? __float2half2_rn(1.f) : __float2half2_rn(0.f);
+    // B = 64: q's fp16 planes [4][128] each: hi at 0, -hi at 4*128, lo at
+    // 8*128, then 128 zeros; this lane reads (hi | -hi), (0 | hi), (0 | lo)
+    const uint16_t* qpl = reinterpret_cast<const uint16_t*>(qsm);
+    const uint16_t* q_n = qpl + (part ? 4 * kD : 0) + hbq * kD + 8 * tq;
+    const uint16_t* q_z = part ? qpl + hbq * kD + 8 * tq : qpl + 12 * kD + 8 * tq;
+    const uint16_t* q_l = part ? qpl + 8 * kD + hbq * kD + 8 * tq : qpl + 12 * kD + 8 * tq;
+    if constexpr (kLean) reinterpret_cast<uint2*>(qsm)[3 * kD + lane] = make_uint2(0u, 0u);   // the zero line (byte 3072)
 
     auto unit_setup = [&]() {
         __syncwarp();
@@ -183,7 +199,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         }
         __syncwarp();
         if constexpr (kLean) {
-            // fp16 hi | lo planes [4][128] each, over the fp32 copy (rows of heads >= G zero)
+            // fp16 hi, -hi and lo planes [4][128] each, over the fp32 copy (rows of heads >= G zero)
             float4 qv[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -191,7 +207,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                               : make_float4(0.f, 0.f, 0.f, 0.f);
             __syncwarp();
             uint16_t* qhp = reinterpret_cast<uint16_t*>(qsm);
-            uint16_t* qlp = qhp + 4 * kD;
+            uint16_t* qlp = qhp + 8 * kD;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float v[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
@@ -203,6 +219,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                     lw[k] = pack_h2(v[2 * k] - __half2float(h0), v[2 * k + 1] - __half2float(h1));
                 }
                 *reinterpret_cast<uint2*>(qhp + j * kD + 4 * lane) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(qhp + (4 + j) * kD + 4 * lane) =
+                    make_uint2(hw[0] ^ 0x80008000u, hw[1] ^ 0x80008000u);
                 *reinterpret_cast<uint2*>(qlp + j * kD + 4 * lane) = make_uint2(lw[0], lw[1]);
             }
         } else {
@@ -298,30 +316,30 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             for (int g = 0; g < 4; ++g) {
                 const uint4 c4 = *reinterpret_cast<const uint4*>(KC + 32 * g + 8 * tq);
                 const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
-                uint32_t hw[4], lw[4];
                 if constexpr (kLean) {
-                    const uint16_t* qhp = reinterpret_cast<const uint16_t*>(qsm) + hbq * kD + 8 * tq + 32 * g;
-                    const uint4 h4 = *reinterpret_cast<const uint4*>(qhp);
-                    uint4 l4 = *reinterpret_cast<const uint4*>(qhp + 4 * kD);
-                    if (!part) l4 = make_uint4(0, 0, 0, 0);   // the lo term only on the lo-column lanes
-                    hw[0] = h4.x; hw[1] = h4.y; hw[2] = h4.z; hw[3] = h4.w;
-                    lw[0] = l4.x; lw[1] = l4.y; lw[2] = l4.z; lw[3] = l4.w;
+                    const uint4 n4 = *reinterpret_cast<const uint4*>(q_n + 32 * g);
+                    const uint4 z4 = *reinterpret_cast<const uint4*>(q_z + 32 * g);
+                    const uint4 l4 = *reinterpret_cast<const uint4*>(q_l + 32 * g);
+                    const uint32_t nw[4] = {n4.x, n4.y, n4.z, n4.w};
+                    const uint32_t zw[4] = {z4.x, z4.y, z4.z, z4.w};
+                    const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
+                        __half2 r = __hfma2(u32_as_h2(zw[e2]), C2, __hmul2(u32_as_h2(nw[e2]), C2));
+                        r = __hfma2(u32_as_h2(lw[e2]), C2, r);
+                        bq[4 * g + e2] = h2_as_u32(r);
+                    }
                 } else {
 #pragma unroll
                     for (int e2 = 0; e2 < 4; ++e2) {
-                        hw[e2] = Qh[4 * g + e2];
-                        lw[e2] = Ql[4 * g + e2];
+                        const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
+                        const __half2 qh = u32_as_h2(Qh[4 * g + e2]);
+                        const __half2 mneg = __hmul2(__hmul2(qh, C2), nmask);   // -RN(qh*C) | 0
+                        __half2 r = __hfma2(qh, C2, mneg);
+                        r = __hfma2(u32_as_h2(Ql[4 * g + e2]), C2, r);
+                        bq[4 * g + e2] = h2_as_u32(r);
                     }
-                }
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const int i = 4 * g + e2;
-                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
-                    const __half2 qh = u32_as_h2(hw[e2]);
-                    const __half2 mneg = __hmul2(__hmul2(qh, C2), nmask);   // -RN(qh*C) | 0
-                    __half2 r = __hfma2(qh, C2, mneg);
-                    r = __hfma2(u32_as_h2(lw[e2]), C2, r);
-                    bq[i] = h2_as_u32(r);
                 }
             }
             // ---- Q'_g for this lane's head: an MMA with all-ones A sums each group
@@ -499,11 +517,13 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 }
                 const uint32_t ph[4] = {phv.x, phv.y, phv.z, phv.w};
                 const uint32_t pl[4] = {plv.x, plv.y, plv.z, plv.w};
-                uint32_t plm[4], pa[4];
+                uint32_t plm[4], pa[4], hpn[4], hpz[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    plm[k] = part ? pl[k] : 0u;
+                    plm[k] = h2_as_u32(__hmul2(u32_as_h2(pl[k]), pone));
                     pa[k] = part ? pl[k] : ph[k];
+                    hpn[k] = h2_as_u32(__hmul2(u32_as_h2(ph[k]), pneg));
+                    hpz[k] = h2_as_u32(__hmul2(u32_as_h2(ph[k]), pone));
                 }
                 uint32_t bv[4][4];   // [group][token pair]
 #pragma unroll
@@ -513,9 +533,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const __half2 s2 = u32_as_h2(sw[k]);
-                        const __half2 hp = u32_as_h2(ph[k]);
-                        const __half2 mneg = __hmul2(__hmul2(hp, s2), nmask);   // -RN(p*s) | 0
-                        __half2 r = __hfma2(hp, s2, mneg);
+                        __half2 r = __hfma2(u32_as_h2(hpz[k]), s2, __hmul2(u32_as_h2(hpn[k]), s2));
                         r = __hfma2(u32_as_h2(plm[k]), s2, r);
                         bv[g][k] = h2_as_u32(r);
                     }
@@ -629,7 +647,7 @@ constexpr int stages_for() { return B == 32 ? 4 : 2; }
 
 template <int B, int BITS>
 size_t attn_smem_bytes() {
-    return (size_t)stages_for<B, BITS>() * 2 * head_block_bytes(B, BITS) + 64 + 4 * kD * sizeof(float) +
+    return (size_t)stages_for<B, BITS>() * 2 * head_block_bytes(B, BITS) + 64 + attn_q_bytes(B) +
            2 * 4 * B * sizeof(uint16_t);
 }
 
