@@ -26,9 +26,10 @@
 //         cores keep fp32 accuracy; q_rot is scaled to 2^12 per unit and C by
 //         a power of two per block so both halves stay normal fp16 (fp16
 //         subnormal operands lose precision on the tensor cores).
-//   Q'_g = sum_{c in g} q'_c            (MMA with an all-ones A operand)
+//   Q'_g = sum_{c in g} q'_c            (MMA with an all-(-1) A operand)
 //   QK:  acc_g[t][h] = -Q'_g + sum_{c in g} a[t][c] q'[c][h]  (one accumulator
-//        per 32-channel group, started at -Q'_g), then
+//        per 32-channel group, its hi and lo columns started at the negated
+//        hi and lo sums: the output quad of the Q'_g MMA), then
 //        score[t][h] = 4 R_t (sum_g s_tg acc_g + z_tg Q'_g / 4)
 //   softmax over the block (running max and sum per head, log2 domain)
 //   PV:  P'[t][h,g] = p_t R_t s_tg lam (hi | lo), lam a power of two per
@@ -174,6 +175,9 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const uint16_t* q_z = part ? qpl + hbq * kD + 8 * tq : qpl + 12 * kD + 8 * tq;
     const uint16_t* q_l = part ? qpl + 8 * kD + hbq * kD + 8 * tq : qpl + 12 * kD + 8 * tq;
     if constexpr (kLean) reinterpret_cast<uint2*>(qsm)[3 * kD + lane] = make_uint2(0u, 0u);   // the zero line (byte 3072)
+    // B = 64: this lane's P'' hi | lo rows of pex (the zero line for heads >= G)
+    const uint16_t* px_h = bcol_ok ? pex + hbq * B + 8 * tq : qpl + 12 * kD + 8 * tq;
+    const uint16_t* px_l = bcol_ok ? pex + (4 + hbq) * B + 8 * tq : qpl + 12 * kD + 8 * tq;
 
     auto unit_setup = [&]() {
         __syncwarp();
@@ -342,16 +346,17 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                     }
                 }
             }
-            // ---- Q'_g for this lane's head: an MMA with all-ones A sums each group
-            float Qneg[4], Qq[4];
+            // ---- -Q'_g for this lane's head: an MMA with all-(-1) A sums each group;
+            // its quad (-sum hi, -sum lo per row) is the C operand that starts the
+            // group's QK chains
+            float Qq[4], cq[4][4];
+            constexpr uint32_t kNegOnes = 0xBC00BC00u;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma16816(d, kOnes, kOnes, kOnes, kOnes, bq[4 * g], bq[4 * g + 1]);
-                mma16816(d, kOnes, kOnes, kOnes, kOnes, bq[4 * g + 2], bq[4 * g + 3]);
-                const float qg = d[0] + d[1];
-                Qneg[g] = -qg;
-                Qq[g] = qg * (1.0f / kLevels);
+                cq[g][0] = cq[g][1] = cq[g][2] = cq[g][3] = 0.f;
+                mma16816(cq[g], kNegOnes, kNegOnes, kNegOnes, kNegOnes, bq[4 * g], bq[4 * g + 1]);
+                mma16816(cq[g], kNegOnes, kNegOnes, kNegOnes, kNegOnes, bq[4 * g + 2], bq[4 * g + 3]);
+                Qq[g] = (cq[g][0] + cq[g][1]) * (-1.0f / kLevels);
             }
             const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, BITS));
             const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B, BITS));
@@ -408,7 +413,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                                 a3 = code_quad(kw[i1], kw8[i1], j + 1);
                             }
                             if (kk == 0)
-                                mma16816_from(acc[g][mt], a0, a1, a2, a3, b0, b1, Qneg[g], 0.f);
+                                mma16816_c4(acc[g][mt], a0, a1, a2, a3, b0, b1, cq[g]);
                             else
                                 mma16816(acc[g][mt], a0, a1, a2, a3, b0, b1);
                         }
@@ -510,10 +515,16 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll 1
             for (int sb = 0; sb < NSB; ++sb) {
                 // this lane's B column (head hbq, part) for tokens 32sb + 8tq .. +7
-                uint4 phv = make_uint4(0, 0, 0, 0), plv = make_uint4(0, 0, 0, 0);
-                if (bcol_ok) {
-                    phv = *reinterpret_cast<const uint4*>(pex + (0 * 4 + hbq) * B + 32 * sb + 8 * tq);
-                    plv = *reinterpret_cast<const uint4*>(pex + (1 * 4 + hbq) * B + 32 * sb + 8 * tq);
+                uint4 phv, plv;
+                if constexpr (kLean) {
+                    phv = *reinterpret_cast<const uint4*>(px_h + 32 * sb);
+                    plv = *reinterpret_cast<const uint4*>(px_l + 32 * sb);
+                } else {
+                    phv = make_uint4(0, 0, 0, 0); plv = make_uint4(0, 0, 0, 0);
+                    if (bcol_ok) {
+                        phv = *reinterpret_cast<const uint4*>(pex + (0 * 4 + hbq) * B + 32 * sb + 8 * tq);
+                        plv = *reinterpret_cast<const uint4*>(pex + (1 * 4 + hbq) * B + 32 * sb + 8 * tq);
+                    }
                 }
                 const uint32_t ph[4] = {phv.x, phv.y, phv.z, phv.w};
                 const uint32_t pl[4] = {plv.x, plv.y, plv.z, plv.w};

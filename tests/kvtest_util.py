@@ -19,6 +19,7 @@ already-validated rounded values so one boundary case cannot cascade):
 from __future__ import annotations
 
 import math
+import os
 from collections import Counter
 
 import numpy as np
@@ -109,6 +110,10 @@ def attn_close(got: np.ndarray, ref: np.ndarray, tol: float = 2e-3):
     worst = float(np.nanmax(err)) if err.size else 0.0
     assert np.all(np.isfinite(got)), "non-finite attention output"
     assert worst <= tol, f"attention error {worst:.3e} > {tol}"
+    log = os.environ.get("KVARN_ERROR_LOG")   # optional: one line per check, for margin reports
+    if log:
+        with open(log, "a") as f:
+            f.write(f"{os.environ.get('PYTEST_CURRENT_TEST', '?').split(' ')[0]} {worst:.4e}\n")
     return worst
 
 
