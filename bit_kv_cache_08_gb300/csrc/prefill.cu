@@ -59,16 +59,11 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// 8 fp16 at a 16-byte aligned shared address -> 8 floats
-__device__ __forceinline__ void load8h(const uint16_t* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 f = __half22float2(u32_as_h2(w[k]));
-        v[2 * k] = f.x;
-        v[2 * k + 1] = f.y;
-    }
+// halves i and i + 4 (i = 0..3) of 8 fp16 at a 16-byte aligned shared address,
+// as an fp32 pair
+__device__ __forceinline__ float2 pair_i4(const uint4& u, int i) {
+    const __half2 a = u32_as_h2(i < 2 ? u.x : u.y), b = u32_as_h2(i < 2 ? u.z : u.w);
+    return __half22float2((i & 1) ? __highs2half2(a, b) : __lows2half2(a, b));
 }
 
 }  // namespace
@@ -202,11 +197,11 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
         if (issue(s, s)) okmask |= 1u << s;
 
     float m_run = -INFINITY, l_part = 0.f;
-    float O[4][8];   // vector gq, channels 32g + 8tq + k
+    float2 O[4][4];   // vector gq, channels 32g + 8tq + f and + 4 + f
 #pragma unroll
     for (int g = 0; g < 4; ++g)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) O[g][k] = 0.f;
+        for (int f = 0; f < 4; ++f) O[g][f] = make_float2(0.f, 0.f);
 
     int stage = 0;
     uint32_t phase = 0;
@@ -289,14 +284,24 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
 #pragma unroll
                 for (int k = 0; k < RW; ++k) kw8[k] = kw[k] >> 8;
                 const int t0 = 32 * sb + 8 * tq;
-                float Rv[8];
-                load8h(KR + t0, Rv);
-                float sv[4][8], zv[4][8];
+                // R, s and z of tokens (t0 + i, t0 + 4 + i) as fp32 pairs
+                float2 Rv[4], sv[4][4], zv[4][4];
+                {
+                    const uint4 r4 = *reinterpret_cast<const uint4*>(KR + t0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) Rv[i] = pair_i4(r4, i);
+                }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    load8h(Ks + g * B + t0, sv[g]);
-                    load8h(Kz + g * B + t0, zv[g]);
+                    const uint4 s4 = *reinterpret_cast<const uint4*>(Ks + g * B + t0);
+                    const uint4 z4 = *reinterpret_cast<const uint4*>(Kz + g * B + t0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        sv[g][i] = pair_i4(s4, i);
+                        zv[g][i] = pair_i4(z4, i);
+                    }
                 }
+                const float2 kmb2 = make_float2(kmb, kmb);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {   // n-tile i: tokens 4n + i; this lane's columns 2tq, 2tq + 1
                     float acc[4][4];
@@ -327,18 +332,17 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                                 mma16816(acc[g], qa_h[qi], qa_l[qi], qa_h[qi + 1], qa_l[qi + 1], b0, b1);
                         }
                     }
-                    // column 2tq: token t0 + i; column 2tq + 1: token t0 + 4 + i
+                    // column 2tq: token t0 + i; column 2tq + 1: token t0 + 4 + i (hi + lo rows)
+                    float2 s_ = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int tt = i + 4 * c;
-                        float s_ = 0.f;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            s_ = fmaf(sv[g][tt], acc[g][c] + acc[g][2 + c], s_);
-                            s_ = fmaf(zv[g][tt], Qq[g], s_);
-                        }
-                        sc[sb][tt] = s_ * Rv[tt] * kmb;
+                    for (int g = 0; g < 4; ++g) {
+                        const float2 d = __fadd2_rn(make_float2(acc[g][0], acc[g][1]), make_float2(acc[g][2], acc[g][3]));
+                        s_ = __ffma2_rn(sv[g][i], d, s_);
+                        s_ = __ffma2_rn(zv[g][i], make_float2(Qq[g], Qq[g]), s_);
                     }
+                    const float2 v = __fmul2_rn(__fmul2_rn(s_, Rv[i]), kmb2);
+                    sc[sb][i] = v.x;
+                    sc[sb][i + 4] = v.y;
                 }
             }
             // causal cut: tokens at or past this vector's visible length
@@ -364,25 +368,32 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
             const uint16_t* Vs = reinterpret_cast<const uint16_t*>(Vb + off_s(B, BITS));
             const uint16_t* Vz = reinterpret_cast<const uint16_t*>(Vb + off_z(B, BITS));
             const uint16_t* VR = reinterpret_cast<const uint16_t*>(Vb + off_R(B, BITS));
-            float pR[NSB][8], psum = 0.f, pmax = 0.f;
+            float2 pR[NSB][4];   // tokens 8tq + 2k, + 1
+            float psum = 0.f, pmax = 0.f;
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
-                float Rv[8];
-                load8h(VR + 32 * sb + 8 * tq, Rv);
+                const uint4 r4 = *reinterpret_cast<const uint4*>(VR + 32 * sb + 8 * tq);
+                const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                    const float p = (m_new == -INFINITY) ? 0.f : ex2(sc[sb][tt] - m_new);
-                    psum += p;
-                    pR[sb][tt] = p * Rv[tt];
-                    pmax = fmaxf(pmax, pR[sb][tt]);
+                for (int k = 0; k < 4; ++k) {
+                    float2 p;
+                    p.x = (m_new == -INFINITY) ? 0.f : ex2(sc[sb][2 * k] - m_new);
+                    p.y = (m_new == -INFINITY) ? 0.f : ex2(sc[sb][2 * k + 1] - m_new);
+                    psum += p.x;
+                    psum += p.y;
+                    pR[sb][k] = __fmul2_rn(p, __half22float2(u32_as_h2(rw[k])));
+                    pmax = fmaxf(pmax, fmaxf(pR[sb][k].x, pR[sb][k].y));
                 }
             }
             l_part = l_part * alpha + psum;
             m_run = m_new;
+            {
+                const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
+                for (int g = 0; g < 4; ++g)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) O[g][k] *= alpha;
+                    for (int f = 0; f < 4; ++f) O[g][f] = __fmul2_rn(O[g][f], al2);
+            }
             pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 1));
             pmax = fmaxf(pmax, __shfl_xor_sync(kFull, pmax, 2));
             float smax;
@@ -413,11 +424,10 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
             for (int sb = 0; sb < NSB; ++sb)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float v0 = pR[sb][2 * k] * lam, v1 = pR[sb][2 * k + 1] * lam;
-                    const __half2 hh = __floats2half2_rn(v0, v1);
-                    const float2 hf = __half22float2(hh);
+                    const float2 v = __fmul2_rn(pR[sb][k], make_float2(lam, lam));
+                    const __half2 hh = __float22half2_rn(v);
                     ph[sb][k] = h2_as_u32(hh);
-                    pl[sb][k] = pack_h2(v0 - hf.x, v1 - hf.y);
+                    pl[sb][k] = h2_as_u32(__float22half2_rn(__ffma2_rn(__half22float2(hh), make_float2(-1.f, -1.f), v)));
                 }
             const float il4 = kLevels / lam;
             const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
@@ -502,12 +512,12 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 }
                 // O += 2^BITS C_c / lam * (Ob + Z/2^BITS - S): lane holds channels 32g + 8tq + f (column 2tq)
                 // and 32g + 8tq + 4 + f (column 2tq + 1)
-                float cf[8];
-                load8h(VC + 32 * g + 8 * tq, cf);
+                const uint4 c4 = *reinterpret_cast<const uint4*>(VC + 32 * g + 8 * tq);
+                const float2 il42 = make_float2(il4, il4), zq2 = make_float2(zq[g], zq[g]);
 #pragma unroll
                 for (int f = 0; f < 4; ++f) {
-                    O[g][f] = fmaf(cf[f] * il4, (Ob[f][0] + Ob[f][2]) + zq[g], O[g][f]);
-                    O[g][4 + f] = fmaf(cf[4 + f] * il4, (Ob[f][1] + Ob[f][3]) + zq[g], O[g][4 + f]);
+                    const float2 t = __fadd2_rn(__fadd2_rn(make_float2(Ob[f][0], Ob[f][1]), make_float2(Ob[f][2], Ob[f][3])), zq2);
+                    O[g][f] = __ffma2_rn(__fmul2_rn(pair_i4(c4, f), il42), t, O[g][f]);
                 }
             }
         }
@@ -535,8 +545,8 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             float4* dst = reinterpret_cast<float4*>(base + 4 + 32 * g + 8 * tq);
-            dst[0] = make_float4(O[g][0], O[g][1], O[g][2], O[g][3]);
-            dst[1] = make_float4(O[g][4], O[g][5], O[g][6], O[g][7]);
+            dst[0] = make_float4(O[g][0].x, O[g][1].x, O[g][2].x, O[g][3].x);
+            dst[1] = make_float4(O[g][0].y, O[g][1].y, O[g][2].y, O[g][3].y);
         }
     }
 }
