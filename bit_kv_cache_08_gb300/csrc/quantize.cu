@@ -135,6 +135,25 @@ __device__ __forceinline__ float step_for(float zf, float M) {
 }
 
 // Quantise the tile held in x (rows of this warp) into q.image.
+// fwht128 with the five cross-lane butterfly stages as packed fp32 pairs: the
+// same operations on every value (bit-identical), fewer instructions
+__device__ __forceinline__ void fwht128_x2(float (&v)[4], int lane) {
+    float a0 = v[0] + v[1], a1 = v[0] - v[1];
+    float a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2; v[2] = a0 - a2;
+    v[1] = a1 + a3; v[3] = a1 - a3;
+#pragma unroll
+    for (int m = 1; m <= 16; m <<= 1) {
+        const float sgn = (lane & m) ? -1.0f : 1.0f;
+        const float2 s2 = make_float2(sgn, sgn);
+        const float2 o01 = make_float2(__shfl_xor_sync(kFull, v[0], m), __shfl_xor_sync(kFull, v[1], m));
+        const float2 o23 = make_float2(__shfl_xor_sync(kFull, v[2], m), __shfl_xor_sync(kFull, v[3], m));
+        const float2 r01 = __ffma2_rn(s2, make_float2(v[0], v[1]), o01);
+        const float2 r23 = __ffma2_rn(s2, make_float2(v[2], v[3]), o23);
+        v[0] = r01.x; v[1] = r01.y; v[2] = r23.x; v[3] = r23.y;
+    }
+}
+
 template <int B, int BITS>
 __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p, QuantSmem<B, BITS>& q,
                               int warp, int lane) {
@@ -152,9 +171,10 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
     for (int i = 0; i < RPW && rotate; ++i) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) x[i][k] = ((sw >> k) & 1u) ? -x[i][k] : x[i][k];
-        fwht128(x[i], lane);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) x[i][k] *= kInvSqrtD;
+        fwht128_x2(x[i], lane);
+        const float2 r2 = make_float2(kInvSqrtD, kInvSqrtD);
+        const float2 a = __fmul2_rn(make_float2(x[i][0], x[i][1]), r2), b = __fmul2_rn(make_float2(x[i][2], x[i][3]), r2);
+        x[i][0] = a.x; x[i][1] = a.y; x[i][2] = b.x; x[i][3] = b.y;
     }
 
     // ---- VarN: token pass then channel pass, p.iters times
@@ -165,26 +185,32 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
     for (int it = 0; it < p.iters; ++it) {
         // token pass: R_t = population std over channels of x_rot[t][c] / C_c
         if (!(p.flags & KVARN_FLAG_NO_TOKEN_PASS)) {
-            float u[RPW][4], mu[RPW], var[RPW];
+            float2 u[RPW][2];   // channels (0, 1), (2, 3) of this lane's 4
+            float mu[RPW], var[RPW];
+            const float2 rc01 = make_float2(rCf[0], rCf[1]), rc23 = make_float2(rCf[2], rCf[3]);
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) u[i][k] = x[i][k] * rCf[k];
-                mu[i] = (u[i][0] + u[i][1]) + (u[i][2] + u[i][3]);
+                u[i][0] = __fmul2_rn(make_float2(x[i][0], x[i][1]), rc01);
+                u[i][1] = __fmul2_rn(make_float2(x[i][2], x[i][3]), rc23);
+                mu[i] = (u[i][0].x + u[i][0].y) + (u[i][1].x + u[i][1].y);
             }
             row_totals<RPW>(mu, lane);
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
-                mu[i] *= (1.0f / kD);
-                float d0 = u[i][0] - mu[i], d1 = u[i][1] - mu[i], d2 = u[i][2] - mu[i], d3 = u[i][3] - mu[i];
-                // every multiply-add written out as one fma (no contraction left to the
-                // compiler, so the statistics are the same in every kernel and build)
+                // every product, sum and multiply-add of the statistics is an explicit
+                // fp32 operation (packed in pairs where the channels pair up): nothing is
+                // left for the compiler to contract, so the bytes are the same in every
+                // kernel and build
+                mu[i] = __fmul_rn(mu[i], 1.0f / kD);
+                const float2 nmu = make_float2(-mu[i], -mu[i]);
+                const float2 d01 = __fadd2_rn(u[i][0], nmu), d23 = __fadd2_rn(u[i][1], nmu);
+                const float d0 = d01.x, d1 = d01.y, d2 = d23.x, d3 = d23.y;
                 var[i] = fmaf(d0, d0, __fmul_rn(d1, d1)) + fmaf(d2, d2, __fmul_rn(d3, d3));
             }
             row_totals<RPW>(var, lane);
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
-                const float v = var[i] * (1.0f / kD);
+                const float v = __fmul_rn(var[i], 1.0f / kD);
                 if (usable_variance(v, mu[i])) {
                     rR[i] = rsqrtf(v);        // within 2 ulp; the factor is rounded to fp16 below
                     Rf[i] = v * rR[i];
@@ -193,29 +219,40 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
         }
         if (p.flags & KVARN_FLAG_NO_CHANNEL_PASS) continue;   // (uniform over the CTA)
         // channel pass: C_c = population std over tokens of x_rot[t][c] / R_t
-        float cs[4] = {0.f, 0.f, 0.f, 0.f};
+        float cs[4];
+        {
+            float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < RPW; ++i)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) cs[k] = fmaf(x[i][k], rR[i], cs[k]);
+            for (int i = 0; i < RPW; ++i) {
+                const float2 r2 = make_float2(rR[i], rR[i]);
+                c01 = __ffma2_rn(make_float2(x[i][0], x[i][1]), r2, c01);
+                c23 = __ffma2_rn(make_float2(x[i][2], x[i][3]), r2, c23);
+            }
+            cs[0] = c01.x; cs[1] = c01.y; cs[2] = c23.x; cs[3] = c23.y;
+        }
         const float4 m4 = column_totals<B, BITS>(q, cs, warp, lane, buf);
         buf ^= 1;
-        const float cmu[4] = {m4.x * (1.0f / B), m4.y * (1.0f / B), m4.z * (1.0f / B), m4.w * (1.0f / B)};
+        const float cmu[4] = {__fmul_rn(m4.x, 1.0f / B), __fmul_rn(m4.y, 1.0f / B), __fmul_rn(m4.z, 1.0f / B),
+                              __fmul_rn(m4.w, 1.0f / B)};
+        {
+            float2 c01 = make_float2(0.f, 0.f), c23 = make_float2(0.f, 0.f);
+            const float2 n01 = make_float2(-cmu[0], -cmu[1]), n23 = make_float2(-cmu[2], -cmu[3]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cs[k] = 0.f;
-#pragma unroll
-        for (int i = 0; i < RPW; ++i)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float d = fmaf(x[i][k], rR[i], -cmu[k]);
-                cs[k] = fmaf(d, d, cs[k]);
+            for (int i = 0; i < RPW; ++i) {
+                const float2 r2 = make_float2(rR[i], rR[i]);
+                const float2 d01 = __ffma2_rn(make_float2(x[i][0], x[i][1]), r2, n01);
+                const float2 d23 = __ffma2_rn(make_float2(x[i][2], x[i][3]), r2, n23);
+                c01 = __ffma2_rn(d01, d01, c01);
+                c23 = __ffma2_rn(d23, d23, c23);
             }
+            cs[0] = c01.x; cs[1] = c01.y; cs[2] = c23.x; cs[3] = c23.y;
+        }
         const float4 v4 = column_totals<B, BITS>(q, cs, warp, lane, buf);
         buf ^= 1;
         const float cvar[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float vk = cvar[k] * (1.0f / B);
+            const float vk = __fmul_rn(cvar[k], 1.0f / B);
             if (usable_variance(vk, cmu[k])) {
                 rCf[k] = rsqrtf(vk);
                 Cf[k] = vk * rCf[k];
@@ -237,8 +274,12 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
         const float R16 = __half2float(__float2half_rn(fminf(fmaxf(Rf[i], kF16MinNormal), kF16Max)));
         const float rRq = __frcp_rn(R16);
         float yq[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) yq[k] = (x[i][k] * rRq) * rC[k];
+        {
+            const float2 r2 = make_float2(rRq, rRq);
+            const float2 y01 = __fmul2_rn(__fmul2_rn(make_float2(x[i][0], x[i][1]), r2), make_float2(rC[0], rC[1]));
+            const float2 y23 = __fmul2_rn(__fmul2_rn(make_float2(x[i][2], x[i][3]), r2), make_float2(rC[2], rC[3]));
+            yq[0] = y01.x; yq[1] = y01.y; yq[2] = y23.x; yq[3] = y23.y;
+        }
         float mn = fminf(fminf(yq[0], yq[1]), fminf(yq[2], yq[3]));
         float mx = fmaxf(fmaxf(yq[0], yq[1]), fmaxf(yq[2], yq[3]));
 #pragma unroll
