@@ -509,10 +509,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             // ---------------- PV over the block's tokens
             float Ob[8][4], Dz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) Ob[mt][0] = Ob[mt][1] = Ob[mt][2] = Ob[mt][3] = 0.f;
-            // kept rolled: the smaller body (fewer instruction-cache misses) measured
-            // 8 % faster at B = 64 than the unrolled one
-#pragma unroll 1
+            // unrolled, each accumulator chain started by its first MMA from a zero C
+#pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
                 // this lane's B column (head hbq, part) for tokens 32sb + 8tq .. +7
                 uint4 phv, plv;
@@ -574,14 +572,14 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         const uint32_t wd = vw[2 * g + m], wd8 = vw8[2 * g + m];
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt)
-                            mma16816(Ob[mt], cpair(wd, wd8, 4 * kt + 0), cpair(wd, wd8, 4 * kt + 1),
+                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, cpair(wd, wd8, 4 * kt + 0), cpair(wd, wd8, 4 * kt + 1),
                                      cpair(wd, wd8, 4 * kt + 2), cpair(wd, wd8, 4 * kt + 3),
                                      bv[g][2 * kt], bv[g][2 * kt + 1]);
                     } else if (BITS == 3) {   // 2-bit word 2g + f/2; high bits in word 8 + g, bit 8(f/2) + j
                         const int wl = 2 * g + m, wh = 8 + g;
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt)
-                            mma16816(Ob[mt],
+                            mma16816_acc(Ob[mt], sb == 0 && kt == 0,
                                      code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 0, 8 * m + 4 * kt + 0),
                                      code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 1, 8 * m + 4 * kt + 1),
                                      code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 2, 8 * m + 4 * kt + 2),
@@ -591,7 +589,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         const int w0 = 4 * g + 2 * m, w1 = w0 + 1;
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt)
-                            mma16816(Ob[mt], code_quad(vw[w0], vw8[w0], 2 * kt), code_quad(vw[w1], vw8[w1], 2 * kt),
+                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code_quad(vw[w0], vw8[w0], 2 * kt),
+                                         code_quad(vw[w1], vw8[w1], 2 * kt),
                                      code_quad(vw[w0], vw8[w0], 2 * kt + 1), code_quad(vw[w1], vw8[w1], 2 * kt + 1),
                                      bv[g][2 * kt], bv[g][2 * kt + 1]);
                     }
