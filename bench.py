@@ -574,7 +574,7 @@ def run_reference(args):
     sample = (f"{seqs} of {w.batch} sequences x 1 of {w.layers} layers (all {w.n_kv} kv heads): "
               f"block quantise + attention")
     return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
-            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 2),
+            "n_gpus": args.gpus, "device": "host cores (the oracle runs on no GPU)", "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "sample": sample},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
