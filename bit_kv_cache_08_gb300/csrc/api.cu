@@ -27,8 +27,9 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
 cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
                                 int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                 const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
-                                int chunk, float* out, void* workspace, int64_t max_slots, int target_warps,
+                                int chunk, float* out, void* workspace, int64_t max_slots, int64_t splits,
                                 cudaStream_t st);
+int64_t prefill_splits(const kvarn_config& cfg, int64_t batch, int64_t chunk, int device);
 int attn_grid_warps(int block_size, int bits, int device);
 int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
@@ -122,19 +123,6 @@ size_t kvarn_staging_bytes(const kvarn_config* cfg, int32_t max_seqs) {
 // Warps the 2-bit prefill kernel aims for: half the resident warps (measured
 // on the Llama-3.1-8B layer: more block splits than that cost more in partials
 // and merging than they gain in occupancy).
-static int prefill_target_warps(int rw) { return rw / 2 > 1 ? rw / 2 : 1; }
-
-// Row tiles of the 2-bit prefill kernel and the block splits it wants: enough
-// warps to reach the target, at most 16 partials per row.
-static int64_t prefill_ideal_splits(const kvarn_config& c, int64_t batch, int64_t chunk, int rw) {
-    const int G = c.n_q_heads / c.n_kv_heads, P = 8 / G;
-    const int64_t units = batch * c.n_kv_heads * ((chunk + P - 1) / P);
-    if (units <= 0) return 1;
-    const int64_t target = prefill_target_warps(rw);
-    const int64_t ns = (target + units - 1) / units;
-    return ns < 1 ? 1 : (ns > 16 ? 16 : ns);
-}
-
 size_t kvarn_prefill_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t chunk,
                                      int32_t max_blocks_per_seq) {
     kvarn_config c;
@@ -142,9 +130,8 @@ size_t kvarn_prefill_workspace_bytes(const kvarn_config* cfg, int32_t batch, int
     if ((int64_t)batch * chunk > 0x7fffffff / c.n_q_heads) return 0;
     const size_t base = ws_bytes(c, batch * chunk);
     if (base == 0 || batch == 0 || chunk == 1) return base;
-    const int rw = resident_warps(c.block_size, c.bits);
     const int64_t rows = (int64_t)batch * chunk * c.n_kv_heads;
-    const size_t split = kWsHeader + (size_t)(rows * prefill_ideal_splits(c, batch, chunk, rw)) *
+    const size_t split = kWsHeader + (size_t)(rows * prefill_splits(c, batch, chunk, current_device())) *
                                          (size_t)(c.n_q_heads / c.n_kv_heads) * 132 * sizeof(float);
     return split > base ? split : base;
 }
@@ -219,13 +206,12 @@ int packed_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const v
     if (need == 0) return KVARN_ERR_CUDA;
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;
     if (chunk > 1) {   // rows of a chunk share each block's operands
-        const int rw = resident_warps(c.block_size, c.bits);
         // partial slots the caller's workspace holds: the block splits adapt to it
         const int64_t slots = (int64_t)((workspace_bytes - kWsHeader) /
                                         ((size_t)(c.n_q_heads / c.n_kv_heads) * 132 * sizeof(float)));
         return cuda_status(launch_prefill_attn(c, q, q_dtype, pool, n_pool_blocks, (int64_t)kvarn_block_bytes(&c),
                                                staging, block_table, max_blocks_per_seq, seq_lens, batch, chunk,
-                                               out, workspace, slots, prefill_target_warps(rw),
+                                               out, workspace, slots, prefill_splits(c, batch, chunk, current_device()),
                                                (cudaStream_t)stream));
     }
     const int nw = attn_grid_warps(c.block_size, c.bits, current_device());

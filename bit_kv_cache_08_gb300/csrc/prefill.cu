@@ -28,9 +28,9 @@
 //       with the group's steps; the zero-point sums of all groups come from
 //       two MMAs per 32 tokens (B columns z_0..z_3 | s_0..s_3).
 // K and V head-blocks stream through a shared-memory ring filled by 1-D bulk
-// copies (lane 0) counted on mbarriers with bounded waits. When there are
-// fewer (sequence, kv head, row tile) units than half the resident warps,
-// each unit's blocks are split over up to 16 warps. Each vector's (max,
+// copies (lane 0) counted on mbarriers with bounded waits. Each (sequence,
+// kv head, row tile) unit's blocks are split over 1 to 16 warps, chosen from
+// the unit count and the kernel's resident warps (prefill_splits). Each vector's (max,
 // sum, 128 rotated accumulators) per split goes to one workspace partial;
 // the merge kernel combines a row's partials, adds the raw bf16 tail rows,
 // rotates back once and normalises. 3- and 4-bit codes take the same path with 48- and 64-byte
@@ -552,10 +552,48 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
 }
 
 // ---------------------------------------------------------------- host side
+// Resident one-warp CTAs of the prefill kernel on `device` (cached per
+// device and configuration).
+static int prefill_grid_warps(int block_size, int bits, int device) {
+    static int cache[2][3][64];
+    const int bi = block_size == 32 ? 0 : 1, wi = bits - 2;
+    if (device < 0 || device >= 64 || wi < 0 || wi > 2) return 0;
+    if (cache[bi][wi][device] > 0) return cache[bi][wi][device];
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+    auto occ = [&](auto kernel, size_t smem) { return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32, smem); };
+    cudaError_t e;
+    if (block_size == 32)
+        e = bits == 4   ? occ(prefill_attn_kernel<32, 4, prefill_stages<32>()>, prefill_smem_bytes<32, 4>())
+            : bits == 3 ? occ(prefill_attn_kernel<32, 3, prefill_stages<32>()>, prefill_smem_bytes<32, 3>())
+                        : occ(prefill_attn_kernel<32, 2, prefill_stages<32>()>, prefill_smem_bytes<32, 2>());
+    else
+        e = bits == 4   ? occ(prefill_attn_kernel<64, 4, prefill_stages<64>()>, prefill_smem_bytes<64, 4>())
+            : bits == 3 ? occ(prefill_attn_kernel<64, 3, prefill_stages<64>()>, prefill_smem_bytes<64, 3>())
+                        : occ(prefill_attn_kernel<64, 2, prefill_stages<64>()>, prefill_smem_bytes<64, 2>());
+    if (e != cudaSuccess || per_sm <= 0) return 0;
+    cache[bi][wi][device] = sms * per_sm;
+    return cache[bi][wi][device];
+}
+
+// Block splits per (sequence, kv head, row tile) unit, 1..16. With at most
+// half a wave of units the split just fills one wave; with more it aims at
+// about two and a half waves, where the last wave's remainder costs little
+// (measured on the Llama-8B layer, 4096 cached tokens: chunks of 4, 16 and
+// 64 rows ran fastest at 0.9, 2.45 and 2.45 waves).
+int64_t prefill_splits(const kvarn_config& cfg, int64_t batch, int64_t chunk, int device) {
+    const int G = cfg.n_q_heads / cfg.n_kv_heads, P = kPrefillVecs / G;
+    const int64_t units = batch * cfg.n_kv_heads * ((chunk + P - 1) / P);
+    const int64_t R = prefill_grid_warps(cfg.block_size, cfg.bits, device);
+    if (units <= 0 || R <= 0) return 1;
+    const int64_t ns = 2 * units <= R ? R / units : (5 * R + units) / (2 * units);
+    return ns < 1 ? 1 : (ns > 16 ? 16 : ns);
+}
+
 cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dtype, const void* pool,
                                 int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                 const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
-                                int chunk, float* out, void* workspace, int64_t max_slots, int target_warps,
+                                int chunk, float* out, void* workspace, int64_t max_slots, int64_t splits,
                                 cudaStream_t st) {
     AttnArgs a;
     a.q = q;
@@ -582,10 +620,10 @@ cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dt
     const int P = kPrefillVecs / a.G;
     const int64_t tiles = (chunk + P - 1) / P;
     const int64_t units = (int64_t)batch * a.n_kv * tiles;
-    // split each unit's blocks when there are too few units to fill the GPU; the
-    // partials of a row must fit the workspace slots and one merge round trip (16)
+    // split each unit's blocks (prefill_splits); the partials of a row must fit
+    // the workspace slots and one merge round trip (16)
     const int64_t rows = (int64_t)batch * chunk * a.n_kv;
-    int64_t ns = units > 0 ? (target_warps + units - 1) / units : 1;
+    int64_t ns = splits;
     ns = std::min<int64_t>(ns, std::min<int64_t>(16, rows > 0 ? max_slots / rows : 1));
     a.single = (int)std::max<int64_t>(ns, 1);
     const int64_t warps = units * a.single;
