@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const int lane = threadIdx.x;
     const int gq = lane >> 2, tq = lane & 3;   // mma groupID, thread-in-group
     const int w = blockIdx.x;
-    constexpr uint32_t kOnes = 0x3C003C00u;    // fp16x2 (1, 1)
 
     // scalar copies of the arguments (the lambdas below must not take the
     // address of the kernel parameter block)
