@@ -407,11 +407,20 @@ def e2e_gpu(args, ctx_objs, state, w, world):
     import torch
     kv, ws, pos, lens, out = ctx_objs
     layers = len(state)
-    hq = torch.stack([st["q"] for st in state]).cpu().pin_memory()
-    hk = torch.stack([st["k_new"] for st in state]).cpu().pin_memory()
-    hv = torch.stack([st["v_new"] for st in state]).cpu().pin_memory()
+    # one pinned row per layer holding its q, new K and new V back to back (one
+    # copy per layer); the device tensors the API gets are views of its copy
+    sq, sk = state[0]["q"].shape, state[0]["k_new"].shape
+    nq, nk = state[0]["q"].numel(), state[0]["k_new"].numel()
+    hbuf = torch.empty(layers, nq + 2 * nk, dtype=state[0]["q"].dtype).pin_memory()
+    for l, st in enumerate(state):
+        hbuf[l, :nq] = st["q"].reshape(-1).cpu()
+        hbuf[l, nq:nq + nk] = st["k_new"].reshape(-1).cpu()
+        hbuf[l, nq + nk:] = st["v_new"].reshape(-1).cpu()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv = hq.to(out.device), hk.to(out.device), hv.to(out.device)
+    dbuf = hbuf.to(out.device)
+    dq = [dbuf[l, :nq].view(sq) for l in range(layers)]
+    dk = [dbuf[l, nq:nq + nk].view(sk) for l in range(layers)]
+    dv = [dbuf[l, nq + nk:].view(sk) for l in range(layers)]
 
     # copies on their own streams, overlapped with the layers' kernels: layer l
     # waits for its inputs only, and its output goes back while the next layers run
@@ -425,12 +434,17 @@ def e2e_gpu(args, ctx_objs, state, w, world):
         s_out.wait_stream(main)
         with torch.cuda.stream(s_in):
             for l in range(layers):
-                dq[l].copy_(hq[l], non_blocking=True)
-                dk[l].copy_(hk[l], non_blocking=True)
-                dv[l].copy_(hv[l], non_blocking=True)
+                dbuf[l].copy_(hbuf[l], non_blocking=True)
                 ev_in[l].record(s_in)
+        # copies on one stream finish in order: layer 0 waits for the first three
+        # layers' inputs and layer 3 for all of them, long copied by then (fewer
+        # cross-stream waits between the layers' kernels)
+        waits = {0: ev_in[min(2, layers - 1)]}
+        if layers > 3:
+            waits[3] = ev_in[layers - 1]
         for l, st in enumerate(state):
-            main.wait_event(ev_in[l])
+            if l in waits:
+                main.wait_event(waits[l])
             kv.append(st["cfg"], st["pool"], st["staging"], st["bt"], pos, dk[l], dv[l], ws)
             kv.decode_attn(st["cfg"], dq[l], st["pool"], st["staging"], st["bt"], lens, out[l], ws)
             ev_out[l].record(main)
@@ -473,7 +487,7 @@ def e2e_gpu(args, ctx_objs, state, w, world):
     ms = (time.perf_counter() - t0) * 1e3 / args.steps
     ms = max_over_ranks(ms, out.device)
     attn_bytes, app_bytes, _, _ = algorithmic_bytes(w, layers)
-    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    h2d = hbuf.numel() * hbuf.element_size()
     d2h = hout.numel() * 4
     return {"value": round(whole_job_gbs(attn_bytes + app_bytes, world, ms), 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
