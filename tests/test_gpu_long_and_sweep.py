@@ -23,8 +23,8 @@ def test_phi4_long_horizon_pseudo_decode(kvlib, layer):
     kv = kvlib
     w = synth.PHI4_LONG
     B, n_q, n_kv, batch = w.block, w.n_q, w.n_kv, w.batch
-    steps = 4096                 # of the workload's 16384 appends (keeps the oracle checks cheap)
-    check_at = {1, 64, 1024, steps}
+    steps = 16384                # the workload's appends, each followed by attention
+    check_at = {1, 64, 1024, 4096, steps}
     prefill = synth.prefill_lengths(batch, 1024, 2048, w.seed)
     Lmax = max(prefill) + steps
     max_blocks = (Lmax + B - 1) // B
@@ -67,7 +67,7 @@ def test_phi4_long_horizon_pseudo_decode(kvlib, layer):
     curve = torch.stack(curve).cpu().numpy()
     assert np.all(np.isfinite(curve))
     print(f"layer {layer}: 2-bit vs bf16 relative output difference (max, mean) at step 1 "
-          f"{curve[0]}, 1024 {curve[1023]}, {steps} {curve[-1]}")
+          f"{curve[0]}, 1024 {curve[1023]}, 4096 {curve[4095]}, {steps} {curve[-1]}")
 
 
 @pytest.mark.parametrize("batch,ctx", [(1, 131072), (8, 32768), (256, 1024), (128, 8192)])
