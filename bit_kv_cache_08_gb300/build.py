@@ -32,7 +32,7 @@ def nvcc() -> str:
 
 
 def _inputs():
-    return ([os.path.join(CSRC, s) for s in SOURCES] + glob.glob(os.path.join(CSRC, "*.cuh"))
+    return ([os.path.join(CSRC, s) for s in SOURCES] + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
             + [os.path.join(INCLUDE, "kvarn.h"), os.path.abspath(__file__)])
 
 

@@ -1,8 +1,6 @@
 // api.cu -- the extern "C" entry points declared in include/kvarn.h: host-side
 // validation, sizes, and kernel launches on the caller's stream.
-#include <math.h>
-
-#include "common.cuh"
+#include "host_checks.h"
 
 namespace kvarn {
 cudaError_t launch_quantize_blocks(const kvarn_config& cfg, int kind, const void* src, int dtype, int64_t n,
@@ -30,58 +28,13 @@ cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dt
                                 int chunk, float* out, void* workspace, int64_t max_slots, int64_t splits,
                                 cudaStream_t st);
 int64_t prefill_splits(const kvarn_config& cfg, int64_t batch, int64_t chunk, int device);
-int attn_grid_warps(int block_size, int bits, int device);
-int attn_bf16_grid_warps(int block_size, int device);
 }  // namespace kvarn
 
 using namespace kvarn;
 
 namespace {
 
-constexpr int kMaxGroup = 4;
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Validates cfg and returns a copy with defaults applied (sm_scale).
-int check_config(const kvarn_config* cfg, kvarn_config* out) {
-    if (!cfg) return KVARN_ERR_INVALID_ARG;
-    if (cfg->head_dim != 128 || cfg->group_size != 32 || (cfg->bits < 2 || cfg->bits > 4))
-        return KVARN_ERR_UNSUPPORTED;
-    if (cfg->block_size != 32 && cfg->block_size != 64) return KVARN_ERR_UNSUPPORTED;
-    if (cfg->varn_iters < 0 || cfg->varn_iters > 8) return KVARN_ERR_INVALID_ARG;
-    if (cfg->flags & ~(KVARN_FLAG_NO_ROTATION | KVARN_FLAG_NO_TOKEN_PASS | KVARN_FLAG_NO_CHANNEL_PASS))
-        return KVARN_ERR_INVALID_ARG;
-    if (cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads) return KVARN_ERR_INVALID_ARG;
-    if (cfg->n_q_heads % cfg->n_kv_heads != 0) return KVARN_ERR_INVALID_ARG;
-    if (cfg->n_q_heads / cfg->n_kv_heads > kMaxGroup) return KVARN_ERR_UNSUPPORTED;
-    if (!(cfg->sm_scale >= 0.0f) || isinf(cfg->sm_scale)) return KVARN_ERR_INVALID_ARG;
-    *out = *cfg;
-    if (out->sm_scale == 0.0f) out->sm_scale = 1.0f / sqrtf(128.0f);
-    return KVARN_OK;
-}
-
-int current_device() {
-    int d = 0;
-    if (cudaGetDevice(&d) != cudaSuccess) return -1;
-    return d;
-}
-
-int resident_warps(int block_size, int bits) {
-    const int d = current_device();
-    if (d < 0) return 0;
-    const int a = attn_grid_warps(block_size, bits, d);
-    const int b = attn_bf16_grid_warps(block_size, d);
-    return a > b ? a : b;
-}
-
-size_t ws_bytes(const kvarn_config& c, int32_t batch) {
-    if (batch <= 0) return kWsHeader;
-    const int nw = resident_warps(c.block_size, c.bits);
-    if (nw <= 0) return 0;
-    const size_t G = (size_t)(c.n_q_heads / c.n_kv_heads);
-    const size_t slots = (size_t)batch * c.n_kv_heads + (size_t)nw;
-    return kWsHeader + slots * G * 132 * sizeof(float);
-}
+size_t ws_bytes(const kvarn_config& c, int32_t batch) { return decode_ws_bytes(c, batch); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA; }
 
@@ -192,16 +145,10 @@ int packed_attn(const kvarn_config* cfg, const void* q, int32_t q_dtype, const v
     kvarn_config c;
     int r = check_config(cfg, &c);
     if (r != KVARN_OK) return r;
-    if (q_dtype != KVARN_BF16 && q_dtype != KVARN_FP32) return KVARN_ERR_INVALID_ARG;
-    if (batch < 0 || chunk < 1 || max_blocks_per_seq < 0 || n_pool_blocks < 1) return KVARN_ERR_INVALID_ARG;
-    if ((int64_t)batch * chunk > 0x7fffffff / c.n_q_heads) return KVARN_ERR_INVALID_ARG;
-    if (batch == 0) return KVARN_OK;
-    if (!q || !pool || !staging || !block_table || !seq_lens || !out || !workspace) return KVARN_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(pool, 16) || !aligned(staging, 16) || !aligned(out, 16) ||
-        !aligned(workspace, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
-        return KVARN_ERR_INVALID_ARG;
-    if ((int64_t)max_blocks_per_seq * c.block_size > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
-    if (n_pool_blocks > 0x7fffffff || kvarn_block_bytes(&c) > 0x7fffffff) return KVARN_ERR_INVALID_ARG;
+    r = check_packed_attn_args(c, q, q_dtype, pool, n_pool_blocks, staging, block_table, max_blocks_per_seq,
+                               seq_lens, batch, chunk, out);
+    if (r != KVARN_OK || batch == 0) return r;
+    if (!workspace || !aligned(workspace, 16)) return KVARN_ERR_INVALID_ARG;
     const size_t need = ws_bytes(c, batch * chunk);
     if (need == 0) return KVARN_ERR_CUDA;
     if (workspace_bytes < need) return KVARN_ERR_WORKSPACE;

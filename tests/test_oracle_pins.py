@@ -194,6 +194,38 @@ def test_varn_degenerate_rows_and_columns_keep_factor_one():
     assert np.all(dec == dec[0])
 
 
+@pytest.mark.parametrize("mu", [1.0, -1.0, 4.0])
+def test_varn_variance_threshold_is_two_sided(mu):
+    # Reading R-5: a row or column is normalised only when its population
+    # variance v exceeds 2^-30 * mu^2 (mu its mean). A line of alternating
+    # mu + d, mu - d has mean mu and variance d^2 exactly in fp64, so the
+    # factor is |d| just above the threshold and stays 1 at and below it.
+    thr_d = 2.0 ** -15 * abs(mu)                 # d^2 = 2^-30 mu^2
+    cases = [(thr_d * (1 + 2.0 ** -11), thr_d * (1 + 2.0 ** -11)),   # just above: factor d
+             (thr_d, 1.0),                                         # at the threshold: kept
+             (thr_d * (1 - 2.0 ** -11), 1.0)]                      # just below: kept
+    rng = np.random.default_rng(21)
+    for d, want in cases:
+        alt = np.where(np.arange(D) % 2 == 0, mu + d, mu - d)
+        Xr = rng.standard_normal((32, D))
+        Xr[0] = alt
+        _, R, _, _ = oracle.varn(Xr, 1, flags=oracle.NO_CHANNEL_PASS)
+        assert R[0] == want, (mu, d, R[0])
+        assert np.all(R[1:] != 1.0)                # the ordinary rows are normalised
+        Xc = rng.standard_normal((32, D))
+        Xc[:, 5] = np.where(np.arange(32) % 2 == 0, mu + d, mu - d)
+        _, _, C, _ = oracle.varn(Xc, 1, flags=oracle.NO_TOKEN_PASS)
+        assert C[5] == want, (mu, d, C[5])
+    # the mean enters squared: at mu = 4 a variance 4 x 2^-30 (above 2^-30 mu
+    # but below 2^-30 mu^2) keeps the factor
+    if mu == 4.0:
+        d = 2.0 ** -14
+        Xr = rng.standard_normal((32, D))
+        Xr[0] = np.where(np.arange(D) % 2 == 0, mu + d, mu - d)
+        _, R, _, _ = oracle.varn(Xr, 1, flags=oracle.NO_CHANNEL_PASS)
+        assert R[0] == 1.0
+
+
 def test_round_factor_clamps_to_fp16_normal_range():
     assert oracle.round_factor(1e-9) == 2.0 ** -14
     assert oracle.round_factor(1e9) == 65504.0

@@ -1,8 +1,10 @@
 """kvarn_decode_attn_noalloc: the decode-attention entry point that allocates
 nothing (its scratch is compiled into the library), for callers that can
 only pass inputs and outputs. Called through the C ABI twice in a row, each
-result must match kvarn_decode_attn on the same cache within the attention
-tolerance the other tests use. Kept in the file pytest collects last."""
+result must match kvarn_decode_attn on the same cache, and the fp64 oracle
+over the same cache bytes, within the attention tolerance the other tests
+use; at both block sizes and at 2- and 4-bit codes. Kept in the file pytest
+collects last."""
 import ctypes
 
 import numpy as np
@@ -10,7 +12,7 @@ import pytest
 import torch
 
 import synth
-from kvtest_util import PagedCache, attn_close
+from kvtest_util import PagedCache, attn_close, oracle_attention
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -25,13 +27,14 @@ def _noalloc(kv, cfg, q, cache, lens, out, err):
         ctypes.c_void_p(err.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-def test_noalloc_matches_workspace_entry_point_twice(kvlib):
+@pytest.mark.parametrize("B,bits", [(32, 2), (64, 2), (32, 4), (64, 4)])
+def test_noalloc_matches_workspace_entry_point_and_oracle_twice(kvlib, B, bits):
     kv = kvlib
-    B, n_q, n_kv = 32, 8, 2
+    n_q, n_kv = 8, 2
     lens_list = [5 * B + 7, 3 * B, 1, 700]
     batch = len(lens_list)
     sb = synth.sign_bits(31)
-    cfg = kv.make_config(n_q, n_kv, B, 3, sb)
+    cfg = kv.make_config(n_q, n_kv, B, 3, sb, bits=bits)
     g = synth.make_gen(31)
     K = synth.kv_values(g, batch, n_kv, max(lens_list), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
     V = synth.kv_values(g, batch, n_kv, max(lens_list), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
@@ -48,7 +51,9 @@ def test_noalloc_matches_workspace_entry_point_twice(kvlib):
         assert _noalloc(kv, cfg, q, cache, lens, out, err) == 0
         torch.cuda.synchronize()
         assert int(err.item()) == 0, f"call {call}: device error flags {int(err.item())}"
-        attn_close(out.cpu().double().numpy(), ref.cpu().double().numpy())
+        got = out.cpu().double().numpy()
+        attn_close(got, ref.cpu().double().numpy())
+        attn_close(got, oracle_attention(cache, q, lens_list, sb))
 
 
 def test_noalloc_refuses_batches_beyond_its_scratch(kvlib):
