@@ -19,36 +19,34 @@
 // shared-memory stages with 1-D bulk copies (cp.async.bulk) counted on
 // mbarriers; all lanes wait with a bounded try_wait. Each lane reads one
 // 32-byte code record per 32 tokens and turns every pair of 2-bit codes into
-// an fp16x2 tensor-core operand a = 1 + code/4 (exact) with one LOP3 after a
-// left shift. Everything below runs on mma.sync m16n8k16 (f16 in, f32
-// accumulate) with fp32 epilogues; code*s + z = 4 s (a - 1) + z.
+// an fp16x2 tensor-core operand a = code * 2^-9 (exact): one LOP3 masks the
+// pair in place, leaving an fp16 subnormal whose value is the code times a
+// power of two fixed by its bit position, and one HMUL2 by the inverse power
+// makes it normal. Everything below runs on mma.sync m16n8k16 (f16 in, f32
+// accumulate) with fp32 epilogues; code * s + z = 2^9 s a + z.
 //   q'  = q_rot * C per block, as two fp16 halves (hi | lo) so the tensor
 //         cores keep fp32 accuracy; q_rot is scaled to 2^12 per unit and C by
 //         a power of two per block so both halves stay normal fp16 (fp16
 //         subnormal operands lose precision on the tensor cores).
-//   Q'_g = sum_{c in g} q'_c            (MMA with an all-(-1) A operand)
-//   QK:  acc_g[t][h] = -Q'_g + sum_{c in g} a[t][c] q'[c][h]  (one accumulator
-//        per 32-channel group, its hi and lo columns started at the negated
-//        hi and lo sums: the output quad of the Q'_g MMA), then
-//        score[t][h] = 4 R_t (sum_g s_tg acc_g + z_tg Q'_g / 4)
+//   Q'_g = sum_{c in g} q'_c * 2^-9     (MMA with an A operand of 2^-9)
+//   QK:  acc_g[t][h] = sum_{c in g} a[t][c] q'[c][h]  (one accumulator per
+//        32-channel group, hi and lo columns), then
+//        score[t][h] = 2^9 R_t sum_g (s_tg acc_g + z_tg Q'_g)
 //   softmax over the block (running max and sum per head, log2 domain)
 //   PV:  P'[t][h,g] = p_t R_t s_tg lam (hi | lo), lam a power of two per
 //        (head, block) keeping P' inside fp16;
 //        Ob[c][h] = sum_t a[t][c] P'[t][h, g(c)]
-//        zs[h][g] = sum_t p_t R_t lam (z_tg - 4 s_tg)  (MMA with p as A, z|s as B)
-//        O[c][h] += 4 C_c / lam * (Ob[c][h] + zs[h][g(c)] / 4)  once per block.
+//        zs[h][g] = sum_t p_t R_t lam z_tg  (MMA with p as A, z | s as B)
+//        O[c][h] += 2^9 C_c / lam * (Ob[c][h] + zs[h][g(c)] * 2^-9)  once per block.
 // Operand order inside each MMA (which token is row r, which channel is
 // k-slot j) is chosen so that the packed record order gives every lane its
 // operands directly; the writer packs codes in that order.
 // 3- and 4-bit codes (BITS = 3, 4) take the same path: a lane's record is
-// 48 or 64 bytes, a = 1 + code/8 or 1 + code/16 (the code in fraction bits
-// 7..9 or 6..9 of 1.0), and every factor 4 above becomes 8 or 16
-// (code * s + z = 2^BITS s (a - 1) + z). The kernel's name keeps the
-// method's width. At B = 64 q's hi | lo halves are read from shared memory
-// per block (32 fewer registers) and the 2-bit operand shifts run as
-// multiplies by powers of two from the kernel arguments (integer
-// multiply-adds on the FMA pipe, which has room, instead of shifts on the
-// ALU pipe, which binds).
+// 48 or 64 bytes and a = code * 2^-9 as well (a 3-bit field is joined from
+// the 2-bit word and the 1-bit plane by one shift and two LOP3s; a 4-bit
+// field is masked in place). The kernel's name keeps the method's width. At
+// B = 64 q's hi | lo halves are read from shared memory per block (32 fewer
+// registers).
 #include "attn_common.cuh"
 
 namespace kvarn {
@@ -72,7 +70,6 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     wait_prior_grids();
     constexpr int HB = head_block_bytes(B, BITS);
     constexpr int RW = 4 * BITS;             // 32-bit words per lane record
-    constexpr float kLevels = 1 << BITS;     // code = 2^BITS (a - 1)
     constexpr int NSB = B / 32;
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                              // S x (K, V)
@@ -97,12 +94,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const uint32_t sb0 = a.sb[0], sb1 = a.sb[1], sb2 = a.sb[2], sb3 = a.sb[3];
     const bool rotate_q = !(a.flags & KVARN_FLAG_NO_ROTATION);
     // B = 64 (measured): q's hi | lo halves live in shared memory instead of 32
-    // registers and the 2-bit operand shifts run as integer multiplies
+    // registers
     constexpr bool kLean = B == 64;
-    const uint32_t mulv[4] = {a.mul[0], a.mul[1], a.mul[2], a.mul[3]};
-    auto cpair = [&](uint32_t w, uint32_t w8, int j) {
-        return kLean ? code_pair_m(w, w8, j, mulv) : code_pair(w, w8, j);
-    };
 
     const SplitArgs sp{a.seq_lens, a.batch, n_kv, max_blocks, B, 0, 1};
     Cursor cc;
@@ -151,7 +144,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 
     // per-unit state
     uint32_t Qh[kLean ? 1 : 16], Ql[kLean ? 1 : 16];   // q_rot*2^(12-e) as fp16 hi | lo (lo only on lo-column lanes)
-    float kmul = 0.f;          // 2^BITS * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
+    float kmul = 0.f;          // 2^9 * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
     float m_run = -INFINITY, l_part = 0.f;
     float2 O[8];               // rotated output, channels 32g + 4gq + 2m + {0, 1}, head tq
     const float sgn4[4] = {sign_of4(sb0, sb1, sb2, sb3, 4 * lane), sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 1),
@@ -198,7 +191,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             const float sc = exp2i(12 - e);
             *reinterpret_cast<float4*>(&qsm[j * kD + 4 * lane]) =
                 make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
-            if (j == tq) kmul = kLevels * exp2i(e - 12) * sm_scale * kLog2e;
+            if (j == tq) kmul = (1.0f / kCodeScale) * exp2i(e - 12) * sm_scale * kLog2e;
         }
         __syncwarp();
         if constexpr (kLean) {
@@ -345,17 +338,16 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                     }
                 }
             }
-            // ---- -Q'_g for this lane's head: an MMA with all-(-1) A sums each group;
-            // its quad (-sum hi, -sum lo per row) is the C operand that starts the
-            // group's QK chains
-            float Qq[4], cq[4][4];
-            constexpr uint32_t kNegOnes = 0xBC00BC00u;
+            // ---- Q'_g * 2^-9 for this lane's head: an MMA whose A operand is 2^-9
+            // everywhere sums each group (hi + lo columns), at the codes' scale
+            float Qq[4];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                cq[g][0] = cq[g][1] = cq[g][2] = cq[g][3] = 0.f;
-                mma16816(cq[g], kNegOnes, kNegOnes, kNegOnes, kNegOnes, bq[4 * g], bq[4 * g + 1]);
-                mma16816(cq[g], kNegOnes, kNegOnes, kNegOnes, kNegOnes, bq[4 * g + 2], bq[4 * g + 3]);
-                Qq[g] = (cq[g][0] + cq[g][1]) * (-1.0f / kLevels);
+                float cq[4];
+                mma16816_acc(cq, true, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, bq[4 * g],
+                             bq[4 * g + 1]);
+                mma16816(cq, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, bq[4 * g + 2], bq[4 * g + 3]);
+                Qq[g] = cq[0] + cq[1];
             }
             const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, BITS));
             const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B, BITS));
@@ -379,7 +371,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 }
 #pragma unroll
                 for (int k = 0; k < RW; ++k) kw8[k] = kw[k] >> 8;
-                float acc[4][2][4];   // chains start from (-Q'_g, 0) per row
+                float acc[4][2][4];   // one chain per (group, 16-token tile)
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
@@ -391,30 +383,27 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                             if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
                                 const int j = 4 * (g & 1) + 2 * kk;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
-                                a0 = cpair(kw[i0], kw8[i0], j);
-                                a1 = cpair(kw[i1], kw8[i1], j);
-                                a2 = cpair(kw[i0], kw8[i0], j + 1);
-                                a3 = cpair(kw[i1], kw8[i1], j + 1);
+                                a0 = code2_s(kw[i0], kw8[i0], j);
+                                a1 = code2_s(kw[i1], kw8[i1], j);
+                                a2 = code2_s(kw[i0], kw8[i0], j + 1);
+                                a3 = code2_s(kw[i1], kw8[i1], j + 1);
                             } else if (BITS == 3) {   // 2-bit word 2i + g/2; high bits in word 8 + i
                                 const int j = 4 * (g & 1) + 2 * kk, jh = 8 * (g >> 1) + j;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
                                 const int h0 = 8 + 2 * mt, h1 = 8 + 2 * mt + 1;
-                                a0 = code_triple(kw[i0], kw8[i0], kw[h0], kw8[h0], j, jh);
-                                a1 = code_triple(kw[i1], kw8[i1], kw[h1], kw8[h1], j, jh);
-                                a2 = code_triple(kw[i0], kw8[i0], kw[h0], kw8[h0], j + 1, jh + 1);
-                                a3 = code_triple(kw[i1], kw8[i1], kw[h1], kw8[h1], j + 1, jh + 1);
+                                a0 = code3_s(kw[i0], kw8[i0], kw[h0], j, jh);
+                                a1 = code3_s(kw[i1], kw8[i1], kw[h1], j, jh);
+                                a2 = code3_s(kw[i0], kw8[i0], kw[h0], j + 1, jh + 1);
+                                a3 = code3_s(kw[i1], kw8[i1], kw[h1], j + 1, jh + 1);
                             } else {           // word 4i + g, field e/2
                                 const int j = 2 * kk;
                                 const int i0 = 4 * (2 * mt) + g, i1 = 4 * (2 * mt + 1) + g;
-                                a0 = code_quad(kw[i0], kw8[i0], j);
-                                a1 = code_quad(kw[i1], kw8[i1], j);
-                                a2 = code_quad(kw[i0], kw8[i0], j + 1);
-                                a3 = code_quad(kw[i1], kw8[i1], j + 1);
+                                a0 = code4_s(kw[i0], kw8[i0], j);
+                                a1 = code4_s(kw[i1], kw8[i1], j);
+                                a2 = code4_s(kw[i0], kw8[i0], j + 1);
+                                a3 = code4_s(kw[i1], kw8[i1], j + 1);
                             }
-                            if (kk == 0)
-                                mma16816_c4(acc[g][mt], a0, a1, a2, a3, b0, b1, cq[g]);
-                            else
-                                mma16816(acc[g][mt], a0, a1, a2, a3, b0, b1);
+                            mma16816_acc(acc[g][mt], kk == 0, a0, a1, a2, a3, b0, b1);
                         }
                     }
                 // scores of tokens 32sb + 4gq + 2mt + {0, 1}, head tq, as fp32 pairs
@@ -571,47 +560,44 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         const uint32_t wd = vw[2 * g + m], wd8 = vw8[2 * g + m];
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt)
-                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, cpair(wd, wd8, 4 * kt + 0), cpair(wd, wd8, 4 * kt + 1),
-                                     cpair(wd, wd8, 4 * kt + 2), cpair(wd, wd8, 4 * kt + 3),
-                                     bv[g][2 * kt], bv[g][2 * kt + 1]);
+                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code2_s(wd, wd8, 4 * kt + 0),
+                                         code2_s(wd, wd8, 4 * kt + 1), code2_s(wd, wd8, 4 * kt + 2),
+                                         code2_s(wd, wd8, 4 * kt + 3), bv[g][2 * kt], bv[g][2 * kt + 1]);
                     } else if (BITS == 3) {   // 2-bit word 2g + f/2; high bits in word 8 + g, bit 8(f/2) + j
                         const int wl = 2 * g + m, wh = 8 + g;
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt)
                             mma16816_acc(Ob[mt], sb == 0 && kt == 0,
-                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 0, 8 * m + 4 * kt + 0),
-                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 1, 8 * m + 4 * kt + 1),
-                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 2, 8 * m + 4 * kt + 2),
-                                     code_triple(vw[wl], vw8[wl], vw[wh], vw8[wh], 4 * kt + 3, 8 * m + 4 * kt + 3),
-                                     bv[g][2 * kt], bv[g][2 * kt + 1]);
+                                         code3_s(vw[wl], vw8[wl], vw[wh], 4 * kt + 0, 8 * m + 4 * kt + 0),
+                                         code3_s(vw[wl], vw8[wl], vw[wh], 4 * kt + 1, 8 * m + 4 * kt + 1),
+                                         code3_s(vw[wl], vw8[wl], vw[wh], 4 * kt + 2, 8 * m + 4 * kt + 2),
+                                         code3_s(vw[wl], vw8[wl], vw[wh], 4 * kt + 3, 8 * m + 4 * kt + 3),
+                                         bv[g][2 * kt], bv[g][2 * kt + 1]);
                     } else {           // word 4g + f, field d/2
                         const int w0 = 4 * g + 2 * m, w1 = w0 + 1;
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt)
-                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code_quad(vw[w0], vw8[w0], 2 * kt),
-                                         code_quad(vw[w1], vw8[w1], 2 * kt),
-                                     code_quad(vw[w0], vw8[w0], 2 * kt + 1), code_quad(vw[w1], vw8[w1], 2 * kt + 1),
-                                     bv[g][2 * kt], bv[g][2 * kt + 1]);
+                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code4_s(vw[w0], vw8[w0], 2 * kt),
+                                         code4_s(vw[w1], vw8[w1], 2 * kt), code4_s(vw[w0], vw8[w0], 2 * kt + 1),
+                                         code4_s(vw[w1], vw8[w1], 2 * kt + 1), bv[g][2 * kt], bv[g][2 * kt + 1]);
                     }
                 }
             }
             __syncwarp();   // pex is rewritten by the next block
-            // zs[h][g] = z-sum - 2^BITS s-sum, hi + lo rows; delivered to the lanes of head tq
+            // zs[h][g] = the z-sum, hi + lo rows, at the codes' scale; delivered to the
+            // lanes of head tq
             float zq[4];
             {
-                const float v0 = Dz[0] + __shfl_xor_sync(kFull, Dz[0], 4);
-                const float v1 = Dz[1] + __shfl_xor_sync(kFull, Dz[1], 4);
-                const float zA = v0 - kLevels * __shfl_xor_sync(kFull, v0, 2);   // valid where tq < 2:
-                const float zB = v1 - kLevels * __shfl_xor_sync(kFull, v1, 2);   // groups 2tq, 2tq+1 of head gq/2
-                constexpr float kInv = 1.0f / kLevels;
-                zq[0] = kInv * __shfl_sync(kFull, zA, 8 * tq);
-                zq[1] = kInv * __shfl_sync(kFull, zB, 8 * tq);
-                zq[2] = kInv * __shfl_sync(kFull, zA, 8 * tq + 1);
-                zq[3] = kInv * __shfl_sync(kFull, zB, 8 * tq + 1);
+                const float zA = Dz[0] + __shfl_xor_sync(kFull, Dz[0], 4);   // valid where tq < 2:
+                const float zB = Dz[1] + __shfl_xor_sync(kFull, Dz[1], 4);   // groups 2tq, 2tq+1 of head gq/2
+                zq[0] = kCodeScale * __shfl_sync(kFull, zA, 8 * tq);
+                zq[1] = kCodeScale * __shfl_sync(kFull, zB, 8 * tq);
+                zq[2] = kCodeScale * __shfl_sync(kFull, zA, 8 * tq + 1);
+                zq[3] = kCodeScale * __shfl_sync(kFull, zB, 8 * tq + 1);
             }
-            // ---------------- O += 2^BITS C_c / lam * (Ob + zs / 2^BITS)
+            // ---------------- O += 2^9 C_c / lam * (Ob + zs * 2^-9)
             {
-                const float il4 = kLevels / lam;
+                const float il4 = (1.0f / kCodeScale) / lam;
                 const float2 il42 = make_float2(il4, il4);
                 const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 #pragma unroll

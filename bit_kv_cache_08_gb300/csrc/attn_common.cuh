@@ -104,6 +104,43 @@ __device__ __forceinline__ uint32_t code_quad(uint32_t w, uint32_t w8, int j) {
     return (x & 0x03C003C0u) | 0x3C003C00u;
 }
 
+// Scaled-subnormal operands (decode kernel). A code field masked out of a
+// record word in place is an fp16 subnormal, its value the code times a
+// power of two set by the field's bit position; one multiply by the inverse
+// power brings every code to the same exact normal value code * 2^-9. One
+// LOP3 (the mask) on the ALU pipe and one HMUL2 on the fp16 pipe per pair,
+// no shift: fields j >= 4 come from w8 = w >> 8, taken once per word.
+constexpr float kCodeScale = 1.0f / 512.0f;   // an operand holds code * 2^-9
+constexpr uint32_t kCodeScaleH2 = 0x18001800u;   // 2^-9 as fp16x2
+
+__device__ __forceinline__ uint32_t scale_sub(uint32_t x, uint32_t pow2_h2) {
+    return h2_as_u32(__hmul2(u32_as_h2(x), u32_as_h2(pow2_h2)));
+}
+// fp16x2 2^(15 - 2k) for k = 0..3: 2^15, 2^13, 2^11, 2^9
+__device__ __forceinline__ constexpr uint32_t pow2_for_field2(int k) {
+    return k == 0 ? 0x78007800u : (k == 1 ? 0x70007000u : (k == 2 ? 0x68006800u : 0x60006000u));
+}
+// 2-bit pair j (0..7): bits 2j, 2j + 1 of each half of w -> (c_lo, c_hi) * 2^-9
+__device__ __forceinline__ uint32_t code2_s(uint32_t w, uint32_t w8, int j) {
+    const int k = j & 3;
+    return scale_sub((j < 4 ? w : w8) & (0x00030003u << (2 * k)), pow2_for_field2(k));
+}
+// 3-bit pair: the low two bits at 2-bit pair j of w, the high bit at bit jh
+// of each half of the 1-bit plane word hw, joined into a 3-bit field at bits
+// 2k..2k+2 (k = j & 3) and scaled by 2^(15 - 2k): (c_lo, c_hi) * 2^-9
+__device__ __forceinline__ uint32_t code3_s(uint32_t w, uint32_t w8, uint32_t hw, int j, int jh) {
+    const int k = j & 3, d = 2 * k + 2 - jh;
+    const uint32_t hs = d >= 0 ? (hw << d) : (hw >> (-d));
+    const uint32_t x = ((j < 4 ? w : w8) & (0x00030003u << (2 * k))) | (hs & (0x00040004u << (2 * k)));
+    return scale_sub(x, pow2_for_field2(k));
+}
+// 4-bit pair j (0..3): bits 4j..4j+3 of each half of w (w8 for j >= 2),
+// scaled by 2^15 or 2^11: (c_lo, c_hi) * 2^-9
+__device__ __forceinline__ uint32_t code4_s(uint32_t w, uint32_t w8, int j) {
+    const int k = j & 1;
+    return scale_sub((j < 2 ? w : w8) & (0x000F000Fu << (4 * k)), k == 0 ? 0x78007800u : 0x68006800u);
+}
+
 // 2^k as a float for k in [-126, 127]
 __device__ __forceinline__ float exp2i(int k) {
     k = max(-126, min(127, k));

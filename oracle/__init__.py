@@ -98,6 +98,8 @@ def lib():
                 "orc_normalise": (None, [_i, _f64p, _f64p, _f64p, _f64p]),
                 "orc_group_params_all": (None, [_i, _i, _f64p, _f64p, _f64p, _f64p, _f64p]),
                 "orc_codes_given": (None, [_i, _i, _f64p, _f64p, _f64p, _i32p, _f64p]),
+                "orc_set_threads": (None, [_i]),
+                "orc_max_threads": (_i, []),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -105,6 +107,15 @@ def lib():
                 fn.argtypes = args
             _lib = L
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's OpenMP loops from now on (n >= 1)."""
+    lib().orc_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().orc_max_threads())
 
 
 # --------------------------------------------------------------------------
