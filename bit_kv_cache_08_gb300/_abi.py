@@ -25,6 +25,7 @@ DEVERR_BLOCK_ID, DEVERR_POSITION, DEVERR_NONFINITE, DEVERR_WAIT_TIMEOUT = 0x1, 0
 BF16, FP32 = 0, 1
 KIND_K, KIND_V = 0, 1
 FLAG_NO_ROTATION, FLAG_NO_TOKEN_PASS, FLAG_NO_CHANNEL_PASS = 0x1, 0x2, 0x4
+FLAG_TEST_WAIT_TIMEOUT = 0x100   # test only: the decode kernel's first copy waits give up at once
 
 
 class KVarNError(RuntimeError):

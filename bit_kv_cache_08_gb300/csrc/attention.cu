@@ -263,16 +263,25 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     unit_setup();
     int stage = 0;
     uint32_t phase = 0;
+    // A wait that runs out raises the error flag, lets every copy still in
+    // flight into this CTA's shared memory land (again with a limit) and ends
+    // the warp. The first wait is taken here, outside the block loop, with the
+    // launch's limit for it (kWaitLimit; zero under the test switch).
+    auto give_up = [&](int64_t x0) {
+        if (lane == 0) raise_error(err, KVARN_DEVERR_WAIT_TIMEOUT);
+        uint32_t ph = phase;
+        for (int k = 0, st2 = stage; k < S && x0 + k < s_end; ++k) {
+            mbar_wait_bounded(&bars[st2], ph, kWaitLimit);
+            if (++st2 == S) { st2 = 0; ph ^= 1u; }
+        }
+    };
+    if (!mbar_wait_bounded(&bars[0], 0, a.first_wait_limit)) {
+        give_up(s_beg);
+        return;
+    }
     for (int64_t x = s_beg; x < s_end; ++x) {
         if (!mbar_wait_bounded(&bars[stage], phase, kWaitLimit)) {
-            if (lane == 0) raise_error(err, KVARN_DEVERR_WAIT_TIMEOUT);
-            // let every copy still in flight into this CTA's shared memory land
-            // (again with a limit) before the CTA exits
-            uint32_t ph = phase;
-            for (int k = 0, st2 = stage; k < S && x + k < s_end; ++k) {
-                mbar_wait_bounded(&bars[st2], ph, kWaitLimit);
-                if (++st2 == S) { st2 = 0; ph ^= 1u; }
-            }
+            give_up(x);
             return;
         }
         const uint8_t* Kb = stages + stage * 2 * HB;
@@ -682,7 +691,7 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
                                int64_t n_pool_blocks, int64_t block_bytes, const void* staging,
                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
                                int batch, float* out, void* workspace, int nw, cudaStream_t st) {
-    AttnArgs a;
+    AttnArgs a = {};
     a.q = q;
     a.q_dtype = q_dtype;
     a.pool = (const uint8_t*)pool;
@@ -704,10 +713,9 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.nw = nw;
     a.sm_scale = cfg.sm_scale;
     a.flags = cfg.flags;
-    a.mul[0] = 256;
-    a.mul[1] = 64;
-    a.mul[2] = 16;
-    a.mul[3] = 4;
+    // test switch: every warp's first copy wait gives up at once (the
+    // wait-timeout path, run without a hang)
+    a.first_wait_limit = (cfg.flags & KVARN_FLAG_TEST_WAIT_TIMEOUT) ? 0u : kWaitLimit;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
     const unsigned mgrid = (unsigned)(((int64_t)a.batch * a.n_q + 3) / 4);
     return with_attn_kernel(cfg.block_size, cfg.bits, [&](auto k) {

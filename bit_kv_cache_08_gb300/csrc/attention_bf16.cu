@@ -275,7 +275,7 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
                                     int64_t n_pool_blocks, const int32_t* block_table, int max_blocks,
                                     const int32_t* seq_lens, int batch, float* out, void* workspace, int nw,
                                     cudaStream_t st) {
-    AttnArgs a;
+    AttnArgs a = {};
     a.q = q;
     a.q_dtype = q_dtype;
     a.pool = (const uint8_t*)kv_pool;

@@ -32,8 +32,8 @@ struct AttnArgs {
     int single;       // > 0: that many partials per (row, kv head) unit u, in slots u * single ..
     float sm_scale;
     uint32_t flags;   // KVARN_FLAG_*: the cache's ablation switches
+    uint32_t first_wait_limit;   // polls of each warp's first stage wait (kWaitLimit; less only in tests)
     uint32_t sb[4];
-    uint32_t mul[4];   // 256, 64, 16, 4, passed at run time (see code_pair_m)
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -76,15 +76,6 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int j) {
     const uint32_t x = (j < 4) ? w * (1u << (8 - 2 * j)) : (j == 4 ? w : w8 * (1u << (16 - 2 * j)));
     return (x & 0x03000300u) | 0x3C003C00u;
 }
-// code_pair with the shifts written as multiplies by powers of two that the
-// compiler cannot see (m = {256, 64, 16, 4} from the kernel arguments): they
-// become integer multiply-adds on the FMA pipe instead of shifts on the ALU
-// pipe, which the LOP3s and the epilogues already keep busy.
-__device__ __forceinline__ uint32_t code_pair_m(uint32_t w, uint32_t w8, int j, const uint32_t (&m)[4]) {
-    const uint32_t x = j < 4 ? w * m[j] : (j == 4 ? w : w8 * m[j - 4]);
-    return (x & 0x03000300u) | 0x3C003C00u;
-}
-
 // The 3-bit analogue: the low two bits of a pair from its 2-bit word w (pair
 // j, w8 = w >> 8) moved to fraction bits 7..8, the high bit from the 1-bit
 // plane word hw (bit jh of each half, hw8 = hw >> 8 for jh >= 8) moved to
@@ -173,19 +164,20 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// ---------------------------------------------------------------- merge kernel
-// One warp per (sequence, query head): LSE-merge the unit's partials. For the
-// 2-bit cache (ROT = true) the merged accumulator is in the rotated space: it
-// is rotated back once and the raw bf16 tail tokens (unrotated) are added;
-// the bf16 cache (ROT = false) has every token in its pages.
+// ---------------------------------------------------------------- merge
+// One (row, query head) output: LSE-merge the np partials of its unit
+// (p0: the first, consecutive partials G * kPartialStride floats apart; np =
+// 0 when the unit has no pool blocks), add the raw tail rows, normalise and
+// store. For the 2-bit cache (ROT = true) the merged accumulator is in the
+// rotated space: it is rotated back once and the raw bf16 tail tokens
+// (unrotated) are added; the bf16 cache (ROT = false) has every token in its
+// pages. qsh: 128 floats of this warp's shared memory. gw = row * n_q +
+// query head.
 template <int B, bool ROT>
-__global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
-    wait_prior_grids();
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (gw >= (int64_t)a.batch * a.n_q) return;
+__device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np, const float* p0, float* qsh,
+                                          int lane) {
     const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);   // b: a (virtual) row sequence
-    const int h = hq / a.G, jq = hq % a.G;
+    const int h = hq / a.G;
     const int rb = a.chunk == 1 ? b : b / a.chunk;              // its real sequence
     const int L = a.seq_lens[rb];
     float* out = a.out + gw * kD;
@@ -208,34 +200,17 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
         }
     }
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (nb > 0) {
-        const int64_t u = (int64_t)b * a.n_kv + h;
-        int np;                                                     // this unit's partials
-        const float* p0;
-        if (a.single > 0) {
-            np = a.single;
-            p0 = a.partials + (u * a.single * a.G + jq) * kPartialStride;
-        } else {
-            int64_t before, total;
-            split_prefix(sp, b, lane, before, total);
-            const int64_t W = total * a.n_kv;
-            const int64_t nwe =
-                split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, ROT ? kSplitRatio2bit * B : 0.f);
-            const int64_t Su = before * a.n_kv + (int64_t)h * nb;
-            const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);
-            np = (int)(w1 - w0 + 1);
-            p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
-        }
+    if (nb > 0 && np > 0) {
         const int64_t pstride = (int64_t)a.G * kPartialStride;     // next warp's partial of the unit
         if (np <= 16) {
             // one round trip: lane i holds partial i's (m, l); every lane loads its
             // 4 channels of all partials at once, then weighs them
-            const float pm = lane < np ? p0[lane * pstride] : -INFINITY;
-            const float pl = lane < np ? p0[lane * pstride + 1] : 0.f;
+            const float pm = lane < np ? __ldcg(p0 + lane * pstride) : -INFINITY;
+            const float pl = lane < np ? __ldcg(p0 + lane * pstride + 1) : 0.f;
             float4 pa[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                if (i < np) pa[i] = reinterpret_cast<const float4*>(p0 + i * pstride + 4)[lane];
+                if (i < np) pa[i] = __ldcg(reinterpret_cast<const float4*>(p0 + i * pstride + 4) + lane);
             m = warp_max(pm);
             if (m != -INFINITY) {
                 const float wl = lane < np ? exp2f(pm - m) : 0.f;
@@ -254,19 +229,19 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
         } else {
             // the common maximum and the weighted sum of l, lanes over partials
             float mx = -INFINITY;
-            for (int i = lane; i < np; i += 32) mx = fmaxf(mx, p0[i * pstride]);
+            for (int i = lane; i < np; i += 32) mx = fmaxf(mx, __ldcg(p0 + i * pstride));
             m = warp_max(mx);
             if (m != -INFINITY) {
                 float ls = 0.f;
-                for (int i = lane; i < np; i += 32) ls += p0[i * pstride + 1] * exp2f(p0[i * pstride] - m);
+                for (int i = lane; i < np; i += 32) ls += __ldcg(p0 + i * pstride + 1) * exp2f(__ldcg(p0 + i * pstride) - m);
                 l = warp_sum(ls);
                 // every lane its 4 channels over all partials (independent loads; a
                 // deep unroll keeps many in flight when one unit has hundreds of partials)
 #pragma unroll 16
                 for (int i = 0; i < np; ++i) {
                     const float* bp = p0 + i * pstride;
-                    const float wgt = exp2f(bp[0] - m);
-                    const float4 pa = reinterpret_cast<const float4*>(bp + 4)[lane];
+                    const float wgt = exp2f(__ldcg(bp) - m);
+                    const float4 pa = __ldcg(reinterpret_cast<const float4*>(bp + 4) + lane);
                     acc[0] = fmaf(wgt, pa.x, acc[0]);
                     acc[1] = fmaf(wgt, pa.y, acc[1]);
                     acc[2] = fmaf(wgt, pa.z, acc[2]);
@@ -285,8 +260,7 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
         // this warp's query (unrotated, times sm_scale log2 e) in shared memory, so
         // that lane r can score tail row r (and r + 32) over all 128 channels
         // with its loads issued at once
-        __shared__ __align__(16) float q_all[4][kD];
-        float* qsh = q_all[threadIdx.x >> 5];
+        __syncwarp();
         {
             float qv[4];
             load_q4(a.q, a.q_dtype, gw, lane, qv);
@@ -328,8 +302,8 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
         const float mt = warp_max(fmaxf(mine[0], mine[1]));
         const float mn = fmaxf(m, mt);                      // finite: ntail > 0
         const float fa = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-        const float p0 = exp2f(mine[0] - mn), p1 = exp2f(mine[1] - mn);   // 0 for empty slots
-        l = l * fa + warp_sum(p0 + p1);
+        const float p0t = exp2f(mine[0] - mn), p1t = exp2f(mine[1] - mn);   // 0 for empty slots
+        l = l * fa + warp_sum(p0t + p1t);
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] *= fa;
         m = mn;
@@ -343,7 +317,7 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
             for (int k = 0; k < 8; ++k) {
                 const int r = r0 + k;
                 if (r < ntail) {
-                    const float p = __shfl_sync(kFull, (r < 32) ? p0 : p1, r & 31);
+                    const float p = __shfl_sync(kFull, (r < 32) ? p0t : p1t, r & 31);
                     acc[0] = fmaf(p, __uint_as_float(vu[k].x << 16), acc[0]);
                     acc[1] = fmaf(p, __uint_as_float(vu[k].x & 0xffff0000u), acc[1]);
                     acc[2] = fmaf(p, __uint_as_float(vu[k].y << 16), acc[2]);
@@ -354,6 +328,45 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     }
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
     reinterpret_cast<float4*>(out)[lane] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+}
+
+// The merge kernel: one warp per (row, query head), which finds its unit's
+// partials from the split arithmetic.
+template <int B, bool ROT>
+__global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
+    wait_prior_grids();
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (gw >= (int64_t)a.batch * a.n_q) return;
+    __shared__ __align__(16) float q_all[4][kD];
+    const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);
+    const int h = hq / a.G, jq = hq % a.G;
+    const int rb = a.chunk == 1 ? b : b / a.chunk;
+    const int L = a.seq_lens[rb];
+    int np = 0;
+    const float* p0 = nullptr;
+    if (L >= 0 && L <= a.max_blocks * B) {
+        const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1, a.chunk};
+        const int nb = split_nblocks(sp, b);
+        if (nb > 0) {
+            const int64_t u = (int64_t)b * a.n_kv + h;
+            if (a.single > 0) {
+                np = a.single;
+                p0 = a.partials + (u * a.single * a.G + jq) * kPartialStride;
+            } else {
+                int64_t before, total;
+                split_prefix(sp, b, lane, before, total);
+                const int64_t W = total * a.n_kv;
+                const int64_t nwe =
+                    split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, ROT ? kSplitRatio2bit * B : 0.f);
+                const int64_t Su = before * a.n_kv + (int64_t)h * nb;
+                const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);
+                np = (int)(w1 - w0 + 1);
+                p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
+            }
+        }
+    }
+    merge_row<B, ROT>(a, gw, np, p0, q_all[threadIdx.x >> 5], lane);
 }
 
 }  // namespace kvarn

@@ -24,7 +24,8 @@ inline int check_config(const kvarn_config* cfg, kvarn_config* out) {
         return KVARN_ERR_UNSUPPORTED;
     if (cfg->block_size != 32 && cfg->block_size != 64) return KVARN_ERR_UNSUPPORTED;
     if (cfg->varn_iters < 0 || cfg->varn_iters > 8) return KVARN_ERR_INVALID_ARG;
-    if (cfg->flags & ~(KVARN_FLAG_NO_ROTATION | KVARN_FLAG_NO_TOKEN_PASS | KVARN_FLAG_NO_CHANNEL_PASS))
+    if (cfg->flags & ~(KVARN_FLAG_NO_ROTATION | KVARN_FLAG_NO_TOKEN_PASS | KVARN_FLAG_NO_CHANNEL_PASS |
+                       KVARN_FLAG_TEST_WAIT_TIMEOUT))
         return KVARN_ERR_INVALID_ARG;
     if (cfg->n_kv_heads < 1 || cfg->n_q_heads < cfg->n_kv_heads) return KVARN_ERR_INVALID_ARG;
     if (cfg->n_q_heads % cfg->n_kv_heads != 0) return KVARN_ERR_INVALID_ARG;

@@ -595,7 +595,7 @@ cudaError_t launch_prefill_attn(const kvarn_config& cfg, const void* q, int q_dt
                                 const int32_t* block_table, int max_blocks, const int32_t* seq_lens, int batch,
                                 int chunk, float* out, void* workspace, int64_t max_slots, int64_t splits,
                                 cudaStream_t st) {
-    AttnArgs a;
+    AttnArgs a = {};
     a.q = q;
     a.q_dtype = q_dtype;
     a.pool = (const uint8_t*)pool;

@@ -63,8 +63,8 @@
  *           at its 2-bit (w, p); words 8..11 hold its high bit at word
  *           8 + w/2, bit 8*(w%2) + j + 16*h, where p = 2j + 16h
  *   (each lane of the attention kernel's warp reads exactly one record per
- *   32 tokens and turns it into tensor-core operands with one shift and one
- *   mask per pair of codes).
+ *   32 tokens and turns it into tensor-core operands with one mask and one
+ *   fp16 multiply per pair of codes).
  *   Pool: physical block p holds its head-blocks at
  *     pool + p*kvarn_block_bytes + (2*h + kind)*kvarn_head_block_bytes,
  *   kind 0 = K, 1 = V. pool must be 16-byte aligned.
@@ -126,6 +126,16 @@ typedef struct kvarn_config {
 #define KVARN_FLAG_NO_ROTATION 0x1u
 #define KVARN_FLAG_NO_TOKEN_PASS 0x2u
 #define KVARN_FLAG_NO_CHANNEL_PASS 0x4u
+/*
+ * Test switch (no counterpart in the paper): with it, every warp of
+ * kvarn_decode_attn's split kernel gives up its first shared-memory copy
+ * wait at once, so the wait-timeout path runs without anything hanging:
+ * KVARN_DEVERR_WAIT_TIMEOUT is raised, the copies already in flight are
+ * waited for, the warp stops, the call's outputs are unspecified and the
+ * workspace stays usable (clear the error word and call again). Ignored by
+ * the other entry points; never set it outside tests.
+ */
+#define KVARN_FLAG_TEST_WAIT_TIMEOUT 0x100u
 
 /* Library version string, e.g. "kvarn 0.1 sm_103a". */
 const char* kvarn_version(void);
@@ -310,8 +320,9 @@ int kvarn_decode_attn_bf16(const kvarn_config* cfg, const void* q, int32_t q_dty
  *
  * Arguments and results are those of kvarn_decode_attn, without the
  * workspace. error_word (device uint32, may be NULL) receives this call's
- * KVARN_DEVERR_* flags (0 when none). The scratch must hold 256 + (batch *
- * n_kv + resident warps) * G * 528 bytes; larger problems are refused with
+ * KVARN_DEVERR_* flags (0 when none). The scratch must hold
+ * kvarn_workspace_bytes(cfg, batch, max_blocks_per_seq) bytes (256 + (batch *
+ * n_kv + resident warps) * G * 528); larger problems are refused with
  * KVARN_ERR_WORKSPACE before anything is enqueued.
  *
  * The first call on each device looks up the array's device address (with

@@ -221,3 +221,36 @@ def test_small_call_after_large_on_one_workspace(kvlib, B, iters):
     for j in range(n_q):
         ref = oracle.attention(qd[0, j], Kd[0, j // 4, :L], Vd[0, j // 4, :L], 1 / math.sqrt(D))
         attn_close(got[0, j], ref)
+
+
+@pytest.mark.parametrize("B", [32, 64])
+def test_wait_timeout_path_flags_and_workspace_stays_usable(kvlib, B):
+    """The bounded copy wait run out on purpose (the test switch gives every
+    warp's first wait a limit of zero): the call raises
+    KVARN_DEVERR_WAIT_TIMEOUT and returns without hanging, the copies in
+    flight are waited for, and after the error word is cleared the next call
+    on the same workspace matches the oracle."""
+    kv = kvlib
+    n_q, n_kv = 8, 2
+    lens = [5 * B + 3, 9 * B, 2 * B + B // 2, 1]
+    batch = len(lens)
+    sb = synth.sign_bits(77 + B)
+    cfg = kv.make_config(n_q, n_kv, B, 3, sb)
+    cfg_t = kv.make_config(n_q, n_kv, B, 3, sb, flags=kv.FLAG_TEST_WAIT_TIMEOUT)
+    g = synth.make_gen(77)
+    K = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    V = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    q = synth.queries(g, batch, n_q).to(torch.bfloat16).cuda()
+    cache = PagedCache(kv, cfg, batch, (max(lens) + B - 1) // B, perm_seed=7)
+    cache.prefill(K, V, lens)
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = kv.alloc_workspace(cfg, batch, cache.max_blocks)
+    out = torch.zeros(batch, n_q, D, device="cuda")
+    for _ in range(2):
+        kv.decode_attn(cfg_t, q, cache.pool, cache.staging, cache.block_table, sl, out, ws)
+        assert kv.read_error(ws) & kv.DEVERR_WAIT_TIMEOUT
+        kv.clear_error(ws)
+    out = torch.full((batch, n_q, D), float("nan"), device="cuda")
+    kv.decode_attn(cfg, q, cache.pool, cache.staging, cache.block_table, sl, out, ws)
+    assert kv.read_error(ws) == 0
+    attn_close(out.cpu().double().numpy(), oracle_attention(cache, q, lens, sb))
