@@ -47,6 +47,15 @@ def parse():
     p.add_argument("--prefill", action="store_true",
                    help="instead of the step: chunked prefill attention over the Llama-3.1-8B layer "
                         "(batch 16 x 4096 cached tokens) for several chunk lengths, one JSON line each")
+    p.add_argument("--llama-layer", action="store_true",
+                   help="instead of the step: the Llama-3.1-8B layer (batch 16 x 4096, block 32): one append "
+                        "that completes every open block, then decode attention; each rep after an "
+                        "L2-flushing write, median; one JSON line")
+    p.add_argument("--long", action="store_true",
+                   help="instead of the step: the Phi-4-14B long-horizon workload (40 layers, batch 8, "
+                        "prefill 1024-2048 then 16384 x (append + attention) per layer): us per step over "
+                        "the horizon and the 2-bit vs bf16-cache output error at steps 1 .. 16384")
+    p.add_argument("--long-steps", type=int, default=16384, help="appends per layer in --long")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
                         "lengths), 2-, 3- and 4-bit vs bf16-cache decode attention, one JSON line per point")
@@ -773,6 +782,219 @@ def run_sweep(args):
                               "speedup_4bit_vs_bf16": round(ms16 / ms4, 2)}), flush=True)
 
 
+# ---------------------------------------------------------------------------- Llama-3.1-8B layer
+
+def run_llama_layer(args):
+    """The Llama-3.1-8B layer workload: 16 sequences cached to 4095 tokens
+    (127 blocks of 32 in the pool, 31 rows in staging); one step = the append
+    of token 4096 (which completes every open block and quantises it) and
+    decode attention over the 128 blocks. The cache (61 MB) fits in L2, so
+    every rep runs after a 1 GiB L2-flushing write; CUDA events around each
+    call, median over the reps."""
+    import numpy as np
+    import torch
+    import bit_kv_cache_08_gb300 as kv
+    import synth
+    kv.build()
+    dev = "cuda"
+    w = synth.LLAMA8B_LAYER
+    B, n_kv, n_q, batch, L = w.block, w.n_kv, w.n_q, w.batch, w.ctx
+    nb = L // B
+    sb = synth.sign_bits(w.seed)
+    cfg = kv.make_config(n_q, n_kv, B, w.iters, sb)
+    g = synth.make_gen(w.seed, dev)
+    perm = np.random.default_rng(w.seed).permutation(batch * nb).astype(np.int32)
+    bt = torch.from_numpy(perm.reshape(batch, nb)).to(dev)
+    pool = kv.alloc_pool(cfg, batch * nb, dev)
+    staging = kv.alloc_staging(cfg, batch, dev)
+    ws = kv.alloc_workspace(cfg, batch, nb, dev)
+    hb, bb = kv.head_block_bytes(cfg), kv.block_bytes(cfg)
+    new = []
+    for kind in (0, 1):
+        T = synth.kv_values(g, batch, n_kv, L, w.sigma_m, w.n_out, w.out_factor, dev).to(torch.bfloat16)
+        offs = (bt[:, None, :nb - 1].long() * bb + (2 * torch.arange(n_kv, device=dev)[None, :, None] + kind)
+                * hb).reshape(-1).contiguous()
+        kv.quantize_block(cfg, kind, T[:, :, :(nb - 1) * B].contiguous(), pool, ws, dst_offsets=offs,
+                          n_head_blocks=offs.numel())
+        staging[:, :, kind, :B - 1] = T[:, :, (nb - 1) * B:L - 1]
+        new.append(T[:, :, L - 1].contiguous())
+        del T
+    q = synth.queries(g, batch, n_q, dev).to(torch.bfloat16)
+    pos = torch.full((batch,), L - 1, dtype=torch.int32, device=dev)
+    lens = torch.full((batch,), L, dtype=torch.int32, device=dev)
+    out = torch.empty(batch, n_q, D, device=dev)
+    flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    reps = max(50, args.steps)
+    app, att, stp = [], [], []
+    for r in range(args.warmup + reps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        kv.append(cfg, pool, staging, bt, pos, new[0], new[1], ws)
+        e[1].record()
+        kv.decode_attn(cfg, q, pool, staging, bt, lens, out, ws)
+        e[2].record()
+        torch.cuda.synchronize()
+        if r >= args.warmup:
+            app.append(e[0].elapsed_time(e[1]))
+            att.append(e[1].elapsed_time(e[2]))
+            stp.append(e[0].elapsed_time(e[2]))
+    assert kv.read_error(ws) == 0
+    peak, peak_kind = measured_peaks()
+    attn_bytes = batch * L * n_kv * (2 * (32 + 16 + 2) + 2 * 256 / B) + batch * n_q * (D * 2 + D * 4) + batch * nb * 4
+    app_bytes = batch * n_kv * 2 * (D * 2 + (B - 1) * D * 2 + hb)
+    ma, mt, ms = statistics.median(app), statistics.median(att), statistics.median(stp)
+    with ClockSampler(torch.cuda.current_device()) as clk:   # clocks over a second pass of the same reps
+        for _ in range(reps):
+            flush.zero_()
+            kv.append(cfg, pool, staging, bt, pos, new[0], new[1], ws)
+            kv.decode_attn(cfg, q, pool, staging, bt, lens, out, ws)
+        torch.cuda.synchronize()
+    print(json.dumps({
+        "workload": w.name, "batch": batch, "seq_len": L, "n_q_heads": n_q, "n_kv_heads": n_kv, "block": B,
+        "varn_iters": w.iters, "reps": reps,
+        "timing": "CUDA events on the launching stream, median of reps each after a 1 GiB L2-flushing write",
+        "append": {"us": round(ma * 1e3, 2), "algorithmic_bytes": int(app_bytes),
+                   "GB_per_s": round(app_bytes / ma / 1e6, 1),
+                   "head_blocks_quantised": batch * n_kv * 2,
+                   "rows_per_s": round(batch * n_kv * 2 / (ma * 1e-3), 1)},
+        "decode_attn": {"us": round(mt * 1e3, 2), "algorithmic_bytes": int(attn_bytes),
+                        "GB_per_s": round(attn_bytes / mt / 1e6, 1),
+                        "frac_of_hbm_peak": round(attn_bytes / mt / 1e6 / peak, 4), "peak": peak,
+                        "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "step": {"us": round(ms * 1e3, 2), "decode_tokens_per_s": round(batch / (ms * 1e-3), 1)},
+        "roofline_time_us_at_100_70_pct": [round(attn_bytes / peak / 1e3, 2),
+                                           round(attn_bytes / peak / 1e3 / 0.7, 2)],
+        "clocks": clk.summary()}), flush=True)
+
+
+# ---------------------------------------------------------------------------- Phi-4 long horizon
+
+LONG_CHECK = (1, 64, 1024, 4096, 16384)
+
+
+def run_long(args):
+    """The Phi-4-14B long-horizon pseudo-decode: 40 layers, 40 query / 10 kv
+    heads, batch 8 with prefill lengths uniform in [1024, 2048], then
+    --long-steps steps, each appending one token per sequence to every layer
+    and running decode attention on it (eager C-ABI calls, CUDA events per
+    window of steps). At the checkpoint steps, every layer's output is also
+    computed over a bf16 cache holding the same tokens (the repo's bf16-cache
+    kernel), and the 2-bit error against it is reported: max and mean of
+    |o_2bit - o_bf16| / max(1, |o_bf16|) and the relative L2 norm over all
+    layers, sequences and heads."""
+    import numpy as np
+    import torch
+    import bit_kv_cache_08_gb300 as kv
+    import synth
+    kv.build()
+    dev = "cuda"
+    w = synth.PHI4_LONG
+    B, n_kv, n_q, batch, layers = w.block, w.n_kv, w.n_q, w.batch, w.layers
+    steps = args.long_steps
+    prefill = synth.prefill_lengths(batch, 1024, 2048, w.seed)
+    Lmax = max(prefill) + steps
+    mb = (Lmax + B - 1) // B
+    st = []
+    t_setup = time.time()
+    for l in range(layers):
+        sb = synth.sign_bits(100 + l)
+        cfg = kv.make_config(n_q, n_kv, B, w.iters, sb)
+        g = synth.make_gen(w.seed * 100 + l, dev)
+        perm = np.random.default_rng([w.seed, l]).permutation(batch * mb).astype(np.int32)
+        bt = torch.from_numpy(perm.reshape(batch, mb)).to(dev)
+        pool = kv.alloc_pool(cfg, batch * mb, dev)
+        staging = kv.alloc_staging(cfg, batch, dev)
+        ws = kv.alloc_workspace(cfg, batch, mb, dev)
+        kvp = torch.zeros(batch * mb, n_kv, 2, B, D, dtype=torch.bfloat16, device=dev)   # bf16 pages
+        hb, bb = kv.head_block_bytes(cfg), kv.block_bytes(cfg)
+        steps_idx = torch.arange(steps, device=dev)[:, None] + torch.tensor(prefill, device=dev)[None, :]
+        news = []
+        for kind in (0, 1):
+            T = synth.kv_values(g, batch, n_kv, mb * B, w.sigma_m, w.n_out, w.out_factor, dev).to(torch.bfloat16)
+            # every token in the bf16 pages (tokens past a sequence's length are never read)
+            kvp[bt.reshape(-1).long(), :, kind] = T.view(batch, n_kv, mb, B, D).permute(0, 2, 1, 3, 4).reshape(
+                batch * mb, n_kv, B, D)
+            # the 2-bit cache: the prefill's full blocks quantised, its open tail in staging
+            for b, Lb in enumerate(prefill):
+                nbf = Lb // B
+                offs = (bt[b, :nbf].long()[None, :] * bb + (2 * torch.arange(n_kv, device=dev)[:, None] + kind)
+                        * hb).reshape(-1).contiguous()
+                kv.quantize_block(cfg, kind, T[b, :, :nbf * B].contiguous(), pool, ws, dst_offsets=offs,
+                                  n_head_blocks=offs.numel())
+                staging[b, :, kind, :Lb - nbf * B] = T[b, :, nbf * B:Lb]
+            # the appended tokens of every step: [steps][batch][n_kv][128]
+            news.append(T[torch.arange(batch, device=dev)[None, :], :, steps_idx].contiguous())
+            del T
+        q = synth.queries(g, batch, n_q, dev).to(torch.bfloat16)
+        st.append(dict(cfg=cfg, bt=bt, pool=pool, staging=staging, ws=ws, kvp=kvp, k=news[0], v=news[1], q=q,
+                       out=torch.empty(batch, n_q, D, device=dev)))
+        torch.cuda.synchronize()
+        assert kv.read_error(ws) == 0
+    t_setup = time.time() - t_setup
+    pos = torch.tensor(prefill, dtype=torch.int32, device=dev)
+    lens = pos + 1
+    ws16 = kv.alloc_workspace(st[0]["cfg"], batch, mb, dev)
+    ref = torch.empty(batch, n_q, D, device=dev)
+    window = 256
+    windows, curve = [], []
+    win_ms, win_n = 0.0, 0
+
+    def mark():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+    ev0 = mark()
+    t_loop = time.time()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for s in range(1, steps + 1):
+            for x in st:
+                kv.append(x["cfg"], x["pool"], x["staging"], x["bt"], pos, x["k"][s - 1], x["v"][s - 1], x["ws"])
+                kv.decode_attn(x["cfg"], x["q"], x["pool"], x["staging"], x["bt"], lens, x["out"], x["ws"])
+            pos += 1
+            lens += 1
+            win_n += 1
+            check = s in LONG_CHECK or s == steps
+            if check or s % window == 0 or s == steps:
+                ev1 = mark()
+                torch.cuda.synchronize()
+                win_ms += ev0.elapsed_time(ev1)
+                if s % window == 0 or s == steps:
+                    windows.append((s, win_ms * 1e3 / win_n))
+                    win_ms, win_n = 0.0, 0
+                if check:      # outside the timed windows
+                    num = den = 0.0
+                    emax = emean = 0.0
+                    for x in st:
+                        kv.decode_attn_bf16(x["cfg"], x["q"], x["kvp"], x["bt"], lens, ref, ws16)
+                        d = (x["out"] - ref).abs() / ref.abs().clamp_min(1.0)
+                        emax = max(emax, float(d.max()))
+                        emean += float(d.mean()) / layers
+                        num += float(((x["out"] - ref) ** 2).sum())
+                        den += float((ref ** 2).sum())
+                    curve.append({"step": s, "tokens_min": int(lens.min()), "tokens_max": int(lens.max()),
+                                  "max_rel": round(emax, 5), "mean_rel": round(emean, 6),
+                                  "rel_l2": round(math.sqrt(num / den), 6)})
+                ev0 = mark()
+    t_loop = time.time() - t_loop
+    for x in st:
+        assert kv.read_error(x["ws"]) == 0
+    assert kv.read_error(ws16) == 0
+    us = [u for _, u in windows]
+    print(json.dumps({
+        "workload": w.name, "layers": layers, "batch": batch, "n_q_heads": n_q, "n_kv_heads": n_kv, "block": B,
+        "varn_iters": w.iters, "prefill_lengths": prefill, "steps": steps,
+        "timing": f"CUDA events per window of {window} steps (each step: for every layer kvarn_append + "
+                  "kvarn_decode_attn, eager calls); the error checkpoints are outside the windows",
+        "us_per_step": {"first_window": round(us[0], 1), "last_window": round(us[-1], 1),
+                        "mean": round(sum(us) / len(us), 1),
+                        "by_step": [[s_, round(u, 1)] for s_, u in windows[::max(1, len(windows) // 16)]]},
+        "decode_tokens_per_s_mean": round(batch / (sum(us) / len(us) * 1e-6), 1),
+        "error_vs_bf16_cache": curve, "setup_s": round(t_setup, 1), "loop_s": round(t_loop, 1),
+        "clocks": clk.summary()}), flush=True)
+
+
 # ---------------------------------------------------------------------------- chunked prefill
 
 PREFILL_CHUNKS = (1, 4, 16, 64)
@@ -908,6 +1130,12 @@ def run_ablation(args):
 
 def main():
     args = parse()
+    if args.llama_layer:
+        run_llama_layer(args)
+        return
+    if args.long:
+        run_long(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
