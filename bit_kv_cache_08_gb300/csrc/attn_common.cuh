@@ -58,44 +58,7 @@ __device__ __forceinline__ void mma16816_acc(float (&d)[4], bool first, uint32_t
         mma16816(d, a0, a1, a2, a3, b0, b1);
 }
 
-// d = A B + C with C given as four floats (a quad another MMA produced)
-__device__ __forceinline__ void mma16816_c4(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                            uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4]) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-}
-
-// Two 2-bit codes at bits 2j and 16+2j of w -> an fp16x2 operand whose
-// halves are 1 + code/4 (code placed in the top two fraction bits of 1.0):
-// exact, one LOP3 after a left shift (a multiply by a power of two). w8 is
-// w >> 8, taken once per word, so pairs j >= 4 need no right shift. The
-// constant 1 is removed in the fp32 epilogues.
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w8, int j) {
-    const uint32_t x = (j < 4) ? w * (1u << (8 - 2 * j)) : (j == 4 ? w : w8 * (1u << (16 - 2 * j)));
-    return (x & 0x03000300u) | 0x3C003C00u;
-}
-// The 3-bit analogue: the low two bits of a pair from its 2-bit word w (pair
-// j, w8 = w >> 8) moved to fraction bits 7..8, the high bit from the 1-bit
-// plane word hw (bit jh of each half, hw8 = hw >> 8 for jh >= 8) moved to
-// bit 9, or-ed with 1.0: the exact fp16x2 (1 + code_lo/8, 1 + code_hi/8).
-__device__ __forceinline__ uint32_t code_triple(uint32_t w, uint32_t w8, uint32_t hw, uint32_t hw8, int j,
-                                                int jh) {
-    const uint32_t x2 = (j < 4) ? w * (1u << (7 - 2 * j)) : w8 * (1u << (15 - 2 * j));
-    const uint32_t x1 = (jh < 8) ? hw * (1u << (9 - jh)) : hw8 * (1u << (17 - jh));
-    return (x2 & 0x01800180u) | ((x1 & 0x02000200u) | 0x3C003C00u);
-}
-
-// The 4-bit analogue: field j (0..3) of each half of w (bits 4j..4j+3 and
-// 16+4j..) moved to fp16 mantissa bits 6..9 and or-ed with 1.0, giving the
-// exact fp16x2 (1 + code_lo/16, 1 + code_hi/16); w8 = w >> 8 as above.
-__device__ __forceinline__ uint32_t code_quad(uint32_t w, uint32_t w8, int j) {
-    const uint32_t x = (j < 2) ? w * (1u << (6 - 4 * j)) : w8 * (1u << (14 - 4 * j));
-    return (x & 0x03C003C0u) | 0x3C003C00u;
-}
-
-// Scaled-subnormal operands (decode kernel). A code field masked out of a
+// Scaled-subnormal code operands (decode and prefill). A code field masked out of a
 // record word in place is an fp16 subnormal, its value the code times a
 // power of two set by the field's bit position; one multiply by the inverse
 // power brings every code to the same exact normal value code * 2^-9. One

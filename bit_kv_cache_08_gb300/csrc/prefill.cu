@@ -15,15 +15,16 @@
 // are the MMA rows and the keys the columns, so every 2-bit code is turned
 // into a tensor-core operand once for all 8 vectors:
 //   QK  A = q' (vector gq in row gq as fp16 hi, row gq + 8 as lo), B = the
-//       K codes as exact fp16 1 + code/4, straight from the lane's record
-//       (n-tile i holds tokens 4n + i of a 32-token sub-block); one
-//       accumulator per 32-channel group started at (-Q'_g, 0)
+//       K codes as exact fp16 code * 2^-9, straight from the lane's record
+//       (one mask leaves a subnormal, one fp16 multiply by a power of two
+//       makes it normal; n-tile i holds tokens 4n + i of a 32-token
+//       sub-block); one accumulator per 32-channel group
 //   the score accumulator layout leaves lane (gq, tq) with tokens
 //   8tq .. 8tq + 7 of each sub-block for vector gq, which is exactly the
 //   A-operand layout of the PV product, so P never leaves registers
 //   PV  A = P'_g = p R s_g lam (hi rows, lo rows), B = the V codes
 //       (n = channel, k = token), one group at a time; the block's result
-//       is folded into O with the per-channel factor 4 C / lam at once.
+//       is folded into O with the per-channel factor 2^9 C / lam at once.
 //       P' is an fp16 two-product of P'' = p R lam (hi | lo once per token)
 //       with the group's steps; the zero-point sums of all groups come from
 //       two MMAs per 32 tokens (B columns z_0..z_3 | s_0..s_3).
@@ -34,8 +35,7 @@
 // sum, 128 rotated accumulators) per split goes to one workspace partial;
 // the merge kernel combines a row's partials, adds the raw bf16 tail rows,
 // rotates back once and normalises. 3- and 4-bit codes take the same path with 48- and 64-byte
-// records and a = 1 + code/8 or 1 + code/16 (every factor 4 above becomes 8
-// or 16).
+// records (the same code * 2^-9 operands).
 #include <algorithm>
 
 #include "attn_common.cuh"
@@ -43,15 +43,6 @@
 namespace kvarn {
 
 namespace {
-
-// d = A B + (c0, c0, c1, c1): rows gq start at c0, rows gq + 8 at c1
-__device__ __forceinline__ void mma16816_rows(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1, float c0, float c1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%10,%10,%11,%11};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
-}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -86,7 +77,6 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
     constexpr int HB = head_block_bytes(B, BITS);
     constexpr int NSB = B / 32;
     constexpr int RW = 4 * BITS;              // 32-bit words per lane record
-    constexpr float kLevels = 1 << BITS;      // a = 1 + code / 2^BITS
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                                    // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);           // S mbarriers
@@ -96,7 +86,6 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
 
     const int lane = threadIdx.x;
     const int gq = lane >> 2, tq = lane & 3;
-    constexpr uint32_t kOnes = 0x3C003C00u;
 
     const int G = a.G, n_kv = a.n_kv, n_q = a.n_q, chunk = a.chunk, max_blocks = a.max_blocks;
     const int P = kPrefillVecs / G;                       // chunk rows per warp
@@ -156,7 +145,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 const float sc = exp2i(12 - e);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) x[k] *= sc;
-                km = kLevels * exp2i(e - 12) * a.sm_scale * kLog2e;
+                km = (1.0f / kCodeScale) * exp2i(e - 12) * a.sm_scale * kLog2e;
             }
             uint16_t hi[4], lo[4];
 #pragma unroll
@@ -253,16 +242,16 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                     qa_l[4 * g + e2] = h2_as_u32(lo);
                 }
             }
-            // ---- Q'_g of vector gq: the same A against an all-ones B
-            float Qneg[4], Qq[4];
+            // ---- Q'_g * 2^-9 of vector gq: the same A against a B of 2^-9 everywhere
+            float Qq[4];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma16816(d, qa_h[4 * g], qa_l[4 * g], qa_h[4 * g + 1], qa_l[4 * g + 1], kOnes, kOnes);
-                mma16816(d, qa_h[4 * g + 2], qa_l[4 * g + 2], qa_h[4 * g + 3], qa_l[4 * g + 3], kOnes, kOnes);
-                const float qg = d[0] + d[2];
-                Qneg[g] = -qg;
-                Qq[g] = qg * (1.0f / kLevels);
+                float d[4];
+                mma16816_acc(d, true, qa_h[4 * g], qa_l[4 * g], qa_h[4 * g + 1], qa_l[4 * g + 1], kCodeScaleH2,
+                             kCodeScaleH2);
+                mma16816(d, qa_h[4 * g + 2], qa_l[4 * g + 2], qa_h[4 * g + 3], qa_l[4 * g + 3], kCodeScaleH2,
+                         kCodeScaleH2);
+                Qq[g] = d[0] + d[2];
             }
             const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, BITS));
             const uint16_t* Kz = reinterpret_cast<const uint16_t*>(Kb + off_z(B, BITS));
@@ -312,24 +301,20 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                             uint32_t b0, b1;
                             if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
                                 const int wi = 2 * i + (g >> 1), jj = 4 * (g & 1) + 2 * kk;
-                                b0 = code_pair(kw[wi], kw8[wi], jj);
-                                b1 = code_pair(kw[wi], kw8[wi], jj + 1);
+                                b0 = code2_s(kw[wi], kw8[wi], jj);
+                                b1 = code2_s(kw[wi], kw8[wi], jj + 1);
                             } else if (BITS == 3) {   // + the high bit: word 8 + i, bit 8(g/2) + pair
                                 const int wi = 2 * i + (g >> 1), jj = 4 * (g & 1) + 2 * kk, wh = 8 + i;
                                 const int jh = 8 * (g >> 1) + jj;
-                                b0 = code_triple(kw[wi], kw8[wi], kw[wh], kw8[wh], jj, jh);
-                                b1 = code_triple(kw[wi], kw8[wi], kw[wh], kw8[wh], jj + 1, jh + 1);
+                                b0 = code3_s(kw[wi], kw8[wi], kw[wh], jj, jh);
+                                b1 = code3_s(kw[wi], kw8[wi], kw[wh], jj + 1, jh + 1);
                             } else {           // word 4i + g, field e/2
                                 const int wi = 4 * i + g;
-                                b0 = code_quad(kw[wi], kw8[wi], 2 * kk);
-                                b1 = code_quad(kw[wi], kw8[wi], 2 * kk + 1);
+                                b0 = code4_s(kw[wi], kw8[wi], 2 * kk);
+                                b1 = code4_s(kw[wi], kw8[wi], 2 * kk + 1);
                             }
                             const int qi = 4 * g + 2 * kk;
-                            if (kk == 0)
-                                mma16816_rows(acc[g], qa_h[qi], qa_l[qi], qa_h[qi + 1], qa_l[qi + 1], b0, b1,
-                                              Qneg[g], 0.f);
-                            else
-                                mma16816(acc[g], qa_h[qi], qa_l[qi], qa_h[qi + 1], qa_l[qi + 1], b0, b1);
+                            mma16816_acc(acc[g], kk == 0, qa_h[qi], qa_l[qi], qa_h[qi + 1], qa_l[qi + 1], b0, b1);
                         }
                     }
                     // column 2tq: token t0 + i; column 2tq + 1: token t0 + 4 + i (hi + lo rows)
@@ -429,7 +414,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                     ph[sb][k] = h2_as_u32(hh);
                     pl[sb][k] = h2_as_u32(__float22half2_rn(__ffma2_rn(__half22float2(hh), make_float2(-1.f, -1.f), v)));
                 }
-            const float il4 = kLevels / lam;
+            const float il4 = (1.0f / kCodeScale) / lam;
             const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 
             // ---------------- zero-point sums by MMA: A = P'' (hi rows, lo rows), B columns
@@ -443,13 +428,11 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 mma16816(Dz, ph[sb][2], pl[sb][2], ph[sb][3], pl[sb][3], zs4.z, zs4.w);
             }
             // this lane: columns 2tq, 2tq + 1 of vector gq (hi + lo rows): tq < 2 holds
-            // Z of groups 2tq, 2tq + 1, tq >= 2 holds S of groups 2tq - 4, 2tq - 3;
-            // zq[g] = Z_g / 2^BITS - S_g for the 4 lanes of vector gq
+            // Z of groups 2tq, 2tq + 1; zq[g] = Z_g * 2^-9 for the 4 lanes of vector gq
             float zq[4];
             {
                 const float c0 = Dz[0] + Dz[2], c1 = Dz[1] + Dz[3];
-                const float s0 = __shfl_xor_sync(kFull, c0, 2), s1 = __shfl_xor_sync(kFull, c1, 2);
-                const float zA = c0 * (1.0f / kLevels) - s0, zB = c1 * (1.0f / kLevels) - s1;   // valid at tq < 2
+                const float zA = c0 * kCodeScale, zB = c1 * kCodeScale;   // valid at tq < 2
                 const int base = lane & ~3;
                 zq[0] = __shfl_sync(kFull, zA, base);
                 zq[1] = __shfl_sync(kFull, zB, base);
@@ -496,21 +479,21 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                         for (int f = 0; f < 4; ++f) {
                             if (BITS == 2) {   // pair 4(d/4) + 2((d%4)/2) + f%2
                                 const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
-                                mma16816(Ob[f], a0, a1, a2, a3, code_pair(w, w8, 4 * kt + (f & 1)),
-                                         code_pair(w, w8, 4 * kt + 2 + (f & 1)));
+                                mma16816(Ob[f], a0, a1, a2, a3, code2_s(w, w8, 4 * kt + (f & 1)),
+                                         code2_s(w, w8, 4 * kt + 2 + (f & 1)));
                             } else if (BITS == 3) {   // + the high bit at 8(f/2) + pair in word 8 + g
                                 const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
                                 const int j0 = 4 * kt + (f & 1), j1 = j0 + 2, hb = 8 * (f >> 1);
-                                mma16816(Ob[f], a0, a1, a2, a3, code_triple(w, w8, vw[2], vw8[2], j0, hb + j0),
-                                         code_triple(w, w8, vw[2], vw8[2], j1, hb + j1));
+                                mma16816(Ob[f], a0, a1, a2, a3, code3_s(w, w8, vw[2], j0, hb + j0),
+                                         code3_s(w, w8, vw[2], j1, hb + j1));
                             } else {           // field d/2
-                                mma16816(Ob[f], a0, a1, a2, a3, code_quad(vw[f], vw8[f], 2 * kt),
-                                         code_quad(vw[f], vw8[f], 2 * kt + 1));
+                                mma16816(Ob[f], a0, a1, a2, a3, code4_s(vw[f], vw8[f], 2 * kt),
+                                         code4_s(vw[f], vw8[f], 2 * kt + 1));
                             }
                         }
                     }
                 }
-                // O += 2^BITS C_c / lam * (Ob + Z/2^BITS - S): lane holds channels 32g + 8tq + f (column 2tq)
+                // O += 2^9 C_c / lam * (Ob + Z * 2^-9): lane holds channels 32g + 8tq + f (column 2tq)
                 // and 32g + 8tq + 4 + f (column 2tq + 1)
                 const uint4 c4 = *reinterpret_cast<const uint4*>(VC + 32 * g + 8 * tq);
                 const float2 il42 = make_float2(il4, il4), zq2 = make_float2(zq[g], zq[g]);
