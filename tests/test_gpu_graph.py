@@ -61,3 +61,59 @@ def test_captured_decode_step_equals_eager(kvlib, B):
     for st, p in zip(layers, pools):
         assert torch.equal(st["cache"].pool, p)
     assert np.isfinite(eager.cpu().numpy()).all()
+
+
+def test_bench_step_state_after_replays_matches_the_oracle(kvlib):
+    """The benchmark's own step on the Qwen3-4B workload (two of its layers at
+    full size, built by bench.py's recipe), captured as a CUDA graph and
+    replayed: afterwards the block every append completed and the attention
+    output of sampled sequences of the last layer match the oracle over the
+    GPU's cache bytes."""
+    import bench
+    import oracle
+    from kvtest_util import assert_code_flip_rate, attn_close, bf16_bits, staged_quantize_parity
+    from collections import Counter
+    kv = kvlib
+    w = synth.QWEN3_4B_CACHE
+    state = bench.build_layers(kv, w, 2, "cuda")
+    B, nb = w.block, w.ctx // w.block
+    ws = kv.alloc_workspace(state[0]["cfg"], w.batch, nb)
+    pos = torch.full((w.batch,), w.ctx - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((w.batch,), w.ctx, dtype=torch.int32, device="cuda")
+    out = torch.full((2, w.batch, w.n_q, D), float("nan"), device="cuda")
+
+    def step():
+        for l, st in enumerate(state):
+            kv.append(st["cfg"], st["pool"], st["staging"], st["bt"], pos, st["k_new"], st["v_new"], ws)
+            kv.decode_attn(st["cfg"], st["q"], st["pool"], st["staging"], st["bt"], lens, out[l], ws)
+
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    out.fill_(float("nan"))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert kv.read_error(ws) == 0
+    st = state[1]
+    sb = [int(x) for x in st["cfg"].sign_bits]
+    pool_np = st["pool"].cpu().numpy()
+    bt_np = st["bt"].cpu().numpy()
+    hb, bb = kv.head_block_bytes(st["cfg"]), kv.block_bytes(st["cfg"])
+    # the completed block of (sequence 63, kv head 5): staged rows + the appended one
+    b, h = 63, 5
+    total = Counter()
+    for kind, new in ((0, st["k_new"]), (1, st["v_new"])):
+        rows = np.concatenate([oracle.bf16_array_to_f64(bf16_bits(st["staging"][b, h, kind, :B - 1])),
+                               oracle.bf16_array_to_f64(bf16_bits(new[b, h][None]))])
+        o = int(bt_np[b, nb - 1]) * bb + (2 * h + kind) * hb
+        total.update(staged_quantize_parity(rows[None], pool_np.reshape(-1)[o:o + hb][None], B, w.iters, kind, sb))
+    assert_code_flip_rate(total)
+    seqs = [0, 37, 63]
+    qn = st["q"][seqs].double().cpu().numpy()
+    ref = oracle.decode_attention(B, w.n_q, w.n_kv, sb, 1.0 / np.sqrt(D), qn, pool_np,
+                                  bf16_bits(st["staging"][seqs]), np.ascontiguousarray(bt_np[seqs]),
+                                  np.full(len(seqs), w.ctx, dtype=np.int32))
+    attn_close(out[1].cpu().double().numpy()[seqs], ref)

@@ -70,7 +70,8 @@ def test_phi4_long_horizon_pseudo_decode(kvlib, layer):
           f"{curve[0]}, 1024 {curve[1023]}, 4096 {curve[4095]}, {steps} {curve[-1]}")
 
 
-@pytest.mark.parametrize("batch,ctx", [(1, 131072), (8, 32768), (256, 1024), (128, 8192), (32, 131072), (256, 32768)])
+@pytest.mark.parametrize("batch,ctx", [(1, 131072), (8, 32768), (256, 1024), (128, 8192), (32, 131072), (256, 32768),
+                                       (128, 32768), (256, 131072)])
 def test_llama_sweep_point(kvlib, batch, ctx):
     kv = kvlib
     w = synth.sweep_point(batch, ctx)
