@@ -61,8 +61,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // ---------------------------------------------------------------- the split-K kernel
 // Shared memory for q: fp32 [4][128] at B = 32; at B = 64 the fp16 planes hi,
-// -hi, lo ([4][128] each, the first two over the fp32 copy) and a zero line.
-__host__ __device__ constexpr int attn_q_bytes(int B) { return B == 64 ? 3 * 4 * kD * 2 + 2 * kD : 4 * kD * 4; }
+// -hi, lo ([4][128] each, over the fp32 copy) and a zero line.
+// At B = 64 the planes sit at byte offsets 0, 1088, 2176 and 3264 (in fp16
+// elements below): a lane reading the hi | lo column of the B operand and its
+// neighbour reading the other part of the same head then hit opposite halves
+// of the banks (offsets 64 bytes apart mod 128). The 192 bytes this adds keep
+// a CTA at 18 432 bytes, 12 per SM.
+constexpr int kQHi = 0, kQNegHi = 544, kQLo = 1088, kQZero = 1632;
+__host__ __device__ constexpr int attn_q_bytes(int B) { return B == 64 ? 2 * kQZero + 2 * kD : 4 * kD * 4; }
+// P'' exchange rows [hi|lo][4 heads][B] fp16: row r holds its tokens rotated
+// by pex_rot(r) elements (mod B), so that the four heads' rows written by one
+// store instruction fall on different banks without padding
+__host__ __device__ constexpr int pex_rot(int B, int r) { return B == 64 ? 16 * r : 16 * (r >> 1); }
 
 template <int B, int BITS, int S>
 __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
@@ -163,13 +173,21 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     // B = 64: q's fp16 planes [4][128] each: hi at 0, -hi at 4*128, lo at
     // 8*128, then 128 zeros; this lane reads (hi | -hi), (0 | hi), (0 | lo)
     const uint16_t* qpl = reinterpret_cast<const uint16_t*>(qsm);
-    const uint16_t* q_n = qpl + (part ? 4 * kD : 0) + hbq * kD + 8 * tq;
-    const uint16_t* q_z = part ? qpl + hbq * kD + 8 * tq : qpl + 12 * kD + 8 * tq;
-    const uint16_t* q_l = part ? qpl + 8 * kD + hbq * kD + 8 * tq : qpl + 12 * kD + 8 * tq;
-    if constexpr (kLean) reinterpret_cast<uint2*>(qsm)[3 * kD + lane] = make_uint2(0u, 0u);   // the zero line (byte 3072)
+    const uint16_t* q_n = qpl + (part ? kQNegHi : kQHi) + hbq * kD + 8 * tq;
+    const uint16_t* q_z = part ? qpl + kQHi + hbq * kD + 8 * tq : qpl + kQZero + 8 * tq;
+    const uint16_t* q_l = part ? qpl + kQLo + hbq * kD + 8 * tq : qpl + kQZero + 8 * tq;
+    if constexpr (kLean) reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(qsm) + kQZero)[lane] = make_uint2(0u, 0u);
     // B = 64: this lane's P'' hi | lo rows of pex (the zero line for heads >= G)
-    const uint16_t* px_h = bcol_ok ? pex + hbq * B + 8 * tq : qpl + 12 * kD + 8 * tq;
-    const uint16_t* px_l = bcol_ok ? pex + (4 + hbq) * B + 8 * tq : qpl + 12 * kD + 8 * tq;
+    const uint16_t* px_h = bcol_ok ? pex + hbq * B : qpl + kQZero;
+    const uint16_t* px_l = bcol_ok ? pex + (4 + hbq) * B : qpl + kQZero;
+    // this lane's P'' element offsets in those rows (rotated, see pex_rot): the
+    // store of tokens 32 sb + 4 gq .. in row tq, the loads of 32 sb + 8 tq .. in row hbq
+    int px_st[NSB], px_ld[NSB];
+#pragma unroll
+    for (int sb = 0; sb < NSB; ++sb) {
+        px_st[sb] = (32 * sb + 4 * gq + pex_rot(B, tq)) % B;
+        px_ld[sb] = bcol_ok ? (32 * sb + 8 * tq + pex_rot(B, hbq)) % B : 32 * sb + 8 * tq;
+    }
 
     auto unit_setup = [&]() {
         __syncwarp();
@@ -202,8 +220,9 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 qv[j] = j < G ? *reinterpret_cast<const float4*>(&qsm[j * kD + 4 * lane])
                               : make_float4(0.f, 0.f, 0.f, 0.f);
             __syncwarp();
-            uint16_t* qhp = reinterpret_cast<uint16_t*>(qsm);
-            uint16_t* qlp = qhp + 8 * kD;
+            uint16_t* qhp = reinterpret_cast<uint16_t*>(qsm) + kQHi;
+            uint16_t* qnp = reinterpret_cast<uint16_t*>(qsm) + kQNegHi;
+            uint16_t* qlp = reinterpret_cast<uint16_t*>(qsm) + kQLo;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float v[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
@@ -215,7 +234,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                     lw[k] = pack_h2(v[2 * k] - __half2float(h0), v[2 * k + 1] - __half2float(h1));
                 }
                 *reinterpret_cast<uint2*>(qhp + j * kD + 4 * lane) = make_uint2(hw[0], hw[1]);
-                *reinterpret_cast<uint2*>(qhp + (4 + j) * kD + 4 * lane) =
+                *reinterpret_cast<uint2*>(qnp + j * kD + 4 * lane) =
                     make_uint2(hw[0] ^ 0x80008000u, hw[1] ^ 0x80008000u);
                 *reinterpret_cast<uint2*>(qlp + j * kD + 4 * lane) = make_uint2(lw[0], lw[1]);
             }
@@ -496,8 +515,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                     hw[mt] = h2_as_u32(h);
                     lw[mt] = h2_as_u32(__float22half2_rn(__fadd2_rn(v, make_float2(-hf.x, -hf.y))));
                 }
-                uint16_t* ph = pex + (0 * 4 + tq) * B + 32 * sb + 4 * gq;
-                uint16_t* pl = pex + (1 * 4 + tq) * B + 32 * sb + 4 * gq;
+                uint16_t* ph = pex + (0 * 4 + tq) * B + px_st[sb];
+                uint16_t* pl = pex + (1 * 4 + tq) * B + px_st[sb];
                 *reinterpret_cast<uint2*>(ph) = make_uint2(hw[0], hw[1]);
                 *reinterpret_cast<uint2*>(pl) = make_uint2(lw[0], lw[1]);
             }
@@ -512,13 +531,13 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 // this lane's B column (head hbq, part) for tokens 32sb + 8tq .. +7
                 uint4 phv, plv;
                 if constexpr (kLean) {
-                    phv = *reinterpret_cast<const uint4*>(px_h + 32 * sb);
-                    plv = *reinterpret_cast<const uint4*>(px_l + 32 * sb);
+                    phv = *reinterpret_cast<const uint4*>(px_h + px_ld[sb]);
+                    plv = *reinterpret_cast<const uint4*>(px_l + px_ld[sb]);
                 } else {
                     phv = make_uint4(0, 0, 0, 0); plv = make_uint4(0, 0, 0, 0);
                     if (bcol_ok) {
-                        phv = *reinterpret_cast<const uint4*>(pex + (0 * 4 + hbq) * B + 32 * sb + 8 * tq);
-                        plv = *reinterpret_cast<const uint4*>(pex + (1 * 4 + hbq) * B + 32 * sb + 8 * tq);
+                        phv = *reinterpret_cast<const uint4*>(pex + (0 * 4 + hbq) * B + px_ld[sb]);
+                        plv = *reinterpret_cast<const uint4*>(pex + (1 * 4 + hbq) * B + px_ld[sb]);
                     }
                 }
                 const uint32_t ph[4] = {phv.x, phv.y, phv.z, phv.w};
