@@ -44,9 +44,9 @@
 // 3- and 4-bit codes (BITS = 3, 4) take the same path: a lane's record is
 // 48 or 64 bytes and a = code * 2^-9 as well (a 3-bit field is joined from
 // the 2-bit word and the 1-bit plane by one shift and two LOP3s; a 4-bit
-// field is masked in place). The kernel's name keeps the method's width. At
-// B = 64 q's hi | lo halves are read from shared memory per block (32 fewer
-// registers).
+// field is masked in place). The kernel's name keeps the method's width.
+// q's hi | lo halves are read from shared memory per block rather than held
+// in 32 registers per lane.
 #include "attn_common.cuh"
 
 namespace kvarn {
@@ -60,15 +60,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---------------------------------------------------------------- the split-K kernel
-// Shared memory for q: fp32 [4][128] at B = 32; at B = 64 the fp16 planes hi,
-// -hi, lo ([4][128] each, over the fp32 copy) and a zero line.
-// At B = 64 the planes sit at byte offsets 0, 1088, 2176 and 3264 (in fp16
-// elements below): a lane reading the hi | lo column of the B operand and its
-// neighbour reading the other part of the same head then hit opposite halves
-// of the banks (offsets 64 bytes apart mod 128). The 192 bytes this adds keep
-// a CTA at 18 432 bytes, 12 per SM.
+// Shared memory for q: the fp16 planes hi, -hi, lo ([4][128] each, written
+// over the fp32 copy of q) and a zero line, at byte offsets 0, 1088, 2176 and
+// 3264 (in fp16 elements below): a lane reading the hi | lo column of the B
+// operand and its neighbour reading the other part of the same head then hit
+// opposite halves of the banks (offsets 64 bytes apart mod 128). The 192
+// bytes this adds keep a B = 64 CTA at 18 432 bytes, 12 per SM. Keeping q in
+// shared memory rather than in 32 registers per lane lets B = 32 run 16 warps
+// per SM (128 registers) instead of 12.
 constexpr int kQHi = 0, kQNegHi = 544, kQLo = 1088, kQZero = 1632;
-__host__ __device__ constexpr int attn_q_bytes(int B) { return B == 64 ? 2 * kQZero + 2 * kD : 4 * kD * 4; }
+__host__ __device__ constexpr int attn_q_bytes(int) { return 2 * kQZero + 2 * kD; }
 // P'' exchange rows [hi|lo][4 heads][B] fp16: row r holds its tokens rotated
 // by pex_rot(r) elements (mod B), so that the four heads' rows written by one
 // store instruction fall on different banks without padding
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                              // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);     // S mbarriers
-    float* qsm = reinterpret_cast<float*>(smem + S * 2 * HB + 64);       // [4][128] fp32 q (and at B = 64 the fp16 planes below)
+    float* qsm = reinterpret_cast<float*>(smem + S * 2 * HB + 64);       // [4][128] fp32 q, then the fp16 planes below
     uint16_t* pex = reinterpret_cast<uint16_t*>(smem + S * 2 * HB + 64 + attn_q_bytes(B));   // [hi|lo][4 heads][B]
 
     const int lane = threadIdx.x;
@@ -103,9 +104,6 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const float sm_scale = a.sm_scale;
     const uint32_t sb0 = a.sb[0], sb1 = a.sb[1], sb2 = a.sb[2], sb3 = a.sb[3];
     const bool rotate_q = !(a.flags & KVARN_FLAG_NO_ROTATION);
-    // B = 64 (measured): q's hi | lo halves live in shared memory instead of 32
-    // registers
-    constexpr bool kLean = B == 64;
 
     const SplitArgs sp{a.seq_lens, a.batch, n_kv, max_blocks, B, 0, 1};
     Cursor cc;
@@ -153,7 +151,6 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     }
 
     // per-unit state
-    uint32_t Qh[kLean ? 1 : 16], Ql[kLean ? 1 : 16];   // q_rot*2^(12-e) as fp16 hi | lo (lo only on lo-column lanes)
     float kmul = 0.f;          // 2^9 * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
     float m_run = -INFINITY, l_part = 0.f;
     float2 O[8];               // rotated output, channels 32g + 4gq + 2m + {0, 1}, head tq
@@ -162,22 +159,19 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const bool head_ok = tq < G;            // this lane's score / accumulator head
     const int hbq = gq >> 1, part = gq & 1;  // this lane's B-fragment column: (head, hi|lo)
     const bool bcol_ok = hbq < G;
-    // (-1,-1) on the lanes holding a lo column, (0,0) on the hi ones: the
-    // two-product's correction term is multiplied by it instead of selected
-    const __half2 nmask = part ? __float2half2_rn(-1.f) : __float2half2_rn(0.f);
     // The same two-products in three operations: t = RN(x * y) negated on the
     // lo-column lanes, then fma(x_z, y, t) with x_z = x there and 0 on the hi
     // ones (-RN(xy) + xy exact | RN(xy)), then + lo * y.
     const __half2 pneg = part ? __float2half2_rn(-1.f) : __float2half2_rn(1.f);
     const __half2 pone = part ? __float2half2_rn(1.f) : __float2half2_rn(0.f);
-    // B = 64: q's fp16 planes [4][128] each: hi at 0, -hi at 4*128, lo at
-    // 8*128, then 128 zeros; this lane reads (hi | -hi), (0 | hi), (0 | lo)
+    // q's fp16 planes [4][128] each (hi, -hi, lo) and a zero line; this lane
+    // reads (hi | -hi), (0 | hi), (0 | lo) for its B-fragment column
     const uint16_t* qpl = reinterpret_cast<const uint16_t*>(qsm);
     const uint16_t* q_n = qpl + (part ? kQNegHi : kQHi) + hbq * kD + 8 * tq;
     const uint16_t* q_z = part ? qpl + kQHi + hbq * kD + 8 * tq : qpl + kQZero + 8 * tq;
     const uint16_t* q_l = part ? qpl + kQLo + hbq * kD + 8 * tq : qpl + kQZero + 8 * tq;
-    if constexpr (kLean) reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(qsm) + kQZero)[lane] = make_uint2(0u, 0u);
-    // B = 64: this lane's P'' hi | lo rows of pex (the zero line for heads >= G)
+    reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(qsm) + kQZero)[lane] = make_uint2(0u, 0u);
+    // this lane's P'' hi | lo rows of pex (the zero line for heads >= G)
     const uint16_t* px_h = bcol_ok ? pex + hbq * B : qpl + kQZero;
     const uint16_t* px_l = bcol_ok ? pex + (4 + hbq) * B : qpl + kQZero;
     // this lane's P'' element offsets in those rows (rotated, see pex_rot): the
@@ -212,7 +206,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             if (j == tq) kmul = (1.0f / kCodeScale) * exp2i(e - 12) * sm_scale * kLog2e;
         }
         __syncwarp();
-        if constexpr (kLean) {
+        {
             // fp16 hi, -hi and lo planes [4][128] each, over the fp32 copy (rows of heads >= G zero)
             float4 qv[4];
 #pragma unroll
@@ -237,20 +231,6 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 *reinterpret_cast<uint2*>(qnp + j * kD + 4 * lane) =
                     make_uint2(hw[0] ^ 0x80008000u, hw[1] ^ 0x80008000u);
                 *reinterpret_cast<uint2*>(qlp + j * kD + 4 * lane) = make_uint2(lw[0], lw[1]);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c0 = 32 * (i >> 2) + 8 * tq + 2 * (i & 3);
-                uint32_t hv = 0, lv = 0;
-                if (bcol_ok) {
-                    const float v0 = qsm[hbq * kD + c0], v1 = qsm[hbq * kD + c0 + 1];
-                    const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-                    hv = h2_as_u32(__halves2half2(h0, h1));
-                    lv = pack_h2(v0 - __half2float(h0), v1 - __half2float(h1));
-                }
-                Qh[i] = hv;
-                Ql[i] = part ? lv : 0u;
             }
         }
         if (!head_ok) kmul = 0.f;
@@ -340,30 +320,18 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             for (int g = 0; g < 4; ++g) {
                 const uint4 c4 = *reinterpret_cast<const uint4*>(KC + 32 * g + 8 * tq);
                 const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
-                if constexpr (kLean) {
-                    const uint4 n4 = *reinterpret_cast<const uint4*>(q_n + 32 * g);
-                    const uint4 z4 = *reinterpret_cast<const uint4*>(q_z + 32 * g);
-                    const uint4 l4 = *reinterpret_cast<const uint4*>(q_l + 32 * g);
-                    const uint32_t nw[4] = {n4.x, n4.y, n4.z, n4.w};
-                    const uint32_t zw[4] = {z4.x, z4.y, z4.z, z4.w};
-                    const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
+                const uint4 n4 = *reinterpret_cast<const uint4*>(q_n + 32 * g);
+                const uint4 z4 = *reinterpret_cast<const uint4*>(q_z + 32 * g);
+                const uint4 l4 = *reinterpret_cast<const uint4*>(q_l + 32 * g);
+                const uint32_t nw[4] = {n4.x, n4.y, n4.z, n4.w};
+                const uint32_t zw[4] = {z4.x, z4.y, z4.z, z4.w};
+                const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
-                        __half2 r = __hfma2(u32_as_h2(zw[e2]), C2, __hmul2(u32_as_h2(nw[e2]), C2));
-                        r = __hfma2(u32_as_h2(lw[e2]), C2, r);
-                        bq[4 * g + e2] = h2_as_u32(r);
-                    }
-                } else {
-#pragma unroll
-                    for (int e2 = 0; e2 < 4; ++e2) {
-                        const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
-                        const __half2 qh = u32_as_h2(Qh[4 * g + e2]);
-                        const __half2 mneg = __hmul2(__hmul2(qh, C2), nmask);   // -RN(qh*C) | 0
-                        __half2 r = __hfma2(qh, C2, mneg);
-                        r = __hfma2(u32_as_h2(Ql[4 * g + e2]), C2, r);
-                        bq[4 * g + e2] = h2_as_u32(r);
-                    }
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
+                    __half2 r = __hfma2(u32_as_h2(zw[e2]), C2, __hmul2(u32_as_h2(nw[e2]), C2));
+                    r = __hfma2(u32_as_h2(lw[e2]), C2, r);
+                    bq[4 * g + e2] = h2_as_u32(r);
                 }
             }
             // ---- Q'_g * 2^-9 for this lane's head: an MMA whose A operand is 2^-9
@@ -529,17 +497,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
                 // this lane's B column (head hbq, part) for tokens 32sb + 8tq .. +7
-                uint4 phv, plv;
-                if constexpr (kLean) {
-                    phv = *reinterpret_cast<const uint4*>(px_h + px_ld[sb]);
-                    plv = *reinterpret_cast<const uint4*>(px_l + px_ld[sb]);
-                } else {
-                    phv = make_uint4(0, 0, 0, 0); plv = make_uint4(0, 0, 0, 0);
-                    if (bcol_ok) {
-                        phv = *reinterpret_cast<const uint4*>(pex + (0 * 4 + hbq) * B + px_ld[sb]);
-                        plv = *reinterpret_cast<const uint4*>(pex + (1 * 4 + hbq) * B + px_ld[sb]);
-                    }
-                }
+                const uint4 phv = *reinterpret_cast<const uint4*>(px_h + px_ld[sb]);
+                const uint4 plv = *reinterpret_cast<const uint4*>(px_l + px_ld[sb]);
                 const uint32_t ph[4] = {phv.x, phv.y, phv.z, phv.w};
                 const uint32_t pl[4] = {plv.x, plv.y, plv.z, plv.w};
                 uint32_t plm[4], pa[4], hpn[4], hpz[4];
@@ -666,7 +625,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 
 // ---------------------------------------------------------------- host side
 template <int B, int BITS>
-constexpr int stages_for() { return B == 32 ? 4 : 2; }
+constexpr int stages_for() { return 2; }
 
 template <int B, int BITS>
 size_t attn_smem_bytes() {
