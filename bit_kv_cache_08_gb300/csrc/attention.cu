@@ -19,32 +19,37 @@
 // shared-memory stages with 1-D bulk copies (cp.async.bulk) counted on
 // mbarriers; all lanes wait with a bounded try_wait. Each lane reads one
 // 32-byte code record per 32 tokens and turns every pair of 2-bit codes into
-// an fp16x2 tensor-core operand a = code * 2^-9 (exact): one LOP3 masks the
-// pair in place, leaving an fp16 subnormal whose value is the code times a
-// power of two fixed by its bit position, and one HMUL2 by the inverse power
-// makes it normal. Everything below runs on mma.sync m16n8k16 (f16 in, f32
-// accumulate) with fp32 epilogues; code * s + z = 2^9 s a + z.
+// an fp16x2 tensor-core operand without a multiply: the record word is
+// shifted so that a field pair sits at bits 6..9 of each half, and one LOP3
+// keeps the even field at bits 6..7 (an fp16 subnormal, a = code * 2^-18) or
+// the odd one at bits 8..9 (a = code * 2^-16); the tensor cores keep full
+// precision for subnormal operands at those bit positions. The factor 4
+// between the two is put into q' for QK (even k-slots x 4) and into the
+// output rows for PV. Below, "a" is the operand at the odd fields' scale
+// (code * 2^-16 = code * kA). Everything runs on mma.sync m16n8k16 (f16 in,
+// f32 accumulate) with fp32 epilogues; code * s + z = s a / kA + z.
 //   q'  = q_rot * C per block, as two fp16 halves (hi | lo) so the tensor
 //         cores keep fp32 accuracy; q_rot is scaled to 2^12 per unit and C by
 //         a power of two per block so both halves stay normal fp16 (fp16
 //         subnormal operands lose precision on the tensor cores).
-//   Q'_g = sum_{c in g} q'_c * 2^-9     (MMA with an A operand of 2^-9)
+//   Q'_g = sum_{c in g} q'_c * kA      (MMA with code-1 A operands)
 //   QK:  acc_g[t][h] = sum_{c in g} a[t][c] q'[c][h]  (one accumulator per
 //        32-channel group, hi and lo columns), then
-//        score[t][h] = 2^9 R_t sum_g (s_tg acc_g + z_tg Q'_g)
+//        score[t][h] = R_t / kA sum_g (s_tg acc_g + z_tg Q'_g)
 //   softmax over the block (running max and sum per head, log2 domain)
 //   PV:  P'[t][h,g] = p_t R_t s_tg lam (hi | lo), lam a power of two per
 //        (head, block) keeping P' inside fp16;
 //        Ob[c][h] = sum_t a[t][c] P'[t][h, g(c)]
 //        zs[h][g] = sum_t p_t R_t lam z_tg  (MMA with p as A, z | s as B)
-//        O[c][h] += 2^9 C_c / lam * (Ob[c][h] + zs[h][g(c)] * 2^-9)  once per block.
+//        O[c][h] += C_c / (kA lam) * (Ob[c][h] + zs[h][g(c)] * kA)  once per block.
 // Operand order inside each MMA (which token is row r, which channel is
 // k-slot j) is chosen so that the packed record order gives every lane its
 // operands directly; the writer packs codes in that order.
-// 3- and 4-bit codes (BITS = 3, 4) take the same path: a lane's record is
-// 48 or 64 bytes and a = code * 2^-9 as well (a 3-bit field is joined from
-// the 2-bit word and the 1-bit plane by one shift and two LOP3s; a 4-bit
-// field is masked in place). The kernel's name keeps the method's width.
+// 3- and 4-bit codes (BITS = 3, 4) take the same path with a lane record of
+// 48 or 64 bytes, but their operands are a = code * 2^-9 for every field
+// (kA = 2^-9): a field masked in place is scaled to that value by one HMUL2
+// (a 3-bit field is first joined from the 2-bit word and the 1-bit plane by
+// one shift and two LOP3s). The kernel's name keeps the method's width.
 // q's hi | lo halves are read from shared memory per block rather than held
 // in 32 registers per lane.
 #include "attn_common.cuh"
@@ -82,6 +87,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     constexpr int HB = head_block_bytes(B, BITS);
     constexpr int RW = 4 * BITS;             // 32-bit words per lane record
     constexpr int NSB = B / 32;
+    // kA: the operand scale of a code (2-bit: odd fields' raw subnormals)
+    constexpr float kA = BITS == 2 ? kRawScale : kCodeScale;
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                              // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);     // S mbarriers
@@ -203,7 +210,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             const float sc = exp2i(12 - e);
             *reinterpret_cast<float4*>(&qsm[j * kD + 4 * lane]) =
                 make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
-            if (j == tq) kmul = (1.0f / kCodeScale) * exp2i(e - 12) * sm_scale * kLog2e;
+            if (j == tq) kmul = (1.0f / kA) * exp2i(e - 12) * sm_scale * kLog2e;
         }
         __syncwarp();
         {
@@ -313,6 +320,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             }
             const int ec = ceil_log2(fmaxf(cmax, kF16MinNormal));
             const __half2 cinv = __float2half2_rn(exp2i(-ec));
+            // 2-bit: the even k-slot of each pair meets codes at 2^-18, so its q' is x 4
+            const __half2 cinv_e = BITS == 2 ? __float2half2_rn(exp2i(2 - ec)) : cinv;
             const float kmb = kmul * exp2i(ec);
             // ---- QK B operand: q' = q_s * C * 2^-ec as fp16 hi | lo (two-product)
             uint32_t bq[16];
@@ -328,21 +337,22 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
-                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
+                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), (e2 & 1) ? cinv : cinv_e);
                     __half2 r = __hfma2(u32_as_h2(zw[e2]), C2, __hmul2(u32_as_h2(nw[e2]), C2));
                     r = __hfma2(u32_as_h2(lw[e2]), C2, r);
                     bq[4 * g + e2] = h2_as_u32(r);
                 }
             }
-            // ---- Q'_g * 2^-9 for this lane's head: an MMA whose A operand is 2^-9
-            // everywhere sums each group (hi + lo columns), at the codes' scale
+            // ---- Q'_g * kA for this lane's head: an MMA whose A operand is a code of
+            // 1 everywhere sums each group (hi + lo columns), at the codes' scale
+            constexpr uint32_t kOneE = BITS == 2 ? kRawOneEven : kCodeScaleH2;
+            constexpr uint32_t kOneO = BITS == 2 ? kRawOneOdd : kCodeScaleH2;
             float Qq[4];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float cq[4];
-                mma16816_acc(cq, true, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, bq[4 * g],
-                             bq[4 * g + 1]);
-                mma16816(cq, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, kCodeScaleH2, bq[4 * g + 2], bq[4 * g + 3]);
+                mma16816_acc(cq, true, kOneE, kOneE, kOneO, kOneO, bq[4 * g], bq[4 * g + 1]);
+                mma16816(cq, kOneE, kOneE, kOneO, kOneO, bq[4 * g + 2], bq[4 * g + 3]);
                 Qq[g] = cq[0] + cq[1];
             }
             const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, BITS));
@@ -365,8 +375,10 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         kw[4 * r] = rr.x; kw[4 * r + 1] = rr.y; kw[4 * r + 2] = rr.z; kw[4 * r + 3] = rr.w;
                     }
                 }
+                if (BITS != 2) {
 #pragma unroll
-                for (int k = 0; k < RW; ++k) kw8[k] = kw[k] >> 8;
+                    for (int k = 0; k < RW; ++k) kw8[k] = kw[k] >> 8;
+                }
                 float acc[4][2][4];   // one chain per (group, 16-token tile)
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
@@ -379,10 +391,11 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                             if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
                                 const int j = 4 * (g & 1) + 2 * kk;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
-                                a0 = code2_s(kw[i0], kw8[i0], j);
-                                a1 = code2_s(kw[i1], kw8[i1], j);
-                                a2 = code2_s(kw[i0], kw8[i0], j + 1);
-                                a3 = code2_s(kw[i1], kw8[i1], j + 1);
+                                const uint32_t c0 = code2_copy(kw[i0], j >> 1), c1 = code2_copy(kw[i1], j >> 1);
+                                a0 = code2_r(c0, j);
+                                a1 = code2_r(c1, j);
+                                a2 = code2_r(c0, j + 1);
+                                a3 = code2_r(c1, j + 1);
                             } else if (BITS == 3) {   // 2-bit word 2i + g/2; high bits in word 8 + i
                                 const int j = 4 * (g & 1) + 2 * kk, jh = 8 * (g >> 1) + j;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
@@ -538,18 +551,22 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         vw[4 * r] = rr.x; vw[4 * r + 1] = rr.y; vw[4 * r + 2] = rr.z; vw[4 * r + 3] = rr.w;
                     }
                 }
+                if (BITS != 2) {
 #pragma unroll
-                for (int k = 0; k < RW; ++k) vw8[k] = vw[k] >> 8;
+                    for (int k = 0; k < RW; ++k) vw8[k] = vw[k] >> 8;
+                }
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     const int g = mt >> 1, m = mt & 1;
                     if (BITS == 2) {   // word 2g + f/2, pair 4(d/4) + 2((d%4)/2) + f%2
-                        const uint32_t wd = vw[2 * g + m], wd8 = vw8[2 * g + m];
+                        // rows gq take the even fields (code * 2^-18), rows gq + 8 the odd ones
+                        const uint32_t wd = vw[2 * g + m];
 #pragma unroll
-                        for (int kt = 0; kt < 2; ++kt)
-                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code2_s(wd, wd8, 4 * kt + 0),
-                                         code2_s(wd, wd8, 4 * kt + 1), code2_s(wd, wd8, 4 * kt + 2),
-                                         code2_s(wd, wd8, 4 * kt + 3), bv[g][2 * kt], bv[g][2 * kt + 1]);
+                        for (int kt = 0; kt < 2; ++kt) {
+                            const uint32_t c0 = code2_copy(wd, 2 * kt), c1 = code2_copy(wd, 2 * kt + 1);
+                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code2_r(c0, 0), code2_r(c0, 1), code2_r(c1, 0),
+                                         code2_r(c1, 1), bv[g][2 * kt], bv[g][2 * kt + 1]);
+                        }
                     } else if (BITS == 3) {   // 2-bit word 2g + f/2; high bits in word 8 + g, bit 8(f/2) + j
                         const int wl = 2 * g + m, wh = 8 + g;
 #pragma unroll
@@ -577,14 +594,16 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             {
                 const float zA = Dz[0] + __shfl_xor_sync(kFull, Dz[0], 4);   // valid where tq < 2:
                 const float zB = Dz[1] + __shfl_xor_sync(kFull, Dz[1], 4);   // groups 2tq, 2tq+1 of head gq/2
-                zq[0] = kCodeScale * __shfl_sync(kFull, zA, 8 * tq);
-                zq[1] = kCodeScale * __shfl_sync(kFull, zB, 8 * tq);
-                zq[2] = kCodeScale * __shfl_sync(kFull, zA, 8 * tq + 1);
-                zq[3] = kCodeScale * __shfl_sync(kFull, zB, 8 * tq + 1);
+                zq[0] = kA * __shfl_sync(kFull, zA, 8 * tq);
+                zq[1] = kA * __shfl_sync(kFull, zB, 8 * tq);
+                zq[2] = kA * __shfl_sync(kFull, zA, 8 * tq + 1);
+                zq[3] = kA * __shfl_sync(kFull, zB, 8 * tq + 1);
             }
-            // ---------------- O += 2^9 C_c / lam * (Ob + zs * 2^-9)
+            // ---------------- O += C_c / (kA lam) * (Ob + zs * kA)
             {
-                const float il4 = (1.0f / kCodeScale) / lam;
+                const float il4 = (1.0f / kA) / lam;
+                // 2-bit: rows gq (x) hold even fields at kA / 4
+                const float2 rw2 = BITS == 2 ? make_float2(4.f, 1.f) : make_float2(1.f, 1.f);
                 const float2 il42 = make_float2(il4, il4);
                 const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 #pragma unroll
@@ -595,7 +614,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {   // channels 32g + 4gq + 2m + {0, 1}
                         const int mt = 2 * g + m;
-                        const float2 t = __fadd2_rn(make_float2(Ob[mt][0] + Ob[mt][1], Ob[mt][2] + Ob[mt][3]), zq2);
+                        const float2 t = __ffma2_rn(make_float2(Ob[mt][0] + Ob[mt][1], Ob[mt][2] + Ob[mt][3]), rw2, zq2);
                         O[mt] = __ffma2_rn(__fmul2_rn(m ? c23 : c01, il42), t, O[mt]);
                     }
                 }

@@ -95,6 +95,29 @@ __device__ __forceinline__ uint32_t code4_s(uint32_t w, uint32_t w8, int j) {
     return scale_sub((j < 2 ? w : w8) & (0x000F000Fu << (4 * k)), k == 0 ? 0x78007800u : 0x68006800u);
 }
 
+// Raw subnormal code operands (2-bit decode). mma.m16n8k16 keeps full
+// precision for subnormal fp16 A operands whose set bits sit at 6 and above:
+// measured against exact sums on the GB300, the worst error is 2^-19.8 of the
+// largest product for a 2-bit field at bits 6..7 and 2^-20 at bits 8..9, as
+// for normal operands, against 2^-13 at bits 0..1 and 2^-18.3 at 4..5. So a
+// record word is shifted four ways (field pairs (0,1), (2,3), (4,5), (6,7) to
+// bits 6..9) and one LOP3 keeps the even field at bits 6..7 (the operand is
+// code * 2^-18) or the odd one at bits 8..9 (code * 2^-16): one shift per
+// two pairs and one mask per pair, all on the ALU pipe, no fp16 multiply.
+// The factor 4 between even and odd fields is carried by the other operand
+// (QK) or by the output row (PV); the common 2^-16 by the fp32 epilogue.
+constexpr float kRawScale = 1.0f / 65536.0f;    // products at the odd fields' scale, code * 2^-16
+constexpr uint32_t kRawOneEven = 0x00400040u;   // code 1 at bits 6..7 of both halves: 2^-18
+constexpr uint32_t kRawOneOdd = 0x01000100u;    // code 1 at bits 8..9 of both halves: 2^-16
+// the shifted copy of w holding fields 2p and 2p + 1 at bits 6..9 of each half
+__device__ __forceinline__ uint32_t code2_copy(uint32_t w, int p) {
+    return p == 0 ? (w << 6) : (p == 1 ? (w << 2) : (p == 2 ? (w >> 2) : (w >> 6)));
+}
+// field j (0..7) of both halves of the word, from its copy code2_copy(w, j >> 1)
+__device__ __forceinline__ uint32_t code2_r(uint32_t copy, int j) {
+    return copy & ((j & 1) ? 0x03000300u : 0x00C000C0u);
+}
+
 // 2^k as a float for k in [-126, 127]
 __device__ __forceinline__ float exp2i(int k) {
     k = max(-126, min(127, k));
