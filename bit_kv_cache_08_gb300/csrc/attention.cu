@@ -19,14 +19,14 @@
 // shared-memory stages with 1-D bulk copies (cp.async.bulk) counted on
 // mbarriers; all lanes wait with a bounded try_wait. Each lane reads one
 // 32-byte code record per 32 tokens and turns every pair of 2-bit codes into
-// an fp16x2 tensor-core operand without a multiply: the record word is
-// shifted so that a field pair sits at bits 6..9 of each half, and one LOP3
-// keeps the even field at bits 6..7 (an fp16 subnormal, a = code * 2^-18) or
-// the odd one at bits 8..9 (a = code * 2^-16); the tensor cores keep full
-// precision for subnormal operands at those bit positions. The factor 4
-// between the two is put into q' for QK (even k-slots x 4) and into the
-// output rows for PV. Below, "a" is the operand at the odd fields' scale
-// (code * 2^-16 = code * kA). Everything runs on mma.sync m16n8k16 (f16 in,
+// an fp16x2 tensor-core operand without a multiply: a shifted or byte-swapped
+// view of the record word holds the pair's field at bits 8..9 (even fields:
+// an fp16 subnormal a = code * 2^-16) or 6..7 (odd fields: code * 2^-18) of
+// each half, and one LOP3 keeps it; the tensor cores keep full precision for
+// subnormal operands at those bit positions. The factor 4 between the two is
+// put into q' for QK (odd k-slots x 4) and into the output rows for PV.
+// Below, "a" is the operand at the even fields' scale (code * 2^-16 =
+// code * kA). Everything runs on mma.sync m16n8k16 (f16 in,
 // f32 accumulate) with fp32 epilogues; code * s + z = s a / kA + z.
 //   q'  = q_rot * C per block, as two fp16 halves (hi | lo) so the tensor
 //         cores keep fp32 accuracy; q_rot is scaled to 2^12 per unit and C by
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     constexpr int HB = head_block_bytes(B, BITS);
     constexpr int RW = 4 * BITS;             // 32-bit words per lane record
     constexpr int NSB = B / 32;
-    // kA: the operand scale of a code (2-bit: odd fields' raw subnormals)
+    // kA: the operand scale of a code (2-bit: even fields' raw subnormals)
     constexpr float kA = BITS == 2 ? kRawScale : kCodeScale;
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                              // S x (K, V)
@@ -320,8 +320,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             }
             const int ec = ceil_log2(fmaxf(cmax, kF16MinNormal));
             const __half2 cinv = __float2half2_rn(exp2i(-ec));
-            // 2-bit: the even k-slot of each pair meets codes at 2^-18, so its q' is x 4
-            const __half2 cinv_e = BITS == 2 ? __float2half2_rn(exp2i(2 - ec)) : cinv;
+            // 2-bit: the odd k-slot of each pair meets codes at 2^-18, so its q' is x 4
+            const __half2 cinv_o = BITS == 2 ? __float2half2_rn(exp2i(2 - ec)) : cinv;
             const float kmb = kmul * exp2i(ec);
             // ---- QK B operand: q' = q_s * C * 2^-ec as fp16 hi | lo (two-product)
             uint32_t bq[16];
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
-                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), (e2 & 1) ? cinv : cinv_e);
+                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), (e2 & 1) ? cinv_o : cinv);
                     __half2 r = __hfma2(u32_as_h2(zw[e2]), C2, __hmul2(u32_as_h2(nw[e2]), C2));
                     r = __hfma2(u32_as_h2(lw[e2]), C2, r);
                     bq[4 * g + e2] = h2_as_u32(r);
@@ -391,11 +391,11 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                             if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
                                 const int j = 4 * (g & 1) + 2 * kk;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
-                                const uint32_t c0 = code2_copy(kw[i0], j >> 1), c1 = code2_copy(kw[i1], j >> 1);
-                                a0 = code2_r(c0, j);
-                                a1 = code2_r(c1, j);
-                                a2 = code2_r(c0, j + 1);
-                                a3 = code2_r(c1, j + 1);
+                                const int ve = code2_view_of(j), vo = code2_view_of(j + 1);
+                                a0 = code2_r(code2_view(kw[i0], ve), j);
+                                a1 = code2_r(code2_view(kw[i1], ve), j);
+                                a2 = code2_r(code2_view(kw[i0], vo), j + 1);
+                                a3 = code2_r(code2_view(kw[i1], vo), j + 1);
                             } else if (BITS == 3) {   // 2-bit word 2i + g/2; high bits in word 8 + i
                                 const int j = 4 * (g & 1) + 2 * kk, jh = 8 * (g >> 1) + j;
                                 const int i0 = 2 * (2 * mt) + (g >> 1), i1 = 2 * (2 * mt + 1) + (g >> 1);
@@ -559,13 +559,16 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 for (int mt = 0; mt < 8; ++mt) {
                     const int g = mt >> 1, m = mt & 1;
                     if (BITS == 2) {   // word 2g + f/2, pair 4(d/4) + 2((d%4)/2) + f%2
-                        // rows gq take the even fields (code * 2^-18), rows gq + 8 the odd ones
+                        // rows gq take the even fields (code * 2^-16), rows gq + 8 the odd ones (2^-18)
                         const uint32_t wd = vw[2 * g + m];
 #pragma unroll
                         for (int kt = 0; kt < 2; ++kt) {
-                            const uint32_t c0 = code2_copy(wd, 2 * kt), c1 = code2_copy(wd, 2 * kt + 1);
-                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code2_r(c0, 0), code2_r(c0, 1), code2_r(c1, 0),
-                                         code2_r(c1, 1), bv[g][2 * kt], bv[g][2 * kt + 1]);
+                            const int f = 4 * kt;
+                            mma16816_acc(Ob[mt], sb == 0 && kt == 0, code2_r(code2_view(wd, code2_view_of(f)), f),
+                                         code2_r(code2_view(wd, code2_view_of(f + 1)), f + 1),
+                                         code2_r(code2_view(wd, code2_view_of(f + 2)), f + 2),
+                                         code2_r(code2_view(wd, code2_view_of(f + 3)), f + 3), bv[g][2 * kt],
+                                         bv[g][2 * kt + 1]);
                         }
                     } else if (BITS == 3) {   // 2-bit word 2g + f/2; high bits in word 8 + g, bit 8(f/2) + j
                         const int wl = 2 * g + m, wh = 8 + g;
@@ -602,8 +605,8 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             // ---------------- O += C_c / (kA lam) * (Ob + zs * kA)
             {
                 const float il4 = (1.0f / kA) / lam;
-                // 2-bit: rows gq (x) hold even fields at kA / 4
-                const float2 rw2 = BITS == 2 ? make_float2(4.f, 1.f) : make_float2(1.f, 1.f);
+                // 2-bit: rows gq + 8 (y) hold odd fields at kA / 4
+                const float2 rw2 = BITS == 2 ? make_float2(1.f, 4.f) : make_float2(1.f, 1.f);
                 const float2 il42 = make_float2(il4, il4);
                 const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 #pragma unroll
