@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     const int64_t n_pool_blocks = a.n_pool_blocks, block_bytes = a.block_bytes;
     const void* qptr = a.q;
     float* partials = a.partials;
+    int32_t* umap = a.unit_map;
     uint32_t* err = a.err;
     const float sm_scale = a.sm_scale;
     const uint32_t sb0 = a.sb[0], sb1 = a.sb[1], sb2 = a.sb[2], sb3 = a.sb[3];
@@ -190,7 +191,11 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         px_ld[sb] = bcol_ok ? (32 * sb + 8 * tq + pex_rot(B, hbq)) % B : 32 * sb + 8 * tq;
     }
 
+    // the merge finds a unit's partials from its first and last warp, which
+    // unit_flush records: this warp is the first if it took the unit's block 0
+    bool u_first = false;
     auto unit_setup = [&]() {
+        u_first = cc.j == 0;
         __syncwarp();
         for (int j = 0; j < G; ++j) {
             float v[4];
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
         for (int mt = 0; mt < 8; ++mt) O[mt] = make_float2(0.f, 0.f);
     };
 
-    auto unit_flush = [&]() {
+    auto unit_flush = [&](bool last) {
         float l = l_part;
         l += __shfl_xor_sync(kFull, l, 4);
         l += __shfl_xor_sync(kFull, l, 8);
@@ -263,6 +268,11 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             for (int g = 0; g < 4; ++g)   // channels 32g + 4gq + {0,1,2,3}
                 *reinterpret_cast<float4*>(base + 4 + 32 * g + 4 * gq) =
                     make_float4(O[2 * g].x, O[2 * g].y, O[2 * g + 1].x, O[2 * g + 1].y);
+        }
+        if (lane == 0) {
+            const int64_t u = (int64_t)cc.b * n_kv + cc.h;
+            if (u_first) umap[2 * u] = w;
+            if (last) umap[2 * u + 1] = w;
         }
     };
 
@@ -638,7 +648,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             Cursor done = cc;
             cc.b = pb;
             cc.h = ph_;
-            unit_flush();
+            unit_flush(done.b != pb || done.h != ph_);
             cc = done;
             if (x + 1 < s_end) unit_setup();
         }
@@ -700,6 +710,11 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     a.seq_lens = seq_lens;
     a.err = (uint32_t*)workspace;
     a.partials = (float*)((uint8_t*)workspace + kWsHeader);
+    // the unit map follows this launch's partial slots (the workspace size
+    // counts the largest grid's slots, then the map)
+    a.unit_map = (int32_t*)((uint8_t*)a.partials + ((size_t)batch * cfg.n_kv_heads + (size_t)nw) *
+                                                       (size_t)(cfg.n_q_heads / cfg.n_kv_heads) * kPartialStride *
+                                                       sizeof(float));
     a.out = out;
     a.n_pool_blocks = n_pool_blocks;
     a.block_bytes = block_bytes;

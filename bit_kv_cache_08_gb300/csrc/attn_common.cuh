@@ -34,6 +34,9 @@ struct AttnArgs {
     uint32_t flags;   // KVARN_FLAG_*: the cache's ablation switches
     uint32_t first_wait_limit;   // polls of each warp's first stage wait (kWaitLimit; less only in tests)
     uint32_t sb[4];
+    // (first, last) warp of each (sequence, kv head) unit, written by the split
+    // kernel for the merge; nullptr: the merge finds them from the split arithmetic
+    int32_t* unit_map;
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -341,7 +344,15 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
         const int nb = split_nblocks(sp, b);
         if (nb > 0) {
             const int64_t u = (int64_t)b * a.n_kv + h;
-            if (a.single > 0) {
+            if (a.unit_map != nullptr) {
+                // a range outside the grid (a warp gave up before recording it, its
+                // error flag set) merges nothing rather than reading out of bounds
+                const int2 wm = __ldcg(reinterpret_cast<const int2*>(a.unit_map) + u);
+                if (wm.x >= 0 && wm.y >= wm.x && wm.y < a.nw) {
+                    np = wm.y - wm.x + 1;
+                    p0 = a.partials + ((u + wm.x) * a.G + jq) * kPartialStride;
+                }
+            } else if (a.single > 0) {
                 np = a.single;
                 p0 = a.partials + (u * a.single * a.G + jq) * kPartialStride;
             } else {

@@ -48,9 +48,10 @@ inline int64_t block_bytes_of(const kvarn_config& c) {
 }
 
 // Workspace bytes the decode kernels need for `batch` query rows on the
-// current device: the header plus one partial slot per (row, kv head) and
-// one per resident warp of the larger of the 2-bit and bf16 split kernels.
-// 0 when the device cannot be queried.
+// current device: the header, one partial slot per (row, kv head) and one
+// per resident warp of the larger of the 2-bit and bf16 split kernels, then
+// the 2-bit kernel's unit map (first and last warp of every (row, kv head),
+// 8 bytes each). 0 when the device cannot be queried.
 inline size_t decode_ws_bytes(const kvarn_config& c, int32_t batch) {
     if (batch <= 0) return kWsHeader;
     const int d = current_device();
@@ -61,7 +62,8 @@ inline size_t decode_ws_bytes(const kvarn_config& c, int32_t batch) {
     if (a <= 0 || b <= 0) return 0;
     const size_t G = (size_t)(c.n_q_heads / c.n_kv_heads);
     const size_t slots = (size_t)batch * c.n_kv_heads + (size_t)nw;
-    return kWsHeader + slots * G * 132 * sizeof(float);
+    // header, split-K partials, then the (first, last) warp of every unit
+    return kWsHeader + slots * G * 132 * sizeof(float) + (size_t)batch * c.n_kv_heads * 2 * sizeof(int32_t);
 }
 
 // Arguments of a packed-cache attention call (decode: chunk = 1; chunked

@@ -156,10 +156,12 @@ size_t kvarn_staging_bytes(const kvarn_config* cfg, int32_t max_seqs);
 
 /* Minimum workspace for kvarn_decode_attn / kvarn_decode_attn_bf16 with this
  * batch on the CURRENT device (the split-K partial results depend on its SM
- * count): 256 header bytes (the error word is the first uint32) plus one
+ * count): 256 header bytes (the error word is the first uint32), one
  * partial (max, sum, 128 accumulators per query head) per (sequence, kv
- * head) and per resident warp. batch = 0 gives the 256 bytes that
- * kvarn_quantize_block and kvarn_append need. 0 on a bad config. */
+ * head) and per resident warp, then 8 bytes per (sequence, kv head) in
+ * which the split kernel records the first and last warp of each for the
+ * merge. batch = 0 gives the 256 bytes that kvarn_quantize_block and
+ * kvarn_append need. 0 on a bad config. */
 size_t kvarn_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks_per_seq);
 
 /* Workspace with which kvarn_prefill_attn runs at full speed for this batch
@@ -322,7 +324,7 @@ int kvarn_decode_attn_bf16(const kvarn_config* cfg, const void* q, int32_t q_dty
  * workspace. error_word (device uint32, may be NULL) receives this call's
  * KVARN_DEVERR_* flags (0 when none). The scratch must hold
  * kvarn_workspace_bytes(cfg, batch, max_blocks_per_seq) bytes (256 + (batch *
- * n_kv + resident warps) * G * 528); larger problems are refused with
+ * n_kv + resident warps) * G * 528 + batch * n_kv * 8); larger problems are refused with
  * KVARN_ERR_WORKSPACE before anything is enqueued.
  *
  * The first call on each device looks up the array's device address (with
