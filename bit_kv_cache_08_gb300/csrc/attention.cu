@@ -321,12 +321,11 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                     const uint4 s4 = *reinterpret_cast<const uint4*>(Vb + off_s(B, BITS) + 16 * lane);
                     ms = __hmax2(__hmax2(u32_as_h2(s4.x), u32_as_h2(s4.y)), __hmax2(u32_as_h2(s4.z), u32_as_h2(s4.w)));
                 }
-                __half2 m2 = __hmax2(__lows2half2(mc, ms), __highs2half2(mc, ms));   // (C max, s max)
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    m2 = __hmax2(m2, u32_as_h2(__shfl_xor_sync(kFull, h2_as_u32(m2), o)));
-                cmax = __low2float(m2);
-                smax = __high2float(m2);
+                // (C max, s max) of this lane; both non-negative, so their fp16 bit
+                // patterns order as integers and one redux each finds the warp's maxima
+                const uint32_t m2 = h2_as_u32(__hmax2(__lows2half2(mc, ms), __highs2half2(mc, ms)));
+                cmax = __half2float(__ushort_as_half((uint16_t)__reduce_max_sync(kFull, m2 & 0xffffu)));
+                smax = __half2float(__ushort_as_half((uint16_t)__reduce_max_sync(kFull, m2 >> 16)));
             }
             const int ec = ceil_log2(fmaxf(cmax, kF16MinNormal));
             const __half2 cinv = __float2half2_rn(exp2i(-ec));
@@ -446,7 +445,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 }
                 const float2 kmb2 = make_float2(kmb, kmb);
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) sc[sb][mt] = __fmul2_rn(__fmul2_rn(s_[mt], Rv[mt]), kmb2);
+                for (int mt = 0; mt < 2; ++mt) sc[sb][mt] = __fmul2_rn(s_[mt], __fmul2_rn(Rv[mt], kmb2));
             }
             // ---------------- online softmax over the block (head tq: 8 lanes x 4 tokens per sub-block)
             float bm = -INFINITY;
