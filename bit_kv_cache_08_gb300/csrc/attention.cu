@@ -735,7 +735,10 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     return with_attn_kernel(cfg.block_size, cfg.bits, [&](auto k) {
         using K = decltype(k);
         cudaError_t e = launch_pdl(K::fn, nw, 32, K::smem(), st, a);
-        if (e == cudaSuccess) e = launch_pdl(merge_kernel<K::kB, true>, mgrid, 128, 0, st, a);
+        if (e == cudaSuccess)
+            e = merge_wide(nw, a.batch, a.n_kv)
+                    ? launch_pdl(merge_wide_kernel<K::kB, true>, (unsigned)((int64_t)a.batch * a.n_q), 32 * kWideWarps, 0, st, a)
+                    : launch_pdl(merge_kernel<K::kB, true>, mgrid, 128, 0, st, a);
         return e;
     });
 }

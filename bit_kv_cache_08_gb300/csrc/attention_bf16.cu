@@ -304,7 +304,10 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
         e = launch_pdl(decode_attn_bf16_kernel<32>, nw, 32, attn_bf16_smem_bytes(), st, a);
     else
         e = launch_pdl(decode_attn_bf16_kernel<64>, nw, 32, attn_bf16_smem_bytes(), st, a);
-    if (e == cudaSuccess) e = launch_pdl(merge_kernel<kChunk, false>, mgrid, 128, 0, st, a);
+    if (e == cudaSuccess)
+        e = merge_wide(nw, batch, a.n_kv)
+                ? launch_pdl(merge_wide_kernel<kChunk, false>, (unsigned)((int64_t)batch * a.n_q), 32 * kWideWarps, 0, st, a)
+                : launch_pdl(merge_kernel<kChunk, false>, mgrid, 128, 0, st, a);
     return e;
 }
 

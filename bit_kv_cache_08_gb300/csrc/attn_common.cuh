@@ -159,6 +159,115 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 }
 
 // ---------------------------------------------------------------- merge
+// LSE merge of np >= 1 partials starting at p0, pstride floats apart: the
+// common maximum m, the weighted sum l and this lane's 4 weighted
+// accumulators (channels 4 lane .. 4 lane + 3).
+__device__ __forceinline__ void lse_partials(const float* p0, int np, int64_t pstride, int lane, float& m, float& l,
+                                             float (&acc)[4]) {
+    if (np <= 16) {
+        // one round trip: lane i holds partial i's (m, l); every lane loads its
+        // 4 channels of all partials at once, then weighs them
+        const float pm = lane < np ? __ldcg(p0 + lane * pstride) : -INFINITY;
+        const float pl = lane < np ? __ldcg(p0 + lane * pstride + 1) : 0.f;
+        float4 pa[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i < np) pa[i] = __ldcg(reinterpret_cast<const float4*>(p0 + i * pstride + 4) + lane);
+        m = warp_max(pm);
+        if (m != -INFINITY) {
+            const float wl = lane < np ? exp2f(pm - m) : 0.f;
+            l = warp_sum(pl * wl);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i < np) {
+                    const float wgt = __shfl_sync(kFull, wl, i);
+                    acc[0] = fmaf(wgt, pa[i].x, acc[0]);
+                    acc[1] = fmaf(wgt, pa[i].y, acc[1]);
+                    acc[2] = fmaf(wgt, pa[i].z, acc[2]);
+                    acc[3] = fmaf(wgt, pa[i].w, acc[3]);
+                }
+            }
+        }
+    } else {
+        // the common maximum and the weighted sum of l, lanes over partials
+        float mx = -INFINITY;
+        for (int i = lane; i < np; i += 32) mx = fmaxf(mx, __ldcg(p0 + i * pstride));
+        m = warp_max(mx);
+        if (m != -INFINITY) {
+            float ls = 0.f;
+            for (int i = lane; i < np; i += 32) ls += __ldcg(p0 + i * pstride + 1) * exp2f(__ldcg(p0 + i * pstride) - m);
+            l = warp_sum(ls);
+            // every lane its 4 channels over all partials (independent loads; a
+            // deep unroll keeps many in flight when one unit has hundreds of partials)
+#pragma unroll 16
+            for (int i = 0; i < np; ++i) {
+                const float* bp = p0 + i * pstride;
+                const float wgt = exp2f(__ldcg(bp) - m);
+                const float4 pa = __ldcg(reinterpret_cast<const float4*>(bp + 4) + lane);
+                acc[0] = fmaf(wgt, pa.x, acc[0]);
+                acc[1] = fmaf(wgt, pa.y, acc[1]);
+                acc[2] = fmaf(wgt, pa.z, acc[2]);
+                acc[3] = fmaf(wgt, pa.w, acc[3]);
+            }
+        }
+    }
+}
+
+// The same LSE merge in batches of 8 partials with a running rescale, for
+// the wide merge's warps (fewer registers than lse_partials); m, l and acc
+// start at -inf, 0 and 0.
+__device__ __forceinline__ void lse_stream(const float* p0, int np, int64_t pstride, int lane, float& m, float& l,
+                                           float (&acc)[4]) {
+    for (int i0 = 0; i0 < np; i0 += 8) {
+        const int cnt = min(8, np - i0);
+        const float* q = p0 + i0 * pstride;
+        const float pm = lane < cnt ? __ldcg(q + lane * pstride) : -INFINITY;
+        const float pl = lane < cnt ? __ldcg(q + lane * pstride + 1) : 0.f;
+        float4 pa[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < cnt) pa[i] = __ldcg(reinterpret_cast<const float4*>(q + i * pstride + 4) + lane);
+        const float bm = warp_max(pm);
+        if (bm == -INFINITY) continue;
+        const float mn = fmaxf(m, bm);
+        const float fa = m == -INFINITY ? 0.f : exp2f(m - mn);
+        const float wl = lane < cnt ? exp2f(pm - mn) : 0.f;
+        l = l * fa + warp_sum(pl * wl);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] *= fa;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < cnt) {
+                const float wgt = __shfl_sync(kFull, wl, i);
+                acc[0] = fmaf(wgt, pa[i].x, acc[0]);
+                acc[1] = fmaf(wgt, pa[i].y, acc[1]);
+                acc[2] = fmaf(wgt, pa[i].z, acc[2]);
+                acc[3] = fmaf(wgt, pa[i].w, acc[3]);
+            }
+        }
+        m = mn;
+    }
+}
+
+// The same merge over the per-warp results (m, l, acc[128], at 0, 1 and 4 of
+// each kPartialStride-float row) of the n <= 32 warps of a wide merge.
+__device__ __forceinline__ void combine_slices(const float* sl, int n, int lane, float& m, float& l, float (&acc)[4]) {
+    const float pm = lane < n ? sl[lane * kPartialStride] : -INFINITY;
+    const float pl = lane < n ? sl[lane * kPartialStride + 1] : 0.f;
+    m = warp_max(pm);
+    if (m == -INFINITY) return;
+    const float wl = (lane < n && pm != -INFINITY) ? exp2f(pm - m) : 0.f;
+    l = warp_sum(pl * wl);
+    for (int i = 0; i < n; ++i) {
+        const float wgt = __shfl_sync(kFull, wl, i);
+        const float4 pa = *reinterpret_cast<const float4*>(sl + i * kPartialStride + 4 + 4 * lane);
+        acc[0] = fmaf(wgt, pa.x, acc[0]);
+        acc[1] = fmaf(wgt, pa.y, acc[1]);
+        acc[2] = fmaf(wgt, pa.z, acc[2]);
+        acc[3] = fmaf(wgt, pa.w, acc[3]);
+    }
+}
+
 // One (row, query head) output: LSE-merge the np partials of its unit
 // (p0: the first, consecutive partials G * kPartialStride floats apart; np =
 // 0 when the unit has no pool blocks), add the raw tail rows, normalise and
@@ -167,9 +276,9 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 // (unrotated) are added; the bf16 cache (ROT = false) has every token in its
 // pages. qsh: 128 floats of this warp's shared memory. gw = row * n_q +
 // query head.
-template <int B, bool ROT>
+template <int B, bool ROT, int NWIDE = 0>
 __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np, const float* p0, float* qsh,
-                                          int lane) {
+                                          int lane, const float* wide = nullptr) {
     const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);   // b: a (virtual) row sequence
     const int h = hq / a.G;
     const int rb = a.chunk == 1 ? b : b / a.chunk;              // its real sequence
@@ -195,54 +304,8 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np,
     }
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (nb > 0 && np > 0) {
-        const int64_t pstride = (int64_t)a.G * kPartialStride;     // next warp's partial of the unit
-        if (np <= 16) {
-            // one round trip: lane i holds partial i's (m, l); every lane loads its
-            // 4 channels of all partials at once, then weighs them
-            const float pm = lane < np ? __ldcg(p0 + lane * pstride) : -INFINITY;
-            const float pl = lane < np ? __ldcg(p0 + lane * pstride + 1) : 0.f;
-            float4 pa[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (i < np) pa[i] = __ldcg(reinterpret_cast<const float4*>(p0 + i * pstride + 4) + lane);
-            m = warp_max(pm);
-            if (m != -INFINITY) {
-                const float wl = lane < np ? exp2f(pm - m) : 0.f;
-                l = warp_sum(pl * wl);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (i < np) {
-                        const float wgt = __shfl_sync(kFull, wl, i);
-                        acc[0] = fmaf(wgt, pa[i].x, acc[0]);
-                        acc[1] = fmaf(wgt, pa[i].y, acc[1]);
-                        acc[2] = fmaf(wgt, pa[i].z, acc[2]);
-                        acc[3] = fmaf(wgt, pa[i].w, acc[3]);
-                    }
-                }
-            }
-        } else {
-            // the common maximum and the weighted sum of l, lanes over partials
-            float mx = -INFINITY;
-            for (int i = lane; i < np; i += 32) mx = fmaxf(mx, __ldcg(p0 + i * pstride));
-            m = warp_max(mx);
-            if (m != -INFINITY) {
-                float ls = 0.f;
-                for (int i = lane; i < np; i += 32) ls += __ldcg(p0 + i * pstride + 1) * exp2f(__ldcg(p0 + i * pstride) - m);
-                l = warp_sum(ls);
-                // every lane its 4 channels over all partials (independent loads; a
-                // deep unroll keeps many in flight when one unit has hundreds of partials)
-#pragma unroll 16
-                for (int i = 0; i < np; ++i) {
-                    const float* bp = p0 + i * pstride;
-                    const float wgt = exp2f(__ldcg(bp) - m);
-                    const float4 pa = __ldcg(reinterpret_cast<const float4*>(bp + 4) + lane);
-                    acc[0] = fmaf(wgt, pa.x, acc[0]);
-                    acc[1] = fmaf(wgt, pa.y, acc[1]);
-                    acc[2] = fmaf(wgt, pa.z, acc[2]);
-                    acc[3] = fmaf(wgt, pa.w, acc[3]);
-                }
-            }
-        }
+        if constexpr (NWIDE > 0) combine_slices(wide, NWIDE, lane, m, l, acc);
+        else lse_partials(p0, np, (int64_t)a.G * kPartialStride, lane, m, l, acc);
         if (ROT && !(a.flags & KVARN_FLAG_NO_ROTATION)) {
             // rotate back: x = sigma . H(acc) / sqrt(128)
             fwht128(acc, lane);
@@ -324,8 +387,46 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np,
     reinterpret_cast<float4*>(out)[lane] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
 }
 
+// The partials of row gw's unit: their count np and the first p0 (np = 0
+// when the unit has no pool blocks or the row's length is out of range).
+template <int B, bool ROT>
+__device__ __forceinline__ void merge_locate(const AttnArgs& a, int64_t gw, int lane, int& np, const float*& p0) {
+    np = 0;
+    p0 = nullptr;
+    const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);
+    const int h = hq / a.G, jq = hq % a.G;
+    const int rb = a.chunk == 1 ? b : b / a.chunk;
+    const int L = a.seq_lens[rb];
+    if (L < 0 || L > a.max_blocks * B) return;
+    const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1, a.chunk};
+    const int nb = split_nblocks(sp, b);
+    if (nb <= 0) return;
+    const int64_t u = (int64_t)b * a.n_kv + h;
+    if (a.unit_map != nullptr) {
+        // a range outside the grid (a warp gave up before recording it, its
+        // error flag set) merges nothing rather than reading out of bounds
+        const int2 wm = __ldcg(reinterpret_cast<const int2*>(a.unit_map) + u);
+        if (wm.x >= 0 && wm.y >= wm.x && wm.y < a.nw) {
+            np = wm.y - wm.x + 1;
+            p0 = a.partials + ((u + wm.x) * a.G + jq) * kPartialStride;
+        }
+    } else if (a.single > 0) {
+        np = a.single;
+        p0 = a.partials + (u * a.single * a.G + jq) * kPartialStride;
+    } else {
+        int64_t before, total;
+        split_prefix(sp, b, lane, before, total);
+        const int64_t W = total * a.n_kv;
+        const int64_t nwe = split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, ROT ? kSplitRatio2bit * B : 0.f);
+        const int64_t Su = before * a.n_kv + (int64_t)h * nb;
+        const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);
+        np = (int)(w1 - w0 + 1);
+        p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
+    }
+}
+
 // The merge kernel: one warp per (row, query head), which finds its unit's
-// partials from the split arithmetic.
+// partials from the split arithmetic or the split kernel's unit map.
 template <int B, bool ROT>
 __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     wait_prior_grids();
@@ -333,42 +434,43 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     const int64_t gw = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (gw >= (int64_t)a.batch * a.n_q) return;
     __shared__ __align__(16) float q_all[4][kD];
-    const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);
-    const int h = hq / a.G, jq = hq % a.G;
-    const int rb = a.chunk == 1 ? b : b / a.chunk;
-    const int L = a.seq_lens[rb];
-    int np = 0;
-    const float* p0 = nullptr;
-    if (L >= 0 && L <= a.max_blocks * B) {
-        const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1, a.chunk};
-        const int nb = split_nblocks(sp, b);
-        if (nb > 0) {
-            const int64_t u = (int64_t)b * a.n_kv + h;
-            if (a.unit_map != nullptr) {
-                // a range outside the grid (a warp gave up before recording it, its
-                // error flag set) merges nothing rather than reading out of bounds
-                const int2 wm = __ldcg(reinterpret_cast<const int2*>(a.unit_map) + u);
-                if (wm.x >= 0 && wm.y >= wm.x && wm.y < a.nw) {
-                    np = wm.y - wm.x + 1;
-                    p0 = a.partials + ((u + wm.x) * a.G + jq) * kPartialStride;
-                }
-            } else if (a.single > 0) {
-                np = a.single;
-                p0 = a.partials + (u * a.single * a.G + jq) * kPartialStride;
-            } else {
-                int64_t before, total;
-                split_prefix(sp, b, lane, before, total);
-                const int64_t W = total * a.n_kv;
-                const int64_t nwe =
-                    split_active_warps(W, a.nw, (int64_t)a.batch * a.n_kv, ROT ? kSplitRatio2bit * B : 0.f);
-                const int64_t Su = before * a.n_kv + (int64_t)h * nb;
-                const int64_t w0 = split_last_warp_at(Su, W, nwe), w1 = split_last_warp_at(Su + nb - 1, W, nwe);
-                np = (int)(w1 - w0 + 1);
-                p0 = a.partials + ((u + w0) * a.G + jq) * kPartialStride;
-            }
-        }
-    }
+    int np;
+    const float* p0;
+    merge_locate<B, ROT>(a, gw, lane, np, p0);
     merge_row<B, ROT>(a, gw, np, p0, q_all[threadIdx.x >> 5], lane);
 }
+
+// The wide merge, for units cut into many partials (few long sequences):
+// one CTA of kWideWarps warps per (row, query head). Warp k LSE-merges its
+// share of the unit's partials, the shares meet in shared memory and warp 0
+// combines them and finishes the row.
+constexpr int kWideWarps = 8;
+template <int B, bool ROT>
+__global__ void __launch_bounds__(32 * kWideWarps, 4) merge_wide_kernel(AttnArgs a) {
+    wait_prior_grids();
+    const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+    const int64_t gw = blockIdx.x;
+    if (gw >= (int64_t)a.batch * a.n_q) return;   // (uniform over the CTA)
+    __shared__ __align__(16) float slices[kWideWarps][kPartialStride];
+    __shared__ __align__(16) float qsh[kD];
+    int np;
+    const float* p0;
+    merge_locate<B, ROT>(a, gw, lane, np, p0);
+    float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const int i0 = (int)((int64_t)np * wp / kWideWarps), i1 = (int)((int64_t)np * (wp + 1) / kWideWarps);
+    const int64_t pstride = (int64_t)a.G * kPartialStride;
+    if (i1 > i0) lse_stream(p0 + i0 * pstride, i1 - i0, pstride, lane, m, l, acc);
+    if (lane == 0) {
+        slices[wp][0] = m;
+        slices[wp][1] = l;
+    }
+    *reinterpret_cast<float4*>(&slices[wp][4 + 4 * lane]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    __syncthreads();
+    if (wp == 0) merge_row<B, ROT, kWideWarps>(a, gw, np, p0, qsh, lane, &slices[0][0]);
+}
+
+// Whether the merge of a launch with nw split warps over batch * n_kv units
+// takes the wide kernel: 16 or more partials per unit on average.
+inline bool merge_wide(int64_t nw, int64_t batch, int n_kv) { return nw >= 16 * batch * (int64_t)n_kv; }
 
 }  // namespace kvarn
