@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                 }
                 const float2 kmb2 = make_float2(kmb, kmb);
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) sc[sb][mt] = __fmul2_rn(s_[mt], __fmul2_rn(Rv[mt], kmb2));
+                for (int mt = 0; mt < 2; ++mt) sc[sb][mt] = __fmul2_rn(__fmul2_rn(s_[mt], Rv[mt]), kmb2);
             }
             // ---------------- online softmax over the block (head tq: 8 lanes x 4 tokens per sub-block)
             float bm = -INFINITY;

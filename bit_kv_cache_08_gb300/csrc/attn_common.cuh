@@ -9,8 +9,9 @@ namespace kvarn {
 constexpr uint32_t kWaitLimit = 1u << 22;
 // Cost of one 2-bit block per token of block size, in units of merging one
 // partial; see split_active_warps. Chosen from batch-1 timings of the
-// Llama-shaped sweep (1K-128K tokens), where 2-4 blocks per warp beat one.
-constexpr float kSplitRatio2bit = 0.5f;
+// Llama-shaped cache (8K-128K tokens) with the wide merge, where 2 beat 0.5,
+// 1 and 4 (0.5 had been best while one warp merged a row's partials).
+constexpr float kSplitRatio2bit = 2.0f;
 
 struct AttnArgs {
     const void* q;
