@@ -375,6 +375,15 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
             float2 sc[NSB][2];   // tokens 32sb + 4gq + 2mt + {0, 1}
 #pragma unroll
             for (int sb = 0; sb < NSB; ++sb) {
+                // the score combine's steps, zero points and R, loaded ahead of the MMAs
+                const int t0 = 32 * sb + 4 * gq;
+                uint2 s2h[4], z2h[4];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    s2h[g] = *reinterpret_cast<const uint2*>(Ks + g * B + t0);
+                    z2h[g] = *reinterpret_cast<const uint2*>(Kz + g * B + t0);
+                }
+                const uint2 Rr = *reinterpret_cast<const uint2*>(KR + t0);
                 uint32_t kw[RW], kw8[RW];
                 {
                     const uint4* rec = reinterpret_cast<const uint4*>(Kb) + (RW / 4) * (32 * sb + lane);
@@ -425,14 +434,11 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
                         }
                     }
                 // scores of tokens 32sb + 4gq + 2mt + {0, 1}, head tq, as fp32 pairs
-                const int t0 = 32 * sb + 4 * gq;
-                const uint2 Rr = *reinterpret_cast<const uint2*>(KR + t0);
                 const float2 Rv[2] = {__half22float2(u32_as_h2(Rr.x)), __half22float2(u32_as_h2(Rr.y))};
                 float2 s_[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    const uint2 s2 = *reinterpret_cast<const uint2*>(Ks + g * B + t0);
-                    const uint2 z2 = *reinterpret_cast<const uint2*>(Kz + g * B + t0);
+                    const uint2 s2 = s2h[g], z2 = z2h[g];
                     const float2 sv[2] = {__half22float2(u32_as_h2(s2.x)), __half22float2(u32_as_h2(s2.y))};
                     const float2 zv[2] = {__half22float2(u32_as_h2(z2.x)), __half22float2(u32_as_h2(z2.y))};
                     const float2 qq = make_float2(Qq[g], Qq[g]);
