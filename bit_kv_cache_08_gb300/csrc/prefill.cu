@@ -15,16 +15,19 @@
 // are the MMA rows and the keys the columns, so every 2-bit code is turned
 // into a tensor-core operand once for all 8 vectors:
 //   QK  A = q' (vector gq in row gq as fp16 hi, row gq + 8 as lo), B = the
-//       K codes as exact fp16 code * 2^-9, straight from the lane's record
-//       (one mask leaves a subnormal, one fp16 multiply by a power of two
-//       makes it normal; n-tile i holds tokens 4n + i of a 32-token
-//       sub-block); one accumulator per 32-channel group
+//       K codes straight from the lane's record as raw fp16 subnormals (a
+//       shifted or byte-swapped view of the word and one mask: even fields
+//       code * 2^-16 at bits 8..9, odd fields code * 2^-18 at bits 6..7,
+//       exact on the tensor cores at those positions; q' of the odd k-slots
+//       x 4; n-tile i holds tokens 4n + i of a 32-token sub-block); one
+//       accumulator per 32-channel group
 //   the score accumulator layout leaves lane (gq, tq) with tokens
 //   8tq .. 8tq + 7 of each sub-block for vector gq, which is exactly the
 //   A-operand layout of the PV product, so P never leaves registers
 //   PV  A = P'_g = p R s_g lam (hi rows, lo rows), B = the V codes
-//       (n = channel, k = token), one group at a time; the block's result
-//       is folded into O with the per-channel factor 2^9 C / lam at once.
+//       (n = channel, k = token; the odd fields' output columns x 4), one
+//       group at a time; the block's result is folded into O with the
+//       per-channel factor C / (kA lam) at once.
 //       P' is an fp16 two-product of P'' = p R lam (hi | lo once per token)
 //       with the group's steps; the zero-point sums of all groups come from
 //       two MMAs per 32 tokens (B columns z_0..z_3 | s_0..s_3).
@@ -35,7 +38,7 @@
 // sum, 128 rotated accumulators) per split goes to one workspace partial;
 // the merge kernel combines a row's partials, adds the raw bf16 tail rows,
 // rotates back once and normalises. 3- and 4-bit codes take the same path with 48- and 64-byte
-// records (the same code * 2^-9 operands).
+// records, their operands code * 2^-9 (a mask and one fp16 multiply per pair).
 #include <algorithm>
 
 #include "attn_common.cuh"
@@ -77,6 +80,8 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
     constexpr int HB = head_block_bytes(B, BITS);
     constexpr int NSB = B / 32;
     constexpr int RW = 4 * BITS;              // 32-bit words per lane record
+    // kA: the operand scale of a code (2-bit: even fields' raw subnormals)
+    constexpr float kA = BITS == 2 ? kRawScale : kCodeScale;
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* stages = smem;                                                    // S x (K, V)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * 2 * HB);           // S mbarriers
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 const float sc = exp2i(12 - e);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) x[k] *= sc;
-                km = (1.0f / kCodeScale) * exp2i(e - 12) * a.sm_scale * kLog2e;
+                km = (1.0f / kA) * exp2i(e - 12) * a.sm_scale * kLog2e;
             }
             uint16_t hi[4], lo[4];
 #pragma unroll
@@ -220,6 +225,8 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
             }
             const int ec = ceil_log2(fmaxf(cmax, kF16MinNormal));
             const __half2 cinv = __float2half2_rn(exp2i(-ec));
+            // 2-bit: the odd k-slot of each pair meets codes at 2^-18, so its q' is x 4
+            const __half2 cinv_o = BITS == 2 ? __float2half2_rn(exp2i(2 - ec)) : cinv;
             const float kmb = kmul * exp2i(ec);
             // ---- QK A operand for vector gq: q' = q_s * C * 2^-ec, hi (row gq) | lo (row gq + 8)
             uint32_t qa_h[16], qa_l[16];
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 const uint32_t lw[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
-                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), cinv);
+                    const __half2 C2 = __hmul2(u32_as_h2(cw[e2]), (e2 & 1) ? cinv_o : cinv);
                     const __half2 qh = u32_as_h2(hw[e2]);
                     const __half2 hi = __hmul2(qh, C2);
                     __half2 lo = __hfma2(qh, C2, __hneg2(hi));
@@ -242,15 +249,15 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                     qa_l[4 * g + e2] = h2_as_u32(lo);
                 }
             }
-            // ---- Q'_g * 2^-9 of vector gq: the same A against a B of 2^-9 everywhere
+            // ---- Q'_g * kA of vector gq: the same A against a B of codes of 1
+            constexpr uint32_t kOneE = BITS == 2 ? kRawOneEven : kCodeScaleH2;
+            constexpr uint32_t kOneO = BITS == 2 ? kRawOneOdd : kCodeScaleH2;
             float Qq[4];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float d[4];
-                mma16816_acc(d, true, qa_h[4 * g], qa_l[4 * g], qa_h[4 * g + 1], qa_l[4 * g + 1], kCodeScaleH2,
-                             kCodeScaleH2);
-                mma16816(d, qa_h[4 * g + 2], qa_l[4 * g + 2], qa_h[4 * g + 3], qa_l[4 * g + 3], kCodeScaleH2,
-                         kCodeScaleH2);
+                mma16816_acc(d, true, qa_h[4 * g], qa_l[4 * g], qa_h[4 * g + 1], qa_l[4 * g + 1], kOneE, kOneO);
+                mma16816(d, qa_h[4 * g + 2], qa_l[4 * g + 2], qa_h[4 * g + 3], qa_l[4 * g + 3], kOneE, kOneO);
                 Qq[g] = d[0] + d[2];
             }
             const uint16_t* Ks = reinterpret_cast<const uint16_t*>(Kb + off_s(B, BITS));
@@ -301,8 +308,8 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                             uint32_t b0, b1;
                             if (BITS == 2) {   // word 2i + g/2, pair 4(g%2) + e/2
                                 const int wi = 2 * i + (g >> 1), jj = 4 * (g & 1) + 2 * kk;
-                                b0 = code2_s(kw[wi], kw8[wi], jj);
-                                b1 = code2_s(kw[wi], kw8[wi], jj + 1);
+                                b0 = code2_r(code2_view(kw[wi], code2_view_of(jj)), jj);
+                                b1 = code2_r(code2_view(kw[wi], code2_view_of(jj + 1)), jj + 1);
                             } else if (BITS == 3) {   // + the high bit: word 8 + i, bit 8(g/2) + pair
                                 const int wi = 2 * i + (g >> 1), jj = 4 * (g & 1) + 2 * kk, wh = 8 + i;
                                 const int jh = 8 * (g >> 1) + jj;
@@ -414,7 +421,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                     ph[sb][k] = h2_as_u32(hh);
                     pl[sb][k] = h2_as_u32(__float22half2_rn(__ffma2_rn(__half22float2(hh), make_float2(-1.f, -1.f), v)));
                 }
-            const float il4 = (1.0f / kCodeScale) / lam;
+            const float il4 = (1.0f / kA) / lam;
             const uint16_t* VC = reinterpret_cast<const uint16_t*>(Vb + off_C(B, BITS));
 
             // ---------------- zero-point sums by MMA: A = P'' (hi rows, lo rows), B columns
@@ -432,7 +439,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
             float zq[4];
             {
                 const float c0 = Dz[0] + Dz[2], c1 = Dz[1] + Dz[3];
-                const float zA = c0 * kCodeScale, zB = c1 * kCodeScale;   // valid at tq < 2
+                const float zA = c0 * kA, zB = c1 * kA;   // valid at tq < 2
                 const int base = lane & ~3;
                 zq[0] = __shfl_sync(kFull, zA, base);
                 zq[1] = __shfl_sync(kFull, zB, base);
@@ -478,9 +485,10 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
 #pragma unroll
                         for (int f = 0; f < 4; ++f) {
                             if (BITS == 2) {   // pair 4(d/4) + 2((d%4)/2) + f%2
-                                const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
-                                mma16816(Ob[f], a0, a1, a2, a3, code2_s(w, w8, 4 * kt + (f & 1)),
-                                         code2_s(w, w8, 4 * kt + 2 + (f & 1)));
+                                const uint32_t w = vw[f >> 1];
+                                const int j0 = 4 * kt + (f & 1), j1 = j0 + 2;
+                                mma16816(Ob[f], a0, a1, a2, a3, code2_r(code2_view(w, code2_view_of(j0)), j0),
+                                         code2_r(code2_view(w, code2_view_of(j1)), j1));
                             } else if (BITS == 3) {   // + the high bit at 8(f/2) + pair in word 8 + g
                                 const uint32_t w = vw[f >> 1], w8 = vw8[f >> 1];
                                 const int j0 = 4 * kt + (f & 1), j1 = j0 + 2, hb = 8 * (f >> 1);
@@ -499,7 +507,10 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 const float2 il42 = make_float2(il4, il4), zq2 = make_float2(zq[g], zq[g]);
 #pragma unroll
                 for (int f = 0; f < 4; ++f) {
-                    const float2 t = __fadd2_rn(__fadd2_rn(make_float2(Ob[f][0], Ob[f][1]), make_float2(Ob[f][2], Ob[f][3])), zq2);
+                    // 2-bit: odd f columns hold odd fields at kA / 4
+                    const float wf = (BITS == 2 && (f & 1)) ? 4.f : 1.f;
+                    const float2 t = __ffma2_rn(__fadd2_rn(make_float2(Ob[f][0], Ob[f][1]), make_float2(Ob[f][2], Ob[f][3])),
+                                                make_float2(wf, wf), zq2);
                     O[g][f] = __ffma2_rn(__fmul2_rn(pair_i4(c4, f), il42), t, O[g][f]);
                 }
             }
