@@ -59,6 +59,8 @@ def parse():
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
                         "lengths), 2-, 3- and 4-bit vs bf16-cache decode attention, one JSON line per point")
+    p.add_argument("--point", type=int, nargs=2, metavar=("BATCH", "CTX"),
+                   help="with --sweep: only this grid point")
     return p.parse_args()
 
 
@@ -706,8 +708,8 @@ def run_sweep(args):
     kv.build()
     dev = "cuda"
     flush = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    for batch in SWEEP_BATCH:
-        for ctx in SWEEP_CTX:
+    for batch in ((args.point[0],) if args.point else SWEEP_BATCH):
+        for ctx in ((args.point[1],) if args.point else SWEEP_CTX):
             w = synth.sweep_point(batch, ctx)
             B, n_kv, n_q = w.block, w.n_kv, w.n_q
             lens = np.array(w.seq_lens, dtype=np.int64)
