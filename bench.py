@@ -56,6 +56,8 @@ def parse():
                         "prefill 1024-2048 then 16384 x (append + attention) per layer): us per step over "
                         "the horizon and the 2-bit vs bf16-cache output error at steps 1 .. 16384")
     p.add_argument("--long-steps", type=int, default=16384, help="appends per layer in --long")
+    p.add_argument("--long-eager", action="store_true",
+                   help="with --long: every step as eager calls (no CUDA graph after the first window)")
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: the Llama-3.1-8B layer grid (batch x context, ragged "
                         "lengths), 2-, 3- and 4-bit vs bf16-cache decode attention, one JSON line per point")
@@ -879,8 +881,13 @@ def run_long(args):
     """The Phi-4-14B long-horizon pseudo-decode: 40 layers, 40 query / 10 kv
     heads, batch 8 with prefill lengths uniform in [1024, 2048], then
     --long-steps steps, each appending one token per sequence to every layer
-    and running decode attention on it (eager C-ABI calls, CUDA events per
-    window of steps). At the checkpoint steps, every layer's output is also
+    and running decode attention on it. The first window of steps runs as
+    eager C-ABI calls; after it the whole step (one gather of the step's new
+    tokens for every layer, then every layer's kvarn_append and
+    kvarn_decode_attn, then the position counters) is captured once as a
+    CUDA graph and replayed, the serving loop's form: the entry points only
+    enqueue kernels with fixed grids, and lengths and positions live in
+    device tensors. CUDA events per window of steps. At the checkpoint steps, every layer's output is also
     computed over a bf16 cache holding the same tokens (the repo's bf16-cache
     kernel), and the 2-bit error against it is reported: max and mean of
     |o_2bit - o_bf16| / max(1, |o_bf16|) and the relative L2 norm over all
@@ -898,6 +905,8 @@ def run_long(args):
     Lmax = max(prefill) + steps
     mb = (Lmax + B - 1) // B
     st = []
+    # every layer's appended tokens: [K|V][layer][step][batch][n_kv][128]
+    NEWS = torch.empty(2, layers, steps, batch, n_kv, D, dtype=torch.bfloat16, device=dev)
     t_setup = time.time()
     for l in range(layers):
         sb = synth.sign_bits(100 + l)
@@ -911,7 +920,6 @@ def run_long(args):
         kvp = torch.zeros(batch * mb, n_kv, 2, B, D, dtype=torch.bfloat16, device=dev)   # bf16 pages
         hb, bb = kv.head_block_bytes(cfg), kv.block_bytes(cfg)
         steps_idx = torch.arange(steps, device=dev)[:, None] + torch.tensor(prefill, device=dev)[None, :]
-        news = []
         for kind in (0, 1):
             T = synth.kv_values(g, batch, n_kv, mb * B, w.sigma_m, w.n_out, w.out_factor, dev).to(torch.bfloat16)
             # every token in the bf16 pages (tokens past a sequence's length are never read)
@@ -926,10 +934,10 @@ def run_long(args):
                                   n_head_blocks=offs.numel())
                 staging[b, :, kind, :Lb - nbf * B] = T[b, :, nbf * B:Lb]
             # the appended tokens of every step: [steps][batch][n_kv][128]
-            news.append(T[torch.arange(batch, device=dev)[None, :], :, steps_idx].contiguous())
+            NEWS[kind, l] = T[torch.arange(batch, device=dev)[None, :], :, steps_idx]
             del T
         q = synth.queries(g, batch, n_q, dev).to(torch.bfloat16)
-        st.append(dict(cfg=cfg, bt=bt, pool=pool, staging=staging, ws=ws, kvp=kvp, k=news[0], v=news[1], q=q,
+        st.append(dict(cfg=cfg, bt=bt, pool=pool, staging=staging, ws=ws, kvp=kvp, q=q,
                        out=torch.empty(batch, n_q, D, device=dev)))
         torch.cuda.synchronize()
         assert kv.read_error(ws) == 0
@@ -947,15 +955,34 @@ def run_long(args):
         e.record()
         return e
 
+    # the step's new tokens for every layer, gathered into fixed buffers
+    sidx = torch.zeros(1, dtype=torch.long, device=dev)
+    buf = torch.empty(2, layers, 1, batch, n_kv, D, dtype=torch.bfloat16, device=dev)
+
+    kbuf = [buf[0, l, 0] for l in range(layers)]
+    vbuf = [buf[1, l, 0] for l in range(layers)]
+    torch.index_select(NEWS, 2, sidx, out=buf)   # loads the gather's kernel before the timed windows
+    torch.cuda.synchronize()
+
+    def one_step():
+        torch.index_select(NEWS, 2, sidx, out=buf)
+        for l, x in enumerate(st):
+            kv.append(x["cfg"], x["pool"], x["staging"], x["bt"], pos, kbuf[l], vbuf[l], x["ws"])
+            kv.decode_attn(x["cfg"], x["q"], x["pool"], x["staging"], x["bt"], lens, x["out"], x["ws"])
+        pos.add_(1)
+        lens.add_(1)
+        sidx.add_(1)
+
+    eager_steps = min(window, steps)   # the first window runs eagerly
+    graph = None
     ev0 = mark()
     t_loop = time.time()
     with ClockSampler(torch.cuda.current_device()) as clk:
         for s in range(1, steps + 1):
-            for x in st:
-                kv.append(x["cfg"], x["pool"], x["staging"], x["bt"], pos, x["k"][s - 1], x["v"][s - 1], x["ws"])
-                kv.decode_attn(x["cfg"], x["q"], x["pool"], x["staging"], x["bt"], lens, x["out"], x["ws"])
-            pos += 1
-            lens += 1
+            if graph is None:
+                one_step()
+            else:
+                graph.replay()
             win_n += 1
             check = s in LONG_CHECK or s == steps
             if check or s % window == 0 or s == steps:
@@ -965,6 +992,10 @@ def run_long(args):
                 if s % window == 0 or s == steps:
                     windows.append((s, win_ms * 1e3 / win_n))
                     win_ms, win_n = 0.0, 0
+                if s == eager_steps and s < steps and not args.long_eager:   # capture once, outside the timed windows
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph):
+                        one_step()
                 if check:      # outside the timed windows
                     num = den = 0.0
                     emax = emean = 0.0
@@ -984,15 +1015,20 @@ def run_long(args):
         assert kv.read_error(x["ws"]) == 0
     assert kv.read_error(ws16) == 0
     us = [u for _, u in windows]
+    ug = us[1:] if len(us) > 1 else us   # the graph-replayed windows (eager with --long-eager)
     print(json.dumps({
         "workload": w.name, "layers": layers, "batch": batch, "n_q_heads": n_q, "n_kv_heads": n_kv, "block": B,
         "varn_iters": w.iters, "prefill_lengths": prefill, "steps": steps,
-        "timing": f"CUDA events per window of {window} steps (each step: for every layer kvarn_append + "
-                  "kvarn_decode_attn, eager calls); the error checkpoints are outside the windows",
-        "us_per_step": {"first_window": round(us[0], 1), "last_window": round(us[-1], 1),
-                        "mean": round(sum(us) / len(us), 1),
+        "timing": f"CUDA events per window of {window} steps (each step: one gather of the step's new tokens, "
+                  "then for every layer kvarn_append + kvarn_decode_attn); the first window as eager calls, the "
+                  "rest as replays of the step captured once as a CUDA graph; the error checkpoints and the "
+                  "capture are outside the windows",
+        "us_per_step": {"first_window_eager": round(us[0], 1),
+                        "second_window_graph": round(us[1], 1) if len(us) > 1 else None,
+                        "last_window": round(us[-1], 1),
+                        "mean_graph": round(sum(ug) / len(ug), 1),
                         "by_step": [[s_, round(u, 1)] for s_, u in windows[::max(1, len(windows) // 16)]]},
-        "decode_tokens_per_s_mean": round(batch / (sum(us) / len(us) * 1e-6), 1),
+        "decode_tokens_per_s_mean": round(batch / (sum(ug) / len(ug) * 1e-6), 1),
         "error_vs_bf16_cache": curve, "setup_s": round(t_setup, 1), "loop_s": round(t_loop, 1),
         "clocks": clk.summary()}), flush=True)
 
