@@ -277,9 +277,63 @@ __device__ __forceinline__ void combine_slices(const float* sl, int n, int lane,
 // (unrotated) are added; the bf16 cache (ROT = false) has every token in its
 // pages. qsh: 128 floats of this warp's shared memory. gw = row * n_q +
 // query head.
+// LSE slice of the raw tail rows r = first, first + step, ... < ntail (at most
+// 64 / step of them) of one (row, query head): unrotated q (times sm_scale
+// log2 e, this lane's 4 channels in qv) against the bf16 staging rows. Each
+// lane scores its 4 channels of every row, a warp sum gives the score; m, l
+// and acc (this lane's 4 channels) start at -inf, 0 and 0.
+template <int B, int STEP>
+__device__ __forceinline__ void tail_slice(const uint16_t* kst, int ntail, int first, const float (&qv)[4], int lane,
+                                           float& m, float& l, float (&acc)[4]) {
+    constexpr int R = (B + STEP - 1) / STEP;   // rows of this slice at most
+    const uint16_t* vst = kst + B * kD;
+    uint2 ku[R], vu[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int r = first + i * STEP;
+        if (r < ntail) {
+            ku[i] = reinterpret_cast<const uint2*>(kst + (int64_t)r * kD)[lane];
+            vu[i] = reinterpret_cast<const uint2*>(vst + (int64_t)r * kD)[lane];
+        }
+    }
+    float sc[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        float d = 0.f;
+        if (first + i * STEP < ntail) {
+            d = fmaf(qv[0], __uint_as_float(ku[i].x << 16), d);
+            d = fmaf(qv[1], __uint_as_float(ku[i].x & 0xffff0000u), d);
+            d = fmaf(qv[2], __uint_as_float(ku[i].y << 16), d);
+            d = fmaf(qv[3], __uint_as_float(ku[i].y & 0xffff0000u), d);
+        }
+        sc[i] = d;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < R; ++i) sc[i] += __shfl_xor_sync(kFull, sc[i], o);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+        if (first + i * STEP < ntail) mx = fmaxf(mx, sc[i]);
+    if (mx == -INFINITY) return;
+    m = mx;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        if (first + i * STEP < ntail) {
+            const float p = exp2f(sc[i] - mx);
+            l += p;
+            acc[0] = fmaf(p, __uint_as_float(vu[i].x << 16), acc[0]);
+            acc[1] = fmaf(p, __uint_as_float(vu[i].x & 0xffff0000u), acc[1]);
+            acc[2] = fmaf(p, __uint_as_float(vu[i].y << 16), acc[2]);
+            acc[3] = fmaf(p, __uint_as_float(vu[i].y & 0xffff0000u), acc[3]);
+        }
+    }
+}
+
 template <int B, bool ROT, int NWIDE = 0>
 __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np, const float* p0, float* qsh,
-                                          int lane, const float* wide = nullptr) {
+                                          int lane, const float* wide = nullptr, const float* tails = nullptr) {
     const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);   // b: a (virtual) row sequence
     const int h = hq / a.G;
     const int rb = a.chunk == 1 ? b : b / a.chunk;              // its real sequence
@@ -294,7 +348,7 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np,
     const int nb = split_nblocks(sp, b);
     // raw rows in staging (< B <= 64): the visible tokens past the pool blocks
     const int ntail = ROT ? max(0, split_visible(sp, b, L) - nb * B) : 0;
-    if (ntail > 0) {   // start the tail rows on their way to L2 while the partials merge
+    if (NWIDE == 0 && ntail > 0) {   // start the tail rows on their way to L2 while the partials merge
         const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
         for (int r = lane; r < ntail; r += 32) {
             prefetch_l2(kst + (int64_t)r * kD);
@@ -314,7 +368,20 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np,
             for (int k = 0; k < 4; ++k) acc[k] *= kInvSqrtD * sign_of4(a.sb[0], a.sb[1], a.sb[2], a.sb[3], 4 * lane + k);
         }
     }
-    if (ntail > 0) {
+    if constexpr (NWIDE > 0) {
+        // the wide merge's warps scored the tail rows: fold their slices in (the
+        // slices are unrotated, like the accumulator after the inverse FWHT)
+        float mt = -INFINITY, lt = 0.f, at[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ntail > 0) combine_slices(tails, NWIDE, lane, mt, lt, at);
+        if (mt != -INFINITY) {
+            const float mn = fmaxf(m, mt);
+            const float fa = m == -INFINITY ? 0.f : exp2f(m - mn), ft = exp2f(mt - mn);
+            l = l * fa + lt * ft;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = acc[k] * fa + at[k] * ft;
+            m = mn;
+        }
+    } else if (ntail > 0) {
         // this warp's query (unrotated, times sm_scale log2 e) in shared memory, so
         // that lane r can score tail row r (and r + 32) over all 128 channels
         // with its loads issued at once
@@ -443,8 +510,10 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
 
 // The wide merge, for units cut into many partials (few long sequences):
 // one CTA of kWideWarps warps per (row, query head). Warp k LSE-merges its
-// share of the unit's partials, the shares meet in shared memory and warp 0
-// combines them and finishes the row.
+// share of the unit's partials and scores its share of the raw tail rows
+// (rows k, k + kWideWarps, ...); the shares meet in shared memory and warp 0
+// combines the partials, rotates them back, folds in the tail shares and
+// finishes the row.
 constexpr int kWideWarps = 8;
 template <int B, bool ROT>
 __global__ void __launch_bounds__(32 * kWideWarps, 4) merge_wide_kernel(AttnArgs a) {
@@ -453,10 +522,31 @@ __global__ void __launch_bounds__(32 * kWideWarps, 4) merge_wide_kernel(AttnArgs
     const int64_t gw = blockIdx.x;
     if (gw >= (int64_t)a.batch * a.n_q) return;   // (uniform over the CTA)
     __shared__ __align__(16) float slices[kWideWarps][kPartialStride];
+    __shared__ __align__(16) float tails[kWideWarps][kPartialStride];
     __shared__ __align__(16) float qsh[kD];
     int np;
     const float* p0;
     merge_locate<B, ROT>(a, gw, lane, np, p0);
+    // this warp's share of the raw tail rows (2-bit cache): rows wp, wp + 8, ...
+    float tm = -INFINITY, tl = 0.f, tacc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ROT) {
+        const int b = (int)(gw / a.n_q), h = (int)(gw % a.n_q) / a.G;
+        const int rb = a.chunk == 1 ? b : b / a.chunk;
+        const int L = a.seq_lens[rb];
+        if (L >= 0 && L <= a.max_blocks * B) {
+            const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, 0, a.chunk};
+            const int ntail = max(0, split_visible(sp, b, L) - split_nblocks(sp, b) * B);
+            if (wp < ntail) {
+                float qv[4];
+                load_q4(a.q, a.q_dtype, gw, lane, qv);
+                const float qs = a.sm_scale * kLog2e;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) qv[k] *= qs;
+                const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
+                tail_slice<B, kWideWarps>(kst, ntail, wp, qv, lane, tm, tl, tacc);
+            }
+        }
+    }
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int i0 = (int)((int64_t)np * wp / kWideWarps), i1 = (int)((int64_t)np * (wp + 1) / kWideWarps);
     const int64_t pstride = (int64_t)a.G * kPartialStride;
@@ -464,10 +554,13 @@ __global__ void __launch_bounds__(32 * kWideWarps, 4) merge_wide_kernel(AttnArgs
     if (lane == 0) {
         slices[wp][0] = m;
         slices[wp][1] = l;
+        tails[wp][0] = tm;
+        tails[wp][1] = tl;
     }
     *reinterpret_cast<float4*>(&slices[wp][4 + 4 * lane]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(&tails[wp][4 + 4 * lane]) = make_float4(tacc[0], tacc[1], tacc[2], tacc[3]);
     __syncthreads();
-    if (wp == 0) merge_row<B, ROT, kWideWarps>(a, gw, np, p0, qsh, lane, &slices[0][0]);
+    if (wp == 0) merge_row<B, ROT, kWideWarps>(a, gw, np, p0, qsh, lane, &slices[0][0], &tails[0][0]);
 }
 
 // Whether the merge of a launch with nw split warps over batch * n_kv units
