@@ -12,8 +12,9 @@
 // takes blocks [w*W/nw, (w+1)*W/nw) of the W blocks in total, so ragged
 // lengths stay balanced. A warp writes one partial (running max, sum and 128
 // rotated accumulators per query head) for every unit its range touches, in
-// slot unit + w; the merge kernel finds the warps of a unit by the same
-// arithmetic.
+// slot unit + w, and records in the workspace's unit map whether it took the
+// unit's first or last block, so that the merge kernel reads the unit's
+// consecutive slots without redoing the split arithmetic.
 //
 // Per warp: lane 0 streams each block's K and V head-blocks into a ring of
 // shared-memory stages with 1-D bulk copies (cp.async.bulk) counted on
