@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     }
 
     // per-unit state
-    float kmul = 0.f;          // 2^9 * 2^(e-12) * sm_scale * log2(e) for this lane's head tq
+    float kmul = 0.f;          // 2^(e-12) * sm_scale * log2(e) / kA for this lane's head tq
     float m_run = -INFINITY, l_part = 0.f;
     float2 O[8];               // rotated output, channels 32g + 4gq + 2m + {0, 1}, head tq
     const float sgn4[4] = {sign_of4(sb0, sb1, sb2, sb3, 4 * lane), sign_of4(sb0, sb1, sb2, sb3, 4 * lane + 1),
