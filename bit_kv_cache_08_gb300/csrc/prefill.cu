@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                 mma16816(Dz, ph[sb][2], pl[sb][2], ph[sb][3], pl[sb][3], zs4.z, zs4.w);
             }
             // this lane: columns 2tq, 2tq + 1 of vector gq (hi + lo rows): tq < 2 holds
-            // Z of groups 2tq, 2tq + 1; zq[g] = Z_g * 2^-9 for the 4 lanes of vector gq
+            // Z of groups 2tq, 2tq + 1; zq[g] = Z_g * kA for the 4 lanes of vector gq
             float zq[4];
             {
                 const float c0 = Dz[0] + Dz[2], c1 = Dz[1] + Dz[3];
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(32) prefill_attn_kernel(AttnArgs a) {
                         }
                     }
                 }
-                // O += 2^9 C_c / lam * (Ob + Z * 2^-9): lane holds channels 32g + 8tq + f (column 2tq)
+                // O += C_c / (kA lam) * (Ob + Z * kA): lane holds channels 32g + 8tq + f (column 2tq)
                 // and 32g + 8tq + 4 + f (column 2tq + 1)
                 const uint4 c4 = *reinterpret_cast<const uint4*>(VC + 32 * g + 8 * tq);
                 const float2 il42 = make_float2(il4, il4), zq2 = make_float2(zq[g], zq[g]);
