@@ -108,8 +108,9 @@ struct QuantParams {
 
 // A variance that is zero up to rounding (v <= 2^-30 mu^2), not positive or
 // not finite leaves its row/column factor unchanged (a constant column keeps C).
+// (v > 2^-30 mu^2 already rules out v <= 0, and a NaN fails both comparisons.)
 __device__ __forceinline__ bool usable_variance(float v, float mu) {
-    return v > 0.f && isfinite(v) && v > 0x1p-30f * (mu * mu);
+    return v > 0x1p-30f * (mu * mu) && v < INFINITY;
 }
 
 // Least fp16 s >= 0 with z + L s >= M (L = 2^bits - 1 steps), for fp16 z <= M
@@ -211,10 +212,10 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
                 const float v = __fmul_rn(var[i], 1.0f / kD);
-                if (usable_variance(v, mu[i])) {
-                    rR[i] = rsqrtf(v);        // within 2 ulp; the factor is rounded to fp16 below
-                    Rf[i] = v * rR[i];
-                }
+                const float r = rsqrtf(v);    // within 2 ulp; the factor is rounded to fp16 below
+                const bool ok = usable_variance(v, mu[i]);
+                rR[i] = ok ? r : rR[i];
+                Rf[i] = ok ? v * r : Rf[i];
             }
         }
         if (p.flags & KVARN_FLAG_NO_CHANNEL_PASS) continue;   // (uniform over the CTA)
@@ -253,10 +254,10 @@ __device__ void quantize_tile(float (&x)[kRowsPerWarp][4], const QuantParams& p,
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const float vk = __fmul_rn(cvar[k], 1.0f / B);
-            if (usable_variance(vk, cmu[k])) {
-                rCf[k] = rsqrtf(vk);
-                Cf[k] = vk * rCf[k];
-            }
+            const float r = rsqrtf(vk);
+            const bool ok = usable_variance(vk, cmu[k]);
+            rCf[k] = ok ? r : rCf[k];
+            Cf[k] = ok ? vk * r : Cf[k];
         }
     }
 
