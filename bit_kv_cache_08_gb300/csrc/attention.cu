@@ -738,14 +738,12 @@ cudaError_t launch_decode_attn(const kvarn_config& cfg, const void* q, int q_dty
     // wait-timeout path, run without a hang)
     a.first_wait_limit = (cfg.flags & KVARN_FLAG_TEST_WAIT_TIMEOUT) ? 0u : kWaitLimit;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
-    const unsigned mgrid = (unsigned)(((int64_t)a.batch * a.n_q + 3) / 4);
     return with_attn_kernel(cfg.block_size, cfg.bits, [&](auto k) {
         using K = decltype(k);
         cudaError_t e = launch_pdl(K::fn, nw, 32, K::smem(), st, a);
-        if (e == cudaSuccess)
-            e = merge_wide(nw, a.batch, a.n_kv)
-                    ? launch_pdl(merge_wide_kernel<K::kB, true>, (unsigned)((int64_t)a.batch * a.n_q), 32 * kWideWarps, 0, st, a)
-                    : launch_pdl(merge_kernel<K::kB, true>, mgrid, 128, 0, st, a);
+        // up to one wave of wide CTAs (4 per SM), so that 8 warps share each
+        // row's raw tail rows
+        if (e == cudaSuccess) e = launch_merge<K::kB, true>(a, nw, 4, st);
         return e;
     });
 }

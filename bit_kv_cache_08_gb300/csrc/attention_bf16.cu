@@ -298,16 +298,13 @@ cudaError_t launch_decode_attn_bf16(const kvarn_config& cfg, const void* q, int 
     a.sm_scale = cfg.sm_scale;
     a.flags = cfg.flags;
     for (int i = 0; i < 4; ++i) a.sb[i] = cfg.sign_bits[i];
-    const unsigned mgrid = (unsigned)(((int64_t)batch * a.n_q + 3) / 4);
     cudaError_t e;
     if (cfg.block_size == 32)
         e = launch_pdl(decode_attn_bf16_kernel<32>, nw, 32, attn_bf16_smem_bytes(), st, a);
     else
         e = launch_pdl(decode_attn_bf16_kernel<64>, nw, 32, attn_bf16_smem_bytes(), st, a);
-    if (e == cudaSuccess)
-        e = merge_wide(nw, batch, a.n_kv)
-                ? launch_pdl(merge_wide_kernel<kChunk, false>, (unsigned)((int64_t)batch * a.n_q), 32 * kWideWarps, 0, st, a)
-                : launch_pdl(merge_kernel<kChunk, false>, mgrid, 128, 0, st, a);
+    // (no raw tail rows: the wide kernel only for many partials per unit)
+    if (e == cudaSuccess) e = launch_merge<kChunk, false>(a, nw, 0, st);
     return e;
 }
 

@@ -155,8 +155,8 @@ __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t row,
     }
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 // ---------------------------------------------------------------- merge
@@ -214,19 +214,20 @@ __device__ __forceinline__ void lse_partials(const float* p0, int np, int64_t ps
     }
 }
 
-// The same LSE merge in batches of 8 partials with a running rescale, for
+// The same LSE merge in batches of NB partials with a running rescale, for
 // the wide merge's warps (fewer registers than lse_partials); m, l and acc
 // start at -inf, 0 and 0.
+template <int NB>
 __device__ __forceinline__ void lse_stream(const float* p0, int np, int64_t pstride, int lane, float& m, float& l,
                                            float (&acc)[4]) {
-    for (int i0 = 0; i0 < np; i0 += 8) {
-        const int cnt = min(8, np - i0);
+    for (int i0 = 0; i0 < np; i0 += NB) {
+        const int cnt = min(NB, np - i0);
         const float* q = p0 + i0 * pstride;
         const float pm = lane < cnt ? __ldcg(q + lane * pstride) : -INFINITY;
         const float pl = lane < cnt ? __ldcg(q + lane * pstride + 1) : 0.f;
-        float4 pa[8];
+        float4 pa[NB];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < NB; ++i)
             if (i < cnt) pa[i] = __ldcg(reinterpret_cast<const float4*>(q + i * pstride + 4) + lane);
         const float bm = warp_max(pm);
         if (bm == -INFINITY) continue;
@@ -237,7 +238,7 @@ __device__ __forceinline__ void lse_stream(const float* p0, int np, int64_t pstr
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[k] *= fa;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < NB; ++i) {
             if (i < cnt) {
                 const float wgt = __shfl_sync(kFull, wl, i);
                 acc[0] = fmaf(wgt, pa[i].x, acc[0]);
@@ -348,13 +349,15 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np,
     const int nb = split_nblocks(sp, b);
     // raw rows in staging (< B <= 64): the visible tokens past the pool blocks
     const int ntail = ROT ? max(0, split_visible(sp, b, L) - nb * B) : 0;
-    if (NWIDE == 0 && ntail > 0) {   // start the tail rows on their way to L2 while the partials merge
+    float qt[4] = {0.f, 0.f, 0.f, 0.f};   // the query for the tail rows, loaded with them
+    if (NWIDE == 0 && ntail > 0) {   // start the tail rows on their way to L1 while the partials merge
+        load_q4(a.q, a.q_dtype, gw, lane, qt);
         const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
         for (int r = lane; r < ntail; r += 32) {
-            prefetch_l2(kst + (int64_t)r * kD);
-            prefetch_l2(kst + (int64_t)r * kD + 64);
-            prefetch_l2(kst + (int64_t)(B + r) * kD);
-            prefetch_l2(kst + (int64_t)(B + r) * kD + 64);
+            prefetch_l1(kst + (int64_t)r * kD);
+            prefetch_l1(kst + (int64_t)r * kD + 64);
+            prefetch_l1(kst + (int64_t)(B + r) * kD);
+            prefetch_l1(kst + (int64_t)(B + r) * kD + 64);
         }
     }
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -387,10 +390,8 @@ __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np,
         // with its loads issued at once
         __syncwarp();
         {
-            float qv[4];
-            load_q4(a.q, a.q_dtype, gw, lane, qv);
             const float qs = a.sm_scale * kLog2e;
-            *reinterpret_cast<float4*>(qsh + 4 * lane) = make_float4(qv[0] * qs, qv[1] * qs, qv[2] * qs, qv[3] * qs);
+            *reinterpret_cast<float4*>(qsh + 4 * lane) = make_float4(qt[0] * qs, qt[1] * qs, qt[2] * qs, qt[3] * qs);
         }
         __syncwarp();
         const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
@@ -464,16 +465,18 @@ __device__ __forceinline__ void merge_locate(const AttnArgs& a, int64_t gw, int 
     const int b = (int)(gw / a.n_q), hq = (int)(gw % a.n_q);
     const int h = hq / a.G, jq = hq % a.G;
     const int rb = a.chunk == 1 ? b : b / a.chunk;
+    const int64_t u = (int64_t)b * a.n_kv + h;
+    // the unit map entry does not depend on the length: both loads in flight at once
+    int2 wm = make_int2(-1, -1);
+    if (a.unit_map != nullptr) wm = __ldcg(reinterpret_cast<const int2*>(a.unit_map) + u);
     const int L = a.seq_lens[rb];
     if (L < 0 || L > a.max_blocks * B) return;
     const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, ROT ? 0 : 1, a.chunk};
     const int nb = split_nblocks(sp, b);
     if (nb <= 0) return;
-    const int64_t u = (int64_t)b * a.n_kv + h;
     if (a.unit_map != nullptr) {
         // a range outside the grid (a warp gave up before recording it, its
         // error flag set) merges nothing rather than reading out of bounds
-        const int2 wm = __ldcg(reinterpret_cast<const int2*>(a.unit_map) + u);
         if (wm.x >= 0 && wm.y >= wm.x && wm.y < a.nw) {
             np = wm.y - wm.x + 1;
             p0 = a.partials + ((u + wm.x) * a.G + jq) * kPartialStride;
@@ -514,9 +517,11 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
 // (rows k, k + kWideWarps, ...); the shares meet in shared memory and warp 0
 // combines the partials, rotates them back, folds in the tail shares and
 // finishes the row.
+// NB: partials per load round trip of a warp's LSE merge. With 8 the kernel
+// needs 110 registers (2 CTAs per SM); with 4, 64 (4 CTAs per SM).
 constexpr int kWideWarps = 8;
-template <int B, bool ROT>
-__global__ void __launch_bounds__(32 * kWideWarps, 4) merge_wide_kernel(AttnArgs a) {
+template <int B, bool ROT, int NB>
+__global__ void __launch_bounds__(32 * kWideWarps, NB == 8 ? 2 : 4) merge_wide_kernel(AttnArgs a) {
     wait_prior_grids();
     const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
     const int64_t gw = blockIdx.x;
@@ -524,33 +529,43 @@ __global__ void __launch_bounds__(32 * kWideWarps, 4) merge_wide_kernel(AttnArgs
     __shared__ __align__(16) float slices[kWideWarps][kPartialStride];
     __shared__ __align__(16) float tails[kWideWarps][kPartialStride];
     __shared__ __align__(16) float qsh[kD];
+    // q (for the raw tail rows) and the unit's length and partial range are
+    // independent loads: issue them together
+    float qv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ROT) load_q4(a.q, a.q_dtype, gw, lane, qv);
     int np;
     const float* p0;
     merge_locate<B, ROT>(a, gw, lane, np, p0);
-    // this warp's share of the raw tail rows (2-bit cache): rows wp, wp + 8, ...
-    float tm = -INFINITY, tl = 0.f, tacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // this warp's share of the raw tail rows (2-bit cache): rows wp, wp + 8, ...;
+    // their lines are requested now and read after the partials' LSE merge
+    int ntail = 0;
+    const uint16_t* kst = nullptr;
     if (ROT) {
         const int b = (int)(gw / a.n_q), h = (int)(gw % a.n_q) / a.G;
         const int rb = a.chunk == 1 ? b : b / a.chunk;
         const int L = a.seq_lens[rb];
         if (L >= 0 && L <= a.max_blocks * B) {
             const SplitArgs sp{a.seq_lens, a.batch, a.n_kv, a.max_blocks, B, 0, a.chunk};
-            const int ntail = max(0, split_visible(sp, b, L) - split_nblocks(sp, b) * B);
-            if (wp < ntail) {
-                float qv[4];
-                load_q4(a.q, a.q_dtype, gw, lane, qv);
-                const float qs = a.sm_scale * kLog2e;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) qv[k] *= qs;
-                const uint16_t* kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
-                tail_slice<B, kWideWarps>(kst, ntail, wp, qv, lane, tm, tl, tacc);
-            }
+            ntail = max(0, split_visible(sp, b, L) - split_nblocks(sp, b) * B);
+            kst = a.staging + (((int64_t)rb * a.n_kv + h) * 2 + 0) * B * kD;
+            // lane: row wp + 8 (lane / 4), K or V (bit 1), first or second 128-byte line (bit 0)
+            constexpr int R = (B + kWideWarps - 1) / kWideWarps;
+            const int r = wp + kWideWarps * (lane >> 2);
+            if ((lane >> 2) < R && r < ntail)
+                prefetch_l1(kst + ((lane & 2) ? B * kD : 0) + (int64_t)r * kD + (lane & 1) * 64);
         }
     }
     float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int i0 = (int)((int64_t)np * wp / kWideWarps), i1 = (int)((int64_t)np * (wp + 1) / kWideWarps);
     const int64_t pstride = (int64_t)a.G * kPartialStride;
-    if (i1 > i0) lse_stream(p0 + i0 * pstride, i1 - i0, pstride, lane, m, l, acc);
+    if (i1 > i0) lse_stream<NB>(p0 + i0 * pstride, i1 - i0, pstride, lane, m, l, acc);
+    float tm = -INFINITY, tl = 0.f, tacc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (wp < ntail) {
+        const float qs = a.sm_scale * kLog2e;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qv[k] *= qs;
+        tail_slice<B, kWideWarps>(kst, ntail, wp, qv, lane, tm, tl, tacc);
+    }
     if (lane == 0) {
         slices[wp][0] = m;
         slices[wp][1] = l;
@@ -563,8 +578,48 @@ __global__ void __launch_bounds__(32 * kWideWarps, 4) merge_wide_kernel(AttnArgs
     if (wp == 0) merge_row<B, ROT, kWideWarps>(a, gw, np, p0, qsh, lane, &slices[0][0], &tails[0][0]);
 }
 
-// Whether the merge of a launch with nw split warps over batch * n_kv units
-// takes the wide kernel: 16 or more partials per unit on average.
-inline bool merge_wide(int64_t nw, int64_t batch, int n_kv) { return nw >= 16 * batch * (int64_t)n_kv; }
+// Whether the merge of a launch with nw split warps over `units` (sequence,
+// kv head) units and `rows` query rows takes the wide kernel: 16 or more
+// partials per unit on average, or no more rows than wide_rows (the 2-bit
+// cache: one wave of wide CTAs, so that 8 warps share each row's raw tail
+// rows; 0 for the bf16 cache, which has no tail rows).
+inline bool merge_wide(int64_t nw, int64_t units, int64_t rows, int64_t wide_rows) {
+    return nw >= 16 * units || rows <= wide_rows;
+}
+
+// The wide merge's partials per round trip: 8 when its warps average more
+// than 4 partials each and the rows fit one wave at 2 CTAs per SM (few long
+// sequences), else 4.
+inline int wide_merge_batch(int64_t nw, int64_t units, int64_t rows, int64_t sms) {
+    return (nw > 4 * kWideWarps * units && rows <= 2 * sms) ? 8 : 4;
+}
+
+// SMs of the current device (cached per device; 0 when it cannot be queried).
+inline int64_t current_device_sms() {
+    static int cache[64];
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return 0;
+    if (cache[d] <= 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+        cache[d] = sms;
+    }
+    return cache[d];
+}
+
+// Launches the merge of a split launch with nw warps: the wide kernel (with
+// its batch) or the one-warp-per-row kernel. wide_ctas_per_sm > 0 also takes
+// the wide kernel for up to that many rows per SM.
+template <int B, bool ROT>
+cudaError_t launch_merge(const AttnArgs& a, int64_t nw, int wide_ctas_per_sm, cudaStream_t st) {
+    const int64_t units = (int64_t)a.batch * a.n_kv, rows = (int64_t)a.batch * a.n_q;
+    const int64_t sms = current_device_sms();
+    if (merge_wide(nw, units, rows, wide_ctas_per_sm * sms)) {
+        if (wide_merge_batch(nw, units, rows, sms) == 8)
+            return launch_pdl(merge_wide_kernel<B, ROT, 8>, (unsigned)rows, 32 * kWideWarps, 0, st, a);
+        return launch_pdl(merge_wide_kernel<B, ROT, 4>, (unsigned)rows, 32 * kWideWarps, 0, st, a);
+    }
+    return launch_pdl(merge_kernel<B, ROT>, (unsigned)((rows + 3) / 4), 128, 0, st, a);
+}
 
 }  // namespace kvarn

@@ -65,6 +65,32 @@ def test_ragged_paged_with_tails(kvlib, B, iters, qdtype):
     attn_close(got, ref)
 
 
+@pytest.mark.parametrize("B", [32, 64])
+def test_many_rows_with_tails(kvlib, B):
+    """24 sequences x 32 query heads: more rows than one wave of the wide merge
+    holds (4 CTAs per SM) and fewer split warps than 16 per unit, so the
+    one-warp-per-row merge scores each row's raw tail rows (1 to 3 blocks and
+    a tail of 1 .. B - 1 rows). Sampled sequences against the oracle."""
+    kv = kvlib
+    n_q, n_kv, batch = 32, 8, 24
+    lens = [B * (1 + i % 3) + 1 + (7 * i) % (B - 1) for i in range(batch)]
+    assert all(L % B for L in lens)
+    max_blocks = max(lens) // B + 1
+    sb = synth.sign_bits(300 + B)
+    cfg = kv.make_config(n_q, n_kv, B, 2, sb)
+    g = synth.make_gen(300 + B)
+    K = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    V = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
+    q = synth.queries(g, batch, n_q).to(torch.bfloat16).cuda()
+    cache = PagedCache(kv, cfg, batch, max_blocks, perm_seed=B + 1)
+    cache.prefill(K, V, lens)
+    got, err = _run_attn(kv, cache, q, lens)
+    assert err == 0
+    seqs = [0, 7, 23]
+    ref = oracle_attention(cache, q, lens, sb, seqs=seqs)
+    attn_close(got[seqs], ref)
+
+
 @pytest.mark.parametrize("G", [1, 2, 3, 4])
 @pytest.mark.parametrize("B", [32, 64])
 def test_group_sizes(kvlib, G, B):
