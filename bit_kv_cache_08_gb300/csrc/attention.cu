@@ -82,7 +82,7 @@ __host__ __device__ constexpr int attn_q_bytes(int) { return 2 * kQZero + 2 * kD
 __host__ __device__ constexpr int pex_rot(int B, int r) { return B == 64 ? 16 * r : 16 * (r >> 1); }
 
 template <int B, int BITS, int S>
-__global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
+__device__ __forceinline__ void decode_attn_2bit_body(const AttnArgs& a) {
     static_assert(BITS >= 2 && BITS <= 4, "2-, 3- or 4-bit codes");
     wait_prior_grids();
     constexpr int HB = head_block_bytes(B, BITS);
@@ -661,9 +661,38 @@ __global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
     }
 }
 
+// The split kernel at ptxas's own register target, and with a minimum of
+// MINB resident CTAs per SM (at most 65536 / (32 MINB) registers a thread).
+template <int B, int BITS, int S>
+__global__ void __launch_bounds__(32) decode_attn_2bit_kernel(AttnArgs a) {
+    decode_attn_2bit_body<B, BITS, S>(a);
+}
+template <int B, int BITS, int S, int MINB>
+__global__ void __launch_bounds__(32, MINB) decode_attn_2bit_kernel_minb(AttnArgs a) {
+    decode_attn_2bit_body<B, BITS, S>(a);
+}
+
 // ---------------------------------------------------------------- host side
 template <int B, int BITS>
 constexpr int stages_for() { return 2; }
+
+// Minimum resident CTAs per SM that the split kernel is compiled for (0: the
+// plain kernel), chosen by timing each instantiation on the 64 x 8192-token
+// Llama-shaped cache. 3-bit, B = 64: shared memory holds 9 CTAs per SM
+// whatever the registers, and with the bound at 1 ptxas takes 191 registers
+// instead of 156 (237 -> 200 us). 3-bit, B = 32: 16 gives 128 registers
+// without spills, 15 warps per SM (shared memory) instead of 12 (218 -> 207
+// us). The 2- and 4-bit instantiations were fastest plain (bounds of 1, 10,
+// 11 at 2 bits, B = 64: 142, 129.5, 129.4 against 128.7 us).
+template <int B, int BITS>
+constexpr int attn_min_ctas() { return BITS != 3 ? 0 : (B == 64 ? 1 : 16); }
+
+template <int B, int BITS>
+constexpr auto attn_kernel_fn() {
+    constexpr int S = stages_for<B, BITS>(), M = attn_min_ctas<B, BITS>();
+    if constexpr (M > 0) return decode_attn_2bit_kernel_minb<B, BITS, S, M>;
+    else return decode_attn_2bit_kernel<B, BITS, S>;
+}
 
 template <int B, int BITS>
 size_t attn_smem_bytes() {
@@ -674,7 +703,7 @@ size_t attn_smem_bytes() {
 template <int B, int BITS>
 struct AttnKernel {
     static constexpr int kB = B;
-    static constexpr auto fn = decode_attn_2bit_kernel<B, BITS, stages_for<B, BITS>()>;
+    static constexpr auto fn = attn_kernel_fn<B, BITS>();
     static size_t smem() { return attn_smem_bytes<B, BITS>(); }
 };
 
