@@ -125,6 +125,15 @@ __device__ __forceinline__ void decode_attn_2bit_body(const AttnArgs& a) {
     split_locate(sp, s_beg, lane, cc.b, cc.h, cc.j);
     cc.nb = split_nblocks(sp, cc.b);
     Cursor ic = cc;   // issue cursor
+    {
+        // the first unit's query rows on their way to L1 while the block table
+        // and the first copies are fetched (unit_setup reads them)
+        const int qbytes = q_dtype == KVARN_FP32 ? 4 : 2, lines = qbytes;   // 128-byte lines per row
+        if (lane < G * lines) {
+            const int64_t row = (int64_t)cc.b * n_q + (int64_t)cc.h * G + lane / lines;
+            prefetch_l1(static_cast<const uint8_t*>(qptr) + row * kD * qbytes + 128 * (lane % lines));
+        }
+    }
 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
