@@ -1,6 +1,7 @@
 // attn_common.cuh -- pieces shared by the decode-attention kernels: the
-// argument block, tensor-core and exponent helpers, and the kernel that
-// merges the split-K partials.
+// argument block, tensor-core and exponent helpers, and the kernels that
+// merge the split-K partials (one warp per query row, or eight) with the
+// launch that picks between them.
 #pragma once
 #include "split.cuh"
 
@@ -270,14 +271,6 @@ __device__ __forceinline__ void combine_slices(const float* sl, int n, int lane,
     }
 }
 
-// One (row, query head) output: LSE-merge the np partials of its unit
-// (p0: the first, consecutive partials G * kPartialStride floats apart; np =
-// 0 when the unit has no pool blocks), add the raw tail rows, normalise and
-// store. For the 2-bit cache (ROT = true) the merged accumulator is in the
-// rotated space: it is rotated back once and the raw bf16 tail tokens
-// (unrotated) are added; the bf16 cache (ROT = false) has every token in its
-// pages. qsh: 128 floats of this warp's shared memory. gw = row * n_q +
-// query head.
 // LSE slice of the raw tail rows r = first, first + step, ... < ntail (at most
 // 64 / step of them) of one (row, query head): unrotated q (times sm_scale
 // log2 e, this lane's 4 channels in qv) against the bf16 staging rows. Each
@@ -332,6 +325,15 @@ __device__ __forceinline__ void tail_slice(const uint16_t* kst, int ntail, int f
     }
 }
 
+// One (row, query head) output: LSE-merge the np partials of its unit
+// (p0: the first, consecutive partials G * kPartialStride floats apart; np =
+// 0 when the unit has no pool blocks), add the raw tail rows, normalise and
+// store. For the 2-bit cache (ROT = true) the merged accumulator is in the
+// rotated space: it is rotated back once and the raw bf16 tail tokens
+// (unrotated) are added; the bf16 cache (ROT = false) has every token in its
+// pages. qsh: 128 floats of this warp's shared memory. gw = row * n_q +
+// query head. With NWIDE > 0 (the wide merge's warp 0) the partials and the
+// tail rows arrive as NWIDE per-warp LSE slices in shared memory (wide, tails).
 template <int B, bool ROT, int NWIDE = 0>
 __device__ __forceinline__ void merge_row(const AttnArgs& a, int64_t gw, int np, const float* p0, float* qsh,
                                           int lane, const float* wide = nullptr, const float* tails = nullptr) {
@@ -511,8 +513,9 @@ __global__ void __launch_bounds__(128) merge_kernel(AttnArgs a) {
     merge_row<B, ROT>(a, gw, np, p0, q_all[threadIdx.x >> 5], lane);
 }
 
-// The wide merge, for units cut into many partials (few long sequences):
-// one CTA of kWideWarps warps per (row, query head). Warp k LSE-merges its
+// The wide merge, for units cut into many partials (few long sequences) or
+// few enough rows for one wave of its CTAs: one CTA of kWideWarps warps per
+// (row, query head). Warp k LSE-merges its
 // share of the unit's partials and scores its share of the raw tail rows
 // (rows k, k + kWideWarps, ...); the shares meet in shared memory and warp 0
 // combines the partials, rotates them back, folds in the tail shares and
