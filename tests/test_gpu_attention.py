@@ -65,20 +65,24 @@ def test_ragged_paged_with_tails(kvlib, B, iters, qdtype):
     attn_close(got, ref)
 
 
+@pytest.mark.parametrize("batch", [24, 16])
 @pytest.mark.parametrize("B", [32, 64])
-def test_many_rows_with_tails(kvlib, B):
-    """24 sequences x 32 query heads: more rows than one wave of the wide merge
-    holds (4 CTAs per SM) and fewer split warps than 16 per unit, so the
-    one-warp-per-row merge scores each row's raw tail rows (1 to 3 blocks and
-    a tail of 1 .. B - 1 rows). Sampled sequences against the oracle."""
+def test_merge_paths_with_tails(kvlib, B, batch):
+    """32 query heads over 8 kv heads, every sequence with raw tail rows (1 to
+    3 blocks and a tail of 1 .. B - 1 rows). 24 sequences: more rows than one
+    wave of the wide merge holds (4 CTAs per SM) and fewer split warps than
+    16 per unit, so the one-warp-per-row merge scores the tails. 16
+    sequences: 512 rows fit one wave, so the 8-warp merge takes them, its
+    warps loading 4 partials per round trip. Sampled sequences against the
+    oracle."""
     kv = kvlib
-    n_q, n_kv, batch = 32, 8, 24
+    n_q, n_kv = 32, 8
     lens = [B * (1 + i % 3) + 1 + (7 * i) % (B - 1) for i in range(batch)]
     assert all(L % B for L in lens)
     max_blocks = max(lens) // B + 1
     sb = synth.sign_bits(300 + B)
     cfg = kv.make_config(n_q, n_kv, B, 2, sb)
-    g = synth.make_gen(300 + B)
+    g = synth.make_gen(300 + B + batch)
     K = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
     V = synth.kv_values(g, batch, n_kv, max(lens), 1.5, 4, 20.0).to(torch.bfloat16).cuda()
     q = synth.queries(g, batch, n_q).to(torch.bfloat16).cuda()
@@ -86,7 +90,7 @@ def test_many_rows_with_tails(kvlib, B):
     cache.prefill(K, V, lens)
     got, err = _run_attn(kv, cache, q, lens)
     assert err == 0
-    seqs = [0, 7, 23]
+    seqs = [0, 7, batch - 1]
     ref = oracle_attention(cache, q, lens, sb, seqs=seqs)
     attn_close(got[seqs], ref)
 
